@@ -1,0 +1,388 @@
+"""Benchmark of the paged KV-cache decode step on GB300.
+
+Workload: GQA 32 q / 8 kv heads, head_dim 128, bf16, block size 16, 256
+sequences with context lengths clip(round(LogNormal(ln 4096, 1)), 64, 32768),
+K/V/Q ~ N(0,1), blocks drawn from a shuffled pool sized to fit.  One step is
+the whole decode step: host ledger (on-demand blocks, block table, slot
+mapping) -> block table / lengths / slots to the GPU -> cache write of the new
+token's K/V -> paged decode attention over every sequence.
+
+Metric: KV GB/s of the decode-attention step (algorithmic bytes: K and V of
+every context token + q + out + table entries, per step, over step time), with
+seq-tokens/s (context tokens attended per second, one layer) beside it.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun each rank runs its own batch of 256 sequences (weak scaling, no
+collective on the data path; only a barrier and a max over ranks of the time).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV GB/s as % of GB300 HBM peak; seq-tokens/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.lines = []
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxes.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if args.impl != "reference" else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- oracle arm
+class OracleSample:
+    """The oracle (fp64 C, all host cores) on the first ``k`` sequences of the
+    workload: the same length law, shapes and dtype, bounded in size."""
+
+    def __init__(self, seed: int, k: int):
+        import oracle
+        from oracle.allocator_model import BlockLedger
+        from paged_kv_cache_146_gb300 import workloads
+
+        self.o = oracle.load()
+        self.threads = self.o.max_threads()
+        w = workloads.gqa_long(seed, num_seqs=k, growth_tokens=16)
+        v = workloads.host_values(w)
+        led = BlockLedger(w.num_blocks, 16, w.free_order)
+        tables = [[-1] * w.max_blocks_per_seq for _ in range(k)]
+        slots_p = led.append([0] * k, [int(x) for x in w.prior_lens], tables)
+        slots_n = led.append([int(x) for x in w.prior_lens], [1] * k, tables)
+        shape = (w.num_blocks, w.num_kv_heads, 16, w.head_dim)
+        self.kp = np.zeros(shape, dtype=np.uint16)
+        self.vp = np.zeros(shape, dtype=np.uint16)
+        self.o.cache_write(v["k_prompt"], v["v_prompt"], np.array(slots_p, dtype=np.int64),
+                           self.kp, self.vp, 16)
+        self.o.cache_write(v["k_new"], v["v_new"], np.array(slots_n, dtype=np.int64),
+                           self.kp, self.vp, 16)
+        self.w, self.q = w, v["q"]
+        self.tables = np.array(tables, dtype=np.int32)
+        self.lens = (w.prior_lens + 1).astype(np.int32)
+        self.tokens = int(self.lens.astype(np.int64).sum())
+        self.nbytes = self.tokens * w.num_kv_heads * w.head_dim * 2 * 2 + \
+            2 * k * w.num_q_heads * w.head_dim * 2 + \
+            4 * int(sum(-(-int(n) // 16) for n in self.lens)) + 4 * k
+        self.desc = f"first {k} of 256 sequences ({self.tokens} context tokens), one decode call"
+
+    def run(self) -> float:
+        t0 = time.perf_counter()
+        self.o.paged_decode(self.q, self.kp, self.vp, self.tables, self.lens, self.w.scale, True,
+                            self.threads)
+        return time.perf_counter() - t0
+
+
+def oracle_calibrated(seed: int, target_s: float) -> OracleSample:
+    """An oracle sample whose one call takes about ``target_s`` seconds."""
+    probe = OracleSample(seed, 2)
+    dt = probe.run()
+    k = int(min(256, max(2, round(2 * target_s / max(dt, 1e-3)))))
+    return OracleSample(seed, k)
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference implementation, timed on the host cores."""
+    if rank != 0:
+        return
+    per_step = min(args.ref_seconds, 150.0 / (args.steps + args.warmup))
+    sample = oracle_calibrated(args.seed, per_step)
+    for _ in range(args.warmup):
+        sample.run()
+    secs = [sample.run() for _ in range(args.steps)]
+    value = sample.nbytes / statistics.median(secs) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.median(secs), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "gqa_long", "num_seqs": 256, "q_heads": 32, "kv_heads": 8,
+                       "head_dim": 128, "block_size": 16, "kv_dtype": "bf16",
+                       "lengths": "clip(round(LogNormal(ln 4096, 1)), 64, 32768)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": sample.threads,
+                             "kind": "oracle", "sample": sample.desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def our_arm(args, world, rank, local):
+    import torch
+    from paged_kv_cache_146_gb300 import KVPool, cache_write, paged_decode_attention, workloads
+    from paged_kv_cache_146_gb300.engine import DecodeEngine
+
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    e2e_steps = args.e2e_steps
+    n_steps = args.warmup + args.steps + e2e_steps
+    w = workloads.gqa_long(args.seed + rank, growth_tokens=n_steps + 16)
+    S, hq, hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+    vals = workloads.device_values(w, dev)
+    pool = KVPool(w.num_blocks, hkv, d, w.dtype, free_order=w.free_order, device=dev)
+    eng = DecodeEngine(pool, S, hq, w.max_blocks_per_seq, w.scale, dev)
+    eng.prefill(vals["k_prompt"], vals["v_prompt"], w.prior_lens)
+    del vals["k_prompt"], vals["v_prompt"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 7 + rank)
+
+    def draw(*shape):
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    qs = [draw(S, hq, d) for _ in range(args.warmup + args.steps)]
+    ks = [draw(S, hkv, d) for _ in range(args.warmup + args.steps)]
+    vs = [draw(S, hkv, d) for _ in range(args.warmup + args.steps)]
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        eng.host_step()
+        cache_write(pool, ks[i], vs[i], eng.d_slots, eng.status)
+        if ev:
+            ev[0].record(stream)
+        paged_decode_attention(pool, qs[i], eng.d_tables, eng.d_lens, w.scale, eng.workspace,
+                               eng.status, out=eng.out)
+        if ev:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    rc, word = eng.check()
+    if rc != 0:
+        raise SystemExit(f"device status {rc} word {word:#x} after warm-up")
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid)
+    bytes_total, toks_total = 0, 0
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        step(args.warmup + k, attn_ev[k])
+        bytes_total += eng.step_bytes()
+        toks_total += int(eng.lens.astype(np.int64).sum())
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    rc, word = eng.check()
+    if rc != 0:
+        raise SystemExit(f"device status {rc} word {word:#x} in the timed steps")
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    bytes_all = bytes_total * world
+    toks_all = toks_total * world
+    value = bytes_all / (elapsed_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    bytes_per_launch = bytes_total / args.steps
+    achieved = bytes_per_launch / (attn_avg_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if e2e_steps > 0:
+        hq_h = [qs[i % len(qs)].cpu().pin_memory() for i in range(e2e_steps)]
+        hk_h = [ks[i % len(ks)].cpu().pin_memory() for i in range(e2e_steps)]
+        hv_h = [vs[i % len(vs)].cpu().pin_memory() for i in range(e2e_steps)]
+        out_h = torch.empty_like(eng.out, device="cpu").pin_memory()
+        dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(ks[0]), torch.empty_like(vs[0])
+        e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_bytes = 0
+        barrier(world)
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for i in range(e2e_steps):
+            dq.copy_(hq_h[i], non_blocking=True)
+            dk.copy_(hk_h[i], non_blocking=True)
+            dv.copy_(hv_h[i], non_blocking=True)
+            eng.decode_step(dq, dk, dv)
+            out_h.copy_(eng.out, non_blocking=True)
+            e_bytes += eng.step_bytes()
+        e_stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e_ms = max_over_ranks(e_start.elapsed_time(e_stop), world)
+        h2d = (dq.numel() + dk.numel() + dv.numel()) * 2 + eng.h_tables.numel() * 4 + \
+            eng.h_lens.numel() * 4 + eng.h_slots.numel() * 8
+        e2e = {"value": round(e_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h.numel() * 2),
+               "ms_per_step": round(e_ms / e2e_steps, 4)}
+        rc, word = eng.check()
+        if rc != 0:
+            raise SystemExit(f"device status {rc} word {word:#x} in the e2e steps")
+
+    if rank != 0:
+        return
+    cpu = None
+    if args.cpu_seconds > 0 and world == 1:
+        sample = oracle_calibrated(args.seed, args.cpu_seconds)
+        dt = sample.run()
+        cpu = {"value": round(sample.nbytes / dt / 1e9, 4), "unit": "GB/s",
+               "cores": sample.threads, "kind": "oracle", "sample": sample.desc,
+               "seconds": round(dt, 2)}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "gqa_long", "num_seqs": S, "q_heads": hq, "kv_heads": hkv,
+                   "head_dim": d, "block_size": 16, "kv_dtype": "bf16",
+                   "lengths": "clip(round(LogNormal(ln 4096, 1)), 64, 32768)",
+                   "mean_context": round(toks_total / args.steps / S, 1),
+                   "pool_blocks": w.num_blocks,
+                   "l2": "inputs larger than L2 (KV per step ~%.1f GB vs 129 MB L2)" % (bytes_per_launch / 1e9),
+                   "step": "host ledger + table/lens/slots H2D + cache_write + paged attention"},
+        "seq_tokens_per_s": round(toks_all / (elapsed_ms * 1e-3), 1),
+        "pct_of_peak": round(100.0 * value / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": args.traffic, "peak_kind": peak_kind,
+                     "kernel": "paged_decode_attention (prep + main kernel)",
+                     "bytes_per_launch": int(bytes_per_launch),
+                     "launch_ms": round(attn_avg_ms, 4)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=8.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per attention launch from an ncu capture, if current")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+    else:
+        our_arm(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,250 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: a paged KV cache and its decode step
+ * (host block ledger, cache-write kernel, paged decode attention) for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation, as the source pages state it:
+ *   - "vLLM의 핵심 원리 PagedAttention 파헤치기" (donmain.dev), section
+ *     "KV Cache를 블록으로 쪼개다": the KV cache is cut into fixed blocks of 16
+ *     tokens; each sequence owns a block table mapping its logical blocks to
+ *     physical blocks anywhere in a pool; blocks are taken one at a time as the
+ *     sequence grows; attention gathers a sequence's blocks through its table.
+ *   - "LLM 추론 배칭 전략 정리" (velog.io), section 5 ("누가 배치를 다시
+ *     짜는가", "한 스텝의 전체 흐름", "왜 이게 가능한가"): the ledger of who
+ *     owns which block lives on the CPU and reaches the GPU each step as a
+ *     block table; the pool is one region reserved up front, a physical block
+ *     is a block number inside it.
+ *   - "vLLM-and-PagedAttention-KR" (ghkdgus29.github.io), sections
+ *     "가장 기본적인 decoding" and "Parallel Sampling decoding": a new token's
+ *     K/V goes after the tokens already in its logical block; blocks shared by
+ *     several sequences carry a reference count; a finished request releases
+ *     its blocks.
+ *
+ * Conventions the pages leave open (the library's readings):
+ *   R1  K and V pools are separate arrays laid out
+ *       [num_blocks][num_kv_heads][block_size][head_dim], fp16 or bf16;
+ *       one (block, kv head) slab is contiguous.
+ *   R2  slot = physical_block * block_size + offset_in_block (int64);
+ *       a negative slot means "no token here" and is skipped.
+ *   R3  query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   R4  a decode step writes this step's K/V first, then attends;
+ *       context_lens include the token just written.
+ *   R6  q and out are [num_seqs][num_q_heads][head_dim] in the pool's dtype;
+ *       block_tables is int32 [num_seqs][max_blocks_per_seq] (row-major);
+ *       context_lens is int32 [num_seqs].
+ *   R7  context_len == 0 yields an all-zero output row.
+ *
+ * Ownership: the caller owns every device buffer (pools, q, out, tables,
+ * slot mapping, workspace, status word).  The library never allocates device
+ * memory.  A pkv_pool owns host memory only (free stack and refcounts).
+ *
+ * Errors: every call returns a pkv_status.  Kernel launches are asynchronous
+ * on the given stream (a cudaStream_t passed as void*, NULL = legacy default
+ * stream); their arguments are validated on the host before launch, and
+ * nothing is launched when validation fails.  Range errors inside device
+ * data (a slot or block id outside the pool, a context length longer than its
+ * table row) are recorded with atomicOr in the caller's device status word;
+ * the offending token is skipped or the offending sequence's output row is
+ * written as zeros, and no kernel ever traps.  kv_status_check() reads and
+ * clears that word.  A pkv_pool is not thread-safe.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,    /* bad pointer, size, shape or alignment          */
+    PKV_ERR_OUT_OF_BLOCKS = -2,  /* the free pool cannot cover the request         */
+    PKV_ERR_BAD_BLOCK = -3,      /* unknown id, double free, refcount underflow    */
+    PKV_ERR_CUDA = -4,           /* a CUDA runtime call failed                     */
+    PKV_ERR_DEVICE_BOUNDS = -5,  /* device status word reports a range error       */
+    PKV_ERR_DEVICE_TIMEOUT = -6, /* a kernel gave up waiting (status word bit)     */
+    PKV_ERR_SHARED_BLOCK = -7,   /* append would write into a block shared by others */
+    PKV_ERR_UNSUPPORTED = -8     /* shape the kernels do not implement             */
+} pkv_status;
+
+/* Bits of the device status word (int32, caller-allocated, zero before use). */
+#define PKV_DEV_BAD_SLOT  0x1   /* cache write: slot >= num_blocks * block_size     */
+#define PKV_DEV_BAD_BLOCK 0x2   /* attention: table entry outside [0, num_blocks)   */
+#define PKV_DEV_BAD_LEN   0x4   /* attention: context_len < 0 or longer than table  */
+#define PKV_DEV_TIMEOUT   0x8   /* a bounded wait inside a kernel ran out           */
+
+typedef struct pkv_pool pkv_pool;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int pkv_version(void);
+
+/* Static, human-readable name of a pkv_status value. */
+const char *pkv_status_string(int status);
+
+/* ------------------------------------------------------------------ sizing */
+
+/* Bytes of KV cache per token: 2 (K and V) x kv_heads x head_dim x elem_bytes
+ * per layer, times layers.  "vLLM-and-PagedAttention-KR", section
+ * "KV Cache Size 계산 방법" (2 x H x L x B = 819,200 bytes for OPT-13B);
+ * "kv-cache-by-model" (sotaaz.com), section 1.  Returns -1 on a negative
+ * argument. */
+int64_t kv_bytes_per_token(int32_t layers, int32_t kv_heads, int32_t head_dim,
+                           int32_t elem_bytes);
+
+/* Blocks a sequence of num_tokens tokens owns: ceil(num_tokens / block_size)
+ * ("PagedAttention 파헤치기", section "낭비가 4% 밑으로": 100 tokens -> 7
+ * blocks).  Returns -1 on a bad argument. */
+int64_t kv_blocks_for_tokens(int64_t num_tokens, int32_t block_size);
+
+/* Bytes of ONE of the K or V pools under layout R1. 0 on a bad argument. */
+size_t kv_pool_bytes(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                     int32_t head_dim, pkv_dtype dtype);
+
+/* ---------------------------------------------------- host block ledger (a1) */
+
+/* Create the ledger of a pool of num_blocks blocks.  initial_free_order, if not
+ * NULL, is a permutation of 0..num_blocks-1 giving the order in which free
+ * blocks are handed out (NULL = 0, 1, 2, ...).  Free blocks form a LIFO stack:
+ * the pages allow any free block ("KV Cache를 블록으로 쪼개다"); this policy
+ * makes ids reproducible.  A released block is the next one handed out.
+ * num_kv_heads, head_dim and dtype describe the device pools the caller pairs
+ * with this ledger; the kernels take the geometry from here.
+ * Errors: PKV_ERR_INVALID_ARG (non-positive sizes, unknown dtype, order not a
+ * permutation, out == NULL). */
+int kv_pool_create(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                   int32_t head_dim, pkv_dtype dtype, const int32_t *initial_free_order,
+                   pkv_pool **out);
+
+/* Free the ledger (host memory only).  NULL is accepted. */
+int kv_pool_destroy(pkv_pool *pool);
+
+/* Geometry of a pool; any output pointer may be NULL. */
+int kv_pool_info(const pkv_pool *pool, int32_t *num_blocks, int32_t *block_size,
+                 int32_t *num_kv_heads, int32_t *head_dim, int32_t *dtype);
+
+/* Take n free blocks (all or nothing), each with refcount 1, into out_ids[n].
+ * Errors: PKV_ERR_OUT_OF_BLOCKS (nothing taken), PKV_ERR_INVALID_ARG. */
+int kv_block_alloc(pkv_pool *pool, int32_t n, int32_t *out_ids);
+
+/* Add one reference to each listed block (a sequence starts sharing it:
+ * "Parallel Sampling decoding").  All or nothing.
+ * Errors: PKV_ERR_BAD_BLOCK if any id is not currently allocated. */
+int kv_block_ref(pkv_pool *pool, int32_t n, const int32_t *ids);
+
+/* Drop one reference from each listed block, in order; a block whose count
+ * reaches 0 returns to the top of the free stack ("가장 기본적인 decoding",
+ * step 5).  An id may appear several times.  All or nothing.
+ * Errors: PKV_ERR_BAD_BLOCK if any id would be released more often than it is
+ * referenced (double free, unknown id); nothing changes then. */
+int kv_block_free(pkv_pool *pool, int32_t n, const int32_t *ids);
+
+/* Current reference count of one block (0 = free). */
+int kv_block_refcount(const pkv_pool *pool, int32_t id, int32_t *out);
+
+/* Number of free blocks. */
+int kv_pool_num_free(const pkv_pool *pool, int32_t *out);
+
+/* ------------------------------------- on-demand allocation + slots (a1, a2) */
+
+/* Grow num_seqs sequences: sequence s holds seq_lens[s] tokens and gains
+ * num_new[s] more.  The token at position n needs logical block n / block_size;
+ * when n is a multiple of block_size that block does not exist yet and one
+ * free block is taken into block_tables[s][n / block_size] ("KV Cache를 블록으로
+ * 쪼개다": first token -> first block, token 17 -> a second block).  For every
+ * new token, in sequence order, slot_mapping receives
+ * block_tables[s][n / block_size] * block_size + n % block_size  (R2).
+ *   seq_lens, num_new   host int32 [num_seqs]
+ *   block_tables        host int32 [num_seqs][max_blocks_per_seq], updated
+ *   slot_mapping        host int64 [sum(num_new)], written
+ * All or nothing: on any error nothing changes.
+ * Errors: PKV_ERR_INVALID_ARG (negative length, row too short),
+ * PKV_ERR_OUT_OF_BLOCKS, PKV_ERR_BAD_BLOCK (a partly filled tail block that is
+ * not allocated), PKV_ERR_SHARED_BLOCK (a partly filled tail block with
+ * refcount > 1: the write needs a copy first). */
+int kv_append_slots(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_lens,
+                    const int32_t *num_new, int32_t *block_tables,
+                    int32_t max_blocks_per_seq, int64_t *slot_mapping);
+
+/* ---------------------------------------------------------- cache write (a3) */
+
+/* Store num_tokens new tokens' K and V rows into their slots ("가장 기본적인
+ * decoding", steps 3-4: the new token's KV goes after the tokens already in its
+ * logical block).  Row t of k_new ([num_tokens][num_kv_heads][head_dim],
+ * device) is copied bit for bit to k_pool[slot / bs][h][slot % bs][:] for every
+ * kv head h (layout R1), and the same for v.  slot_mapping is device int64
+ * [num_tokens]; negative slots are skipped; a slot >= num_blocks * block_size is
+ * skipped and sets PKV_DEV_BAD_SLOT in *d_status.  All device pointers must be
+ * 16-byte aligned (head_dim * elem_size must be a multiple of 16).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA (launch failure). */
+int kv_cache_write(const pkv_pool *pool, const void *k_new, const void *v_new,
+                   const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
+                   void *v_pool, int32_t *d_status, void *stream);
+
+/* ------------------------------------------- paged decode attention (a4, a5) */
+
+/* Workspace bytes paged_decode_attention needs for these sizes (split-K
+ * partials, work list, merge counters).  0 on a bad argument. */
+size_t paged_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t max_blocks_per_seq);
+
+/* Single-query attention for every sequence and query head, gathering each
+ * sequence's blocks through its block table ("KV Cache를 블록으로 쪼개다": the
+ * PagedAttention kernel collects the blocks by following the table, so
+ * attention works although KV is not contiguous):
+ *   x_j = scale * <q[s][h], K_s[j][h / G]>,  j < context_lens[s]
+ *   out[s][h] = sum_j softmax(x)_j * V_s[j][h / G],   G = num_q_heads / num_kv_heads
+ * where K_s[j] lives in block block_tables[s][j / bs] at row j % bs (R1).
+ * Work is split along the context into partitions whose (o, max, sum) pieces are
+ * merged with the log-sum-exp rule; accumulation is fp32; out is rounded to the
+ * pool dtype.  Requirements: pool block_size 16; head_dim 64 or 128;
+ * num_q_heads a multiple of num_kv_heads with G <= 16; q/out/pools 16-byte
+ * aligned; workspace of at least paged_decode_workspace_bytes(...) bytes,
+ * 256-byte aligned, contents need not be initialised.  d_status: see the bits.
+ * Sequences with context_len == 0 get zero rows (R7); a sequence with a bad
+ * length or table entry gets a zero row and a status bit.  The result is
+ * identical whatever the physical placement of the blocks.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA. */
+int paged_decode_attention(const pkv_pool *pool, void *out, const void *q,
+                           const void *k_pool, const void *v_pool,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, float scale, void *workspace,
+                           size_t workspace_bytes, int32_t *d_status, void *stream);
+
+/* Same operation with an explicit partition size: each (sequence, kv head) is
+ * cut into partitions of blocks_per_split blocks (>= 1) that run as separate
+ * work items and are merged by log-sum-exp.  paged_decode_attention uses a
+ * default size; results agree within rounding for any size. */
+size_t paged_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t max_blocks_per_seq,
+                                          int32_t blocks_per_split);
+int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
+                                 const void *k_pool, const void *v_pool,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t num_seqs,
+                                 int32_t num_q_heads, float scale, int32_t blocks_per_split,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t *d_status, void *stream);
+
+/* Default partition size (blocks) paged_decode_attention uses. */
+int32_t paged_decode_default_split(void);
+
+/* ------------------------------------------------------------ status word */
+
+/* Wait for the stream, read the device status word into *out_word (may be
+ * NULL), clear it, and map it to a status: PKV_OK, PKV_ERR_DEVICE_BOUNDS,
+ * PKV_ERR_DEVICE_TIMEOUT, or PKV_ERR_CUDA when the stream itself failed. */
+int kv_status_check(int32_t *d_status, void *stream, int32_t *out_word);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,234 @@
+"""Paged KV cache and PagedAttention decode step for NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libpagedkv.so`` (include/pagedkv.h).
+It only marshals arguments: the block ledger runs in the library's C++ code and
+every device step runs in its CUDA kernels.  PyTorch supplies device memory and
+streams.  If the library is not built, every call raises.
+
+Typical decode step (the flow of "LLM 추론 배칭 전략 정리", section 5):
+
+    pool = KVPool(num_blocks, num_kv_heads=8, head_dim=128, dtype="bf16", device="cuda")
+    slots = pool.append_slots(seq_lens, num_new, tables)      # host: on-demand blocks
+    d_tables.copy_(torch.from_numpy(tables)); d_slots.copy_(...)  # H2D hand-off
+    cache_write(pool, k_new, v_new, d_slots, status)          # device: write new K/V
+    paged_decode_attention(pool, q, d_tables, d_lens, scale, ws, status, out=out)
+    pool.free(finished_blocks)                                # host: release
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _native
+from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV_BF16, PKV_F16,
+                      PagedKVError, check, lib)
+
+__all__ = ["KVPool", "PagedKVError", "cache_write", "paged_decode_attention",
+           "decode_workspace_bytes", "status_check", "kv_bytes_per_token",
+           "kv_blocks_for_tokens", "kv_pool_bytes", "default_split", "lib",
+           "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN", "DEV_TIMEOUT"]
+
+_DTYPES = {"f16": PKV_F16, "fp16": PKV_F16, "float16": PKV_F16,
+           "bf16": PKV_BF16, "bfloat16": PKV_BF16}
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _t_ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _torch_dtype(code: int):
+    import torch
+    return torch.bfloat16 if code == PKV_BF16 else torch.float16
+
+
+# ------------------------------------------------------------------ sizing
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    return lib().kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes)
+
+
+def kv_blocks_for_tokens(num_tokens: int, block_size: int = 16) -> int:
+    return lib().kv_blocks_for_tokens(num_tokens, block_size)
+
+
+def kv_pool_bytes(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int,
+                  dtype: str) -> int:
+    return lib().kv_pool_bytes(num_blocks, block_size, num_kv_heads, head_dim, _DTYPES[dtype])
+
+
+def default_split() -> int:
+    return lib().paged_decode_default_split()
+
+
+# ------------------------------------------------------------------ ledger
+class KVPool:
+    """A block pool: the library's host ledger plus (optionally) the device K/V pools.
+
+    ``device=None`` creates the ledger only.  Otherwise ``k_pool``/``v_pool`` are
+    torch tensors [num_blocks][num_kv_heads][block_size][head_dim] on that device
+    (contents uninitialised, as a pool reserved up front).
+    """
+
+    def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, dtype: str = "bf16",
+                 block_size: int = 16, free_order=None, device=None):
+        self.num_blocks, self.num_kv_heads, self.head_dim = num_blocks, num_kv_heads, head_dim
+        self.block_size = block_size
+        self.dtype_code = _DTYPES[dtype]
+        self.dtype = "bf16" if self.dtype_code == PKV_BF16 else "f16"
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(free_order, dtype=np.int32)
+            if order.shape != (num_blocks,):
+                raise ValueError("free_order must have num_blocks entries")
+        h = ctypes.c_void_p()
+        check(lib().kv_pool_create(num_blocks, block_size, num_kv_heads, head_dim,
+                                   self.dtype_code, _np_ptr(order) if order is not None else None,
+                                   ctypes.byref(h)), "kv_pool_create")
+        self._h = h
+        self.k_pool = self.v_pool = None
+        if device is not None:
+            import torch
+            shape = (num_blocks, num_kv_heads, block_size, head_dim)
+            self.k_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
+            self.v_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("pool is closed")
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            lib().kv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.empty(n, dtype=np.int32)
+        check(lib().kv_block_alloc(self.handle, n, _np_ptr(out)), "kv_block_alloc")
+        return out
+
+    def ref(self, ids) -> None:
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        check(lib().kv_block_ref(self.handle, len(ids), _np_ptr(ids)), "kv_block_ref")
+
+    def free(self, ids) -> None:
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        check(lib().kv_block_free(self.handle, len(ids), _np_ptr(ids)), "kv_block_free")
+
+    def refcount(self, block_id: int) -> int:
+        out = ctypes.c_int32()
+        check(lib().kv_block_refcount(self.handle, block_id, ctypes.byref(out)), "kv_block_refcount")
+        return out.value
+
+    def num_free(self) -> int:
+        out = ctypes.c_int32()
+        check(lib().kv_pool_num_free(self.handle, ctypes.byref(out)), "kv_pool_num_free")
+        return out.value
+
+    def append_slots(self, seq_lens, num_new, block_tables: np.ndarray) -> np.ndarray:
+        """Grow sequences by ``num_new`` tokens; updates ``block_tables`` (int32
+        [S][max_blocks], C-contiguous numpy, in place) and returns the int64 slots."""
+        lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        new = np.ascontiguousarray(num_new, dtype=np.int32)
+        if not (isinstance(block_tables, np.ndarray) and block_tables.dtype == np.int32
+                and block_tables.flags.c_contiguous and block_tables.ndim == 2):
+            raise TypeError("block_tables must be a C-contiguous int32 numpy array [S][max_blocks]")
+        if block_tables.shape[0] != len(lens) or len(new) != len(lens):
+            raise ValueError("length mismatch")
+        slots = np.empty(int(new.sum()), dtype=np.int64)
+        check(lib().kv_append_slots(self.handle, len(lens), _np_ptr(lens), _np_ptr(new),
+                                    _np_ptr(block_tables), block_tables.shape[1],
+                                    _np_ptr(slots)), "kv_append_slots")
+        return slots
+
+
+# ------------------------------------------------------------------ device ops
+def cache_write(pool: KVPool, k_new, v_new, slot_mapping, status, k_pool=None, v_pool=None,
+                stream=None) -> None:
+    """Launch the cache-write kernel: rows of ``k_new``/``v_new`` [T][Hkv][D] (device)
+    go to their slots (int64 device tensor [T]) in the pools."""
+    k_pool = pool.k_pool if k_pool is None else k_pool
+    v_pool = pool.v_pool if v_pool is None else v_pool
+    T = int(slot_mapping.shape[0])
+    if k_new.shape[0] != T or v_new.shape[0] != T:
+        raise ValueError("k_new/v_new rows must match slot_mapping")
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("inputs must be contiguous")
+    check(lib().kv_cache_write(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping), T,
+                               _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status), _stream(stream)),
+          "kv_cache_write")
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           max_blocks_per_seq: int, blocks_per_split: int | None = None) -> int:
+    if blocks_per_split is None:
+        return lib().paged_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                  max_blocks_per_seq)
+    return lib().paged_decode_workspace_bytes_split(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                    max_blocks_per_seq, blocks_per_split)
+
+
+def paged_decode_attention(pool: KVPool, q, block_tables, context_lens, scale: float, workspace,
+                           status, out=None, k_pool=None, v_pool=None,
+                           blocks_per_split: int | None = None, stream=None):
+    """Launch paged decode attention.  ``q`` [S][Hq][D] device tensor in the pool dtype;
+    ``block_tables`` int32 device [S][max_blocks]; ``context_lens`` int32 device [S];
+    ``workspace`` a uint8 device tensor of ``decode_workspace_bytes(...)`` bytes.
+    Returns ``out`` [S][Hq][D]."""
+    import torch
+    k_pool = pool.k_pool if k_pool is None else k_pool
+    v_pool = pool.v_pool if v_pool is None else v_pool
+    S, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    for t, name in ((q, "q"), (out, "out"), (block_tables, "block_tables"),
+                    (context_lens, "context_lens")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    maxb = int(block_tables.shape[1])
+    nbytes = workspace.numel() * workspace.element_size()
+    if blocks_per_split is None:
+        rc = lib().paged_decode_attention(pool.handle, _t_ptr(out), _t_ptr(q), _t_ptr(k_pool),
+                                          _t_ptr(v_pool), _t_ptr(block_tables), maxb,
+                                          _t_ptr(context_lens), S, hq, float(scale),
+                                          _t_ptr(workspace), nbytes, _t_ptr(status),
+                                          _stream(stream))
+    else:
+        rc = lib().paged_decode_attention_split(pool.handle, _t_ptr(out), _t_ptr(q),
+                                                _t_ptr(k_pool), _t_ptr(v_pool),
+                                                _t_ptr(block_tables), maxb, _t_ptr(context_lens),
+                                                S, hq, float(scale), int(blocks_per_split),
+                                                _t_ptr(workspace), nbytes, _t_ptr(status),
+                                                _stream(stream))
+    check(rc, "paged_decode_attention")
+    return out
+
+
+def status_check(status, stream=None):
+    """Synchronise the stream, read and clear the device status word.
+    Returns (pkv_status code, raw word)."""
+    word = ctypes.c_int32()
+    rc = lib().kv_status_check(_t_ptr(status), _stream(stream), ctypes.byref(word))
+    return rc, word.value

@@ -1,0 +1,89 @@
+// Cache-write kernel: store this step's K/V rows into their slots.
+//
+// "vLLM-and-PagedAttention-KR", section "가장 기본적인 decoding", steps 3-4:
+// a generated token's KV goes after the tokens already in its logical block.
+// Layout R1 ([block][kv_head][slot_in_block][head_dim]) and slot reading R2
+// (slot = block * block_size + offset, negative = skip).
+//
+// HBM-bound byte copy: one thread moves one 16-byte chunk of one row of K and
+// the same chunk of V, so a warp covers two 256-byte rows (head_dim 128) with
+// fully coalesced 128-bit loads and stores.  Bit-exact by construction.
+#include <cuda_runtime.h>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+cache_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                   const int64_t *__restrict__ slot_mapping, int64_t num_chunks,
+                   int32_t chunks_per_token, int32_t chunks_per_row, int32_t num_kv_heads,
+                   int32_t block_size, int64_t num_slots, uint4 *__restrict__ k_pool,
+                   uint4 *__restrict__ v_pool, int32_t *__restrict__ status)
+{
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < num_chunks;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        int64_t t = e / chunks_per_token;
+        int32_t within = (int32_t)(e - t * chunks_per_token);
+        int32_t h = within / chunks_per_row;
+        int32_t c = within - h * chunks_per_row;
+        int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (within == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        int64_t block = slot / block_size;
+        int64_t offset = slot - block * block_size;
+        int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * chunks_per_row + c;
+        uint4 kv = __ldcs(k_new + e);   // streamed once
+        uint4 vv = __ldcs(v_new + e);
+        k_pool[dst] = kv;
+        v_pool[dst] = vv;
+    }
+}
+
+}  // namespace
+
+extern "C" int kv_cache_write(const pkv_pool *pool, const void *k_new, const void *v_new,
+                              const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
+                              void *v_pool, int32_t *d_status, void *stream)
+{
+    pkv::PoolGeometry g;
+    if (!pkv::pool_geometry(pool, &g) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool || !d_status)
+        return PKV_ERR_INVALID_ARG;
+    const int row_bytes = g.head_dim * 2;
+    if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) || !pkv::aligned16(k_pool) ||
+        !pkv::aligned16(v_pool) || ((uintptr_t)slot_mapping & 7u) || ((uintptr_t)d_status & 3u))
+        return PKV_ERR_INVALID_ARG;
+    const int32_t chunks_per_row = row_bytes / 16;
+    const int32_t chunks_per_token = chunks_per_row * g.num_kv_heads;
+    const int64_t num_chunks = (int64_t)num_tokens * chunks_per_token;
+    const int threads = 256;
+    int64_t blocks = (num_chunks + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;   // grid-stride beyond a few waves
+    cache_write_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        (const uint4 *)k_new, (const uint4 *)v_new, slot_mapping, num_chunks, chunks_per_token,
+        chunks_per_row, g.num_kv_heads, g.block_size, (int64_t)g.num_blocks * g.block_size,
+        (uint4 *)k_pool, (uint4 *)v_pool, d_status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int kv_status_check(int32_t *d_status, void *stream, int32_t *out_word)
+{
+    if (!d_status) return PKV_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t word = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemcpy(&word, d_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (word != 0 && cudaMemset(d_status, 0, sizeof(word)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (out_word) *out_word = word;
+    if (word & PKV_DEV_TIMEOUT) return PKV_ERR_DEVICE_TIMEOUT;
+    if (word) return PKV_ERR_DEVICE_BOUNDS;
+    return PKV_OK;
+}

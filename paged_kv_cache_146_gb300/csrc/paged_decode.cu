@@ -1,0 +1,885 @@
+// PagedAttention decode for sm_103a.
+//
+// The operation ("vLLM의 핵심 원리 PagedAttention 파헤치기", section "KV Cache를
+// 블록으로 쪼개다"): for each sequence, follow its block table to the 16-token
+// blocks that hold its K and V anywhere in the pool, and compute single-query
+// softmax attention for every query head.  Decode attention is bound by the
+// bytes of KV it reads, which grow with the batch and are never reused
+// ("LLM 추론 배칭 전략 정리", section 2.3), so the kernel is built to keep HBM
+// busy:
+//
+//   * Work items are (sequence, kv head, partition of up to P blocks); a
+//     persistent grid walks them in a fixed stride.  A prep kernel turns the
+//     device-side context lengths into the item list (no host round trip).
+//   * Per CTA: one producer warp issues 2-D TMA copies (cp.async.bulk.tensor,
+//     128-byte swizzle) of each block's K and V slab for the item's kv head
+//     into a ring of NST shared-memory stages, completed through mbarriers;
+//     it streams across item boundaries.  Four consumer warps take the blocks
+//     of an item round-robin.
+//   * Consumer, per 16-token block: S = Q K^T on tensor cores (mma.sync
+//     m16n8k16, the G query heads of the GQA group as rows, 16 tokens as
+//     columns, head_dim as the reduction), fp32 online softmax in registers,
+//     then O += P V on tensor cores with P split into a bf16/fp16 high part
+//     and a low part (rows 0-7 carry the high part, rows 8-15 the low part when
+//     G <= 8), which keeps the weights accurate to ~2^-17.
+//   * The four warps' (o, max, sum) are merged in shared memory; items of a
+//     multi-partition sequence write their pieces to the workspace and the last
+//     CTA to finish a (sequence, kv head) merges them by log-sum-exp in
+//     partition order -- deterministic, and independent of where the blocks
+//     physically sit.
+//   * Every wait is bounded (1 s); on expiry the kernel flags PKV_DEV_TIMEOUT,
+//     stops issuing copies, drains the ones in flight and finishes without
+//     trapping.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace decode {
+
+constexpr int kBlock = 16;               // tokens per KV block
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kDefaultSplit = 32;        // blocks per partition (512 tokens)
+constexpr int kBoxCols = 64;             // one TMA box: 64 elements (128 B) x 16 rows
+constexpr int kBoxBytes = kBlock * 128;  // 2 KiB
+constexpr unsigned long long kTimeoutNs = 1000000000ull;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct Params {
+    void *out;
+    const void *q;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
+    int32_t blocks_per_split, num_blocks;
+    float scale_log2;           // softmax scale * log2(e): scores live in the exp2 domain
+    int32_t *header;            // [0] = number of (sequence, partition) pairs
+    int2 *seq_info;             // [S]: first pair index, number of partitions
+    int2 *items;                // [S * ceil(maxb / P)]: (sequence, partition)
+    int32_t *counters;          // [S * Hkv]: finished partitions per (sequence, kv head)
+    float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned
+    float *part_o;              // [pairs * Hkv * G * D]: unnormalised partition output
+    int32_t *status;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of the given parity.  Returns false when the CTA
+// has been told to stop or when the wait ran out (then it raises the stop flag
+// and the status bit itself).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (*abort_flag) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            atomicOr(status, PKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void named_barrier_consumers()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+template <bool BF16>
+struct Elem;
+
+template <>
+struct Elem<true> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi)
+    {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    static __device__ __forceinline__ float2 unpack(uint32_t u)
+    {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u));
+    }
+    static __device__ __forceinline__ T from_float(float x) { return __float2bfloat16_rn(x); }
+    static __device__ __forceinline__ void mma(float c[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1)
+    {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+
+template <>
+struct Elem<false> {
+    using T = __half;
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi)
+    {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    static __device__ __forceinline__ float2 unpack(uint32_t u)
+    {
+        return __half22float2(*reinterpret_cast<__half2 *>(&u));
+    }
+    static __device__ __forceinline__ T from_float(float x) { return __float2half_rn(x); }
+    static __device__ __forceinline__ void mma(float c[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1)
+    {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+
+// Shared-memory footprint of one kernel variant (without the 1 KiB alignment slack).
+template <int D, int GROWS, int NST>
+struct Smem {
+    static constexpr int kStageBytes = 2 * (D / kBoxCols) * kBoxBytes;  // K slab + V slab
+    static constexpr int kStagesBytes = NST * kStageBytes;
+    static constexpr int kBarBytes = 2 * NST * 8;
+    static constexpr int kScratchBytes =
+        kConsumerWarps * GROWS * (D + 2) * 4 + NST * 4 + kConsumerWarps * 4 + 16;
+    static constexpr int kTotal = 1024 + kStagesBytes + kBarBytes + kScratchBytes;
+};
+
+// ----------------------------------------------------------------- prep kernel
+// One CTA: partitions per sequence, their prefix sum, the item list, the merge
+// counters, and zero rows for empty or invalid sequences.
+__global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t head_dim)
+{
+    __shared__ int warp_tot[32];
+    __shared__ int carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
+    for (int base = 0; base < p.num_seqs; base += 1024) {
+        const int s = base + tid;
+        int nsplit = 0;
+        bool zero_row = false;
+        if (s < p.num_seqs) {
+            const int L = p.context_lens[s];
+            if (L < 0 || (int64_t)L > max_tokens) {
+                atomicOr(p.status, PKV_DEV_BAD_LEN);
+                zero_row = true;
+            } else if (L == 0) {
+                zero_row = true;
+            } else {
+                const int nb = (L + kBlock - 1) / kBlock;
+                nsplit = (nb + p.blocks_per_split - 1) / p.blocks_per_split;
+            }
+        }
+        int x = nsplit;   // inclusive scan over the CTA
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int t = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - nsplit;
+        if (s < p.num_seqs) {
+            p.seq_info[s] = make_int2(excl, nsplit);
+            for (int k = 0; k < nsplit; ++k) p.items[excl + k] = make_int2(s, k);
+            for (int g = 0; g < p.num_kv_heads; ++g) p.counters[(int64_t)s * p.num_kv_heads + g] = 0;
+            if (zero_row) {
+                uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(p.out) +
+                                                     (size_t)s * p.num_q_heads * head_dim * 2);
+                const int n16 = p.num_q_heads * head_dim * 2 / 16;
+                for (int i = 0; i < n16; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) carry += warp_tot[31];
+        __syncthreads();
+    }
+    if (tid == 0) p.header[0] = carry;
+}
+
+// ----------------------------------------------------------------- main kernel
+template <int D, bool BF16, int GROWS, int NST, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const Params p)
+{
+    using E = Elem<BF16>;
+    using T = typename E::T;
+    using SM = Smem<D, GROWS, NST>;
+    constexpr int kBoxes = D / kBoxCols;          // TMA boxes per slab
+    constexpr int kSlabBytes = kBoxes * kBoxBytes;
+    constexpr int KSTEPS = D / 16;                // QK reduction steps
+    constexpr int NTILES = D / 8;                 // PV output tiles of 8 dims
+    constexpr int OSTRIDE = D + 2;                // padded scratch row
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stages = base;
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(base + SM::kStagesBytes);
+    uint64_t *empty_bar = full_bar + NST;
+    // per consumer warp, per row: D output sums, then the row's max and sum
+    float *sm_o = reinterpret_cast<float *>(empty_bar + NST);          // [4][GROWS][D + 2]
+    int *stage_bad = reinterpret_cast<int *>(sm_o + kConsumerWarps * GROWS * OSTRIDE);
+    int *sm_bad = stage_bad + NST;
+    volatile int *sm_abort = sm_bad + kConsumerWarps;
+    volatile int *sm_last = sm_abort + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(smem_addr(&full_bar[i]), 1);
+            mbar_init(smem_addr(&empty_bar[i]), 1);
+        }
+        *sm_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int Hkv = p.num_kv_heads, G = p.group, P = p.blocks_per_split;
+    const int total_items = p.header[0] * Hkv;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        uint32_t cnt = 0, issued = 0, issued_par = 0;
+        for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+            const int sj = item / Hkv, g = item - sj * Hkv;
+            const int2 it = p.items[sj];
+            const int L = __ldg(p.context_lens + it.x);
+            const int nb = (L + kBlock - 1) / kBlock;
+            const int b0 = it.y * P, b1 = min(b0 + P, nb);
+            const int32_t *row = p.block_tables + (int64_t)it.x * p.max_blocks_per_seq;
+            for (int cb = b0; cb < b1; cb += 32) {
+                const int n = min(32, b1 - cb);
+                const int my_id = lane < n ? __ldg(row + cb + lane) : 0;
+                for (int j = 0; j < n; ++j) {
+                    const int pid = __shfl_sync(kFull, my_id, j);
+                    if (lane == 0) {
+                        const int slot = (int)(cnt % NST);
+                        const uint32_t par = (cnt / NST) & 1u;
+                        const uint32_t fb = smem_addr(&full_bar[slot]);
+                        if (mbar_wait(smem_addr(&empty_bar[slot]), par ^ 1u, sm_abort, p.status)) {
+                            if (pid >= 0 && pid < p.num_blocks) {
+                                stage_bad[slot] = 0;
+                                mbar_arrive_expect_tx(fb, 2 * kSlabBytes);
+                                const uint32_t dk = smem_addr(stages + slot * SM::kStageBytes);
+                                const uint32_t dv = dk + kSlabBytes;
+                                const int y = (pid * Hkv + g) * kBlock;
+#pragma unroll
+                                for (int bx = 0; bx < kBoxes; ++bx) {
+                                    tma_load_2d(dk + bx * kBoxBytes, &tmK, bx * kBoxCols, y, fb);
+                                    tma_load_2d(dv + bx * kBoxBytes, &tmV, bx * kBoxCols, y, fb);
+                                }
+                                issued |= 1u << slot;
+                                issued_par = (issued_par & ~(1u << slot)) | (par << slot);
+                            } else {
+                                stage_bad[slot] = 1;
+                                atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                                mbar_arrive(fb);
+                            }
+                        }
+                    }
+                    ++cnt;
+                }
+            }
+        }
+        // drain: every copy this warp issued must land before the CTA exits
+        if (lane == 0) {
+            for (int slot = 0; slot < NST; ++slot) {
+                if (!(issued & (1u << slot))) continue;
+                const uint32_t fb = smem_addr(&full_bar[slot]);
+                const uint32_t par = (issued_par >> slot) & 1u;
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(fb, par)) {
+                    if (globaltimer() - t0 > kTimeoutNs) {
+                        atomicOr(p.status, PKV_DEV_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int hrow = lane >> 2, q4 = lane & 3;
+    const int ctid = threadIdx.x;          // 0..127
+    uint32_t cnt_base = 0;
+    // ldmatrix lane offsets inside a slab (128-byte swizzle: chunk ^= row % 8)
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int k_tok = ((mi >> 1) << 3) + r8, k_chunk = mi & 1;   // K: tokens x (chunk, chunk+1)
+    const int v_tok = ((mi & 1) << 3) + r8, v_chunk = mi >> 1;   // V^T pairs of 8-dim tiles
+
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const int sj = item / Hkv, g = item - sj * Hkv;
+        const int2 it = p.items[sj];
+        const int s = it.x;
+        const int L = __ldg(p.context_lens + s);
+        const int nb = (L + kBlock - 1) / kBlock;
+        const int b0 = it.y * P, b1 = min(b0 + P, nb);
+
+        // Q rows of the group as the A operand (rows >= G are zero)
+        uint32_t qa[KSTEPS][4];
+        {
+            const uint32_t *qg = reinterpret_cast<const uint32_t *>(
+                static_cast<const T *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D);
+            const bool r0 = hrow < G, r1 = (GROWS == 16) && (hrow + 8 < G);
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int c = (kk * 16 + 2 * q4) >> 1;    // in 32-bit words
+                qa[kk][0] = r0 ? __ldg(qg + hrow * (D / 2) + c) : 0u;
+                qa[kk][2] = r0 ? __ldg(qg + hrow * (D / 2) + c + 4) : 0u;
+                qa[kk][1] = r1 ? __ldg(qg + (hrow + 8) * (D / 2) + c) : 0u;
+                qa[kk][3] = r1 ? __ldg(qg + (hrow + 8) * (D / 2) + c + 4) : 0u;
+            }
+        }
+        float o[NTILES][4];
+#pragma unroll
+        for (int j = 0; j < NTILES; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        int bad = 0;
+
+        for (int b = b0 + warp; b < b1; b += kConsumerWarps) {
+            const uint32_t c = cnt_base + (uint32_t)(b - b0);
+            const int slot = (int)(c % NST);
+            const uint32_t par = (c / NST) & 1u;
+            // warp-uniform: the ldmatrix/mma below need the whole warp
+            const bool landed = mbar_wait(smem_addr(&full_bar[slot]), par, sm_abort, p.status);
+            if (!__all_sync(kFull, landed)) continue;
+            bad |= stage_bad[slot];
+            const int valid = min(kBlock, L - b * kBlock);
+            const uint32_t kb = smem_addr(stages + slot * SM::kStageBytes);
+            const uint32_t vb = kb + kSlabBytes;
+
+            // ---- S = Q K^T : two 8-token tiles
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int chunk = 2 * kk + k_chunk;
+                const uint32_t addr = kb + (chunk >> 3) * kBoxBytes + k_tok * 128 +
+                                      (((chunk & 7) ^ r8) << 4);
+                uint32_t kr[4];
+                ldsm_x4(kr, addr);
+                E::mma(s0, qa[kk], kr[0], kr[1]);
+                E::mma(s1, qa[kk], kr[2], kr[3]);
+            }
+            // ---- online softmax (row hrow: s0[0..1], s1[0..1]; row hrow+8: [2..3])
+            const int t0 = 2 * q4;
+            float x0 = s0[0] * p.scale_log2, x1 = s0[1] * p.scale_log2;
+            float x2 = s1[0] * p.scale_log2, x3 = s1[1] * p.scale_log2;
+            float y0 = s0[2] * p.scale_log2, y1 = s0[3] * p.scale_log2;
+            float y2 = s1[2] * p.scale_log2, y3 = s1[3] * p.scale_log2;
+            if (valid < kBlock) {
+                if (t0 >= valid) x0 = y0 = -INFINITY;
+                if (t0 + 1 >= valid) x1 = y1 = -INFINITY;
+                if (t0 + 8 >= valid) x2 = y2 = -INFINITY;
+                if (t0 + 9 >= valid) x3 = y3 = -INFINITY;
+            }
+            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+            const float mn0 = fmaxf(m0, mx);
+            const float a0 = exp2f(m0 - mn0);
+            const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn0);
+            const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn0);
+            l0 = l0 * a0 + ((p0 + p1) + (p2 + p3));
+            m0 = mn0;
+            float a1 = 1.f;
+            uint32_t pa[4], pb[4];
+            if constexpr (GROWS == 8) {
+                if (__any_sync(kFull, a0 != 1.f)) {
+#pragma unroll
+                    for (int j = 0; j < NTILES; ++j) {
+                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a0; o[j][3] *= a0;
+                    }
+                }
+                // rows 0-7: high part of P, rows 8-15: low part
+                pa[0] = E::pack(p0, p1);
+                pa[2] = E::pack(p2, p3);
+                const float2 h01 = E::unpack(pa[0]), h23 = E::unpack(pa[2]);
+                pa[1] = E::pack(p0 - h01.x, p1 - h01.y);
+                pa[3] = E::pack(p2 - h23.x, p3 - h23.y);
+            } else {
+                float my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+                my = fmaxf(my, __shfl_xor_sync(kFull, my, 1));
+                my = fmaxf(my, __shfl_xor_sync(kFull, my, 2));
+                const float mn1 = fmaxf(m1, my);
+                a1 = exp2f(m1 - mn1);
+                const float e0 = exp2f(y0 - mn1), e1 = exp2f(y1 - mn1);
+                const float e2 = exp2f(y2 - mn1), e3 = exp2f(y3 - mn1);
+                l1 = l1 * a1 + ((e0 + e1) + (e2 + e3));
+                m1 = mn1;
+                if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                    for (int j = 0; j < NTILES; ++j) {
+                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
+                    }
+                }
+                pa[0] = E::pack(p0, p1);
+                pa[1] = E::pack(e0, e1);
+                pa[2] = E::pack(p2, p3);
+                pa[3] = E::pack(e2, e3);
+                const float2 h0 = E::unpack(pa[0]), h1 = E::unpack(pa[1]);
+                const float2 h2 = E::unpack(pa[2]), h3 = E::unpack(pa[3]);
+                pb[0] = E::pack(p0 - h0.x, p1 - h0.y);
+                pb[1] = E::pack(e0 - h1.x, e1 - h1.y);
+                pb[2] = E::pack(p2 - h2.x, p3 - h2.y);
+                pb[3] = E::pack(e2 - h3.x, e3 - h3.y);
+            }
+            // ---- O += P V
+            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;   // zero V rows past the context
+            if (valid < kBlock) {
+                mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+                mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int jj = 0; jj < NTILES / 2; ++jj) {
+                const int chunk = 2 * jj + v_chunk;
+                const uint32_t addr = vb + (chunk >> 3) * kBoxBytes + v_tok * 128 +
+                                      (((chunk & 7) ^ r8) << 4);
+                uint32_t vr[4];
+                ldsm_x4_trans(vr, addr);
+                vr[0] &= mlo; vr[2] &= mlo;
+                vr[1] &= mhi; vr[3] &= mhi;
+                E::mma(o[2 * jj], pa, vr[0], vr[1]);
+                E::mma(o[2 * jj + 1], pa, vr[2], vr[3]);
+                if constexpr (GROWS == 16) {
+                    E::mma(o[2 * jj], pb, vr[0], vr[1]);
+                    E::mma(o[2 * jj + 1], pb, vr[2], vr[3]);
+                }
+            }
+            (void)a1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
+        }
+        cnt_base += (uint32_t)(b1 - b0);
+
+        // ---- per-warp state into shared memory
+        l0 += __shfl_xor_sync(kFull, l0, 1);
+        l0 += __shfl_xor_sync(kFull, l0, 2);
+        if constexpr (GROWS == 16) {
+            l1 += __shfl_xor_sync(kFull, l1, 1);
+            l1 += __shfl_xor_sync(kFull, l1, 2);
+        }
+        float *wo = sm_o + warp * GROWS * OSTRIDE;
+        if (q4 == 0) {
+            wo[hrow * OSTRIDE + D] = m0;
+            wo[hrow * OSTRIDE + D + 1] = l0;
+            if constexpr (GROWS == 16) {
+                wo[(hrow + 8) * OSTRIDE + D] = m1;
+                wo[(hrow + 8) * OSTRIDE + D + 1] = l1;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NTILES; ++j) {
+            const int d0 = 8 * j + 2 * q4;
+            if constexpr (GROWS == 8) {
+                wo[hrow * OSTRIDE + d0] = o[j][0] + o[j][2];
+                wo[hrow * OSTRIDE + d0 + 1] = o[j][1] + o[j][3];
+            } else {
+                wo[hrow * OSTRIDE + d0] = o[j][0];
+                wo[hrow * OSTRIDE + d0 + 1] = o[j][1];
+                wo[(hrow + 8) * OSTRIDE + d0] = o[j][2];
+                wo[(hrow + 8) * OSTRIDE + d0 + 1] = o[j][3];
+            }
+        }
+        if (lane == 0) sm_bad[warp] = bad;
+        named_barrier_consumers();
+
+        // ---- merge the four warps; write the output or this partition's piece
+        const int bad_any = sm_bad[0] | sm_bad[1] | sm_bad[2] | sm_bad[3];
+        const int2 info = p.seq_info[s];
+        const int nsplit = info.y;
+        const size_t piece = (size_t)(info.x + it.y) * Hkv + g;
+        T *out = static_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D;
+        for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
+            const int h = e / D, d = e - h * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+                M = fmaxf(M, sm_o[(w * GROWS + h) * OSTRIDE + D]);
+            float acc = 0.f, lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float *r = sm_o + (w * GROWS + h) * OSTRIDE;
+                const float f = exp2f(r[D] - M);
+                acc += r[d] * f;
+                lsum += r[D + 1] * f;
+            }
+            if (nsplit == 1) {
+                out[h * D + d] = bad_any ? E::from_float(0.f) : E::from_float(acc / lsum);
+            } else {
+                p.part_o[(piece * G + h) * D + d] = acc;
+                if (d == 0) p.part_ml[piece * G + h] = make_float2(M, bad_any ? -1.f : lsum);
+            }
+        }
+        if (nsplit > 1) {
+            __threadfence();
+            named_barrier_consumers();
+            if (ctid == 0) {
+                const int prev = atomicAdd(p.counters + (size_t)s * Hkv + g, 1);
+                *sm_last = (prev == nsplit - 1);
+            }
+            named_barrier_consumers();
+            if (*sm_last) {
+                __threadfence();
+                const size_t first = (size_t)info.x * Hkv + g;
+                for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
+                    const int h = e / D, d = e - h * D;
+                    float M = -INFINITY;
+                    int poisoned = 0;
+                    for (int k = 0; k < nsplit; ++k) {
+                        const float2 ml = __ldcg(p.part_ml + (first + (size_t)k * Hkv) * G + h);
+                        M = fmaxf(M, ml.x);
+                        poisoned |= ml.y < 0.f;
+                    }
+                    float acc = 0.f, lsum = 0.f;
+                    for (int k = 0; k < nsplit; ++k) {
+                        const size_t pc = first + (size_t)k * Hkv;
+                        const float2 ml = __ldcg(p.part_ml + pc * G + h);
+                        const float f = exp2f(ml.x - M);
+                        acc += __ldcg(p.part_o + (pc * G + h) * D + d) * f;
+                        lsum += ml.y * f;
+                    }
+                    out[h * D + d] = poisoned ? E::from_float(0.f) : E::from_float(acc / lsum);
+                }
+            }
+        }
+        named_barrier_consumers();
+    }
+}
+
+// --------------------------------------------------------------------- host side
+struct WsLayout {
+    size_t header, seq_info, items, counters, part_ml, part_o, total;
+    int64_t max_pairs;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static bool ws_layout(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t maxb, int32_t P,
+                      WsLayout *w)
+{
+    if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || maxb <= 0 || P <= 0 || Hq % Hkv) return false;
+    const int64_t G = Hq / Hkv;
+    w->max_pairs = S * ((maxb + P - 1) / P);
+    size_t off = 0;
+    w->header = off; off += 256;
+    w->seq_info = off; off += align256((size_t)S * 8);
+    w->items = off; off += align256((size_t)w->max_pairs * 8);
+    w->counters = off; off += align256((size_t)S * Hkv * 4);
+    w->part_ml = off; off += align256((size_t)w->max_pairs * Hkv * G * 8);
+    w->part_o = off; off += align256((size_t)w->max_pairs * Hkv * G * D * 4);
+    w->total = off;
+    return true;
+}
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeFn encode_fn()
+{
+    static EncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D view of a pool: rows = num_blocks * Hkv * 16 of head_dim elements; box of
+// 64 columns x 16 rows with the 128-byte swizzle.
+static bool make_pool_map(CUtensorMap *map, const void *pool, const PoolGeometry &g)
+{
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)g.head_dim,
+                          (cuuint64_t)g.num_blocks * g.num_kv_heads * g.block_size};
+    cuuint64_t strides[1] = {(cuuint64_t)g.head_dim * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kBlock};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     2, const_cast<void *>(pool), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
+
+struct Variant {
+    KernelFn fn;
+    int smem;
+};
+
+template <int D, bool BF16, int GROWS, int NST, int MINB>
+static Variant variant()
+{
+    return Variant{reinterpret_cast<KernelFn>(&decode_kernel<D, BF16, GROWS, NST, MINB>),
+                   Smem<D, GROWS, NST>::kTotal};
+}
+
+static bool pick_variant(int D, bool bf16, int G, Variant *v)
+{
+    const bool wide = G > 8;
+#define PKV_PICK(DD, NST, MINB)                                                         \
+    if (D == DD) {                                                                      \
+        if (bf16) *v = wide ? variant<DD, true, 16, NST, MINB>() : variant<DD, true, 8, NST, MINB>(); \
+        else *v = wide ? variant<DD, false, 16, NST, MINB>() : variant<DD, false, 8, NST, MINB>();   \
+        return true;                                                                    \
+    }
+    PKV_PICK(128, 10, 2)
+    PKV_PICK(64, 16, 3)
+#undef PKV_PICK
+    return false;
+}
+
+// Resident CTAs per SM for a variant on the current device, cached per device.
+static int persistent_ctas(const Variant &v, int *num_sms_out)
+{
+    constexpr int kMaxDev = 64, kMaxVar = 16;
+    static std::mutex mu;
+    static KernelFn fns[kMaxDev][kMaxVar];
+    static int ctas[kMaxDev][kMaxVar];
+    static int sms[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return -1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms[dev] == 0 &&
+        cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    *num_sms_out = sms[dev];
+    for (int i = 0; i < kMaxVar; ++i) {
+        if (fns[dev][i] == v.fn) return ctas[dev][i];
+        if (fns[dev][i] == nullptr) {
+            if (cudaFuncSetAttribute(reinterpret_cast<const void *>(v.fn),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     v.smem) != cudaSuccess)
+                return -1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &n, reinterpret_cast<const void *>(v.fn), kThreads, v.smem) != cudaSuccess ||
+                n < 1)
+                return -1;
+            fns[dev][i] = v.fn;
+            ctas[dev][i] = n;
+            return n;
+        }
+    }
+    return -1;
+}
+
+static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
+                  const void *v_pool, const int32_t *block_tables, int32_t maxb,
+                  const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+                  int32_t P, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                  void *stream)
+{
+    PoolGeometry g;
+    if (!pool_geometry(pool, &g)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_q_heads <= 0 || maxb <= 0 || P <= 0) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % g.num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_INVALID_ARG;
+    const int G = num_q_heads / g.num_kv_heads;
+    if (g.block_size != kBlock || G > 16) return PKV_ERR_UNSUPPORTED;
+    Variant v;
+    if (!pick_variant(g.head_dim, g.dtype == PKV_BF16, G, &v)) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !workspace ||
+        !d_status)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        ((uintptr_t)workspace & 255u) || ((uintptr_t)block_tables & 3u) ||
+        ((uintptr_t)context_lens & 3u) || ((uintptr_t)d_status & 3u))
+        return PKV_ERR_INVALID_ARG;
+    WsLayout w;
+    if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, P, &w) ||
+        workspace_bytes < w.total)
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)g.num_blocks * g.num_kv_heads * g.block_size > (int64_t)1 << 31)
+        return PKV_ERR_UNSUPPORTED;   // TMA row coordinate is a signed 32-bit value
+
+    CUtensorMap tk, tv;
+    if (!make_pool_map(&tk, k_pool, g) || !make_pool_map(&tv, v_pool, g)) return PKV_ERR_CUDA;
+
+    char *ws = static_cast<char *>(workspace);
+    Params prm;
+    prm.out = out;
+    prm.q = q;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = g.num_kv_heads;
+    prm.group = G;
+    prm.max_blocks_per_seq = maxb;
+    prm.blocks_per_split = P;
+    prm.num_blocks = g.num_blocks;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.header = reinterpret_cast<int32_t *>(ws + w.header);
+    prm.seq_info = reinterpret_cast<int2 *>(ws + w.seq_info);
+    prm.items = reinterpret_cast<int2 *>(ws + w.items);
+    prm.counters = reinterpret_cast<int32_t *>(ws + w.counters);
+    prm.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
+    prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    prm.status = d_status;
+
+    int num_sms = 0;
+    const int per_sm = persistent_ctas(v, &num_sms);
+    if (per_sm < 1) return PKV_ERR_CUDA;
+    int64_t grid = (int64_t)per_sm * num_sms;
+    const int64_t upper = w.max_pairs * g.num_kv_heads;
+    if (grid > upper) grid = upper;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    decode_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    v.fn<<<(unsigned)grid, kThreads, v.smem, st>>>(tk, tv, prm);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace decode
+}  // namespace pkv
+
+extern "C" {
+
+int32_t paged_decode_default_split(void) { return pkv::decode::kDefaultSplit; }
+
+size_t paged_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t max_blocks_per_seq, int32_t blocks_per_split)
+{
+    pkv::decode::WsLayout w;
+    if (!pkv::decode::ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                blocks_per_split, &w))
+        return 0;
+    return w.total;
+}
+
+size_t paged_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t max_blocks_per_seq)
+{
+    return paged_decode_workspace_bytes_split(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              max_blocks_per_seq, pkv::decode::kDefaultSplit);
+}
+
+int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
+                                 const void *k_pool, const void *v_pool,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t num_seqs,
+                                 int32_t num_q_heads, float scale, int32_t blocks_per_split,
+                                 void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                 void *stream)
+{
+    return pkv::decode::launch(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                               context_lens, num_seqs, num_q_heads, scale, blocks_per_split,
+                               workspace, workspace_bytes, d_status, stream);
+}
+
+int paged_decode_attention(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
+                           const void *v_pool, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t num_q_heads, float scale, void *workspace,
+                           size_t workspace_bytes, int32_t *d_status, void *stream)
+{
+    return pkv::decode::launch(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+                               context_lens, num_seqs, num_q_heads, scale,
+                               pkv::decode::kDefaultSplit, workspace, workspace_bytes, d_status,
+                               stream);
+}
+
+}  // extern "C"
