@@ -217,7 +217,7 @@ def our_arm(args, world, rank, local):
     torch.cuda.set_device(dev)
     e2e_steps = args.e2e_steps
     n_steps = args.warmup + args.steps + e2e_steps
-    w = workloads.gqa_long(args.seed + rank, growth_tokens=n_steps + 16)
+    w = workloads.gqa_long(args.seed + rank, num_seqs=args.num_seqs, growth_tokens=n_steps + 16)
     S, hq, hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     vals = workloads.device_values(w, dev)
     pool = KVPool(w.num_blocks, hkv, d, w.dtype, free_order=w.free_order, device=dev)
@@ -366,6 +366,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--num-seqs", type=int, default=256,
+                    help="sequences per GPU (256 is the workload; fewer only for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=8.0)

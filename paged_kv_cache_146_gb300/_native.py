@@ -10,7 +10,7 @@ import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libpagedkv.so")
+LIB_PATH = os.environ.get("PKV_LIBRARY") or os.path.join(PKG, "libpagedkv.so")
 
 PKV_F16, PKV_BF16 = 0, 1
 PKV_OK = 0

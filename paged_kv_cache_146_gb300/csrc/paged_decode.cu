@@ -15,7 +15,8 @@
 //     128-byte swizzle) of each block's K and V slab for the item's kv head
 //     into a ring of NST shared-memory stages, completed through mbarriers;
 //     it streams across item boundaries.  Four consumer warps take the blocks
-//     of an item round-robin.
+//     round-robin by their position in the CTA's stream, so every ring slot has
+//     a single consumer warp (NST is a multiple of 4).
 //   * Consumer, per 16-token block: S = Q K^T on tensor cores (mma.sync
 //     m16n8k16, the G query heads of the GQA group as rows, 16 tokens as
 //     columns, head_dim as the reduction), fp32 online softmax in registers,
@@ -68,7 +69,24 @@ struct Params {
     float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned
     float *part_o;              // [pairs * Hkv * G * D]: unnormalised partition output
     int32_t *status;
+    int64_t max_pairs;          // capacity of items / partial arrays (checked builds)
+    int32_t *debug;             // first failed check: site << 24 | value (checked builds)
 };
+
+// Checked builds (-DPKV_DEBUG_CHECKS) test every data-dependent index before it
+// is used, record the first failure in the debug word and skip the access.
+// Normal builds compile the checks away.
+__device__ __forceinline__ bool dbg_fail(bool ok, int32_t *dbg, int site, long long val)
+{
+#ifdef PKV_DEBUG_CHECKS
+    if (!ok) {
+        atomicCAS(dbg, 0, (site << 24) | (int)(val & 0xffffff));
+        return true;
+    }
+#endif
+    (void)ok; (void)dbg; (void)site; (void)val;
+    return false;
+}
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -268,6 +286,8 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
         }
         __syncthreads();
         const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - nsplit;
+        if (s < p.num_seqs && dbg_fail((int64_t)excl + nsplit <= p.max_pairs, p.debug, 12, excl))
+            nsplit = 0;
         if (s < p.num_seqs) {
             p.seq_info[s] = make_int2(excl, nsplit);
             for (int k = 0; k < nsplit; ++k) p.items[excl + k] = make_int2(s, k);
@@ -295,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     using E = Elem<BF16>;
     using T = typename E::T;
     using SM = Smem<D, GROWS, NST>;
+    static_assert(NST % kConsumerWarps == 0, "each slot must keep one consumer warp");
     constexpr int kBoxes = D / kBoxCols;          // TMA boxes per slab
     constexpr int kSlabBytes = kBoxes * kBoxBytes;
     constexpr int KSTEPS = D / 16;                // QK reduction steps
@@ -335,9 +356,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
             const int sj = item / Hkv, g = item - sj * Hkv;
             const int2 it = p.items[sj];
+            if (dbg_fail(it.x >= 0 && it.x < p.num_seqs, p.debug, 2, it.x)) continue;
             const int L = __ldg(p.context_lens + it.x);
             const int nb = (L + kBlock - 1) / kBlock;
             const int b0 = it.y * P, b1 = min(b0 + P, nb);
+            if (dbg_fail(b1 <= p.max_blocks_per_seq, p.debug, 3, b1)) continue;
             const int32_t *row = p.block_tables + (int64_t)it.x * p.max_blocks_per_seq;
             for (int cb = b0; cb < b1; cb += 32) {
                 const int n = min(32, b1 - cb);
@@ -404,9 +427,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const int sj = item / Hkv, g = item - sj * Hkv;
         const int2 it = p.items[sj];
         const int s = it.x;
+        if (dbg_fail(s >= 0 && s < p.num_seqs, p.debug, 5, s)) continue;
         const int L = __ldg(p.context_lens + s);
         const int nb = (L + kBlock - 1) / kBlock;
         const int b0 = it.y * P, b1 = min(b0 + P, nb);
+        if (dbg_fail(b1 <= p.max_blocks_per_seq && b0 < b1, p.debug, 6, b1)) continue;
 
         // Q rows of the group as the A operand (rows >= G are zero)
         uint32_t qa[KSTEPS][4];
@@ -429,7 +454,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         int bad = 0;
 
-        for (int b = b0 + warp; b < b1; b += kConsumerWarps) {
+        // Block c of this CTA's stream (c = cnt_base + b - b0) goes to warp c % 4 and
+        // slot c % NST; NST is a multiple of 4, so the previous user of a slot is this
+        // same warp, which has seen that phase complete.  A parity wait is only exact
+        // when the waiter is at most one phase ahead of the barrier.
+        const int first = (warp - (int)(cnt_base % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+        for (int b = b0 + first; b < b1; b += kConsumerWarps) {
             const uint32_t c = cnt_base + (uint32_t)(b - b0);
             const int slot = (int)(c % NST);
             const uint32_t par = (c / NST) & 1u;
@@ -440,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const int valid = min(kBlock, L - b * kBlock);
             const uint32_t kb = smem_addr(stages + slot * SM::kStageBytes);
             const uint32_t vb = kb + kSlabBytes;
+            if (dbg_fail(slot < NST && (kb & 1023u) == 0u, p.debug, 7, slot)) continue;
 
             // ---- S = Q K^T : two 8-token tiles
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -581,6 +612,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const int2 info = p.seq_info[s];
         const int nsplit = info.y;
         const size_t piece = (size_t)(info.x + it.y) * Hkv + g;
+        dbg_fail(info.x >= 0 && (int64_t)info.x + nsplit <= p.max_pairs && it.y < nsplit, p.debug,
+                 9, info.x);
         T *out = static_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D;
         for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
             const int h = e / D, d = e - h * D;
@@ -613,19 +646,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
             named_barrier_consumers();
             if (*sm_last) {
                 __threadfence();
-                const size_t first = (size_t)info.x * Hkv + g;
+                const size_t first_piece = (size_t)info.x * Hkv + g;
                 for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
                     const int h = e / D, d = e - h * D;
                     float M = -INFINITY;
                     int poisoned = 0;
                     for (int k = 0; k < nsplit; ++k) {
-                        const float2 ml = __ldcg(p.part_ml + (first + (size_t)k * Hkv) * G + h);
+                        const float2 ml = __ldcg(p.part_ml + (first_piece + (size_t)k * Hkv) * G + h);
                         M = fmaxf(M, ml.x);
                         poisoned |= ml.y < 0.f;
                     }
                     float acc = 0.f, lsum = 0.f;
                     for (int k = 0; k < nsplit; ++k) {
-                        const size_t pc = first + (size_t)k * Hkv;
+                        const size_t pc = first_piece + (size_t)k * Hkv;
                         const float2 ml = __ldcg(p.part_ml + pc * G + h);
                         const float f = exp2f(ml.x - M);
                         acc += __ldcg(p.part_o + (pc * G + h) * D + d) * f;
@@ -723,7 +756,7 @@ static bool pick_variant(int D, bool bf16, int G, Variant *v)
         else *v = wide ? variant<DD, false, 16, NST, MINB>() : variant<DD, false, 8, NST, MINB>();   \
         return true;                                                                    \
     }
-    PKV_PICK(128, 10, 2)
+    PKV_PICK(128, 8, 2)
     PKV_PICK(64, 16, 3)
 #undef PKV_PICK
     return false;
@@ -818,6 +851,8 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     prm.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
     prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
     prm.status = d_status;
+    prm.max_pairs = w.max_pairs;
+    prm.debug = prm.header + 1;
 
     int num_sms = 0;
     const int per_sm = persistent_ctas(v, &num_sms);
@@ -826,6 +861,9 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     const int64_t upper = w.max_pairs * g.num_kv_heads;
     if (grid > upper) grid = upper;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+#ifdef PKV_DEBUG_CHECKS
+    if (cudaMemsetAsync(prm.header, 0, 8, st) != cudaSuccess) return PKV_ERR_CUDA;
+#endif
     decode_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     v.fn<<<(unsigned)grid, kThreads, v.smem, st>>>(tk, tv, prm);
