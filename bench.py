@@ -210,7 +210,8 @@ def reference_arm(args, world, rank):
 # ------------------------------------------------------------------ our arm
 def our_arm(args, world, rank, local):
     import torch
-    from paged_kv_cache_146_gb300 import KVPool, cache_write, paged_decode_attention, workloads
+    from paged_kv_cache_146_gb300 import (KVPool, cache_write, paged_decode_attention,
+                                          paged_decode_default_split, workloads)
     from paged_kv_cache_146_gb300.engine import DecodeEngine
 
     dev = torch.device("cuda", local if world > 1 else 0)
@@ -353,7 +354,7 @@ def our_arm(args, world, rank, local):
                      "launch_ms": round(attn_avg_ms, 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (4 if eng.maxb > paged_decode_default_split() else 3) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -23,11 +23,14 @@
 //     then O += P V on tensor cores with P split into a bf16/fp16 high part
 //     and a low part (rows 0-7 carry the high part, rows 8-15 the low part when
 //     G <= 8), which keeps the weights accurate to ~2^-17.
+//   * The producer also copies each item's Q rows (one 1-D bulk copy) and the
+//     item's metadata into a double-buffered slot, prefetching the next item's
+//     table entries while the current one streams, so consumers never wait on
+//     global memory at an item boundary.
 //   * The four warps' (o, max, sum) are merged in shared memory; items of a
-//     multi-partition sequence write their pieces to the workspace and the last
-//     CTA to finish a (sequence, kv head) merges them by log-sum-exp in
-//     partition order -- deterministic, and independent of where the blocks
-//     physically sit.
+//     multi-partition sequence write their pieces to the workspace and a small
+//     merge kernel combines them by log-sum-exp in partition order --
+//     deterministic, and independent of where the blocks physically sit.
 //   * Every wait is bounded (1 s); on expiry the kernel flags PKV_DEV_TIMEOUT,
 //     stops issuing copies, drains the ones in flight and finishes without
 //     trapping.
@@ -65,7 +68,6 @@ struct Params {
     int32_t *header;            // [0] = number of (sequence, partition) pairs
     int2 *seq_info;             // [S]: first pair index, number of partitions
     int2 *items;                // [S * ceil(maxb / P)]: (sequence, partition)
-    int32_t *counters;          // [S * Hkv]: finished partitions per (sequence, kv head)
     float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned
     float *part_o;              // [pairs * Hkv * G * D]: unnormalised partition output
     int32_t *status;
@@ -234,15 +236,33 @@ template <int D, int GROWS, int NST>
 struct Smem {
     static constexpr int kStageBytes = 2 * (D / kBoxCols) * kBoxBytes;  // K slab + V slab
     static constexpr int kStagesBytes = NST * kStageBytes;
-    static constexpr int kBarBytes = 2 * NST * 8;
+    static constexpr int kQSlotBytes = 16 * D * 2;                      // 16 query rows
+    static constexpr int kQBytes = 2 * kQSlotBytes;                     // double buffered
+    static constexpr int kBarBytes = (2 * NST + 4) * 8;
+    static constexpr int kMetaBytes = 2 * 8 * 4;
     static constexpr int kScratchBytes =
         kConsumerWarps * GROWS * (D + 2) * 4 + NST * 4 + kConsumerWarps * 4 + 16;
-    static constexpr int kTotal = 1024 + kStagesBytes + kBarBytes + kScratchBytes;
+    static constexpr int kTotal =
+        1024 + kStagesBytes + kQBytes + kBarBytes + kMetaBytes + kScratchBytes;
 };
 
+// Item metadata the producer hands to the consumers with each item's Q rows.
+struct ItemMeta {
+    int s, g, L, b0, b1, nsplit, pair, pad;
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // ----------------------------------------------------------------- prep kernel
-// One CTA: partitions per sequence, their prefix sum, the item list, the merge
-// counters, and zero rows for empty or invalid sequences.
+// One CTA: partitions per sequence, their prefix sum, the item list, and zero
+// rows for empty or invalid sequences.
 __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t head_dim)
 {
     __shared__ int warp_tot[32];
@@ -291,7 +311,6 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
         if (s < p.num_seqs) {
             p.seq_info[s] = make_int2(excl, nsplit);
             for (int k = 0; k < nsplit; ++k) p.items[excl + k] = make_int2(s, k);
-            for (int g = 0; g < p.num_kv_heads; ++g) p.counters[(int64_t)s * p.num_kv_heads + g] = 0;
             if (zero_row) {
                 uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(p.out) +
                                                      (size_t)s * p.num_q_heads * head_dim * 2);
@@ -326,45 +345,100 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = base;
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(base + SM::kStagesBytes);
+    uint8_t *qbuf = base + SM::kStagesBytes;                               // [2][16][D]
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(qbuf + SM::kQBytes);
     uint64_t *empty_bar = full_bar + NST;
+    uint64_t *qfull_bar = empty_bar + NST;
+    uint64_t *qempty_bar = qfull_bar + 2;
+    ItemMeta *sm_meta = reinterpret_cast<ItemMeta *>(qempty_bar + 2);     // [2]
     // per consumer warp, per row: D output sums, then the row's max and sum
-    float *sm_o = reinterpret_cast<float *>(empty_bar + NST);          // [4][GROWS][D + 2]
+    float *sm_o = reinterpret_cast<float *>(sm_meta + 2);                  // [4][GROWS][D + 2]
     int *stage_bad = reinterpret_cast<int *>(sm_o + kConsumerWarps * GROWS * OSTRIDE);
     int *sm_bad = stage_bad + NST;
     volatile int *sm_abort = sm_bad + kConsumerWarps;
-    volatile int *sm_last = sm_abort + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // query rows >= G stay zero for the whole kernel: the copies write G rows only
+    for (int i = threadIdx.x; i < SM::kQBytes / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(qbuf)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(smem_addr(&full_bar[i]), 1);
             mbar_init(smem_addr(&empty_bar[i]), 1);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&qfull_bar[i]), 1);
+            mbar_init(smem_addr(&qempty_bar[i]), kConsumerWarps);
+        }
         *sm_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
 
     const int Hkv = p.num_kv_heads, G = p.group, P = p.blocks_per_split;
     const int total_items = p.header[0] * Hkv;
+    const int stride = gridDim.x;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        uint32_t cnt = 0, issued = 0, issued_par = 0;
-        for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-            const int sj = item / Hkv, g = item - sj * Hkv;
-            const int2 it = p.items[sj];
-            if (dbg_fail(it.x >= 0 && it.x < p.num_seqs, p.debug, 2, it.x)) continue;
-            const int L = __ldg(p.context_lens + it.x);
-            const int nb = (L + kBlock - 1) / kBlock;
-            const int b0 = it.y * P, b1 = min(b0 + P, nb);
-            if (dbg_fail(b1 <= p.max_blocks_per_seq, p.debug, 3, b1)) continue;
-            const int32_t *row = p.block_tables + (int64_t)it.x * p.max_blocks_per_seq;
+        // Metadata of item k+1 is fetched while item k is issued: the item's
+        // (sequence, partition) one item ahead, its length, partition info and
+        // first 32 block ids one item ahead of that.
+        uint32_t cnt = 0, issued = 0, issued_par = 0, q_issued = 0, q_par = 0;
+        const uint32_t q_bytes = (uint32_t)(G * D * 2);
+        int item = blockIdx.x;
+        int2 it_cur = item < total_items ? p.items[item / Hkv] : make_int2(0, 0);
+        int2 it_nxt = item + stride < total_items ? p.items[(item + stride) / Hkv]
+                                                  : make_int2(0, 0);
+        auto fetch = [&](int2 it, int valid, int &L, int2 &info, int &id) {
+            L = 0; info = make_int2(0, 0); id = 0;
+            if (!valid) return;
+            L = __ldg(p.context_lens + it.x);
+            info = __ldg(p.seq_info + it.x);
+            const int b = it.y * P + lane;
+            if (b < p.max_blocks_per_seq)
+                id = __ldg(p.block_tables + (int64_t)it.x * p.max_blocks_per_seq + b);
+        };
+        int L_cur, id_cur;
+        int2 info_cur;
+        fetch(it_cur, item < total_items, L_cur, info_cur, id_cur);
+        for (int k = 0; item < total_items; ++k, item += stride) {
+            // prefetch
+            const int2 it_fut = item + 2 * stride < total_items ? p.items[(item + 2 * stride) / Hkv]
+                                                                : make_int2(0, 0);
+            int L_nxt, id_nxt;
+            int2 info_nxt;
+            fetch(it_nxt, item + stride < total_items, L_nxt, info_nxt, id_nxt);
+
+            const int g = item - (item / Hkv) * Hkv;
+            const int s = it_cur.x;
+            const int nb = (L_cur + kBlock - 1) / kBlock;
+            const int b0 = it_cur.y * P, b1 = min(b0 + P, nb);
+            // Q rows + metadata for the consumers
+            if (lane == 0) {
+                const int qs = k & 1;
+                const uint32_t qpar = (k >> 1) & 1;
+                if (mbar_wait(smem_addr(&qempty_bar[qs]), qpar ^ 1u, sm_abort, p.status)) {
+                    sm_meta[qs] = ItemMeta{s, g, L_cur, b0, b1, info_cur.y, info_cur.x + it_cur.y, 0};
+                    const uint32_t qb = smem_addr(&qfull_bar[qs]);
+                    mbar_arrive_expect_tx(qb, q_bytes);
+                    bulk_load(smem_addr(qbuf + qs * SM::kQSlotBytes),
+                              static_cast<const T *>(p.q) +
+                                  ((size_t)s * p.num_q_heads + (size_t)g * G) * D,
+                              q_bytes, qb);
+                    q_issued |= 1u << qs;
+                    q_par = (q_par & ~(1u << qs)) | (qpar << qs);
+                }
+            }
+            // K/V blocks
             for (int cb = b0; cb < b1; cb += 32) {
                 const int n = min(32, b1 - cb);
-                const int my_id = lane < n ? __ldg(row + cb + lane) : 0;
+                int my_id = id_cur;
+                if (cb != b0)
+                    my_id = lane < n ? __ldg(p.block_tables + (int64_t)s * p.max_blocks_per_seq +
+                                             cb + lane)
+                                     : 0;
                 for (int j = 0; j < n; ++j) {
                     const int pid = __shfl_sync(kFull, my_id, j);
                     if (lane == 0) {
@@ -395,13 +469,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     ++cnt;
                 }
             }
+            it_cur = it_nxt; it_nxt = it_fut;
+            L_cur = L_nxt; id_cur = id_nxt; info_cur = info_nxt;
         }
         // drain: every copy this warp issued must land before the CTA exits
         if (lane == 0) {
-            for (int slot = 0; slot < NST; ++slot) {
-                if (!(issued & (1u << slot))) continue;
-                const uint32_t fb = smem_addr(&full_bar[slot]);
-                const uint32_t par = (issued_par >> slot) & 1u;
+            for (int slot = 0; slot < NST + 2; ++slot) {
+                const bool is_q = slot >= NST;
+                const int sl = is_q ? slot - NST : slot;
+                if (!((is_q ? q_issued : issued) & (1u << sl))) continue;
+                const uint32_t fb = smem_addr(is_q ? &qfull_bar[sl] : &full_bar[sl]);
+                const uint32_t par = ((is_q ? q_par : issued_par) >> sl) & 1u;
                 const unsigned long long t0 = globaltimer();
                 while (!mbar_try_wait(fb, par)) {
                     if (globaltimer() - t0 > kTimeoutNs) {
@@ -422,32 +500,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int mi = lane >> 3, r8 = lane & 7;
     const int k_tok = ((mi >> 1) << 3) + r8, k_chunk = mi & 1;   // K: tokens x (chunk, chunk+1)
     const int v_tok = ((mi & 1) << 3) + r8, v_chunk = mi >> 1;   // V^T pairs of 8-dim tiles
+    const int q_row = ((mi & 1) << 3) + r8, q_chunk = mi >> 1;   // Q: rows x (chunk, chunk+1)
 
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int sj = item / Hkv, g = item - sj * Hkv;
-        const int2 it = p.items[sj];
-        const int s = it.x;
-        if (dbg_fail(s >= 0 && s < p.num_seqs, p.debug, 5, s)) continue;
-        const int L = __ldg(p.context_lens + s);
-        const int nb = (L + kBlock - 1) / kBlock;
-        const int b0 = it.y * P, b1 = min(b0 + P, nb);
-        if (dbg_fail(b1 <= p.max_blocks_per_seq && b0 < b1, p.debug, 6, b1)) continue;
-
-        // Q rows of the group as the A operand (rows >= G are zero)
+    for (int k = 0, item = blockIdx.x; item < total_items; ++k, item += stride) {
+        const int qs = k & 1;
+        const bool q_landed = mbar_wait(smem_addr(&qfull_bar[qs]), (k >> 1) & 1, sm_abort, p.status);
+        const bool q_ok = __all_sync(kFull, q_landed);
+        // after a timed-out wait the slot may be stale: run the item empty
+        const ItemMeta mt = q_ok ? sm_meta[qs] : ItemMeta{0, 0, 0, 0, 0, 1, 0, 0};
+        // Q rows of the group as the A operand (rows >= G are zero in shared memory)
         uint32_t qa[KSTEPS][4];
         {
-            const uint32_t *qg = reinterpret_cast<const uint32_t *>(
-                static_cast<const T *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D);
-            const bool r0 = hrow < G, r1 = (GROWS == 16) && (hrow + 8 < G);
+            const uint32_t qb = smem_addr(qbuf + qs * SM::kQSlotBytes);
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int c = (kk * 16 + 2 * q4) >> 1;    // in 32-bit words
-                qa[kk][0] = r0 ? __ldg(qg + hrow * (D / 2) + c) : 0u;
-                qa[kk][2] = r0 ? __ldg(qg + hrow * (D / 2) + c + 4) : 0u;
-                qa[kk][1] = r1 ? __ldg(qg + (hrow + 8) * (D / 2) + c) : 0u;
-                qa[kk][3] = r1 ? __ldg(qg + (hrow + 8) * (D / 2) + c + 4) : 0u;
+                if (q_ok)
+                    ldsm_x4(qa[kk], qb + q_row * (D * 2) + ((2 * kk + q_chunk) << 4));
+                else
+                    qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
             }
         }
+        __syncwarp();
+        if (lane == 0 && q_ok) mbar_arrive(smem_addr(&qempty_bar[qs]));
+        const int s = mt.s, g = mt.g, L = mt.L, b0 = mt.b0, b1 = mt.b1;
+
         float o[NTILES][4];
 #pragma unroll
         for (int j = 0; j < NTILES; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -472,8 +548,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const uint32_t vb = kb + kSlabBytes;
             if (dbg_fail(slot < NST && (kb & 1023u) == 0u, p.debug, 7, slot)) continue;
 
-            // ---- S = Q K^T : two 8-token tiles
+            // ---- S = Q K^T : two 8-token tiles, two accumulation chains each
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+            float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int chunk = 2 * kk + k_chunk;
@@ -481,9 +558,16 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                       (((chunk & 7) ^ r8) << 4);
                 uint32_t kr[4];
                 ldsm_x4(kr, addr);
-                E::mma(s0, qa[kk], kr[0], kr[1]);
-                E::mma(s1, qa[kk], kr[2], kr[3]);
+                if (kk & 1) {
+                    E::mma(u0, qa[kk], kr[0], kr[1]);
+                    E::mma(u1, qa[kk], kr[2], kr[3]);
+                } else {
+                    E::mma(s0, qa[kk], kr[0], kr[1]);
+                    E::mma(s1, qa[kk], kr[2], kr[3]);
+                }
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { s0[i] += u0[i]; s1[i] += u1[i]; }
             // ---- online softmax (row hrow: s0[0..1], s1[0..1]; row hrow+8: [2..3])
             const int t0 = 2 * q4;
             float x0 = s0[0] * p.scale_log2, x1 = s0[1] * p.scale_log2;
@@ -505,7 +589,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn0);
             l0 = l0 * a0 + ((p0 + p1) + (p2 + p3));
             m0 = mn0;
-            float a1 = 1.f;
             uint32_t pa[4], pb[4];
             if constexpr (GROWS == 8) {
                 if (__any_sync(kFull, a0 != 1.f)) {
@@ -520,12 +603,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 const float2 h01 = E::unpack(pa[0]), h23 = E::unpack(pa[2]);
                 pa[1] = E::pack(p0 - h01.x, p1 - h01.y);
                 pa[3] = E::pack(p2 - h23.x, p3 - h23.y);
+                (void)pb;
             } else {
                 float my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
                 my = fmaxf(my, __shfl_xor_sync(kFull, my, 1));
                 my = fmaxf(my, __shfl_xor_sync(kFull, my, 2));
                 const float mn1 = fmaxf(m1, my);
-                a1 = exp2f(m1 - mn1);
+                const float a1 = exp2f(m1 - mn1);
                 const float e0 = exp2f(y0 - mn1), e1 = exp2f(y1 - mn1);
                 const float e2 = exp2f(y2 - mn1), e3 = exp2f(y3 - mn1);
                 l1 = l1 * a1 + ((e0 + e1) + (e2 + e3));
@@ -569,7 +653,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     E::mma(o[2 * jj + 1], pb, vr[2], vr[3]);
                 }
             }
-            (void)a1;
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
         }
@@ -595,76 +678,41 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int j = 0; j < NTILES; ++j) {
             const int d0 = 8 * j + 2 * q4;
             if constexpr (GROWS == 8) {
-                wo[hrow * OSTRIDE + d0] = o[j][0] + o[j][2];
-                wo[hrow * OSTRIDE + d0 + 1] = o[j][1] + o[j][3];
+                *reinterpret_cast<float2 *>(&wo[hrow * OSTRIDE + d0]) =
+                    make_float2(o[j][0] + o[j][2], o[j][1] + o[j][3]);
             } else {
-                wo[hrow * OSTRIDE + d0] = o[j][0];
-                wo[hrow * OSTRIDE + d0 + 1] = o[j][1];
-                wo[(hrow + 8) * OSTRIDE + d0] = o[j][2];
-                wo[(hrow + 8) * OSTRIDE + d0 + 1] = o[j][3];
+                *reinterpret_cast<float2 *>(&wo[hrow * OSTRIDE + d0]) = make_float2(o[j][0], o[j][1]);
+                *reinterpret_cast<float2 *>(&wo[(hrow + 8) * OSTRIDE + d0]) =
+                    make_float2(o[j][2], o[j][3]);
             }
         }
         if (lane == 0) sm_bad[warp] = bad;
         named_barrier_consumers();
 
         // ---- merge the four warps; write the output or this partition's piece
-        const int bad_any = sm_bad[0] | sm_bad[1] | sm_bad[2] | sm_bad[3];
-        const int2 info = p.seq_info[s];
-        const int nsplit = info.y;
-        const size_t piece = (size_t)(info.x + it.y) * Hkv + g;
-        dbg_fail(info.x >= 0 && (int64_t)info.x + nsplit <= p.max_pairs && it.y < nsplit, p.debug,
-                 9, info.x);
-        T *out = static_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D;
-        for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-            const int h = e / D, d = e - h * D;
-            float M = -INFINITY;
+        if (q_ok && !*sm_abort) {
+            const int bad_any = sm_bad[0] | sm_bad[1] | sm_bad[2] | sm_bad[3];
+            const size_t piece = (size_t)mt.pair * Hkv + g;
+            T *out = static_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D;
+            for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
+                const int h = e / D, d = e - h * D;
+                float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                M = fmaxf(M, sm_o[(w * GROWS + h) * OSTRIDE + D]);
-            float acc = 0.f, lsum = 0.f;
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    M = fmaxf(M, sm_o[(w * GROWS + h) * OSTRIDE + D]);
+                float acc = 0.f, lsum = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float *r = sm_o + (w * GROWS + h) * OSTRIDE;
-                const float f = exp2f(r[D] - M);
-                acc += r[d] * f;
-                lsum += r[D + 1] * f;
-            }
-            if (nsplit == 1) {
-                out[h * D + d] = bad_any ? E::from_float(0.f) : E::from_float(acc / lsum);
-            } else {
-                p.part_o[(piece * G + h) * D + d] = acc;
-                if (d == 0) p.part_ml[piece * G + h] = make_float2(M, bad_any ? -1.f : lsum);
-            }
-        }
-        if (nsplit > 1) {
-            __threadfence();
-            named_barrier_consumers();
-            if (ctid == 0) {
-                const int prev = atomicAdd(p.counters + (size_t)s * Hkv + g, 1);
-                *sm_last = (prev == nsplit - 1);
-            }
-            named_barrier_consumers();
-            if (*sm_last) {
-                __threadfence();
-                const size_t first_piece = (size_t)info.x * Hkv + g;
-                for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-                    const int h = e / D, d = e - h * D;
-                    float M = -INFINITY;
-                    int poisoned = 0;
-                    for (int k = 0; k < nsplit; ++k) {
-                        const float2 ml = __ldcg(p.part_ml + (first_piece + (size_t)k * Hkv) * G + h);
-                        M = fmaxf(M, ml.x);
-                        poisoned |= ml.y < 0.f;
-                    }
-                    float acc = 0.f, lsum = 0.f;
-                    for (int k = 0; k < nsplit; ++k) {
-                        const size_t pc = first_piece + (size_t)k * Hkv;
-                        const float2 ml = __ldcg(p.part_ml + pc * G + h);
-                        const float f = exp2f(ml.x - M);
-                        acc += __ldcg(p.part_o + (pc * G + h) * D + d) * f;
-                        lsum += ml.y * f;
-                    }
-                    out[h * D + d] = poisoned ? E::from_float(0.f) : E::from_float(acc / lsum);
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float *r = sm_o + (w * GROWS + h) * OSTRIDE;
+                    const float f = exp2f(r[D] - M);
+                    acc += r[d] * f;
+                    lsum += r[D + 1] * f;
+                }
+                if (mt.nsplit == 1) {
+                    out[h * D + d] = bad_any ? E::from_float(0.f) : E::from_float(acc / lsum);
+                } else {
+                    p.part_o[(piece * G + h) * D + d] = acc;
+                    if (d == 0) p.part_ml[piece * G + h] = make_float2(M, bad_any ? -1.f : lsum);
                 }
             }
         }
@@ -672,9 +720,45 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
 }
 
+// ---------------------------------------------------------------- merge kernel
+// One CTA per (sequence, kv head): sequences cut into several partitions get
+// their pieces combined by log-sum-exp, in partition order:
+//   M = max_p m_p,  out = sum_p o_p 2^(m_p - M) / sum_p l_p 2^(m_p - M)
+// (the maxima are in the log2 domain).  A poisoned piece (sum < 0) zeroes the row.
+template <bool BF16>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const Params p, int32_t head_dim)
+{
+    using E = Elem<BF16>;
+    using T = typename E::T;
+    const int Hkv = p.num_kv_heads, G = p.group, D = head_dim;
+    const int s = blockIdx.x / Hkv, g = blockIdx.x - (blockIdx.x / Hkv) * Hkv;
+    if (s >= p.num_seqs) return;
+    const int2 info = p.seq_info[s];
+    if (info.y <= 1) return;
+    T *out = static_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D;
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+        const int h = e / D, d = e - h * D;
+        float M = -INFINITY, acc = 0.f, lsum = 0.f;
+        int poisoned = 0;
+#pragma unroll 4
+        for (int k = 0; k < info.y; ++k) {
+            const size_t pc = (size_t)(info.x + k) * Hkv + g;
+            const float2 ml = p.part_ml[pc * G + h];
+            const float ov = p.part_o[(pc * G + h) * D + d];
+            poisoned |= ml.y < 0.f;
+            const float Mn = fmaxf(M, ml.x);
+            const float a = exp2f(M - Mn), b = exp2f(ml.x - Mn);
+            acc = acc * a + ov * b;
+            lsum = lsum * a + ml.y * b;
+            M = Mn;
+        }
+        out[h * D + d] = poisoned ? E::from_float(0.f) : E::from_float(acc / lsum);
+    }
+}
+
 // --------------------------------------------------------------------- host side
 struct WsLayout {
-    size_t header, seq_info, items, counters, part_ml, part_o, total;
+    size_t header, seq_info, items, part_ml, part_o, total;
     int64_t max_pairs;
 };
 
@@ -690,7 +774,6 @@ static bool ws_layout(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t max
     w->header = off; off += 256;
     w->seq_info = off; off += align256((size_t)S * 8);
     w->items = off; off += align256((size_t)w->max_pairs * 8);
-    w->counters = off; off += align256((size_t)S * Hkv * 4);
     w->part_ml = off; off += align256((size_t)w->max_pairs * Hkv * G * 8);
     w->part_o = off; off += align256((size_t)w->max_pairs * Hkv * G * D * 4);
     w->total = off;
@@ -847,7 +930,6 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     prm.header = reinterpret_cast<int32_t *>(ws + w.header);
     prm.seq_info = reinterpret_cast<int2 *>(ws + w.seq_info);
     prm.items = reinterpret_cast<int2 *>(ws + w.items);
-    prm.counters = reinterpret_cast<int32_t *>(ws + w.counters);
     prm.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
     prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
     prm.status = d_status;
@@ -867,7 +949,16 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     decode_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     v.fn<<<(unsigned)grid, kThreads, v.smem, st>>>(tk, tv, prm);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (maxb > P) {   // some sequence may have several partitions
+        const int64_t pairs = (int64_t)num_seqs * g.num_kv_heads;
+        if (g.dtype == PKV_BF16)
+            decode_merge_kernel<true><<<(unsigned)pairs, 128, 0, st>>>(prm, g.head_dim);
+        else
+            decode_merge_kernel<false><<<(unsigned)pairs, 128, 0, st>>>(prm, g.head_dim);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
 }
 
 }  // namespace decode
