@@ -236,6 +236,39 @@ int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
 /* Default partition size (blocks) paged_decode_attention uses. */
 int32_t paged_decode_default_split(void);
 
+/* Paged decode attention that allocates nothing and takes no workspace.
+ * (An addition of this library: the source pages have no counterpart.)
+ *
+ * Some callers cannot allocate device memory when they decode: an engine that
+ * reserved nearly all free HBM for the KV pool at start-up has none left to
+ * give, and a step loop may not afford cudaMalloc's implicit synchronisation.
+ * This call computes exactly what paged_decode_attention computes, with the
+ * scratch kept in a fixed array inside the library: PKV_NOALLOC_SCRATCH_BYTES
+ * of global memory on every device that loads the library, held until the
+ * process exits.  The caller still passes all inputs and outputs (out, q, the
+ * pools, tables, lengths, status word).
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.
+ *   - The partition size is the default when the scratch fits, otherwise the
+ *     smallest number of partitions per sequence that fits.  Shapes that do
+ *     not fit even with one partition per sequence are rejected with
+ *     PKV_ERR_INVALID_ARG, and nothing is launched.
+ *   - Nothing in the array has to start at zero: every launch rewrites the
+ *     parts it reads.  The array is shared by every call on the device and keeps
+ *     the last call's contents, so calls that overlap on the GPU (concurrent
+ *     streams) race; serialise them.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ * Errors: as paged_decode_attention, plus PKV_ERR_CUDA if the address lookup
+ * fails. */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+int paged_decode_attention_noalloc(const pkv_pool *pool, void *out, const void *q,
+                                   const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, float scale, int32_t *d_status,
+                                   void *stream);
+
 /* ------------------------------------------------------------ status word */
 
 /* Wait for the stream, read the device status word into *out_word (may be

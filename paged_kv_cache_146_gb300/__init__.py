@@ -25,6 +25,7 @@ from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV
                       PagedKVError, check, lib)
 
 __all__ = ["KVPool", "PagedKVError", "cache_write", "paged_decode_attention",
+           "paged_decode_attention_noalloc",
            "decode_workspace_bytes", "status_check", "kv_bytes_per_token",
            "kv_blocks_for_tokens", "kv_pool_bytes", "default_split", "lib",
            "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN", "DEV_TIMEOUT"]
@@ -223,6 +224,24 @@ def paged_decode_attention(pool: KVPool, q, block_tables, context_lens, scale: f
                                                 _t_ptr(workspace), nbytes, _t_ptr(status),
                                                 _stream(stream))
     check(rc, "paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_noalloc(pool: KVPool, q, block_tables, context_lens, scale: float,
+                                   status, out, k_pool=None, v_pool=None, stream=None):
+    """Paged decode attention with the library's fixed scratch instead of a
+    caller workspace; the library allocates nothing (for callers that cannot
+    allocate device memory at decode time).  ``out`` must be given.  Calls on one
+    device share the scratch: do not overlap them on the GPU."""
+    k_pool = pool.k_pool if k_pool is None else k_pool
+    v_pool = pool.v_pool if v_pool is None else v_pool
+    S, hq, d = q.shape
+    rc = lib().paged_decode_attention_noalloc(pool.handle, _t_ptr(out), _t_ptr(q),
+                                              _t_ptr(k_pool), _t_ptr(v_pool),
+                                              _t_ptr(block_tables), int(block_tables.shape[1]),
+                                              _t_ptr(context_lens), S, hq, float(scale),
+                                              _t_ptr(status), _stream(stream))
+    check(rc, "paged_decode_attention_noalloc")
     return out
 
 

@@ -1012,3 +1012,71 @@ int paged_decode_attention(const pkv_pool *pool, void *out, const void *q, const
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------- fixed-scratch variant
+// paged_decode_attention_noalloc runs the same kernels as paged_decode_attention
+// but keeps their scratch (work list and split-K pieces) in a fixed array that
+// belongs to this library, so the caller passes no workspace and nothing is
+// allocated at call time.  The array lives in global memory of every device
+// that loads the library, from module load until the process exits.
+namespace pkv {
+namespace decode {
+
+constexpr size_t kNoallocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// symbol only names a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached; NULL if the lookup fails.
+static void *noalloc_scratch_address()
+{
+    constexpr int kMaxDev = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace decode
+}  // namespace pkv
+
+extern "C" int paged_decode_attention_noalloc(const pkv_pool *pool, void *out, const void *q,
+                                              const void *k_pool, const void *v_pool,
+                                              const int32_t *block_tables,
+                                              int32_t max_blocks_per_seq,
+                                              const int32_t *context_lens, int32_t num_seqs,
+                                              int32_t num_q_heads, float scale,
+                                              int32_t *d_status, void *stream)
+{
+    using namespace pkv::decode;
+    pkv::PoolGeometry g;
+    if (!pkv::pool_geometry(pool, &g) || num_seqs < 0 || num_q_heads <= 0 ||
+        max_blocks_per_seq <= 0)
+        return PKV_ERR_INVALID_ARG;
+    // The default partition size if its scratch fits; otherwise the smallest
+    // partition count per sequence that fits, down to one partition.
+    const int32_t maxb = max_blocks_per_seq;
+    int32_t P = 0;
+    for (int32_t k = (maxb + kDefaultSplit - 1) / kDefaultSplit; k >= 1; --k) {
+        const int32_t cand = (maxb + k - 1) / k;
+        WsLayout w;
+        if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, cand, &w))
+            return PKV_ERR_INVALID_ARG;
+        if (w.total <= kNoallocScratchBytes) {
+            P = cand;
+            break;
+        }
+    }
+    if (P == 0) return PKV_ERR_INVALID_ARG;   // scratch would exceed PKV_NOALLOC_SCRATCH_BYTES
+    void *scratch = noalloc_scratch_address();
+    if (!scratch) return PKV_ERR_CUDA;
+    return launch(pool, out, q, k_pool, v_pool, block_tables, maxb, context_lens, num_seqs,
+                  num_q_heads, scale, P, scratch, kNoallocScratchBytes, d_status, stream);
+}
