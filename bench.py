@@ -118,14 +118,27 @@ def dist_setup(args):
     return world, rank, local
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """Slowest rank's time: the job is done when every rank is."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_workload(seed: int, rank: int, num_seqs: int, growth_tokens: int):
+    """Each rank decodes its own batch of sequences (weak scaling): rank r draws
+    the batch with seed + r, so ranks hold disjoint, independent work."""
+    from paged_kv_cache_146_gb300 import workloads
+    return workloads.gqa_long(seed + rank, num_seqs=num_seqs, growth_tokens=growth_tokens)
+
+
+def job_rate(bytes_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: bytes of all ranks over the slowest rank's time."""
+    return bytes_per_rank * world / (max_ms * 1e-3) / 1e9
 
 
 def barrier(world):
@@ -211,14 +224,14 @@ def reference_arm(args, world, rank):
 def our_arm(args, world, rank, local):
     import torch
     from paged_kv_cache_146_gb300 import (KVPool, cache_write, paged_decode_attention,
-                                          paged_decode_default_split, workloads)
+                                          default_split, workloads)
     from paged_kv_cache_146_gb300.engine import DecodeEngine
 
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     e2e_steps = args.e2e_steps
     n_steps = args.warmup + args.steps + e2e_steps
-    w = workloads.gqa_long(args.seed + rank, num_seqs=args.num_seqs, growth_tokens=n_steps + 16)
+    w = rank_workload(args.seed, rank, args.num_seqs, n_steps + 16)
     S, hq, hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     vals = workloads.device_values(w, dev)
     pool = KVPool(w.num_blocks, hkv, d, w.dtype, free_order=w.free_order, device=dev)
@@ -284,7 +297,7 @@ def our_arm(args, world, rank, local):
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     bytes_all = bytes_total * world
     toks_all = toks_total * world
-    value = bytes_all / (elapsed_ms * 1e-3) / 1e9
+    value = job_rate(bytes_total, world, elapsed_ms)
     peak, peak_kind = peaks()
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     bytes_per_launch = bytes_total / args.steps
@@ -354,7 +367,7 @@ def our_arm(args, world, rank, local):
                      "launch_ms": round(attn_avg_ms, 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (4 if eng.maxb > paged_decode_default_split() else 3) * args.steps,
+        "gpu_launches": (4 if eng.maxb > default_split() else 3) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -520,8 +520,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     qa[kk][0] = qa[kk][1] = qa[kk][2] = qa[kk][3] = 0u;
             }
         }
-        __syncwarp();
-        if (lane == 0 && q_ok) mbar_arrive(smem_addr(&qempty_bar[qs]));
         const int s = mt.s, g = mt.g, L = mt.L, b0 = mt.b0, b1 = mt.b1;
 
         float o[NTILES][4];
@@ -653,10 +651,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     E::mma(o[2 * jj + 1], pb, vr[2], vr[3]);
                 }
             }
+            // The stage's next contents arrive through the async proxy (TMA):
+            // order this warp's generic-proxy reads of it before the release.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
         }
         cnt_base += (uint32_t)(b1 - b0);
+        // Release the Q slot only now, after the QK products have consumed the
+        // fragments read from it (the next copy into it may land at once).
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && q_ok) mbar_arrive(smem_addr(&qempty_bar[qs]));
 
         // ---- per-warp state into shared memory
         l0 += __shfl_xor_sync(kFull, l0, 1);

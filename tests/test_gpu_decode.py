@@ -270,3 +270,18 @@ def test_longest_context_and_widest_group():
     out = c.run_gpu()
     assert status_check(c.status) == (0, 0)
     assert_close(out, c.oracle_out(), "32K + G16")
+
+
+@pytest.mark.parametrize("split", [1, 2, None])
+def test_repeated_launches_are_identical(split):
+    """Many short work items let the producer warp run far ahead of the
+    consumers, which is when shared-memory slots are recycled fastest; every
+    repeated launch must give the same bits, within tolerance of the oracle."""
+    w = workloads.small_random(77, 128, 3000, 32, 8, 128, "bf16")
+    c = _case(w)
+    exp = c.oracle_out()
+    outs = [c.run_gpu(blocks_per_split=split) for _ in range(8)]
+    assert status_check(c.status) == (0, 0)
+    for o in outs:
+        assert torch.equal(o, outs[0])
+    assert_close(outs[0], exp, f"split={split}")
