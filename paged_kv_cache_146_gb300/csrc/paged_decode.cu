@@ -175,6 +175,20 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr)
                  : "r"(addr));
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// serialization attribute may start while the previous kernel in the stream is
+// still running; griddep_wait() blocks until that kernel has finished and its
+// writes are visible.  Without the attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier_consumers()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -268,6 +282,7 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     __shared__ int warp_tot[32];
     __shared__ int carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_launch_dependents();   // the main kernel may set up its CTAs meanwhile
     if (tid == 0) carry = 0;
     __syncthreads();
     const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
@@ -375,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    griddep_wait();                // the work list comes from the prep kernel
 
     const int Hkv = p.num_kv_heads, G = p.group, P = p.blocks_per_split;
     const int total_items = p.header[0] * Hkv;
@@ -727,38 +743,78 @@ __global__ void __launch_bounds__(kThreads, MINB)
 }
 
 // ---------------------------------------------------------------- merge kernel
-// One CTA per (sequence, kv head): sequences cut into several partitions get
-// their pieces combined by log-sum-exp, in partition order:
+// Sequences cut into several partitions get their pieces combined by log-sum-exp:
 //   M = max_p m_p,  out = sum_p o_p 2^(m_p - M) / sum_p l_p 2^(m_p - M)
-// (the maxima are in the log2 domain).  A poisoned piece (sum < 0) zeroes the row.
-template <bool BF16>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const Params p, int32_t head_dim)
+// (maxima in the log2 domain).  One CTA per (sequence, kv head), one warp per
+// query head of the group: lanes reduce M and the denominator over the pieces
+// with a fixed shuffle tree, then each lane sums its D/32 dimensions over the
+// pieces in partition order, with the piece loads independent of the sums so
+// many are in flight.  Deterministic.  A poisoned piece (sum < 0) zeroes the row.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
 {
     using E = Elem<BF16>;
     using T = typename E::T;
-    const int Hkv = p.num_kv_heads, G = p.group, D = head_dim;
+    constexpr int PER_LANE = D / 32;
+    const int Hkv = p.num_kv_heads, G = p.group;
     const int s = blockIdx.x / Hkv, g = blockIdx.x - (blockIdx.x / Hkv) * Hkv;
-    if (s >= p.num_seqs) return;
+    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_wait();                // pieces come from the main kernel
+    if (s >= p.num_seqs || h >= G) return;
     const int2 info = p.seq_info[s];
-    if (info.y <= 1) return;
-    T *out = static_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D;
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-        const int h = e / D, d = e - h * D;
-        float M = -INFINITY, acc = 0.f, lsum = 0.f;
-        int poisoned = 0;
-#pragma unroll 4
-        for (int k = 0; k < info.y; ++k) {
-            const size_t pc = (size_t)(info.x + k) * Hkv + g;
-            const float2 ml = p.part_ml[pc * G + h];
-            const float ov = p.part_o[(pc * G + h) * D + d];
-            poisoned |= ml.y < 0.f;
-            const float Mn = fmaxf(M, ml.x);
-            const float a = exp2f(M - Mn), b = exp2f(ml.x - Mn);
-            acc = acc * a + ov * b;
-            lsum = lsum * a + ml.y * b;
-            M = Mn;
+    const int n = info.y;
+    if (n <= 1) return;
+    const float2 *ml = p.part_ml + ((size_t)info.x * Hkv + g) * G + h;   // stride Hkv * G
+    const size_t mstride = (size_t)Hkv * G;
+    // one pass: each lane keeps (max, sum) of its pieces, then a fixed butterfly
+    // combines the lanes' pairs with rescaling
+    float M = -INFINITY, lsum = 0.f;
+    int poisoned = 0;
+    for (int k = lane; k < n; k += 32) {
+        const float2 v = __ldg(ml + k * mstride);
+        poisoned |= v.y < 0.f;
+        const float Mn = fmaxf(M, v.x);
+        lsum = lsum * exp2f(M - Mn) + v.y * exp2f(v.x - Mn);
+        M = Mn;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float M2 = __shfl_xor_sync(kFull, M, o);
+        const float l2 = __shfl_xor_sync(kFull, lsum, o);
+        poisoned |= __shfl_xor_sync(kFull, poisoned, o);
+        const float Mn = fmaxf(M, M2);
+        const float a = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        const float b = M2 == -INFINITY ? 0.f : exp2f(M2 - Mn);
+        lsum = lsum * a + l2 * b;
+        M = Mn;
+    }
+
+    const float *po = p.part_o + (((size_t)info.x * Hkv + g) * G + h) * D + PER_LANE * lane;
+    const size_t ostride = mstride * D;
+    float acc[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) acc[i] = 0.f;
+#pragma unroll 16
+    for (int k = 0; k < n; ++k) {
+        const float w = exp2f(__ldg(&ml[k * mstride].x) - M);
+        if constexpr (PER_LANE == 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(po + k * ostride));
+            acc[0] += v.x * w; acc[1] += v.y * w; acc[2] += v.z * w; acc[3] += v.w * w;
+        } else {
+            const float2 v = __ldg(reinterpret_cast<const float2 *>(po + k * ostride));
+            acc[0] += v.x * w; acc[1] += v.y * w;
         }
-        out[h * D + d] = poisoned ? E::from_float(0.f) : E::from_float(acc / lsum);
+    }
+    T *out = static_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + (size_t)g * G + h) * D +
+             PER_LANE * lane;
+    const float inv = 1.f / lsum;
+    if constexpr (PER_LANE == 4) {
+        uint2 w2;
+        w2.x = poisoned ? 0u : E::pack(acc[0] * inv, acc[1] * inv);
+        w2.y = poisoned ? 0u : E::pack(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(out) = w2;
+    } else {
+        *reinterpret_cast<uint32_t *>(out) = poisoned ? 0u : E::pack(acc[0] * inv, acc[1] * inv);
     }
 }
 
@@ -954,15 +1010,30 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
 #endif
     decode_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-    v.fn<<<(unsigned)grid, kThreads, v.smem, st>>>(tk, tv, prm);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)v.smem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, v.fn, tk, tv, prm) != cudaSuccess) return PKV_ERR_CUDA;
     if (maxb > P) {   // some sequence may have several partitions
         const int64_t pairs = (int64_t)num_seqs * g.num_kv_heads;
-        if (g.dtype == PKV_BF16)
-            decode_merge_kernel<true><<<(unsigned)pairs, 128, 0, st>>>(prm, g.head_dim);
-        else
-            decode_merge_kernel<false><<<(unsigned)pairs, 128, 0, st>>>(prm, g.head_dim);
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        const bool bf = g.dtype == PKV_BF16;
+        void (*merge)(Params) =
+            g.head_dim == 128 ? (bf ? decode_merge_kernel<true, 128> : decode_merge_kernel<false, 128>)
+                              : (bf ? decode_merge_kernel<true, 64> : decode_merge_kernel<false, 64>);
+        cudaLaunchConfig_t mcfg = {};
+        mcfg.gridDim = dim3((unsigned)pairs);
+        mcfg.blockDim = dim3(32u * (unsigned)G);
+        mcfg.stream = st;
+        mcfg.attrs = pdl;
+        mcfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&mcfg, merge, prm) != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;
 }
