@@ -170,6 +170,44 @@ int kv_append_slots(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_lens,
                     const int32_t *num_new, int32_t *block_tables,
                     int32_t max_blocks_per_seq, int64_t *slot_mapping);
 
+/* ------------------------------------- sharing and copy-on-write (NEXT #1) */
+
+/* A child sequence starts sharing every block of its parent ("vLLM-and-
+ * PagedAttention-KR", "Parallel Sampling decoding": the samples of one prompt
+ * share its blocks, each block's reference count equals its sharers).  The
+ * first ceil(parent_len / block_size) entries of parent_row are copied into
+ * child_row and gain one reference each; the rest of child_row (up to
+ * max_blocks_per_seq entries) is set to -1.  Host arrays.  All or nothing.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_BAD_BLOCK (an entry is not allocated). */
+int kv_seq_fork(pkv_pool *pool, const int32_t *parent_row, int32_t parent_len,
+                int32_t *child_row, int32_t max_blocks_per_seq);
+
+/* kv_append_slots with copy-on-write ("Parallel Sampling decoding": when the
+ * samples write different tokens into a shared block, that block is copied and
+ * its reference count drops; "PagedAttention 파헤치기", "같은 블록을 여러 요청이
+ * 나눠 쓴다").  Sequences are handled in order; a sequence whose partly filled
+ * tail block is still referenced by others takes a fresh block for it, records
+ * the pair (copy_src[i] = shared, copy_dst[i] = fresh), points its table at the
+ * fresh block and drops one reference from the shared one; the last remaining
+ * user of a block writes in place.  Then blocks are taken and slots written as
+ * in kv_append_slots.  copy_src / copy_dst: host int32 [num_seqs] capacity;
+ * *num_copies receives the count.  The caller runs kv_block_copy on the pairs
+ * before writing the new tokens' K/V.  All or nothing.
+ * Errors: as kv_append_slots (no PKV_ERR_SHARED_BLOCK). */
+int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_lens,
+                        const int32_t *num_new, int32_t *block_tables,
+                        int32_t max_blocks_per_seq, int64_t *slot_mapping, int32_t *copy_src,
+                        int32_t *copy_dst, int32_t *num_copies);
+
+/* Device copy of n whole blocks: K and V of block dst_ids[i] become those of
+ * block src_ids[i] (all kv heads and slots, bit for bit).  src_ids / dst_ids:
+ * device int32 [n]; destinations must differ from each other and from every
+ * source (kv_append_slots_cow guarantees it: they are fresh blocks).  A pair
+ * naming a block outside the pool is skipped and sets PKV_DEV_BAD_BLOCK.
+ * Asynchronous on stream.  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA. */
+int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *dst_ids,
+                  int32_t n, void *k_pool, void *v_pool, int32_t *d_status, void *stream);
+
 /* ---------------------------------------------------------- cache write (a3) */
 
 /* Store num_tokens new tokens' K and V rows into their slots ("가장 기본적인

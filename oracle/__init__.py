@@ -47,6 +47,8 @@ def _declare(lib):
     lib.oracle_empty_slots.restype = c_i64
     lib.oracle_cache_write.argtypes = [p, p, p, c_i64, c_i32, c_i32, c_i32, c_i64, p, p]
     lib.oracle_cache_write.restype = c_i64
+    lib.oracle_block_copy.argtypes = [p, p, p, p, c_i64, c_i32, c_i32, c_i32, c_i64]
+    lib.oracle_block_copy.restype = c_i64
     lib.oracle_dense_attention.argtypes = [p, p, p, c_i64, c_i32, c_dbl, p]
     lib.oracle_dense_attention.restype = None
     lib.oracle_paged_decode.argtypes = [p, p, p, p, c_i32, p, c_i32, c_i32, c_i32,
@@ -135,6 +137,15 @@ class Oracle:
         return self.lib.oracle_cache_write(_ptr(k_new), _ptr(v_new), _ptr(slots),
                                            len(slots), hkv, d, bs, num_blocks,
                                            _ptr(k_pool), _ptr(v_pool))
+
+    def block_copy(self, k_pool, v_pool, src_ids, dst_ids) -> int:
+        """Copy whole blocks (K and V) in place, pair by pair."""
+        src = np.ascontiguousarray(src_ids, dtype=np.int32)
+        dst = np.ascontiguousarray(dst_ids, dtype=np.int32)
+        assert k_pool.dtype == np.uint16 and v_pool.dtype == np.uint16
+        num_blocks, hkv, bs, d = k_pool.shape
+        return self.lib.oracle_block_copy(_ptr(k_pool), _ptr(v_pool), _ptr(src), _ptr(dst),
+                                          len(src), hkv, bs, d, num_blocks)
 
     # -- attention
     def dense_attention(self, q, K, V, scale) -> np.ndarray:

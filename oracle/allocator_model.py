@@ -131,6 +131,57 @@ class BlockLedger:
                 slots.append(tables[s][pos // bs] * bs + pos % bs)
         return slots
 
+    def fork(self, parent_row, parent_len: int, child_row) -> None:
+        """A child sequence starts sharing every block of its parent: same ids in
+        its table, one more reference on each ("Parallel Sampling decoding")."""
+        nb = -(-parent_len // self.block_size)
+        ids = [int(b) for b in parent_row[:nb]]
+        self.ref(ids)
+        child_row[:nb] = ids
+        for i in range(nb, len(child_row)):
+            child_row[i] = -1
+
+    def append_cow(self, seq_lens, num_new, tables):
+        """Like :meth:`append`, but a sequence about to write into a partly filled
+        block that others still reference first takes a fresh block, records the
+        copy (shared -> fresh) and drops one reference from the shared block; the
+        last remaining user writes in place.  Sequences are handled in order.
+        Returns (slots, copies).  All or nothing."""
+        bs = self.block_size
+        dec: dict[int, int] = {}
+        need = 0
+        for s, (n0, k) in enumerate(zip(seq_lens, num_new)):
+            if n0 < 0 or k < 0:
+                raise InvalidArg("negative length")
+            if n0 + k > len(tables[s]) * bs:
+                raise InvalidArg("block table row too short")
+            if k > 0 and n0 % bs != 0:
+                tail = tables[s][n0 // bs]
+                if self._refs.get(tail, 0) < 1:
+                    raise BadBlock(f"tail block {tail} is not allocated")
+                if self._refs[tail] - dec.get(tail, 0) > 1:
+                    dec[tail] = dec.get(tail, 0) + 1
+                    need += 1
+            for pos in range(n0, n0 + k):
+                if pos % bs == 0:
+                    need += 1
+        if need > len(self._stack):
+            raise OutOfBlocks(f"{need} blocks wanted, {len(self._stack)} free")
+        slots, copies = [], []
+        for s, (n0, k) in enumerate(zip(seq_lens, num_new)):
+            if k > 0 and n0 % bs != 0:
+                tail = tables[s][n0 // bs]
+                if self._refs[tail] > 1:
+                    fresh = self.alloc(1)[0]
+                    self._refs[tail] -= 1
+                    copies.append((tail, fresh))
+                    tables[s][n0 // bs] = fresh
+            for pos in range(n0, n0 + k):
+                if pos % bs == 0:
+                    tables[s][pos // bs] = self.alloc(1)[0]
+                slots.append(tables[s][pos // bs] * bs + pos % bs)
+        return slots, copies
+
     def fills(self, seq_len: int) -> list[int]:
         """Filled slots of each logical block of a sequence of ``seq_len`` tokens."""
         bs = self.block_size

@@ -140,6 +140,31 @@ int64_t oracle_cache_write(const uint16_t *k_new, const uint16_t *v_new,
     return bad;
 }
 
+/* Copy-on-write: block dst_ids[i] becomes a copy of block src_ids[i], K and V,
+ * every kv head and slot ("vLLM-and-PagedAttention-KR", "Parallel Sampling
+ * decoding": a shared block that one sample writes into is copied first).
+ * Pairs are applied in order.  Returns the number of pairs naming a block
+ * outside the pool (those are skipped). */
+int64_t oracle_block_copy(uint16_t *k_pool, uint16_t *v_pool, const int32_t *src_ids,
+                          const int32_t *dst_ids, int64_t n, int32_t num_kv_heads,
+                          int32_t block_size, int32_t head_dim, int64_t num_blocks)
+{
+    int64_t bad = 0;
+    int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t src = src_ids[i], dst = dst_ids[i];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            ++bad;
+            continue;
+        }
+        for (int64_t e = 0; e < per_block; ++e) {
+            k_pool[dst * per_block + e] = k_pool[src * per_block + e];
+            v_pool[dst * per_block + e] = v_pool[src * per_block + e];
+        }
+    }
+    return bad;
+}
+
 /* ---------------------------------------------------------- attention core */
 
 /* Softmax attention of one query over n contiguous rows, by the definition:

@@ -24,7 +24,7 @@ from . import _native
 from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV_BF16, PKV_F16,
                       PagedKVError, check, lib)
 
-__all__ = ["KVPool", "PagedKVError", "cache_write", "paged_decode_attention",
+__all__ = ["KVPool", "PagedKVError", "cache_write", "block_copy", "paged_decode_attention",
            "paged_decode_attention_noalloc",
            "decode_workspace_bytes", "status_check", "kv_bytes_per_token",
            "kv_blocks_for_tokens", "kv_pool_bytes", "default_split", "lib",
@@ -163,7 +163,47 @@ class KVPool:
         return slots
 
 
+    def fork(self, parent_row: np.ndarray, parent_len: int, child_row: np.ndarray) -> None:
+        """The child sequence's table row shares every block of the parent's."""
+        for r in (parent_row, child_row):
+            if not (r.dtype == np.int32 and r.flags.c_contiguous):
+                raise TypeError("table rows must be C-contiguous int32")
+        check(lib().kv_seq_fork(self.handle, _np_ptr(parent_row), int(parent_len),
+                                _np_ptr(child_row), child_row.shape[0]), "kv_seq_fork")
+
+    def append_slots_cow(self, seq_lens, num_new, block_tables: np.ndarray):
+        """append_slots with copy-on-write of shared tail blocks.
+        Returns (slots int64, copies int32 [n][2] as (shared, fresh))."""
+        lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        new = np.ascontiguousarray(num_new, dtype=np.int32)
+        if not (isinstance(block_tables, np.ndarray) and block_tables.dtype == np.int32
+                and block_tables.flags.c_contiguous and block_tables.ndim == 2):
+            raise TypeError("block_tables must be a C-contiguous int32 numpy array [S][max_blocks]")
+        S = len(lens)
+        slots = np.empty(int(new.sum()), dtype=np.int64)
+        src = np.empty(max(S, 1), dtype=np.int32)
+        dst = np.empty(max(S, 1), dtype=np.int32)
+        n = ctypes.c_int32()
+        check(lib().kv_append_slots_cow(self.handle, S, _np_ptr(lens), _np_ptr(new),
+                                        _np_ptr(block_tables), block_tables.shape[1],
+                                        _np_ptr(slots), _np_ptr(src), _np_ptr(dst),
+                                        ctypes.byref(n)), "kv_append_slots_cow")
+        return slots, np.stack([src[:n.value], dst[:n.value]], axis=1)
+
+
 # ------------------------------------------------------------------ device ops
+def block_copy(pool: KVPool, src_ids, dst_ids, status, k_pool=None, v_pool=None,
+               stream=None) -> None:
+    """Launch the block-copy kernel (int32 device tensors of block ids)."""
+    k_pool = pool.k_pool if k_pool is None else k_pool
+    v_pool = pool.v_pool if v_pool is None else v_pool
+    n = int(src_ids.shape[0])
+    if int(dst_ids.shape[0]) != n:
+        raise ValueError("src_ids and dst_ids differ in length")
+    check(lib().kv_block_copy(pool.handle, _t_ptr(src_ids), _t_ptr(dst_ids), n, _t_ptr(k_pool),
+                              _t_ptr(v_pool), _t_ptr(status), _stream(stream)), "kv_block_copy")
+
+
 def cache_write(pool: KVPool, k_new, v_new, slot_mapping, status, k_pool=None, v_pool=None,
                 stream=None) -> None:
     """Launch the cache-write kernel: rows of ``k_new``/``v_new`` [T][Hkv][D] (device)

@@ -39,6 +39,9 @@ SIGNATURES = [
     ("kv_block_refcount", ctypes.c_int, [_p, _i32, _pi32]),
     ("kv_pool_num_free", ctypes.c_int, [_p, _pi32]),
     ("kv_append_slots", ctypes.c_int, [_p, _i32, _p, _p, _p, _i32, _p]),
+    ("kv_seq_fork", ctypes.c_int, [_p, _p, _i32, _p, _i32]),
+    ("kv_append_slots_cow", ctypes.c_int, [_p, _i32, _p, _p, _p, _i32, _p, _p, _p, _pi32]),
+    ("kv_block_copy", ctypes.c_int, [_p, _p, _p, _i32, _p, _p, _p, _p]),
     ("kv_cache_write", ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _p, _p, _p]),
     ("paged_decode_workspace_bytes", _sz, [_i32, _i32, _i32, _i32, _i32]),
     ("paged_decode_attention", ctypes.c_int,

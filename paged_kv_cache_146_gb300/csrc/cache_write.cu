@@ -44,7 +44,52 @@ cache_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_
     }
 }
 
+// Copy-on-write: block dst[i] receives block src[i] (K and V, all kv heads),
+// 16 bytes per thread; pairs naming a block outside the pool are skipped and
+// flagged.  The destinations are fresh blocks, so pairs never overlap.
+__global__ void __launch_bounds__(256)
+block_copy_kernel(const int32_t *__restrict__ src, const int32_t *__restrict__ dst, int32_t n,
+                  int64_t chunks_per_block, int32_t num_blocks, uint4 *__restrict__ k_pool,
+                  uint4 *__restrict__ v_pool, int32_t *__restrict__ status)
+{
+    const int64_t total = (int64_t)n * chunks_per_block;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / chunks_per_block;
+        const int64_t c = e - i * chunks_per_block;
+        const int32_t a = __ldg(src + i), b = __ldg(dst + i);
+        if (a < 0 || a >= num_blocks || b < 0 || b >= num_blocks) {
+            if (c == 0) atomicOr(status, PKV_DEV_BAD_BLOCK);
+            continue;
+        }
+        k_pool[(int64_t)b * chunks_per_block + c] = k_pool[(int64_t)a * chunks_per_block + c];
+        v_pool[(int64_t)b * chunks_per_block + c] = v_pool[(int64_t)a * chunks_per_block + c];
+    }
+}
+
 }  // namespace
+
+extern "C" int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *dst_ids,
+                             int32_t n, void *k_pool, void *v_pool, int32_t *d_status,
+                             void *stream)
+{
+    pkv::PoolGeometry g;
+    if (!pkv::pool_geometry(pool, &g) || n < 0) return PKV_ERR_INVALID_ARG;
+    if (n == 0) return PKV_OK;
+    if (!src_ids || !dst_ids || !k_pool || !v_pool || !d_status) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(k_pool) || !pkv::aligned16(v_pool) || ((uintptr_t)src_ids & 3u) ||
+        ((uintptr_t)dst_ids & 3u) || ((uintptr_t)d_status & 3u))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)g.num_kv_heads * g.block_size * g.head_dim * 2;
+    if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    const int64_t chunks = block_bytes / 16;
+    const int threads = 256;
+    int64_t blocks = ((int64_t)n * chunks + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    block_copy_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        src_ids, dst_ids, n, chunks, g.num_blocks, (uint4 *)k_pool, (uint4 *)v_pool, d_status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 extern "C" int kv_cache_write(const pkv_pool *pool, const void *k_new, const void *v_new,
                               const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,

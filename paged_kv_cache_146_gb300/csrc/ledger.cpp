@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "pagedkv.h"
@@ -235,6 +236,89 @@ int kv_append_slots(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_lens,
             slot_mapping[t++] = (int64_t)row[pos / bs] * bs + pos % bs;
         }
     }
+    return PKV_OK;
+}
+
+int kv_seq_fork(pkv_pool *pool, const int32_t *parent_row, int32_t parent_len,
+                int32_t *child_row, int32_t max_blocks_per_seq)
+{
+    if (!pool || !parent_row || !child_row || parent_len < 0 || max_blocks_per_seq <= 0)
+        return PKV_ERR_INVALID_ARG;
+    const int64_t nb = (parent_len + (int64_t)pool->block_size - 1) / pool->block_size;
+    if (nb > max_blocks_per_seq) return PKV_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < nb; ++i) {
+        const int32_t id = parent_row[i];
+        if (id < 0 || id >= pool->num_blocks || pool->refs[(size_t)id] < 1) return PKV_ERR_BAD_BLOCK;
+    }
+    for (int64_t i = 0; i < nb; ++i) {
+        pool->refs[(size_t)parent_row[i]] += 1;
+        child_row[i] = parent_row[i];
+    }
+    for (int64_t i = nb; i < max_blocks_per_seq; ++i) child_row[i] = -1;
+    return PKV_OK;
+}
+
+int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_lens,
+                        const int32_t *num_new, int32_t *block_tables,
+                        int32_t max_blocks_per_seq, int64_t *slot_mapping, int32_t *copy_src,
+                        int32_t *copy_dst, int32_t *num_copies)
+{
+    if (!pool || num_seqs < 0 || max_blocks_per_seq <= 0 || !num_copies) return PKV_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!seq_lens || !num_new || !block_tables || !copy_src || !copy_dst))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t bs = pool->block_size;
+    // dry run: blocks needed, counting the copies the sharing will force; a
+    // shared tail loses one reference per copy taken from it, in sequence order
+    std::unordered_map<int32_t, int32_t> taken;
+    int64_t need = 0, total_new = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int64_t n0 = seq_lens[s], k = num_new[s];
+        if (n0 < 0 || k < 0) return PKV_ERR_INVALID_ARG;
+        if (n0 + k > (int64_t)max_blocks_per_seq * bs) return PKV_ERR_INVALID_ARG;
+        if (k > 0 && n0 % bs != 0) {
+            const int32_t tail = block_tables[(int64_t)s * max_blocks_per_seq + n0 / bs];
+            if (tail < 0 || tail >= pool->num_blocks || pool->refs[(size_t)tail] < 1)
+                return PKV_ERR_BAD_BLOCK;
+            int32_t &t = taken[tail];
+            if (pool->refs[(size_t)tail] - t > 1) {
+                ++t;
+                ++need;
+            }
+        }
+        need += (n0 + k + bs - 1) / bs - (n0 + bs - 1) / bs;
+        total_new += k;
+    }
+    if (total_new > 0 && !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (need > (int64_t)pool->stack.size()) return PKV_ERR_OUT_OF_BLOCKS;
+    int64_t t = 0;
+    int32_t copies = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+        const int64_t n0 = seq_lens[s];
+        if (num_new[s] > 0 && n0 % bs != 0) {
+            const int32_t tail = row[n0 / bs];
+            if (pool->refs[(size_t)tail] > 1) {   // copy on write
+                const int32_t fresh = pool->stack.back();
+                pool->stack.pop_back();
+                pool->refs[(size_t)fresh] = 1;
+                pool->refs[(size_t)tail] -= 1;
+                copy_src[copies] = tail;
+                copy_dst[copies] = fresh;
+                ++copies;
+                row[n0 / bs] = fresh;
+            }
+        }
+        for (int64_t pos = n0; pos < n0 + num_new[s]; ++pos) {
+            if (pos % bs == 0) {
+                const int32_t id = pool->stack.back();
+                pool->stack.pop_back();
+                pool->refs[(size_t)id] = 1;
+                row[pos / bs] = id;
+            }
+            slot_mapping[t++] = (int64_t)row[pos / bs] * bs + pos % bs;
+        }
+    }
+    *num_copies = copies;
     return PKV_OK;
 }
 

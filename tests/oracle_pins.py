@@ -187,6 +187,22 @@ def pin_cache_write_layout(o):
     assert bad == 1 and not kp2.any() and not vp2.any()
 
 
+def pin_block_copy(o):
+    """Copy-on-write block copy: the destination becomes the source bit for bit
+    (K and V, all heads and slots); other blocks are untouched; out-of-pool pairs
+    are counted and skipped."""
+    rng = np.random.default_rng(31)
+    shape = (6, 3, 4, 8)
+    kp = rng.integers(0, 65535, size=shape, dtype=np.uint16)
+    vp = rng.integers(0, 65535, size=shape, dtype=np.uint16)
+    k0, v0 = kp.copy(), vp.copy()
+    assert o.block_copy(kp, vp, [4, 0, 9], [1, 5, 2]) == 1
+    assert np.array_equal(kp[1], k0[4]) and np.array_equal(vp[1], v0[4])
+    assert np.array_equal(kp[5], k0[0]) and np.array_equal(vp[5], v0[0])
+    for b in (0, 2, 3, 4):
+        assert np.array_equal(kp[b], k0[b]) and np.array_equal(vp[b], v0[b])
+
+
 # ------------------------------------------------------------------ attention
 def pin_context_one(o):
     """A single cached token: weight exp(0) = 1, sum 1, so the output is V exactly."""
@@ -338,6 +354,7 @@ def pin_rejects_bad_input(o):
 
 
 ALL_PINS = [pin_number_formats, pin_sizing, pin_block_counting, pin_cache_write_layout,
+            pin_block_copy,
             pin_context_one, pin_context_zero, pin_uniform_keys, pin_two_tokens_closed_form,
             pin_large_scores, pin_gqa_grouping, pin_permutation_invariance, pin_bruteforce,
             pin_split_merge, pin_rejects_bad_input]

@@ -142,3 +142,81 @@ def test_trace_sized_pool_is_fast():
     per_step = (time.perf_counter() - t0) / 50
     assert per_step < 5e-3, per_step
     assert pool.num_free() == g["blocks"] - int(sum(-(-int(n) // 16) for n in lens))
+
+
+def test_parallel_sampling_copy_on_write_example():
+    """'Parallel Sampling decoding': samples A1 and A2 share the prompt's blocks
+    (physical 7 and 1, refcount 2); both write a different token into logical
+    block 1, so A1 copies it to a fresh block and block 1's count drops to 1;
+    A2, now its only user, writes in place; logical block 0 stays shared."""
+    ps = golden("pages_numbers.json")["parallel_sampling"]
+    order = ps["physical_of_logical"] + [i for i in range(8) if i not in ps["physical_of_logical"]]
+    pool = KVPool(8, 1, 64, "f16", block_size=4, free_order=order)
+    model = BlockLedger(8, 4, order)
+    t = np.full((2, 4), -1, dtype=np.int32)
+    tm = [[-1] * 4, [-1] * 4]
+    pool.append_slots([0, 0], [7, 0], t)
+    model.append([0, 0], [7, 0], tm)
+    pool.fork(t[0], 7, t[1])
+    model.fork(tm[0], 7, tm[1])
+    assert [pool.refcount(b) for b in ps["physical_of_logical"]] == [ps["refcount"]] * 2
+    slots, copies = pool.append_slots_cow([7, 7], [1, 1], t)          # "fathers" / "mothers"
+    slots_m, copies_m = model.append_cow([7, 7], [1, 1], tm)
+    assert slots.tolist() == slots_m and copies.tolist() == [list(c) for c in copies_m]
+    assert t.tolist() == tm
+    a1, a2 = t[0], t[1]
+    assert a1[0] == a2[0] == ps["physical_of_logical"][0]              # block 0 still shared
+    assert a2[1] == ps["physical_of_logical"][1] and a1[1] != a2[1]    # block 1 diverged
+    assert copies.tolist() == [[ps["physical_of_logical"][1], int(a1[1])]]
+    assert pool.refcount(int(a1[0])) == 2
+    assert pool.refcount(int(a2[1])) == 1 and pool.refcount(int(a1[1])) == 1
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_random_forks_match_model(seed):
+    rng = np.random.default_rng(seed)
+    n, bs, S, maxb = 128, int(rng.choice([4, 16])), 8, 16
+    order = rng.permutation(n)
+    pool = KVPool(n, 2, 64, "bf16", block_size=bs, free_order=order)
+    model = BlockLedger(n, bs, order)
+    lens = np.zeros(S, dtype=np.int32)
+    t = np.full((S, maxb), -1, dtype=np.int32)
+    tm = [[-1] * maxb for _ in range(S)]
+    for step in range(300):
+        op = rng.random()
+        if op < 0.15:                                   # fork a live sequence into an empty row
+            live = [s for s in range(S) if lens[s] > 0]
+            empty = [s for s in range(S) if lens[s] == 0]
+            if live and empty:
+                p, c = int(rng.choice(live)), int(rng.choice(empty))
+                pool.fork(t[p], int(lens[p]), t[c])
+                model.fork(tm[p], int(lens[p]), tm[c])
+                lens[c] = lens[p]
+        elif op < 0.75:
+            new = np.minimum(rng.integers(0, 2 * bs, size=S), maxb * bs - lens).astype(np.int32)
+            err_lib = err_mod = None
+            try:
+                slots, copies = pool.append_slots_cow(lens, new, t)
+            except PagedKVError as e:
+                err_lib = e.code
+            try:
+                slots_m, copies_m = model.append_cow(list(lens), list(new), tm)
+            except OutOfBlocks:
+                err_mod = -2
+            assert err_lib == err_mod
+            if err_lib is None:
+                assert slots.tolist() == slots_m
+                assert copies.tolist() == [list(c) for c in copies_m]
+                lens += new
+        else:
+            s = int(rng.integers(S))
+            nb = -(-int(lens[s]) // bs)
+            pool.free(t[s, :nb].copy())
+            model.free(list(t[s, :nb]))
+            lens[s] = 0
+            t[s, :] = -1
+            tm[s] = [-1] * maxb
+        assert t.tolist() == tm
+        assert pool.num_free() == model.num_free()
+        for b in range(n):
+            assert pool.refcount(b) == model.refcount(b)

@@ -47,6 +47,10 @@ MUTANTS = [
     ("accept_len_over_table", "if (n < 0 || n > (int64_t)max_blocks_per_seq * block_size) {",
      "if (n < 0) {"),
     ("accept_bad_block", "if (block < 0 || block >= num_blocks)", "if (block < 0)"),
+    ("copy_only_k", "            v_pool[dst * per_block + e] = v_pool[src * per_block + e];",
+     "            v_pool[dst * per_block + e] = v_pool[dst * per_block + e];"),
+    ("copy_short", "        for (int64_t e = 0; e < per_block; ++e) {\n            k_pool[dst",
+     "        for (int64_t e = 0; e < per_block - 1; ++e) {\n            k_pool[dst"),
     ("empty_not_zero", "if (n == 0) {\n        for (int32_t d = 0; d < D; ++d) out[d] = 0.0;",
      "if (n == 0) {\n        for (int32_t d = 0; d < D; ++d) out[d] = 1.0;"),
 ]
