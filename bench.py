@@ -34,6 +34,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV GB/s as % of GB300 HBM peak; seq-tokens/s"
+LENGTHS = {
+    "gqa_long": "clip(round(LogNormal(ln 4096, 1)), 64, 32768)",
+    "tiny": "{1, 17, 100, 33} + steps",
+    "opt13b": "U[128, 2048]",
+    "shared_prefix": "1024 shared + U[64, 512] private",
+}
 
 
 def peaks():
@@ -248,18 +254,37 @@ def our_arm(args, world, rank, local):
     torch.cuda.set_device(dev)
     e2e_steps = args.e2e_steps
     n_steps = args.warmup + args.steps + e2e_steps
-    w = rank_workload(args.seed, rank, args.num_seqs, n_steps + 16)
+    if args.workload == "gqa_long":
+        w = rank_workload(args.seed, rank, args.num_seqs, n_steps + 16)
+    else:
+        w = workloads.CONFIGS[args.workload](args.seed + rank)
+        # room for the timed steps' growth
+        need_b = -(-(int(w.prior_lens.max()) + n_steps + 16) // 16)
+        if need_b > w.max_blocks_per_seq:
+            w.max_blocks_per_seq = need_b
+        need = sum(-(-(int(x) + n_steps + 16) // 16) for x in w.prior_lens) + 64
+        if need > w.num_blocks:
+            w.num_blocks = need
+            w.free_order = np.random.default_rng(args.seed + 11).permutation(need).astype(np.int32)
     S, hq, hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     vals = workloads.device_values(w, dev)
     pool = KVPool(w.num_blocks, hkv, d, w.dtype, free_order=w.free_order, device=dev)
     eng = DecodeEngine(pool, S, hq, w.max_blocks_per_seq, w.scale, dev)
-    eng.prefill(vals["k_prompt"], vals["v_prompt"], w.prior_lens)
-    del vals["k_prompt"], vals["v_prompt"]
+    if w.shared_prefix_tokens:
+        first = np.zeros(S, dtype=np.int32)
+        first[0] = w.shared_prefix_tokens
+        eng.prefill(vals["k_shared"], vals["v_shared"], first)
+        eng.share_prefix(w.shared_prefix_tokens)
+        eng.prefill(vals["k_prompt"], vals["v_prompt"], w.prior_lens - w.shared_prefix_tokens)
+    else:
+        eng.prefill(vals["k_prompt"], vals["v_prompt"], w.prior_lens)
+    vals.clear()
     gen = torch.Generator(device=dev)
     gen.manual_seed(args.seed + 7 + rank)
+    tdt = torch.bfloat16 if w.is_bf16 else torch.float16
 
     def draw(*shape):
-        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(tdt)
 
     qs = [draw(S, hq, d) for _ in range(args.warmup + args.steps)]
     ks = [draw(S, hkv, d) for _ in range(args.warmup + args.steps)]
@@ -366,10 +391,11 @@ def our_arm(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "gqa_long", "num_seqs": S, "q_heads": hq, "kv_heads": hkv,
-                   "head_dim": d, "block_size": 16, "kv_dtype": "bf16",
-                   "lengths": "clip(round(LogNormal(ln 4096, 1)), 64, 32768)",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": S, "q_heads": hq, "kv_heads": hkv,
+                   "head_dim": d, "block_size": 16, "kv_dtype": w.dtype,
+                   "lengths": LENGTHS[args.workload],
+                   "shared_prefix_tokens": w.shared_prefix_tokens,
                    "mean_context": round(toks_total / args.steps / S, 1),
                    "pool_blocks": w.num_blocks,
                    "l2": "inputs larger than L2 (KV per step ~%.1f GB vs 129 MB L2)" % (bytes_per_launch / 1e9),
@@ -379,7 +405,8 @@ def our_arm(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": args.traffic if args.traffic is not None else (
-                         profiled_traffic() if (args.num_seqs, args.seed) == (256, 0) else None),
+                         profiled_traffic() if (args.workload, args.num_seqs, args.seed) == ("gqa_long", 256, 0)
+                         else None),
                      "peak_kind": peak_kind,
                      "kernel": "paged_decode_attention (prep + main + merge kernels)",
                      "bytes_per_launch": int(bytes_per_launch),
@@ -392,6 +419,57 @@ def our_arm(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def trace_arm(args, world, rank, local):
+    """Continuous-batching trace: 500 steps (or --steps) of FCFS admission,
+    prefill, decode and release; per-step attention GB/s (CUDA events around the
+    attention call) and whole-step wall time including the host ledger."""
+    import torch
+    from paged_kv_cache_146_gb300 import workloads
+    from paged_kv_cache_146_gb300.trace import TraceRunner
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    sched = workloads.trace(seed=5 + args.seed + rank)
+    steps = min(args.steps, sched.steps) if args.steps != 20 else sched.steps
+    order = np.random.default_rng(sched.seed).permutation(sched.num_blocks).astype(np.int32)
+    run = TraceRunner(sched, dev, free_order=order)
+    rates, walls, attn = [], [], []
+    t_all = time.perf_counter()
+    for t in range(steps):
+        t0 = time.perf_counter()
+        rec = run.step(t)
+        torch.cuda.synchronize()
+        walls.append(time.perf_counter() - t0)
+        e0, e1 = rec.extra["events"]
+        ms = e0.elapsed_time(e1)
+        if ms and rec.kv_bytes:
+            attn.append(ms)
+            rates.append(rec.kv_bytes / (ms * 1e-3) / 1e9)
+    total_s = time.perf_counter() - t_all
+    rc, word = run.check()
+    if rc != 0:
+        raise SystemExit(f"device status {rc} word {word:#x}")
+    if rank != 0:
+        return
+    peak, kind = peaks()
+    rates_sorted = sorted(rates)
+    line = {"metric": METRIC, "value": round(statistics.median(rates), 2), "unit": "GB/s",
+            "n_gpus": world, "steps": steps, "warmup": 0,
+            "ms_per_step": round(1e3 * statistics.median(walls), 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "trace", "arrivals_per_step": 8, "prompt": "U[64,1024]",
+                       "output": "Geometric(1/200) capped at 2048", "max_running": 512,
+                       "pool_blocks": sched.num_blocks,
+                       "value": "median over steps of attention GB/s"},
+            "p90_gbs": round(rates_sorted[int(0.9 * (len(rates) - 1))], 2),
+            "p10_gbs": round(rates_sorted[int(0.1 * (len(rates) - 1))], 2),
+            "pct_of_peak_median": round(100 * statistics.median(rates) / peak, 2),
+            "attention_ms_median": round(statistics.median(attn), 4),
+            "step_wall_ms_median": round(1e3 * statistics.median(walls), 4),
+            "step_wall_ms_p90": round(1e3 * sorted(walls)[int(0.9 * (len(walls) - 1))], 4),
+            "total_s": round(total_s, 2)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -399,6 +477,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--workload", default="gqa_long",
+                    choices=["gqa_long", "tiny", "opt13b", "shared_prefix", "trace"],
+                    help="gqa_long is the headline line; the others report their own config")
     ap.add_argument("--num-seqs", type=int, default=256,
                     help="sequences per GPU (256 is the workload; fewer only for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -412,6 +493,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         reference_arm(args, world, rank)
+    elif args.workload == "trace":
+        trace_arm(args, world, rank, local)
     else:
         our_arm(args, world, rank, local)
     if world > 1:

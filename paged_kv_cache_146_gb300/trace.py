@@ -117,8 +117,12 @@ class TraceRunner:
             cache_write(self.pool, k_new, v_new, d_slots, self.status)
         self.d_tables.copy_(torch.from_numpy(self.tables))
         self.d_ctx.copy_(torch.from_numpy(ctx))
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record()
         paged_decode_attention(self.pool, q, self.d_tables, self.d_ctx, self.scale,
                                self.workspace, self.status, out=self.out)
+        ev1.record()
         kv_bytes = int(ctx.astype(np.int64).sum()) * sc.num_kv_heads * sc.head_dim * 2 * 2
         # finished sequences give their blocks back
         finished = []
@@ -135,6 +139,7 @@ class TraceRunner:
             del self.state[r]
             self.free_rows.append(r)
         rec = StepRecord(t, admitted, decoding, finished, num_new, slots, ctx, kv_bytes)
+        rec.extra["events"] = (ev0, ev1)
         if keep_tensors:
             rec.q, rec.k_new, rec.v_new = q, k_new, v_new
             rec.out = self.out.clone()
