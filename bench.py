@@ -428,7 +428,8 @@ def trace_arm(args, world, rank, local):
     from paged_kv_cache_146_gb300.trace import TraceRunner
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-    sched = workloads.trace(seed=5 + args.seed + rank)
+    sched = workloads.trace(seed=5 + args.seed + rank,
+                            pool_bytes=int(args.pool_gib * 2**30) if args.pool_gib else 40 * 2**30)
     steps = min(args.steps, sched.steps) if args.steps != 20 else sched.steps
     order = np.random.default_rng(sched.seed).permutation(sched.num_blocks).astype(np.int32)
     run = TraceRunner(sched, dev, free_order=order)
@@ -466,7 +467,8 @@ def trace_arm(args, world, rank, local):
             "attention_ms_median": round(statistics.median(attn), 4),
             "step_wall_ms_median": round(1e3 * statistics.median(walls), 4),
             "step_wall_ms_p90": round(1e3 * sorted(walls)[int(0.9 * (len(walls) - 1))], 4),
-            "total_s": round(total_s, 2)}
+            "total_s": round(total_s, 2),
+            "swapped_gb": round(run.swapped_bytes / 1e9, 3)}
     print(json.dumps(line), flush=True)
 
 
@@ -480,6 +482,8 @@ def main():
     ap.add_argument("--workload", default="gqa_long",
                     choices=["gqa_long", "tiny", "opt13b", "shared_prefix", "trace"],
                     help="gqa_long is the headline line; the others report their own config")
+    ap.add_argument("--pool-gib", type=float, default=0.0,
+                    help="trace only: pool size (default 40 GiB); small pools force swapping")
     ap.add_argument("--num-seqs", type=int, default=256,
                     help="sequences per GPU (256 is the workload; fewer only for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)

@@ -208,6 +208,22 @@ int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_len
 int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *dst_ids,
                   int32_t n, void *k_pool, void *v_pool, int32_t *d_status, void *stream);
 
+/* ------------------------------------------------- swap to host (NEXT #4) */
+
+/* Swapping ("vLLM-and-PagedAttention-KR", "Scheduling": when blocks run out, a
+ * whole sequence -- the latest arrival -- is evicted and its KV blocks move to
+ * CPU memory; they come back when space frees up).  The device side packs the
+ * blocks into one contiguous staging buffer so the host copy is a single
+ * transfer, and unpacks a staging buffer into (other) blocks on the way back.
+ * staging layout: [n][2 (K, V)][num_kv_heads][block_size][head_dim], pool dtype,
+ * device memory, 16-byte aligned, 2 * n * block bytes.  ids: device int32 [n].
+ * Ids outside the pool are skipped and set PKV_DEV_BAD_BLOCK.  Asynchronous.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA. */
+int kv_gather_blocks(const pkv_pool *pool, const int32_t *ids, int32_t n, const void *k_pool,
+                     const void *v_pool, void *staging, int32_t *d_status, void *stream);
+int kv_scatter_blocks(const pkv_pool *pool, const int32_t *ids, int32_t n, const void *staging,
+                      void *k_pool, void *v_pool, int32_t *d_status, void *stream);
+
 /* ---------------------------------------------------------- cache write (a3) */
 
 /* Store num_tokens new tokens' K and V rows into their slots ("가장 기본적인

@@ -24,7 +24,8 @@ from . import _native
 from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV_BF16, PKV_F16,
                       PagedKVError, check, lib)
 
-__all__ = ["KVPool", "PagedKVError", "cache_write", "block_copy", "paged_decode_attention",
+__all__ = ["KVPool", "PagedKVError", "cache_write", "block_copy", "gather_blocks",
+           "scatter_blocks", "paged_decode_attention",
            "paged_decode_attention_noalloc",
            "decode_workspace_bytes", "status_check", "kv_bytes_per_token",
            "kv_blocks_for_tokens", "kv_pool_bytes", "default_split", "lib",
@@ -218,6 +219,25 @@ def cache_write(pool: KVPool, k_new, v_new, slot_mapping, status, k_pool=None, v
     check(lib().kv_cache_write(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping), T,
                                _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status), _stream(stream)),
           "kv_cache_write")
+
+
+def gather_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, stream=None):
+    """Pack blocks ``ids`` (int32 device tensor) into ``staging`` (device,
+    [n][2][Hkv][16][D] in the pool dtype) for one host copy (swap out)."""
+    k_pool = pool.k_pool if k_pool is None else k_pool
+    v_pool = pool.v_pool if v_pool is None else v_pool
+    check(lib().kv_gather_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(k_pool),
+                                 _t_ptr(v_pool), _t_ptr(staging), _t_ptr(status),
+                                 _stream(stream)), "kv_gather_blocks")
+
+
+def scatter_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, stream=None):
+    """Unpack ``staging`` into blocks ``ids`` (swap in)."""
+    k_pool = pool.k_pool if k_pool is None else k_pool
+    v_pool = pool.v_pool if v_pool is None else v_pool
+    check(lib().kv_scatter_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(staging),
+                                  _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status),
+                                  _stream(stream)), "kv_scatter_blocks")
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -42,6 +42,8 @@ SIGNATURES = [
     ("kv_seq_fork", ctypes.c_int, [_p, _p, _i32, _p, _i32]),
     ("kv_append_slots_cow", ctypes.c_int, [_p, _i32, _p, _p, _p, _i32, _p, _p, _p, _pi32]),
     ("kv_block_copy", ctypes.c_int, [_p, _p, _p, _i32, _p, _p, _p, _p]),
+    ("kv_gather_blocks", ctypes.c_int, [_p, _p, _i32, _p, _p, _p, _p, _p]),
+    ("kv_scatter_blocks", ctypes.c_int, [_p, _p, _i32, _p, _p, _p, _p, _p]),
     ("kv_cache_write", ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _p, _p, _p]),
     ("paged_decode_workspace_bytes", _sz, [_i32, _i32, _i32, _i32, _i32]),
     ("paged_decode_attention", ctypes.c_int,

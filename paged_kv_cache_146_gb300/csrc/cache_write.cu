@@ -67,7 +67,78 @@ block_copy_kernel(const int32_t *__restrict__ src, const int32_t *__restrict__ d
     }
 }
 
+// Swap staging: gather blocks ids[0..n) into staging [n][K|V][Hkv][16][D]
+// (to_staging = true) or scatter staging back into blocks ids (false).  One
+// thread per 16-byte chunk; out-of-pool ids are skipped and flagged.
+__global__ void __launch_bounds__(256)
+swap_kernel(const int32_t *__restrict__ ids, int32_t n, int64_t chunks_per_block, int32_t num_blocks,
+            uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, uint4 *__restrict__ staging,
+            bool to_staging, int32_t *__restrict__ status)
+{
+    const int64_t total = (int64_t)n * chunks_per_block;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / chunks_per_block;
+        const int64_t c = e - i * chunks_per_block;
+        const int32_t b = __ldg(ids + i);
+        if (b < 0 || b >= num_blocks) {
+            if (c == 0) atomicOr(status, PKV_DEV_BAD_BLOCK);
+            continue;
+        }
+        uint4 *sk = staging + (2 * i) * chunks_per_block + c;
+        uint4 *sv = sk + chunks_per_block;
+        uint4 *pk = k_pool + (int64_t)b * chunks_per_block + c;
+        uint4 *pv = v_pool + (int64_t)b * chunks_per_block + c;
+        if (to_staging) {
+            *sk = __ldcs(pk);
+            *sv = __ldcs(pv);
+        } else {
+            *pk = __ldcs(sk);
+            *pv = __ldcs(sv);
+        }
+    }
+}
+
 }  // namespace
+
+static int launch_swap(const pkv_pool *pool, const int32_t *ids, int32_t n, void *k_pool,
+                       void *v_pool, void *staging, bool to_staging, int32_t *d_status,
+                       void *stream)
+{
+    pkv::PoolGeometry g;
+    if (!pkv::pool_geometry(pool, &g) || n < 0) return PKV_ERR_INVALID_ARG;
+    if (n == 0) return PKV_OK;
+    if (!ids || !k_pool || !v_pool || !staging || !d_status) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(k_pool) || !pkv::aligned16(v_pool) || !pkv::aligned16(staging) ||
+        ((uintptr_t)ids & 3u) || ((uintptr_t)d_status & 3u))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)g.num_kv_heads * g.block_size * g.head_dim * 2;
+    if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    const int64_t chunks = block_bytes / 16;
+    const int threads = 256;
+    int64_t blocks = ((int64_t)n * chunks + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    swap_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+        ids, n, chunks, g.num_blocks, (uint4 *)k_pool, (uint4 *)v_pool, (uint4 *)staging,
+        to_staging, d_status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int kv_gather_blocks(const pkv_pool *pool, const int32_t *ids, int32_t n,
+                                const void *k_pool, const void *v_pool, void *staging,
+                                int32_t *d_status, void *stream)
+{
+    return launch_swap(pool, ids, n, const_cast<void *>(k_pool), const_cast<void *>(v_pool),
+                       staging, true, d_status, stream);
+}
+
+extern "C" int kv_scatter_blocks(const pkv_pool *pool, const int32_t *ids, int32_t n,
+                                 const void *staging, void *k_pool, void *v_pool,
+                                 int32_t *d_status, void *stream)
+{
+    return launch_swap(pool, ids, n, k_pool, v_pool, const_cast<void *>(staging), false,
+                       d_status, stream);
+}
 
 extern "C" int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *dst_ids,
                              int32_t n, void *k_pool, void *v_pool, int32_t *d_status,

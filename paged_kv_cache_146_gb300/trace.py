@@ -10,6 +10,12 @@ reached their output length release all their blocks ("vLLM-and-PagedAttention-K
 "가장 기본적인 decoding", step 5).  Blocks are taken on demand by the library's
 ledger in one ``kv_append_slots`` call per step.
 
+When the pool cannot give every running sequence its next block, the latest
+arrival is evicted whole and its blocks are swapped to pinned host memory
+(same page, "Scheduling": all-or-nothing eviction under FCFS, swapping to CPU
+memory, no new admissions until every evicted sequence is back); evicted
+sequences return, earliest arrival first, as soon as their blocks fit.
+
 Batch rows are fixed ([max_running] rows in every table and tensor); a row with
 context length 0 is idle, so the kernels see one shape for the whole run.
 """
@@ -20,8 +26,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import (KVPool, cache_write, decode_workspace_bytes, paged_decode_attention,
-               status_check)
+from . import (KVPool, cache_write, decode_workspace_bytes, gather_blocks,
+               paged_decode_attention, scatter_blocks, status_check)
 from .workloads import TraceSchedule
 
 
@@ -71,23 +77,86 @@ class TraceRunner:
         self.gen = torch.Generator(device=device)
         self.gen.manual_seed(sched.seed + 2000)
         self.scale = 1.0 / float(np.sqrt(sched.head_dim))
+        self.swapped = deque()                            # evicted: (state, length, host, ids)
+        self.swapped_bytes = 0
+        self.staging = torch.empty((self.maxb, 2, sched.num_kv_heads, bs, sched.head_dim),
+                                   dtype=tdt, device=device)
 
     def _draw(self, *shape):
         t = self.torch
         return t.randn(*shape, generator=self.gen, device=self.device,
                        dtype=t.float32).to(self.tdt)
 
+    # ------------------------------------------------------------ swapping
+    def _swap_out(self, row: int) -> tuple:
+        """Evict a whole sequence: pack its blocks on the device, copy them to
+        pinned host memory in one transfer, release the blocks."""
+        torch, bs = self.torch, self.sched.block_size
+        nb = -(-int(self.lens[row]) // bs)
+        ids = self.tables[row, :nb].copy()
+        d_ids = torch.from_numpy(ids).to(self.device)
+        staging = self.staging[:nb]
+        gather_blocks(self.pool, d_ids, staging, self.status)
+        host = torch.empty(staging.shape, dtype=self.tdt, pin_memory=True)
+        host.copy_(staging, non_blocking=True)
+        self.pool.free(ids)
+        rec = (self.state.pop(row), int(self.lens[row]), host, ids)
+        self.tables[row, :] = -1
+        self.lens[row] = 0
+        self.free_rows.append(row)
+        self.swapped_bytes += host.numel() * host.element_size()
+        return rec
+
+    def _swap_in(self, entry) -> tuple:
+        """Bring an evicted sequence back into fresh blocks of a free row."""
+        torch, bs = self.torch, self.sched.block_size
+        st, length, host, old_ids = entry
+        nb = -(-length // bs)
+        ids = self.pool.alloc(nb)
+        row = self.free_rows.popleft()
+        staging = self.staging[:nb]
+        staging.copy_(host, non_blocking=True)
+        scatter_blocks(self.pool, torch.from_numpy(ids).to(self.device), staging, self.status)
+        self.tables[row, :nb] = ids
+        self.lens[row] = length
+        self.state[row] = st
+        self.swapped_bytes += host.numel() * host.element_size()
+        return row, ids
+
+    def _growth(self, rows) -> int:
+        bs = self.sched.block_size
+        return sum(1 for r in rows if self.lens[r] % bs == 0)
+
     def step(self, t: int, keep_tensors: bool = False) -> StepRecord:
         torch, sc, bs = self.torch, self.sched, self.sched.block_size
         for prompt, out_len in sc.arrivals[t]:
             self.waiting.append((self.next_id, prompt, out_len))
             self.next_id += 1
+        swapped_in, swapped_out = [], []
+        # evicted sequences come back first, earliest arrival first, while their
+        # blocks and every running sequence's next block fit
+        while self.swapped and self.free_rows:
+            st, length, host, _ = self.swapped[0]
+            need = -(-length // bs) + (1 if length % bs == 0 else 0)
+            if need + self._growth(self.state) > self.pool.num_free():
+                break
+            self.swapped.popleft()
+            row, ids = self._swap_in((st, length, host, None))
+            swapped_in.append((row, st[0], ids))
         decoding = sorted(self.state)                     # rows running before this step
-        # FCFS admission while rows and blocks last (all of a prompt or nothing)
+        # out of blocks: evict the latest arrival, all of its blocks (FCFS)
+        while decoding and self._growth(decoding) > self.pool.num_free():
+            victim = max(decoding, key=lambda r: self.state[r][0])
+            entry = self._swap_out(victim)
+            swapped_out.append((victim, entry[0][0], entry[3]))
+            self.swapped.append(entry)
+            self.swapped = deque(sorted(self.swapped, key=lambda e: e[0][0]))
+            decoding.remove(victim)
+        # FCFS admission while rows and blocks last (all of a prompt or nothing);
+        # none while evicted sequences wait to come back
         admitted = []
-        free_blocks = self.pool.num_free() - sum(
-            1 for r in decoding if self.lens[r] % bs == 0)
-        while self.waiting and self.free_rows:
+        free_blocks = self.pool.num_free() - self._growth(decoding)
+        while self.waiting and self.free_rows and not self.swapped:
             rid, prompt, out_len = self.waiting[0]
             need = -(-prompt // bs)
             if need > free_blocks:
@@ -140,6 +209,8 @@ class TraceRunner:
             self.free_rows.append(r)
         rec = StepRecord(t, admitted, decoding, finished, num_new, slots, ctx, kv_bytes)
         rec.extra["events"] = (ev0, ev1)
+        rec.extra["swapped_in"] = swapped_in
+        rec.extra["swapped_out"] = swapped_out
         if keep_tensors:
             rec.q, rec.k_new, rec.v_new = q, k_new, v_new
             rec.out = self.out.clone()
