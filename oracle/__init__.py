@@ -55,6 +55,9 @@ def _declare(lib):
                                         c_i32, c_i32, c_i64, ctypes.c_int, c_dbl, p,
                                         ctypes.c_int]
     lib.oracle_paged_decode.restype = c_i64
+    lib.oracle_paged_prefill.argtypes = [p, p, p, p, c_i32, p, p, c_i32, c_i32, c_i32, c_i32,
+                                         c_i32, c_i64, ctypes.c_int, c_dbl, p, ctypes.c_int]
+    lib.oracle_paged_prefill.restype = c_i64
     lib.oracle_paged_partial.argtypes = [p, p, p, p, c_i32, c_i32, c_i32, c_i64, c_i64,
                                          c_i32, c_i32, c_i32, c_i32, c_i64, ctypes.c_int,
                                          c_dbl, p, p, p]
@@ -172,6 +175,25 @@ class Oracle:
                                            tables.shape[1], _ptr(lens), S, hq, hkv, d, bs,
                                            num_blocks, int(is_bf16), float(scale), _ptr(out),
                                            int(num_threads))
+        return out, bad
+
+    def paged_prefill(self, q, k_pool, v_pool, block_tables, query_start, context_lens, scale,
+                      is_bf16: bool, num_threads: int = 1):
+        """Chunked prefill: returns (out fp64 [T][Hq][D], number of rejected sequences)."""
+        q = _u16(q)
+        k_pool, v_pool = _u16(k_pool), _u16(v_pool)
+        tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        qs = np.ascontiguousarray(query_start, dtype=np.int32)
+        lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+        T, hq, d = q.shape
+        num_blocks, hkv, bs, _ = k_pool.shape
+        S = len(lens)
+        assert len(qs) == S + 1 and qs[-1] == T and tables.shape[0] == S
+        out = np.zeros((T, hq, d), dtype=np.float64)
+        bad = self.lib.oracle_paged_prefill(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(tables),
+                                            tables.shape[1], _ptr(qs), _ptr(lens), S, hq, hkv, d,
+                                            bs, num_blocks, int(is_bf16), float(scale),
+                                            _ptr(out), int(num_threads))
         return out, bad
 
     def paged_partial(self, q, k_pool, v_pool, block_tables, s, h, t0, t1, scale,

@@ -295,6 +295,71 @@ int64_t oracle_paged_decode(const uint16_t *q, const uint16_t *k_pool,
     return bad;
 }
 
+/* Chunked prefill by definition ("vLLM과 Ollama의 차이", chunked prefill: a long
+ * prompt is cut into chunks that join the decode batch; "LLM 추론 배칭 전략
+ * 정리" section 0: a prefill step processes the prompt's tokens together).
+ * Sequence s holds context_lens[s] tokens in the cache, the last C_s of which
+ * (C_s = query_start[s+1] - query_start[s]) are this chunk; its query row
+ * r = query_start[s] + j sits at position p = context_lens[s] - C_s + j and
+ * attends, as in any causal decoder, to the sequence's tokens 0..p, gathered
+ * through the block table.
+ *   q, out  [num_tokens][num_q_heads][head_dim] (out in fp64)
+ * Rows of a sequence with a bad length, chunk or table entry are zero and
+ * counted once per sequence in the return value. */
+int64_t oracle_paged_prefill(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             const int32_t *query_start, const int32_t *context_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                             int is_bf16, double scale, double *out, int num_threads)
+{
+    int32_t group = num_q_heads / num_kv_heads;
+    int64_t bad = 0;
+#ifdef _OPENMP
+    if (num_threads < 1) num_threads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(+ : bad)
+#endif
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int64_t r0 = query_start[s], r1 = query_start[s + 1];
+        int64_t C = r1 - r0, L = context_lens[s];
+        int ok = C >= 0 && L >= C && L <= (int64_t)max_blocks_per_seq * block_size;
+        double *K = NULL, *V = NULL, *x = NULL, *qv = NULL;
+        const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+        if (ok && C > 0) {
+            K = (double *)malloc(sizeof(double) * (size_t)(L * head_dim));
+            V = (double *)malloc(sizeof(double) * (size_t)(L * head_dim));
+            x = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+            qv = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        }
+        for (int32_t g = 0; ok && C > 0 && g < num_kv_heads; ++g) {
+            if (gather_sequence(k_pool, v_pool, row, L, g, num_kv_heads, head_dim, block_size,
+                                num_blocks, is_bf16, K, V) != 0) {
+                ok = 0;
+                break;
+            }
+            for (int32_t hh = 0; hh < group; ++hh) {
+                int32_t h = g * group + hh;
+                for (int64_t j = 0; j < C; ++j) {
+                    int64_t pos = L - C + j;
+                    int64_t r = r0 + j;
+                    for (int32_t d = 0; d < head_dim; ++d)
+                        qv[d] = to_double(q[(r * num_q_heads + h) * head_dim + d], is_bf16);
+                    attend_rows(qv, K, V, pos + 1, head_dim, scale, x,
+                                out + (r * num_q_heads + h) * head_dim, NULL, NULL, NULL);
+                }
+            }
+        }
+        if (!ok) {
+            ++bad;
+            for (int64_t r = r0; r < r1 && C > 0; ++r)
+                for (int64_t e = 0; e < (int64_t)num_q_heads * head_dim; ++e)
+                    out[r * num_q_heads * head_dim + e] = 0.0;
+        }
+        free(K); free(V); free(x); free(qv);
+    }
+    return bad;
+}
+
 /* One split of a sequence: attention pieces over logical tokens [t0, t1) of
  * sequence s, query head h: acc[D] = sum_j w_j v_j with w_j = exp(x_j - m),
  * m = max x_j, l = sum_j w_j.  An empty range gives m = -inf, l = 0, acc = 0. */

@@ -341,6 +341,52 @@ def pin_split_merge(o):
                 assert np.allclose(merged, full[s, h], rtol=1e-12, atol=1e-14), (s, h, cuts)
 
 
+def pin_prefill(o):
+    """Chunked prefill: each chunk query at position p equals plain causal
+    attention over the sequence's first p+1 tokens (numpy/scipy with an explicit
+    causal mask); a one-token chunk is the decode step; a fresh prompt's first
+    query returns V of token 0 exactly; a bad chunk length is rejected."""
+    lens = [37, 100, 1, 50]
+    chunks = [37, 20, 1, 1]                      # whole prompt, tail chunk, tiny, decode
+    p = Problem(o, lens, 8, 2, 64, True, seed=41)
+    rng = np.random.default_rng(42)
+    T = sum(chunks)
+    q = _bits(rng.standard_normal((T, 8, 64)), True)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    scale = 0.125
+    out, bad = o.paged_prefill(q, p.k_pool, p.v_pool, p.tables, qs, p.lens, scale, True, 2)
+    assert bad == 0
+    for s in range(4):
+        Kd = _values(p.K[s], True)
+        Vd = _values(p.V[s], True)
+        n, C = lens[s], chunks[s]
+        for j in range(C):
+            pos = n - C + j
+            for h in range(8):
+                qd = _values(q[qs[s] + j, h], True)
+                x = scale * (Kd[:, h // 4, :] @ qd)
+                x[np.arange(n) > pos] = -np.inf      # causal mask
+                ref = softmax(x) @ Vd[:, h // 4, :]
+                assert np.allclose(out[qs[s] + j, h], ref, rtol=1e-12, atol=1e-13), (s, j, h)
+    # first query of a fresh prompt sees token 0 only
+    for h in range(8):
+        assert np.array_equal(out[0, h], _values(p.V[0][0, h // 4], True))
+    # a one-token chunk is the decode step
+    dec = p.run(scale)
+    qd = q[qs[3]:qs[3] + 1]
+    out1, _ = o.paged_prefill(qd, p.k_pool, p.v_pool, p.tables[3:4], np.array([0, 1], np.int32),
+                              p.lens[3:4], scale, True)
+    p2 = p.q.copy()
+    p2[3] = qd[0]
+    dec2, _ = o.paged_decode(p2, p.k_pool, p.v_pool, p.tables, p.lens, scale, True)
+    assert np.array_equal(out1[0], dec2[3])
+    # a chunk longer than the context is rejected with zero rows
+    qs_bad = np.array([0, 38], np.int32)
+    out_b, bad = o.paged_prefill(q[:38], p.k_pool, p.v_pool, p.tables[:1], qs_bad, p.lens[:1],
+                                 scale, True)
+    assert bad == 1 and not out_b.any()
+
+
 def pin_rejects_bad_input(o):
     p = Problem(o, [20, 20], 2, 1, 64, False, seed=30)
     lens = p.lens.copy()
@@ -357,4 +403,4 @@ ALL_PINS = [pin_number_formats, pin_sizing, pin_block_counting, pin_cache_write_
             pin_block_copy,
             pin_context_one, pin_context_zero, pin_uniform_keys, pin_two_tokens_closed_form,
             pin_large_scores, pin_gqa_grouping, pin_permutation_invariance, pin_bruteforce,
-            pin_split_merge, pin_rejects_bad_input]
+            pin_split_merge, pin_prefill, pin_rejects_bad_input]

@@ -51,6 +51,12 @@ MUTANTS = [
      "            v_pool[dst * per_block + e] = v_pool[dst * per_block + e];"),
     ("copy_short", "        for (int64_t e = 0; e < per_block; ++e) {\n            k_pool[dst",
      "        for (int64_t e = 0; e < per_block - 1; ++e) {\n            k_pool[dst"),
+    ("prefill_not_causal", "attend_rows(qv, K, V, pos + 1, head_dim, scale, x,",
+     "attend_rows(qv, K, V, L, head_dim, scale, x,"),
+    ("prefill_causal_off_by_one", "attend_rows(qv, K, V, pos + 1, head_dim, scale, x,",
+     "attend_rows(qv, K, V, pos, head_dim, scale, x,"),
+    ("prefill_position_base", "int64_t pos = L - C + j;", "int64_t pos = j;"),
+    ("prefill_accepts_long_chunk", "int ok = C >= 0 && L >= C &&", "int ok = C >= 0 &&"),
     ("empty_not_zero", "if (n == 0) {\n        for (int32_t d = 0; d < D; ++d) out[d] = 0.0;",
      "if (n == 0) {\n        for (int32_t d = 0; d < D; ++d) out[d] = 1.0;"),
 ]
