@@ -419,6 +419,79 @@ def our_arm(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def prefill_arm(args, world, rank, local):
+    """Chunked-prefill attention: 16 prompts of 2048 tokens (GQA 32/8, D 128,
+    bf16) whose K/V are cached, attended in one call; causal flops over time."""
+    import torch
+    from paged_kv_cache_146_gb300 import (KVPool, cache_write, paged_prefill_attention,
+                                          prefill_workspace_bytes, workloads)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    S, P, hq, hkv, d = 16, 2048, 32, 8, 128
+    T = S * P
+    maxb = P // 16
+    rng = np.random.default_rng(args.seed + rank)
+    order = rng.permutation(S * maxb + 16).astype(np.int32)
+    pool = KVPool(S * maxb + 16, hkv, d, "bf16", free_order=order, device=dev)
+    tables = np.full((S, maxb), -1, dtype=np.int32)
+    slots = pool.append_slots(np.zeros(S, np.int32), np.full(S, P, np.int32), tables)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 17 + rank)
+    k = torch.randn(T, hkv, d, generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn(T, hkv, d, generator=gen, device=dev).to(torch.bfloat16)
+    q = torch.randn(T, hq, d, generator=gen, device=dev).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    cache_write(pool, k, v, torch.from_numpy(slots).to(dev), status)
+    d_tables = torch.from_numpy(tables).to(dev)
+    qs = torch.from_numpy(np.arange(0, T + 1, P, dtype=np.int32)).to(dev)
+    lens = torch.full((S,), P, dtype=torch.int32, device=dev)
+    ws = torch.empty(prefill_workspace_bytes(S, T, hq, hkv), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(d)
+
+    def call():
+        paged_prefill_attention(pool, q, d_tables, qs, lens, scale, ws, status, out=out)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    start.record()
+    for _ in range(args.steps):
+        call()
+    stop.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(stop) / args.steps, world)
+    rc, word = __import__("paged_kv_cache_146_gb300").status_check(status)
+    if rc != 0:
+        raise SystemExit(f"device status {rc} word {word:#x}")
+    if rank != 0:
+        return
+    # causal attention: each query at position p does 2*D flops per key for QK and
+    # for PV over p + 1 keys
+    flops = S * hq * 4 * d * (P * (P + 1) // 2)
+    tflops = flops * world / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        tpeak, tkind = float(pk["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        tpeak, tkind = 1900.0, "fallback"
+    line = {"metric": "chunked-prefill attention TFLOP/s", "value": round(tflops, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefill", "num_seqs": S, "prompt_tokens": P,
+                       "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
+                         "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                         "traffic": None, "peak_kind": tkind,
+                         "note": "mma.sync m16n8k16; 64 query rows per K/V block"},
+            "gpu_launches": 2 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def trace_arm(args, world, rank, local):
     """Continuous-batching trace: 500 steps (or --steps) of FCFS admission,
     prefill, decode and release; per-step attention GB/s (CUDA events around the
@@ -480,7 +553,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="gqa_long",
-                    choices=["gqa_long", "tiny", "opt13b", "shared_prefix", "trace"],
+                    choices=["gqa_long", "tiny", "opt13b", "shared_prefix", "trace", "prefill"],
                     help="gqa_long is the headline line; the others report their own config")
     ap.add_argument("--pool-gib", type=float, default=0.0,
                     help="trace only: pool size (default 40 GiB); small pools force swapping")
@@ -499,6 +572,8 @@ def main():
         reference_arm(args, world, rank)
     elif args.workload == "trace":
         trace_arm(args, world, rank, local)
+    elif args.workload == "prefill":
+        prefill_arm(args, world, rank, local)
     else:
         our_arm(args, world, rank, local)
     if world > 1:

@@ -287,6 +287,35 @@ int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *d_status, void *stream);
 
+/* ------------------------------------------ chunked-prefill attention (NEXT #2) */
+
+/* Workspace bytes paged_prefill_attention needs.  0 on a bad argument. */
+size_t paged_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                                     int32_t num_kv_heads);
+
+/* Attention of a chunk of prompt tokens per sequence over the paged cache
+ * ("vLLM과 Ollama의 차이": chunked prefill cuts a long prompt into chunks that
+ * run beside the decoding sequences; "LLM 추론 배칭 전략 정리", section 0).
+ * Sequence s's chunk is query rows query_start[s] .. query_start[s+1]-1 of q
+ * and out ([num_tokens][num_q_heads][head_dim], pool dtype, device); its K/V is
+ * already in the cache, which holds context_lens[s] tokens in total, the chunk
+ * last.  Query j of the chunk sits at position context_lens[s] - C_s + j and
+ * attends to the sequence's tokens 0..position (causal), gathered through
+ * block_tables like paged_decode_attention (a one-token chunk is a decode
+ * step).  query_start: device int32 [num_seqs + 1], non-decreasing, last entry
+ * num_tokens.  A sequence whose chunk is longer than its context or whose
+ * context exceeds its table row gets zero rows and PKV_DEV_BAD_LEN; bad table
+ * entries set PKV_DEV_BAD_BLOCK.  Requirements as paged_decode_attention
+ * (block_size 16, head_dim 64 or 128, G <= 16); workspace of
+ * paged_prefill_workspace_bytes(...) bytes, 256-byte aligned.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA. */
+int paged_prefill_attention(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
+                            const void *v_pool, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *query_start,
+                            const int32_t *context_lens, int32_t num_seqs, int32_t num_tokens,
+                            int32_t num_q_heads, float scale, void *workspace,
+                            size_t workspace_bytes, int32_t *d_status, void *stream);
+
 /* Default partition size (blocks) paged_decode_attention uses. */
 int32_t paged_decode_default_split(void);
 

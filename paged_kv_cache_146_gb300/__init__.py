@@ -26,7 +26,8 @@ from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV
 
 __all__ = ["KVPool", "PagedKVError", "cache_write", "block_copy", "gather_blocks",
            "scatter_blocks", "paged_decode_attention",
-           "paged_decode_attention_noalloc",
+           "paged_decode_attention_noalloc", "paged_prefill_attention",
+           "prefill_workspace_bytes",
            "decode_workspace_bytes", "status_check", "kv_bytes_per_token",
            "kv_blocks_for_tokens", "kv_pool_bytes", "default_split", "lib",
            "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN", "DEV_TIMEOUT"]
@@ -302,6 +303,33 @@ def paged_decode_attention_noalloc(pool: KVPool, q, block_tables, context_lens, 
                                               _t_ptr(context_lens), S, hq, float(scale),
                                               _t_ptr(status), _stream(stream))
     check(rc, "paged_decode_attention_noalloc")
+    return out
+
+
+def prefill_workspace_bytes(num_seqs: int, num_tokens: int, num_q_heads: int,
+                            num_kv_heads: int) -> int:
+    return lib().paged_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, num_kv_heads)
+
+
+def paged_prefill_attention(pool: KVPool, q, block_tables, query_start, context_lens,
+                            scale: float, workspace, status, out=None, k_pool=None, v_pool=None,
+                            stream=None):
+    """Chunked-prefill attention: ``q`` [T][Hq][D] device rows of all chunks,
+    ``query_start`` int32 device [S+1], ``context_lens`` int32 device [S]."""
+    import torch
+    k_pool = pool.k_pool if k_pool is None else k_pool
+    v_pool = pool.v_pool if v_pool is None else v_pool
+    T, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    S = int(context_lens.shape[0])
+    nbytes = workspace.numel() * workspace.element_size()
+    check(lib().paged_prefill_attention(pool.handle, _t_ptr(out), _t_ptr(q), _t_ptr(k_pool),
+                                        _t_ptr(v_pool), _t_ptr(block_tables),
+                                        int(block_tables.shape[1]), _t_ptr(query_start),
+                                        _t_ptr(context_lens), S, T, hq, float(scale),
+                                        _t_ptr(workspace), nbytes, _t_ptr(status),
+                                        _stream(stream)), "paged_prefill_attention")
     return out
 
 
