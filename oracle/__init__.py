@@ -58,6 +58,19 @@ def _declare(lib):
     lib.oracle_paged_prefill.argtypes = [p, p, p, p, c_i32, p, p, c_i32, c_i32, c_i32, c_i32,
                                          c_i32, c_i64, ctypes.c_int, c_dbl, p, ctypes.c_int]
     lib.oracle_paged_prefill.restype = c_i64
+    lib.oracle_f32_to_f16_bits.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_f16_bits.restype = ctypes.c_uint16
+    lib.oracle_quantize_q8.argtypes = [p, c_i64, ctypes.c_int, p, p]
+    lib.oracle_quantize_q8.restype = None
+    lib.oracle_q8_bytes_per_token.argtypes = [c_i32, c_i32, c_i32]
+    lib.oracle_q8_bytes_per_token.restype = c_i64
+    lib.oracle_cache_write_q8.argtypes = [p, p, p, c_i64, c_i32, c_i32, c_i32, c_i64,
+                                          ctypes.c_int, p, p, p, p]
+    lib.oracle_cache_write_q8.restype = c_i64
+    lib.oracle_paged_decode_q8.argtypes = [p, p, p, p, p, p, c_i32, p, c_i32, c_i32, c_i32,
+                                           c_i32, c_i32, c_i64, ctypes.c_int, c_dbl, p,
+                                           ctypes.c_int]
+    lib.oracle_paged_decode_q8.restype = c_i64
     lib.oracle_paged_partial.argtypes = [p, p, p, p, c_i32, c_i32, c_i32, c_i64, c_i64,
                                          c_i32, c_i32, c_i32, c_i32, c_i64, ctypes.c_int,
                                          c_dbl, p, p, p]
@@ -175,6 +188,49 @@ class Oracle:
                                            tables.shape[1], _ptr(lens), S, hq, hkv, d, bs,
                                            num_blocks, int(is_bf16), float(scale), _ptr(out),
                                            int(num_threads))
+        return out, bad
+
+    # -- 8-bit cache
+    def f32_to_f16_bits(self, x: float) -> int:
+        return self.lib.oracle_f32_to_f16_bits(float(x))
+
+    def quantize_q8(self, x, is_bf16: bool):
+        """Groups of 32 values -> (int8 codes, fp16 scale bits per group)."""
+        x = _u16(x).ravel()
+        assert x.size % 32 == 0
+        codes = np.zeros(x.size, dtype=np.int8)
+        scales = np.zeros(x.size // 32, dtype=np.uint16)
+        self.lib.oracle_quantize_q8(_ptr(x), x.size // 32, int(is_bf16), _ptr(codes),
+                                    _ptr(scales))
+        return codes, scales
+
+    def q8_bytes_per_token(self, layers, kv_heads, head_dim) -> int:
+        return self.lib.oracle_q8_bytes_per_token(layers, kv_heads, head_dim)
+
+    def cache_write_q8(self, k_new, v_new, slot_mapping, pools, block_size, is_bf16) -> int:
+        """pools = (k_codes, v_codes, k_scales, v_scales), modified in place."""
+        k_new, v_new = _u16(k_new), _u16(v_new)
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        kc, vc, ks, vs = pools
+        num_blocks, hkv, bs, d = kc.shape
+        assert bs == block_size and vc.shape == (num_blocks, hkv, d, bs)
+        return self.lib.oracle_cache_write_q8(_ptr(k_new), _ptr(v_new), _ptr(slots), len(slots),
+                                              hkv, d, bs, num_blocks, int(is_bf16), _ptr(kc),
+                                              _ptr(vc), _ptr(ks), _ptr(vs))
+
+    def paged_decode_q8(self, q, pools, block_tables, context_lens, scale, is_bf16: bool,
+                        num_threads: int = 1):
+        q = _u16(q)
+        kc, vc, ks, vs = pools
+        tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+        S, hq, d = q.shape
+        num_blocks, hkv, bs, _ = kc.shape
+        out = np.zeros((S, hq, d), dtype=np.float64)
+        bad = self.lib.oracle_paged_decode_q8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                              _ptr(tables), tables.shape[1], _ptr(lens), S, hq,
+                                              hkv, d, bs, num_blocks, int(is_bf16), float(scale),
+                                              _ptr(out), int(num_threads))
         return out, bad
 
     def paged_prefill(self, q, k_pool, v_pool, block_tables, query_start, context_lens, scale,

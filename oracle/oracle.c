@@ -165,6 +165,106 @@ int64_t oracle_block_copy(uint16_t *k_pool, uint16_t *v_pool, const int32_t *src
     return bad;
 }
 
+/* ------------------------------------------------------------ 8-bit KV cache */
+
+/* fp32 value -> IEEE binary16 bits, round to nearest, ties to even (finite,
+ * non-negative inputs below 65520).  Written from the format's definition. */
+uint16_t oracle_f32_to_f16_bits(float f)
+{
+    double a = fabs((double)f);
+    uint16_t sign = f < 0 ? 0x8000 : 0;
+    if (a == 0.0) return sign;
+    if (a < ldexp(1.0, -14))                       /* subnormal: units of 2^-24 */
+        return sign | (uint16_t)rint(a / ldexp(1.0, -24));
+    int e;
+    double m = frexp(a, &e);                       /* a = m * 2^e, m in [0.5, 1) */
+    double q = rint((2.0 * m - 1.0) * 1024.0);     /* 10 fraction bits of 1.f * 2^(e-1) */
+    int ex = e - 1 + 15;
+    if (q == 1024.0) { q = 0.0; ++ex; }
+    return sign | (uint16_t)(ex << 10) | (uint16_t)q;
+}
+
+/* 8-bit quantisation of groups of 32 values with one fp16 scale per group
+ * ("kv-cache-by-model", section 1: an 8-bit cache stores a separate scale for
+ * every group of 32 values, 53.1 % of the fp16 size).  Reading of the rule:
+ * amax = max |x|, d = fp16(min(amax / 127, 65504)), code = clamp(rint(x / d),
+ * -127, 127) in fp32 (codes 0 when d = 0); the value the cache holds is
+ * code * d. */
+void oracle_quantize_q8(const uint16_t *x, int64_t num_groups, int is_bf16, int8_t *codes,
+                        uint16_t *scales)
+{
+    for (int64_t gi = 0; gi < num_groups; ++gi) {
+        const uint16_t *xs = x + gi * 32;
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float v = (float)to_double(xs[i], is_bf16);
+            if (fabsf(v) > amax) amax = fabsf(v);
+        }
+        float d32 = amax / 127.0f;
+        if (d32 > 65504.0f) d32 = 65504.0f;
+        uint16_t h = oracle_f32_to_f16_bits(d32);
+        float dq = (float)oracle_f16_to_double(h);
+        scales[gi] = h;
+        for (int i = 0; i < 32; ++i) {
+            float v = (float)to_double(xs[i], is_bf16);
+            int c = 0;
+            if (dq != 0.0f) {
+                float r = rintf(v / dq);
+                c = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);
+            }
+            codes[gi * 32 + i] = (int8_t)c;
+        }
+    }
+}
+
+/* Bytes per token of an 8-bit cache: 2 (K, V) x kv_heads x layers x
+ * (head_dim one-byte codes + head_dim / 32 two-byte scales). */
+int64_t oracle_q8_bytes_per_token(int32_t layers, int32_t kv_heads, int32_t head_dim)
+{
+    return (int64_t)kv_heads * 2 * layers * (head_dim + head_dim / 32 * 2);
+}
+
+/* Cache write into an 8-bit pool.  Layouts (per (block, kv head) slab):
+ *   k_codes [num_blocks][Hkv][block_size][head_dim]   (token rows)
+ *   v_codes [num_blocks][Hkv][head_dim][block_size]   (dimension rows)
+ *   k_scales, v_scales [num_blocks][Hkv][block_size][head_dim / 32]
+ * Slots as in oracle_cache_write.  Returns the number of out-of-pool slots. */
+int64_t oracle_cache_write_q8(const uint16_t *k_new, const uint16_t *v_new,
+                              const int64_t *slot_mapping, int64_t num_tokens,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, int is_bf16, int8_t *k_codes, int8_t *v_codes,
+                              uint16_t *k_scales, uint16_t *v_scales)
+{
+    int64_t bad = 0;
+    int32_t ng = head_dim / 32;
+    int8_t *kc = (int8_t *)malloc((size_t)head_dim);
+    int8_t *vc = (int8_t *)malloc((size_t)head_dim);
+    uint16_t *ks = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)ng);
+    uint16_t *vs = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)ng);
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) { ++bad; continue; }
+        int64_t block = slot / block_size, offset = slot % block_size;
+        for (int32_t g = 0; g < num_kv_heads; ++g) {
+            int64_t src = (t * num_kv_heads + g) * head_dim;
+            oracle_quantize_q8(k_new + src, ng, is_bf16, kc, ks);
+            oracle_quantize_q8(v_new + src, ng, is_bf16, vc, vs);
+            int64_t slab = block * num_kv_heads + g;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                k_codes[(slab * block_size + offset) * head_dim + d] = kc[d];
+                v_codes[(slab * head_dim + d) * block_size + offset] = vc[d];
+            }
+            for (int32_t i = 0; i < ng; ++i) {
+                k_scales[(slab * block_size + offset) * ng + i] = ks[i];
+                v_scales[(slab * block_size + offset) * ng + i] = vs[i];
+            }
+        }
+    }
+    free(kc); free(vc); free(ks); free(vs);
+    return bad;
+}
+
 /* ---------------------------------------------------------- attention core */
 
 /* Softmax attention of one query over n contiguous rows, by the definition:
@@ -354,6 +454,77 @@ int64_t oracle_paged_prefill(const uint16_t *q, const uint16_t *k_pool, const ui
             for (int64_t r = r0; r < r1 && C > 0; ++r)
                 for (int64_t e = 0; e < (int64_t)num_q_heads * head_dim; ++e)
                     out[r * num_q_heads * head_dim + e] = 0.0;
+        }
+        free(K); free(V); free(x); free(qv);
+    }
+    return bad;
+}
+
+/* Gather a sequence's dequantized K/V (code * scale, exact in fp64) from an
+ * 8-bit pool for kv head g.  Returns -1 when a table entry is outside the pool. */
+static int gather_sequence_q8(const int8_t *k_codes, const int8_t *v_codes,
+                              const uint16_t *k_scales, const uint16_t *v_scales,
+                              const int32_t *table_row, int64_t n, int32_t g,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, double *K, double *V)
+{
+    int32_t ng = head_dim / 32;
+    for (int64_t j = 0; j < n; ++j) {
+        int64_t logical = j / block_size;          /* logical block of token j */
+        int64_t block = table_row[logical];
+        int64_t offset = j - logical * block_size;
+        if (block >= num_blocks || block < 0) return -1;
+        int64_t slab = block * num_kv_heads + g;
+        for (int32_t d = 0; d < head_dim; ++d) {
+            double ks = oracle_f16_to_double(k_scales[(slab * block_size + offset) * ng + d / 32]);
+            double vs = oracle_f16_to_double(v_scales[(slab * block_size + offset) * ng + d / 32]);
+            K[j * head_dim + d] = ks * k_codes[(slab * block_size + offset) * head_dim + d];
+            V[j * head_dim + d] = vs * v_codes[(slab * head_dim + d) * block_size + offset];
+        }
+    }
+    return 0;
+}
+
+/* PagedAttention decode over an 8-bit cache: the definition of
+ * oracle_paged_decode with K and V taken as code * scale. */
+int64_t oracle_paged_decode_q8(const uint16_t *q, const int8_t *k_codes, const int8_t *v_codes,
+                               const uint16_t *k_scales, const uint16_t *v_scales,
+                               const int32_t *block_tables, int32_t max_blocks_per_seq,
+                               const int32_t *context_lens, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int64_t num_blocks, int is_bf16,
+                               double scale, double *out, int num_threads)
+{
+    int32_t group = num_q_heads / num_kv_heads;
+    int64_t bad = 0;
+    int64_t rows = (int64_t)num_seqs * num_q_heads;
+#ifdef _OPENMP
+    if (num_threads < 1) num_threads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(+ : bad)
+#endif
+    for (int64_t r = 0; r < rows; ++r) {
+        int32_t s = (int32_t)(r / num_q_heads), h = (int32_t)(r % num_q_heads);
+        int32_t kv_head = h / group;
+        int64_t n = context_lens[s];
+        double *o = out + r * head_dim;
+        if (n < 0 || n > (int64_t)block_size * max_blocks_per_seq) {
+            for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+            if (h == 0) ++bad;
+            continue;
+        }
+        double *K = (double *)malloc(sizeof(double) * (size_t)(n * head_dim + 1));
+        double *V = (double *)malloc(sizeof(double) * (size_t)(n * head_dim + 1));
+        double *x = (double *)malloc(sizeof(double) * (size_t)(n + 1));
+        double *qv = (double *)malloc(sizeof(double) * (size_t)head_dim);
+        const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+        if (gather_sequence_q8(k_codes, v_codes, k_scales, v_scales, row, n, kv_head, num_kv_heads,
+                               head_dim, block_size, num_blocks, K, V) != 0) {
+            for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+            if (h == 0) ++bad;
+        } else {
+            for (int32_t d = 0; d < head_dim; ++d)
+                qv[d] = to_double(q[r * head_dim + d], is_bf16);
+            attend_rows(qv, K, V, n, head_dim, scale, x, o, NULL, NULL, NULL);
         }
         free(K); free(V); free(x); free(qv);
     }

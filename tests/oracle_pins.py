@@ -387,6 +387,108 @@ def pin_prefill(o):
     assert bad == 1 and not out_b.any()
 
 
+def pin_f32_to_f16(o):
+    """fp32 -> fp16 rounding (nearest, ties to even) against numpy's conversion,
+    over random magnitudes, exact halfway cases and subnormals."""
+    rng = np.random.default_rng(51)
+    xs = np.concatenate([
+        (rng.standard_normal(4000) * 3).astype(np.float32),
+        (rng.random(2000) * 60000).astype(np.float32),
+        (rng.random(2000) * 2e-5).astype(np.float32),                      # subnormal range
+        (np.arange(1024, 2048, dtype=np.float32) + 0.5) * np.float32(2.0**-10),  # ties
+        np.array([0.0, 2.0**-24, 2.0**-25, 3 * 2.0**-25, 65504.0, 2.0**-14], dtype=np.float32)])
+    ref = xs.astype(np.float16).view(np.uint16)
+    for x, r in zip(xs, ref):
+        assert o.f32_to_f16_bits(float(x)) == int(r), (float(x), hex(int(r)))
+
+
+def pin_quantize_q8(o):
+    """One fp16 scale per 32 values, 53.1 % of fp16 ("kv-cache-by-model" §1);
+    exact codes when the scale is a power of two; ties to even; zero groups;
+    round-trip error at most half a step."""
+    g = golden("pages_numbers.json")
+    # sizes: Qwen3-8B at 32K, 4,608 MiB in f16 -> 2,448 MiB in 8-bit
+    assert o.q8_bytes_per_token(36, 8, 128) * 32768 == 2448 * 2**20
+    assert o.q8_bytes_per_token(36, 8, 128) * 64 == o.kv_bytes_per_token(36, 8, 128, 2) * 34
+    k = np.arange(-16, 16, dtype=np.float32)
+    k[0] = -127                                              # amax 127 steps
+    x = _bits(k * np.float32(2.0**-6), False)
+    codes, scales = o.quantize_q8(x, False)
+    assert scales.tolist() == [0x2400] and codes.tolist() == k.astype(int).tolist()
+    t = np.zeros(32, dtype=np.float32)
+    t[0] = 127 * 2.0**-4
+    t[1], t[2], t[3] = 2.5 * 2.0**-4, 3.5 * 2.0**-4, -2.5 * 2.0**-4
+    codes, scales = o.quantize_q8(_bits(t, False), False)
+    assert codes[1:4].tolist() == [2, 4, -2]                # ties to even
+    codes, scales = o.quantize_q8(np.zeros(32, np.uint16), True)
+    assert scales.tolist() == [0] and not codes.any()
+    # a tiny group: amax / 127 ~ 2.4 * 2^-24 rounds to the fp16 subnormal 2 * 2^-24,
+    # so amax / scale ~ 151 and the code must saturate at 127
+    tiny = np.zeros(32, dtype=np.float32)
+    tiny[0], tiny[1] = 127 * 2.4 * 2.0**-24, -60 * 2.0**-24
+    codes, scales = o.quantize_q8(_bits(tiny, True), True)
+    assert scales.tolist() == [2] and codes[0] == 127 and codes[1] == -30
+    rng = np.random.default_rng(52)
+    for bf in (False, True):
+        xb = _bits(rng.standard_normal(32 * 64) * 2, bf)
+        codes, scales = o.quantize_q8(xb, bf)
+        xv = _values(xb, bf).reshape(64, 32)
+        d = scales.view(np.float16).astype(np.float64)[:, None]
+        err = np.abs(xv - codes.reshape(64, 32) * d)
+        assert (np.abs(codes) <= 127).all()
+        assert (err <= d / 2 + 1e-12).all()
+        assert np.allclose(d[:, 0], np.abs(xv).max(axis=1) / 127, rtol=2**-10)
+
+
+def _q8_problem(o, lens, hq, hkv, d, bf, seed):
+    p = Problem(o, lens, hq, hkv, d, bf, seed=seed)
+    nb = p.num_blocks
+    pools = (np.zeros((nb, hkv, 16, d), np.int8), np.zeros((nb, hkv, d, 16), np.int8),
+             np.zeros((nb, hkv, 16, d // 32), np.uint16), np.zeros((nb, hkv, 16, d // 32), np.uint16))
+    slots = []
+    for s, n in enumerate(p.lens):
+        for j in range(int(n)):
+            slots.append(p.tables[s][j // 16] * 16 + j % 16)
+    k_rows = np.concatenate([k for k in p.K if len(k)], axis=0)
+    v_rows = np.concatenate([v for v in p.V if len(v)], axis=0)
+    assert o.cache_write_q8(k_rows, v_rows, np.array(slots, np.int64), pools, 16, bf) == 0
+    return p, pools
+
+
+def pin_q8_layout_and_attention(o):
+    """Hand-worked 8-bit layout (golden/q8_layout.json); context 1 returns the
+    dequantized V exactly; attention matches numpy/scipy on dequantized K/V."""
+    g = golden("q8_layout.json")
+    nb, hkv, bs, d = g["num_blocks"], g["num_kv_heads"], g["block_size"], g["head_dim"]
+    pools = (np.zeros((nb, hkv, bs, d), np.int8), np.zeros((nb, hkv, d, bs), np.int8),
+             np.zeros((nb, hkv, bs, d // 32), np.uint16), np.zeros((nb, hkv, bs, d // 32), np.uint16))
+    assert o.cache_write_q8(np.array(g["k_new_bits"], np.uint16), np.array(g["v_new_bits"], np.uint16),
+                            np.array(g["slot_mapping"], np.int64), pools, bs, False) == 0
+    assert pools[0].tolist() == g["expected_k_codes"]
+    assert pools[1].tolist() == g["expected_v_codes"]
+    assert pools[2][1, 0, 1, 0] == pools[3][0, 0, 0, 0] == g["expected_scale_bits"]
+    for bf in (False, True):
+        p, pools = _q8_problem(o, [1, 40, 77], 8, 2, 128, bf, seed=53)
+        scale = 1 / np.sqrt(128)
+        out, bad = o.paged_decode_q8(p.q, pools, p.tables, p.lens, scale, bf)
+        assert bad == 0
+        kc, vc, ks, vs = pools
+        for s in range(3):
+            ids = [p.tables[s][j // 16] for j in range(int(p.lens[s]))]
+            offs = [j % 16 for j in range(int(p.lens[s]))]
+            for h in range(8):
+                gh = h // 4
+                Kd = np.array([kc[b, gh, f] * ks[b, gh, f].view(np.float16).astype(np.float64).repeat(32)
+                               for b, f in zip(ids, offs)])
+                Vd = np.array([vc[b, gh, :, f] * vs[b, gh, f].view(np.float16).astype(np.float64).repeat(32)
+                               for b, f in zip(ids, offs)])
+                qd = _values(p.q[s, h], bf)
+                ref = softmax(scale * (Kd @ qd)) @ Vd
+                assert np.allclose(out[s, h], ref, rtol=1e-12, atol=1e-13), (bf, s, h)
+                if s == 0:
+                    assert np.array_equal(out[s, h], Vd[0])
+
+
 def pin_rejects_bad_input(o):
     p = Problem(o, [20, 20], 2, 1, 64, False, seed=30)
     lens = p.lens.copy()
@@ -403,4 +505,5 @@ ALL_PINS = [pin_number_formats, pin_sizing, pin_block_counting, pin_cache_write_
             pin_block_copy,
             pin_context_one, pin_context_zero, pin_uniform_keys, pin_two_tokens_closed_form,
             pin_large_scores, pin_gqa_grouping, pin_permutation_invariance, pin_bruteforce,
-            pin_split_merge, pin_prefill, pin_rejects_bad_input]
+            pin_split_merge, pin_prefill, pin_f32_to_f16, pin_quantize_q8,
+            pin_q8_layout_and_attention, pin_rejects_bad_input]

@@ -57,6 +57,16 @@ MUTANTS = [
      "attend_rows(qv, K, V, pos, head_dim, scale, x,"),
     ("prefill_position_base", "int64_t pos = L - C + j;", "int64_t pos = j;"),
     ("prefill_accepts_long_chunk", "int ok = C >= 0 && L >= C &&", "int ok = C >= 0 &&"),
+    ("q8_gqa_modulo", "int32_t kv_head = h / group;", "int32_t kv_head = h % num_kv_heads;"),
+    ("q8_no_127", "float d32 = amax / 127.0f;", "float d32 = amax / 128.0f;"),
+    ("q8_floor", "float r = rintf(v / dq);", "float r = floorf(v / dq);"),
+    ("q8_no_clamp", "c = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);", "c = (int)r;"),
+    ("q8_v_not_transposed", "v_codes[(slab * head_dim + d) * block_size + offset] = vc[d];",
+     "v_codes[(slab * block_size + offset) * head_dim + d] = vc[d];"),
+    ("q8_scale_group", "k_scales[(slab * block_size + offset) * ng + d / 32]",
+     "k_scales[(slab * block_size + offset) * ng]"),
+    ("f16_ties_away", "double q = rint((2.0 * m - 1.0) * 1024.0);",
+     "double q = floor((2.0 * m - 1.0) * 1024.0 + 0.5);"),
     ("empty_not_zero", "if (n == 0) {\n        for (int32_t d = 0; d < D; ++d) out[d] = 0.0;",
      "if (n == 0) {\n        for (int32_t d = 0; d < D; ++d) out[d] = 1.0;"),
 ]
