@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention: KV GB/s as % of GB300 HBM peak; seq-tokens/s"
 LENGTHS = {
     "gqa_long": "clip(round(LogNormal(ln 4096, 1)), 64, 32768)",
+    "gqa_long_q8": "clip(round(LogNormal(ln 4096, 1)), 64, 32768)",
     "tiny": "{1, 17, 100, 33} + steps",
     "opt13b": "U[128, 2048]",
     "shared_prefix": "1024 shared + U[64, 512] private",
@@ -175,7 +176,7 @@ class OracleSample:
     """The oracle (fp64 C, all host cores) on the first ``k`` sequences of the
     workload: the same length law, shapes and dtype, bounded in size."""
 
-    def __init__(self, seed: int, k: int):
+    def __init__(self, seed: int, k: int, q8: bool = False):
         import oracle
         from oracle.allocator_model import BlockLedger
         from paged_kv_cache_146_gb300 import workloads
@@ -189,34 +190,49 @@ class OracleSample:
         slots_p = led.append([0] * k, [int(x) for x in w.prior_lens], tables)
         slots_n = led.append([int(x) for x in w.prior_lens], [1] * k, tables)
         shape = (w.num_blocks, w.num_kv_heads, 16, w.head_dim)
-        self.kp = np.zeros(shape, dtype=np.uint16)
-        self.vp = np.zeros(shape, dtype=np.uint16)
-        self.o.cache_write(v["k_prompt"], v["v_prompt"], np.array(slots_p, dtype=np.int64),
-                           self.kp, self.vp, 16)
-        self.o.cache_write(v["k_new"], v["v_new"], np.array(slots_n, dtype=np.int64),
-                           self.kp, self.vp, 16)
+        self.q8 = q8
+        if q8:      # 8-bit cache: codes and fp16 scales written by the oracle's quantiser
+            nb, hkv, d = w.num_blocks, w.num_kv_heads, w.head_dim
+            self.pools = (np.zeros(shape, np.int8), np.zeros((nb, hkv, d, 16), np.int8),
+                          np.zeros((nb, hkv, 16, d // 32), np.uint16),
+                          np.zeros((nb, hkv, 16, d // 32), np.uint16))
+            for kr, vr, sl in ((v["k_prompt"], v["v_prompt"], slots_p),
+                               (v["k_new"], v["v_new"], slots_n)):
+                self.o.cache_write_q8(kr, vr, np.array(sl, dtype=np.int64), self.pools, 16, True)
+        else:
+            self.kp = np.zeros(shape, dtype=np.uint16)
+            self.vp = np.zeros(shape, dtype=np.uint16)
+            self.o.cache_write(v["k_prompt"], v["v_prompt"], np.array(slots_p, dtype=np.int64),
+                               self.kp, self.vp, 16)
+            self.o.cache_write(v["k_new"], v["v_new"], np.array(slots_n, dtype=np.int64),
+                               self.kp, self.vp, 16)
         self.w, self.q = w, v["q"]
         self.tables = np.array(tables, dtype=np.int32)
         self.lens = (w.prior_lens + 1).astype(np.int32)
         self.tokens = int(self.lens.astype(np.int64).sum())
-        self.nbytes = self.tokens * w.num_kv_heads * w.head_dim * 2 * 2 + \
+        per_head = 2 * (w.head_dim + w.head_dim // 16) if q8 else w.head_dim * 2 * 2
+        self.nbytes = self.tokens * w.num_kv_heads * per_head + \
             2 * k * w.num_q_heads * w.head_dim * 2 + \
             4 * int(sum(-(-int(n) // 16) for n in self.lens)) + 4 * k
         self.desc = f"first {k} of 256 sequences ({self.tokens} context tokens), one decode call"
 
     def run(self) -> float:
         t0 = time.perf_counter()
-        self.o.paged_decode(self.q, self.kp, self.vp, self.tables, self.lens, self.w.scale, True,
-                            self.threads)
+        if self.q8:
+            self.o.paged_decode_q8(self.q, self.pools, self.tables, self.lens, self.w.scale, True,
+                                   self.threads)
+        else:
+            self.o.paged_decode(self.q, self.kp, self.vp, self.tables, self.lens, self.w.scale,
+                                True, self.threads)
         return time.perf_counter() - t0
 
 
-def oracle_calibrated(seed: int, target_s: float) -> OracleSample:
+def oracle_calibrated(seed: int, target_s: float, q8: bool = False) -> OracleSample:
     """An oracle sample whose one call takes about ``target_s`` seconds."""
-    probe = OracleSample(seed, 2)
+    probe = OracleSample(seed, 2, q8)
     dt = probe.run()
     k = int(min(256, max(2, round(2 * target_s / max(dt, 1e-3)))))
-    return OracleSample(seed, k)
+    return OracleSample(seed, k, q8)
 
 
 def reference_arm(args, world, rank):
@@ -254,7 +270,8 @@ def our_arm(args, world, rank, local):
     torch.cuda.set_device(dev)
     e2e_steps = args.e2e_steps
     n_steps = args.warmup + args.steps + e2e_steps
-    if args.workload == "gqa_long":
+    q8 = args.workload == "gqa_long_q8"
+    if args.workload in ("gqa_long", "gqa_long_q8"):
         w = rank_workload(args.seed, rank, args.num_seqs, n_steps + 16)
     else:
         w = workloads.CONFIGS[args.workload](args.seed + rank)
@@ -268,7 +285,8 @@ def our_arm(args, world, rank, local):
             w.free_order = np.random.default_rng(args.seed + 11).permutation(need).astype(np.int32)
     S, hq, hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     vals = workloads.device_values(w, dev)
-    pool = KVPool(w.num_blocks, hkv, d, w.dtype, free_order=w.free_order, device=dev)
+    pool = KVPool(w.num_blocks, hkv, d, "q8_" + w.dtype if q8 else w.dtype,
+                  free_order=w.free_order, device=dev)
     eng = DecodeEngine(pool, S, hq, w.max_blocks_per_seq, w.scale, dev)
     if w.shared_prefix_tokens:
         first = np.zeros(S, dtype=np.int32)
@@ -293,11 +311,10 @@ def our_arm(args, world, rank, local):
 
     def step(i, ev=None):
         eng.host_step()
-        cache_write(pool, ks[i], vs[i], eng.d_slots, eng.status)
+        eng.write(ks[i], vs[i])
         if ev:
             ev[0].record(stream)
-        paged_decode_attention(pool, qs[i], eng.d_tables, eng.d_lens, w.scale, eng.workspace,
-                               eng.status, out=eng.out)
+        eng.attend(qs[i])
         if ev:
             ev[1].record(stream)
 
@@ -382,7 +399,7 @@ def our_arm(args, world, rank, local):
         return
     cpu = None
     if args.cpu_seconds > 0 and world == 1:
-        sample = oracle_calibrated(args.seed, args.cpu_seconds)
+        sample = oracle_calibrated(args.seed, args.cpu_seconds, q8)
         dt = sample.run()
         cpu = {"value": round(sample.nbytes / dt / 1e9, 4), "unit": "GB/s",
                "cores": sample.threads, "kind": "oracle", "sample": sample.desc,
@@ -393,7 +410,7 @@ def our_arm(args, world, rank, local):
         "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": S, "q_heads": hq, "kv_heads": hkv,
-                   "head_dim": d, "block_size": 16, "kv_dtype": w.dtype,
+                   "head_dim": d, "block_size": 16, "kv_dtype": pool.dtype,
                    "lengths": LENGTHS[args.workload],
                    "shared_prefix_tokens": w.shared_prefix_tokens,
                    "mean_context": round(toks_total / args.steps / S, 1),
@@ -408,7 +425,8 @@ def our_arm(args, world, rank, local):
                          profiled_traffic() if (args.workload, args.num_seqs, args.seed) == ("gqa_long", 256, 0)
                          else None),
                      "peak_kind": peak_kind,
-                     "kernel": "paged_decode_attention (prep + main + merge kernels)",
+                     "kernel": ("paged_decode_attention_q8" if q8 else "paged_decode_attention")
+                     + " (prep + main + merge kernels)",
                      "bytes_per_launch": int(bytes_per_launch),
                      "launch_ms": round(attn_avg_ms, 4)},
         "cpu_baseline": cpu,
@@ -553,7 +571,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="gqa_long",
-                    choices=["gqa_long", "tiny", "opt13b", "shared_prefix", "trace", "prefill"],
+                    choices=["gqa_long", "gqa_long_q8", "tiny", "opt13b", "shared_prefix", "trace",
+                             "prefill"],
                     help="gqa_long is the headline line; the others report their own config")
     ap.add_argument("--pool-gib", type=float, default=0.0,
                     help="trace only: pool size (default 40 GiB); small pools force swapping")

@@ -58,7 +58,10 @@
 extern "C" {
 #endif
 
-typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* Element type of a pool.  PKV_F16 / PKV_BF16: K and V stored as is.
+ * PKV_Q8_BF16 / PKV_Q8_F16: 8-bit cache (one fp16 scale per 32 values; q and
+ * out in bf16 / fp16), see kv_cache_write_q8. */
+typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1, PKV_Q8_BF16 = 2, PKV_Q8_F16 = 3 } pkv_dtype;
 
 typedef enum pkv_status {
     PKV_OK = 0,
@@ -207,6 +210,43 @@ int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_len
  * Asynchronous on stream.  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA. */
 int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *dst_ids,
                   int32_t n, void *k_pool, void *v_pool, int32_t *d_status, void *stream);
+
+/* ------------------------------------------------- 8-bit cache (NEXT #3) */
+
+/* An 8-bit cache stores each token's K and V as one-byte codes with one fp16
+ * scale per group of 32 values: 34 bytes per 32 values, 53.1 % of fp16
+ * ("kv-cache-by-model", section 1: Qwen3-8B at 32K, 4,608 -> 2,448 MiB).
+ * Quantisation (a reading; the pages give only the group size and the size):
+ * scale = fp16(min(max|x| / 127, 65504)); code = clamp(round-half-even(x /
+ * scale), -127, 127) computed in fp32 (codes 0 when the scale is 0); the
+ * cached value is code * scale.  Pools of a PKV_Q8_* ledger (head_dim 128):
+ *   k_codes  int8 [num_blocks][Hkv][block_size][head_dim]   (token rows)
+ *   v_codes  int8 [num_blocks][Hkv][head_dim][block_size]   (dimension rows)
+ *   k_scales, v_scales  fp16 [num_blocks][Hkv][block_size][head_dim / 32]
+ * kv_pool_scales_bytes gives the size of one scales pool; kv_pool_bytes with a
+ * PKV_Q8_* dtype gives one codes pool. */
+size_t kv_pool_scales_bytes(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                            int32_t head_dim);
+
+/* Quantising cache write: k_new / v_new are bf16 (PKV_Q8_BF16) or fp16
+ * (PKV_Q8_F16) rows [num_tokens][Hkv][128]; slots as in kv_cache_write.
+ * Errors: PKV_ERR_INVALID_ARG (not an 8-bit pool, alignment), PKV_ERR_UNSUPPORTED
+ * (head_dim other than 128), PKV_ERR_CUDA. */
+int kv_cache_write_q8(const pkv_pool *pool, const void *k_new, const void *v_new,
+                      const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
+                      void *v_codes, void *k_scales, void *v_scales, int32_t *d_status,
+                      void *stream);
+
+/* Paged decode attention over an 8-bit cache: the result of
+ * paged_decode_attention with K and V taken as code * scale.  q and out in the
+ * pool's query type; workspace as paged_decode_workspace_bytes(...); head_dim
+ * 128 and G <= 8.  Errors as paged_decode_attention. */
+int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q,
+                              const void *k_codes, const void *v_codes, const void *k_scales,
+                              const void *v_scales, const int32_t *block_tables,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, float scale, void *workspace,
+                              size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /* ------------------------------------------------- swap to host (NEXT #4) */
 

@@ -22,18 +22,21 @@ import numpy as np
 
 from . import _native
 from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV_BF16, PKV_F16,
-                      PagedKVError, check, lib)
+                      PKV_Q8_BF16, PKV_Q8_F16, PagedKVError, check, lib)
 
 __all__ = ["KVPool", "PagedKVError", "cache_write", "block_copy", "gather_blocks",
            "scatter_blocks", "paged_decode_attention",
            "paged_decode_attention_noalloc", "paged_prefill_attention",
+           "cache_write_q8", "paged_decode_attention_q8",
            "prefill_workspace_bytes",
            "decode_workspace_bytes", "status_check", "kv_bytes_per_token",
            "kv_blocks_for_tokens", "kv_pool_bytes", "default_split", "lib",
            "DEV_BAD_SLOT", "DEV_BAD_BLOCK", "DEV_BAD_LEN", "DEV_TIMEOUT"]
 
 _DTYPES = {"f16": PKV_F16, "fp16": PKV_F16, "float16": PKV_F16,
-           "bf16": PKV_BF16, "bfloat16": PKV_BF16}
+           "bf16": PKV_BF16, "bfloat16": PKV_BF16,
+           "q8_bf16": PKV_Q8_BF16, "q8_f16": PKV_Q8_F16}
+_NAMES = {PKV_F16: "f16", PKV_BF16: "bf16", PKV_Q8_BF16: "q8_bf16", PKV_Q8_F16: "q8_f16"}
 
 
 def _np_ptr(a: np.ndarray):
@@ -41,7 +44,7 @@ def _np_ptr(a: np.ndarray):
 
 
 def _t_ptr(t):
-    return ctypes.c_void_p(t.data_ptr())
+    return ctypes.c_void_p(t.data_ptr() if t is not None else None)
 
 
 def _stream(stream):
@@ -54,8 +57,10 @@ def _stream(stream):
 
 
 def _torch_dtype(code: int):
+    """Element type of K/V rows and queries for a pool type (8-bit pools take
+    bf16 / fp16 rows and quantise them)."""
     import torch
-    return torch.bfloat16 if code == PKV_BF16 else torch.float16
+    return torch.bfloat16 if code in (PKV_BF16, PKV_Q8_BF16) else torch.float16
 
 
 # ------------------------------------------------------------------ sizing
@@ -83,6 +88,11 @@ class KVPool:
     ``device=None`` creates the ledger only.  Otherwise ``k_pool``/``v_pool`` are
     torch tensors [num_blocks][num_kv_heads][block_size][head_dim] on that device
     (contents uninitialised, as a pool reserved up front).
+
+    With ``dtype="q8_bf16"`` or ``"q8_f16"`` (8-bit cache, one fp16 scale per 32
+    values) the device pools are ``k_codes`` int8 [nb][Hkv][bs][D], ``v_codes``
+    int8 [nb][Hkv][D][bs] and ``k_scales``/``v_scales`` fp16 [nb][Hkv][bs][D/32];
+    ``k_pool``/``v_pool`` then name the code pools.
     """
 
     def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, dtype: str = "bf16",
@@ -90,7 +100,8 @@ class KVPool:
         self.num_blocks, self.num_kv_heads, self.head_dim = num_blocks, num_kv_heads, head_dim
         self.block_size = block_size
         self.dtype_code = _DTYPES[dtype]
-        self.dtype = "bf16" if self.dtype_code == PKV_BF16 else "f16"
+        self.dtype = _NAMES[self.dtype_code]
+        self.is_q8 = self.dtype_code in (PKV_Q8_BF16, PKV_Q8_F16)
         order = None
         if free_order is not None:
             order = np.ascontiguousarray(free_order, dtype=np.int32)
@@ -102,11 +113,28 @@ class KVPool:
                                    ctypes.byref(h)), "kv_pool_create")
         self._h = h
         self.k_pool = self.v_pool = None
+        self.k_scales = self.v_scales = None
         if device is not None:
             import torch
             shape = (num_blocks, num_kv_heads, block_size, head_dim)
-            self.k_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
-            self.v_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
+            if self.is_q8:
+                self.k_pool = torch.empty(shape, dtype=torch.int8, device=device)
+                self.v_pool = torch.empty((num_blocks, num_kv_heads, head_dim, block_size),
+                                          dtype=torch.int8, device=device)
+                sshape = (num_blocks, num_kv_heads, block_size, head_dim // 32)
+                self.k_scales = torch.empty(sshape, dtype=torch.float16, device=device)
+                self.v_scales = torch.empty(sshape, dtype=torch.float16, device=device)
+            else:
+                self.k_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
+                self.v_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
+
+    @property
+    def k_codes(self):
+        return self.k_pool
+
+    @property
+    def v_codes(self):
+        return self.v_pool
 
     @property
     def handle(self):
@@ -331,6 +359,51 @@ def paged_prefill_attention(pool: KVPool, q, block_tables, query_start, context_
                                         _t_ptr(workspace), nbytes, _t_ptr(status),
                                         _stream(stream)), "paged_prefill_attention")
     return out
+
+
+def cache_write_q8(pool: KVPool, k_new, v_new, slot_mapping, status, stream=None) -> None:
+    """Quantising cache write into an 8-bit pool: rows of ``k_new``/``v_new``
+    [T][Hkv][128] (bf16 for q8_bf16, fp16 for q8_f16) go to their slots as codes
+    and fp16 scales."""
+    T = int(slot_mapping.shape[0])
+    if k_new.shape[0] != T or v_new.shape[0] != T:
+        raise ValueError("k_new/v_new rows must match slot_mapping")
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("inputs must be contiguous")
+    check(lib().kv_cache_write_q8(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping),
+                                  T, _t_ptr(pool.k_pool), _t_ptr(pool.v_pool),
+                                  _t_ptr(pool.k_scales), _t_ptr(pool.v_scales), _t_ptr(status),
+                                  _stream(stream)), "kv_cache_write_q8")
+
+
+def paged_decode_attention_q8(pool: KVPool, q, block_tables, context_lens, scale: float,
+                              workspace, status, out=None, stream=None):
+    """Paged decode attention over an 8-bit pool (head_dim 128, G <= 8); ``q`` and
+    the result in bf16 (q8_bf16) or fp16 (q8_f16); workspace as for
+    ``decode_workspace_bytes``."""
+    import torch
+    S, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    for t, name in ((q, "q"), (out, "out"), (block_tables, "block_tables"),
+                    (context_lens, "context_lens")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    nbytes = workspace.numel() * workspace.element_size()
+    check(lib().paged_decode_attention_q8(pool.handle, _t_ptr(out), _t_ptr(q), _t_ptr(pool.k_pool),
+                                          _t_ptr(pool.v_pool), _t_ptr(pool.k_scales),
+                                          _t_ptr(pool.v_scales), _t_ptr(block_tables),
+                                          int(block_tables.shape[1]), _t_ptr(context_lens), S, hq,
+                                          float(scale), _t_ptr(workspace), nbytes, _t_ptr(status),
+                                          _stream(stream)), "paged_decode_attention_q8")
+    return out
+
+
+def kv_pool_scales_bytes(num_blocks: int, block_size: int, num_kv_heads: int,
+                         head_dim: int) -> int:
+    return lib().kv_pool_scales_bytes(num_blocks, block_size, num_kv_heads, head_dim)
 
 
 def status_check(status, stream=None):

@@ -8,6 +8,7 @@
 // HBM-bound byte copy: one thread moves one 16-byte chunk of one row of K and
 // the same chunk of V, so a warp covers two 256-byte rows (head_dim 128) with
 // fully coalesced 128-bit loads and stores.  Bit-exact by construction.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "pagedkv.h"
@@ -99,14 +100,122 @@ swap_kernel(const int32_t *__restrict__ ids, int32_t n, int64_t chunks_per_block
     }
 }
 
+// 8-bit cache write: quantise 4 values per lane of a 128-value row in groups
+// of 32 (8 lanes): scale = fp16(min(amax / 127, 65504)), code = clamp(rn(x /
+// scale), -127, 127), all decisions in fp32 with IEEE-rounded division.
+template <bool BF16>
+__device__ __forceinline__ void q8_quantise4(const uint16_t *src, int lane, uint32_t &codes,
+                                             uint16_t &scale_bits)
+{
+    const uint2 raw = *reinterpret_cast<const uint2 *>(src + 4 * lane);
+    const uint16_t e[4] = {(uint16_t)(raw.x & 0xffffu), (uint16_t)(raw.x >> 16),
+                           (uint16_t)(raw.y & 0xffffu), (uint16_t)(raw.y >> 16)};
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v[i] = BF16 ? __uint_as_float((uint32_t)e[i] << 16)
+                    : __half2float(__ushort_as_half(e[i]));
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float d32 = fminf(__fdiv_rn(amax, 127.0f), 65504.0f);
+    const __half dh = __float2half_rn(d32);
+    const float dq = __half2float(dh);
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int c = 0;
+        if (dq != 0.0f) c = max(-127, min(127, __float2int_rn(__fdiv_rn(v[i], dq))));
+        w |= (uint32_t)(c & 0xff) << (8 * i);
+    }
+    codes = w;
+    scale_bits = __half_as_ushort(dh);
+}
+
+// One warp per (token, kv head) row, head_dim 128.  K codes go to the token
+// row of the slab, V codes to the dimension rows (byte = slot in the block).
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+cache_write_q8_kernel(const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
+                      const int64_t *__restrict__ slot_mapping, int64_t rows, int32_t num_kv_heads,
+                      int32_t block_size, int64_t num_slots, int8_t *__restrict__ k_codes,
+                      int8_t *__restrict__ v_codes, uint16_t *__restrict__ k_scales,
+                      uint16_t *__restrict__ v_scales, int32_t *__restrict__ status)
+{
+    constexpr int D = 128;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+        const int64_t t = r / num_kv_heads;
+        const int h = (int)(r - t * num_kv_heads);
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (lane == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        const int64_t block = slot / block_size, off = slot - block * block_size;
+        const int64_t slab = block * num_kv_heads + h;
+        uint32_t kc, vc;
+        uint16_t ks, vs;
+        q8_quantise4<BF16>(k_new + r * D, lane, kc, ks);
+        q8_quantise4<BF16>(v_new + r * D, lane, vc, vs);
+        *reinterpret_cast<uint32_t *>(k_codes + (slab * block_size + off) * D + 4 * lane) = kc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v_codes[(slab * D + 4 * lane + i) * block_size + off] = (int8_t)((vc >> (8 * i)) & 0xff);
+        if ((lane & 7) == 0) {
+            k_scales[(slab * block_size + off) * (D / 32) + lane / 8] = ks;
+            v_scales[(slab * block_size + off) * (D / 32) + lane / 8] = vs;
+        }
+    }
+}
+
 }  // namespace
+
+extern "C" int kv_cache_write_q8(const pkv_pool *pool, const void *k_new, const void *v_new,
+                                 const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
+                                 void *v_codes, void *k_scales, void *v_scales, int32_t *d_status,
+                                 void *stream)
+{
+    pkv::PoolGeometry g;
+    if (!pkv::pool_geometry(pool, &g) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (!pkv::is_8bit(g)) return PKV_ERR_INVALID_ARG;
+    if (g.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales ||
+        !d_status)
+        return PKV_ERR_INVALID_ARG;
+    if (((uintptr_t)k_new & 7u) || ((uintptr_t)v_new & 7u) || ((uintptr_t)k_codes & 15u) ||
+        ((uintptr_t)v_codes & 15u) || ((uintptr_t)k_scales & 15u) || ((uintptr_t)v_scales & 15u) ||
+        ((uintptr_t)slot_mapping & 7u) || ((uintptr_t)d_status & 3u))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)num_tokens * g.num_kv_heads;
+    const int threads = 256;
+    int64_t blocks = (rows * 32 + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t slots = (int64_t)g.num_blocks * g.block_size;
+    if (g.dtype == PKV_Q8_BF16)
+        cache_write_q8_kernel<true><<<(unsigned)blocks, threads, 0, st>>>(
+            (const uint16_t *)k_new, (const uint16_t *)v_new, slot_mapping, rows, g.num_kv_heads,
+            g.block_size, slots, (int8_t *)k_codes, (int8_t *)v_codes, (uint16_t *)k_scales,
+            (uint16_t *)v_scales, d_status);
+    else
+        cache_write_q8_kernel<false><<<(unsigned)blocks, threads, 0, st>>>(
+            (const uint16_t *)k_new, (const uint16_t *)v_new, slot_mapping, rows, g.num_kv_heads,
+            g.block_size, slots, (int8_t *)k_codes, (int8_t *)v_codes, (uint16_t *)k_scales,
+            (uint16_t *)v_scales, d_status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 static int launch_swap(const pkv_pool *pool, const int32_t *ids, int32_t n, void *k_pool,
                        void *v_pool, void *staging, bool to_staging, int32_t *d_status,
                        void *stream)
 {
     pkv::PoolGeometry g;
-    if (!pkv::pool_geometry(pool, &g) || n < 0) return PKV_ERR_INVALID_ARG;
+    if (!pkv::pool_geometry(pool, &g) || n < 0 || !pkv::is_16bit(g)) return PKV_ERR_INVALID_ARG;
     if (n == 0) return PKV_OK;
     if (!ids || !k_pool || !v_pool || !staging || !d_status) return PKV_ERR_INVALID_ARG;
     if (!pkv::aligned16(k_pool) || !pkv::aligned16(v_pool) || !pkv::aligned16(staging) ||
@@ -145,7 +254,7 @@ extern "C" int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const
                              void *stream)
 {
     pkv::PoolGeometry g;
-    if (!pkv::pool_geometry(pool, &g) || n < 0) return PKV_ERR_INVALID_ARG;
+    if (!pkv::pool_geometry(pool, &g) || n < 0 || !pkv::is_16bit(g)) return PKV_ERR_INVALID_ARG;
     if (n == 0) return PKV_OK;
     if (!src_ids || !dst_ids || !k_pool || !v_pool || !d_status) return PKV_ERR_INVALID_ARG;
     if (!pkv::aligned16(k_pool) || !pkv::aligned16(v_pool) || ((uintptr_t)src_ids & 3u) ||
@@ -167,7 +276,7 @@ extern "C" int kv_cache_write(const pkv_pool *pool, const void *k_new, const voi
                               void *v_pool, int32_t *d_status, void *stream)
 {
     pkv::PoolGeometry g;
-    if (!pkv::pool_geometry(pool, &g) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (!pkv::pool_geometry(pool, &g) || num_tokens < 0 || !pkv::is_16bit(g)) return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0) return PKV_OK;
     if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool || !d_status)
         return PKV_ERR_INVALID_ARG;

@@ -34,6 +34,14 @@
 //   * Every wait is bounded (1 s); on expiry the kernel flags PKV_DEV_TIMEOUT,
 //     stops issuing copies, drains the ones in flight and finishes without
 //     trapping.
+//   * The 8-bit variant ("kv-cache-by-model", section 1: one-byte codes with a
+//     fp16 scale per 32 values) streams 4,352 bytes per block instead of
+//     8,192.  The MMAs take the codes themselves (exact in fp16/bf16); the K
+//     scales multiply the per-group partial scores, the V scales are folded
+//     into the softmax weights of each 32-dimension group.  Tokens are
+//     permuted inside the two 8-column MMA tiles so that each lane's four
+//     scores belong to four adjacent tokens: one 32-bit word of a dimension
+//     row of V codes, and one 32-byte run of scales.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -67,6 +75,9 @@ struct Params {
     float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned
     float *part_o;              // [pairs * Hkv * G * D]: unnormalised partition output
     int32_t *status;
+    const void *v_codes;        // 8-bit variant: V codes and both scale pools (1-D copies)
+    const void *k_scales;
+    const void *v_scales;
     int64_t max_pairs;          // capacity of items / partial arrays (checked builds)
     int32_t *debug;             // first failed check: site << 24 | value (checked builds)
 };
@@ -86,19 +97,31 @@ __device__ __forceinline__ bool dbg_fail(bool ok, int32_t *dbg, int site, long l
     return false;
 }
 
+// 8-bit stage: K codes as two 1 KiB TMA boxes (128-byte swizzle), box b holding
+// tokens 4a + 2b + c in row 2a + c, then the 2 KiB of V codes (128 dimension rows
+// of 16 bytes); the scales go to a separate ring of 256 bytes per stage (K
+// scales [16][4] fp16, then V scales).
+constexpr int kQ8Stage = 4096;
+constexpr int kQ8Scales = 256;
+constexpr int kQ8TxBytes = kQ8Stage + kQ8Scales;
+
 // Shared-memory footprint of one kernel variant (without the 1 KiB alignment slack).
-template <int D, int GROWS, int NST>
+template <int D, int GROWS, int NST, bool Q8 = false>
 struct Smem {
-    static constexpr int kStageBytes = 2 * (D / kBoxCols) * kBoxBytes;  // K slab + V slab
+    static constexpr int kStageBytes = Q8 ? kQ8Stage : 2 * (D / kBoxCols) * kBoxBytes;
     static constexpr int kStagesBytes = NST * kStageBytes;
+    static constexpr int kSclBytes = Q8 ? NST * kQ8Scales : 0;
     static constexpr int kQSlotBytes = 16 * D * 2;                      // 16 query rows
     static constexpr int kQBytes = 2 * kQSlotBytes;                     // double buffered
     static constexpr int kBarBytes = (2 * NST + 4) * 8;
     static constexpr int kMetaBytes = 2 * 8 * 4;
+    // scratch row: D sums, the row's max and sum; the 8-bit layout stores
+    // column-wise and pads to 4 mod 32 words to spread the banks
+    static constexpr int kRowStride = Q8 ? D + 4 : D + 2;
     static constexpr int kScratchBytes =
-        kConsumerWarps * GROWS * (D + 2) * 4 + NST * 4 + kConsumerWarps * 4 + 16;
+        kConsumerWarps * GROWS * kRowStride * 4 + NST * 4 + kConsumerWarps * 4 + 16;
     static constexpr int kTotal =
-        1024 + kStagesBytes + kQBytes + kBarBytes + kMetaBytes + kScratchBytes;
+        1024 + kStagesBytes + kSclBytes + kQBytes + kBarBytes + kMetaBytes + kScratchBytes;
 };
 
 // Item metadata the producer hands to the consumers with each item's Q rows.
@@ -181,27 +204,151 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     if (tid == 0) p.header[0] = carry;
 }
 
+// ------------------------------------------------------------ 8-bit block step
+// One 16-token block of an 8-bit slab for the G <= 8 query rows of a warp, all
+// products on fp16 tensor cores (codes are exact in fp16; bf16 queries enter as
+// fp16 after a power-of-two prescale of their row, exact in the fp16 normal range).
+//
+// S = Q K^T: Q rows as A (rows 8-15 zero), K codes as B.  Column c of tile b is
+// token 4 (c >> 1) + 2b + (c & 1), so lane (hrow, q4) holds the scores of tokens
+// 4q4 .. 4q4 + 3 of query row hrow; the K scales multiply the partial score of
+// each 32-dimension group.
+//   S[t] = sum_i ks[t][i] * (q . codes[t]) over group i
+// O^T = V^T P^T: V codes as A (16 dimensions per MMA, k = the 16 tokens), the
+// softmax weights times the V scale of the group as B -- exactly the four weights
+// the lane holds -- so o[t] covers dimensions 16t + r and 16t + r + 8 (r = lane/4)
+// of query rows 2q4 and 2q4 + 1.
+//   O[d][h] += sum_t vcode[d][t] * (p[h][t] * vs[t][d / 32])
+template <bool BF16>
+__device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *scales,
+                                                 const uint32_t (&qa)[8][4], float (&o)[16][4],
+                                                 float &m0, float &l0, int valid,
+                                                 float scale_row, int lane)
+{
+    using H = Elem<false>;
+    const int q4 = lane & 3, r8 = lane & 7;
+    // ldmatrix rows: matrix (lane >> 3) = (tile (lane >> 3) & 1, step 2i + (lane >> 4))
+    const uint32_t krow = kb + ((lane >> 3) & 1) * 1024 + r8 * 128;
+    const int kstep_hi = lane >> 4;
+    const uint32_t vb = kb + 2048;
+
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        float ks[4][4];        // [token j][group i]
+        const uint4 a = *reinterpret_cast<const uint4 *>(scales + 32 * q4);
+        const uint4 b = *reinterpret_cast<const uint4 *>(scales + 32 * q4 + 16);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            ks[k >> 1][2 * (k & 1)] = f.x;
+            ks[k >> 1][2 * (k & 1) + 1] = f.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t kr[4];
+            ldsm_x4(kr, krow + (((2 * i + kstep_hi) ^ r8) << 4));
+            float c0[4], c1[4];
+            uint32_t lo, hi;
+            codes_to_pairs<false>(kr[0], lo, hi);
+            H::mma0(c0, qa[2 * i], lo, hi);
+            codes_to_pairs<false>(kr[1], lo, hi);
+            H::mma0(c1, qa[2 * i], lo, hi);
+            codes_to_pairs<false>(kr[2], lo, hi);
+            H::mma(c0, qa[2 * i + 1], lo, hi);
+            codes_to_pairs<false>(kr[3], lo, hi);
+            H::mma(c1, qa[2 * i + 1], lo, hi);
+            sc[0] = fmaf(ks[0][i], c0[0], sc[0]);
+            sc[1] = fmaf(ks[1][i], c0[1], sc[1]);
+            sc[2] = fmaf(ks[2][i], c1[0], sc[2]);
+            sc[3] = fmaf(ks[3][i], c1[1], sc[3]);
+        }
+    }
+    float x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = sc[j] * scale_row;
+    float vs[4][4];
+    {
+        const uint4 a = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4);
+        const uint4 b = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4 + 16);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            vs[k >> 1][2 * (k & 1)] = f.x;
+            vs[k >> 1][2 * (k & 1) + 1] = f.y;
+        }
+    }
+    if (valid < kBlock) {
+        // tokens past the context: no score, and no scale (a stale one may be NaN)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (4 * q4 + j >= valid) {
+                x[j] = -INFINITY;
+                vs[j][0] = vs[j][1] = vs[j][2] = vs[j][3] = 0.f;
+            }
+    }
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float mn = fmaxf(m0, mx);
+    const float a0 = exp2f(m0 - mn);
+    float pj[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pj[j] = exp2f(x[j] - mn);
+    l0 = l0 * a0 + ((pj[0] + pj[1]) + (pj[2] + pj[3]));
+    m0 = mn;
+    if (__any_sync(kFull, a0 != 1.f)) {
+        // this lane's accumulators belong to query rows 2q4 and 2q4 + 1
+        const float f0 = __shfl_sync(kFull, a0, 8 * q4);
+        const float f1 = __shfl_sync(kFull, a0, 8 * q4 + 4);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            o[t][0] *= f0; o[t][1] *= f1; o[t][2] *= f0; o[t][3] *= f1;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b0 = H::pack(pj[0] * vs[0][i], pj[1] * vs[1][i]);
+        const uint32_t b1 = H::pack(pj[2] * vs[2][i], pj[3] * vs[3][i]);
+        // matrix m: dimensions 32i + 8m .. 32i + 8m + 7 (lane row r = dimension)
+        uint32_t vr[4];
+        ldsm_x4(vr, vb + (32 * i + lane) * 16);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            uint32_t a[4];
+            codes_to_pairs<false>(vr[2 * t], a[0], a[2]);
+            codes_to_pairs<false>(vr[2 * t + 1], a[1], a[3]);
+            H::mma(o[2 * i + t], a, b0, b1);
+        }
+    }
+}
+
 // ----------------------------------------------------------------- main kernel
-template <int D, bool BF16, int GROWS, int NST, int MINB>
+// Q8: tmK / tmV are the two K-code box maps of the 8-bit pool (tokens 4a + c and
+// 4a + 2 + c of every slab); V codes and scales come by 1-D bulk copies.
+template <int D, bool BF16, int GROWS, int NST, int MINB, bool Q8 = false>
 __global__ void __launch_bounds__(kThreads, MINB)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const Params p)
 {
     using E = Elem<BF16>;
     using T = typename E::T;
-    using SM = Smem<D, GROWS, NST>;
+    using SM = Smem<D, GROWS, NST, Q8>;
     static_assert(NST % kConsumerWarps == 0, "each slot must keep one consumer warp");
+    static_assert(!Q8 || (D == 128 && GROWS == 8), "8-bit variant: head_dim 128, G <= 8");
     constexpr int kBoxes = D / kBoxCols;          // TMA boxes per slab
     constexpr int kSlabBytes = kBoxes * kBoxBytes;
     constexpr int KSTEPS = D / 16;                // QK reduction steps
     constexpr int NTILES = D / 8;                 // PV output tiles of 8 dims
-    constexpr int OSTRIDE = D + 2;                // padded scratch row
+    constexpr int OSTRIDE = SM::kRowStride;       // padded scratch row
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = base;
-    uint8_t *qbuf = base + SM::kStagesBytes;                               // [2][16][D]
+    uint8_t *scl = base + SM::kStagesBytes;                                // 8-bit: scale ring
+    uint8_t *qbuf = scl + SM::kSclBytes;                                   // [2][16][D]
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(qbuf + SM::kQBytes);
     uint64_t *empty_bar = full_bar + NST;
     uint64_t *qfull_bar = empty_bar + NST;
@@ -305,14 +452,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         if (mbar_wait(smem_addr(&empty_bar[slot]), par ^ 1u, sm_abort, p.status)) {
                             if (pid >= 0 && pid < p.num_blocks) {
                                 stage_bad[slot] = 0;
-                                mbar_arrive_expect_tx(fb, 2 * kSlabBytes);
                                 const uint32_t dk = smem_addr(stages + slot * SM::kStageBytes);
-                                const uint32_t dv = dk + kSlabBytes;
-                                const int y = (pid * Hkv + g) * kBlock;
+                                if constexpr (Q8) {
+                                    mbar_arrive_expect_tx(fb, kQ8TxBytes);
+                                    const int64_t slab = (int64_t)pid * Hkv + g;
+                                    const uint32_t ds = smem_addr(scl + slot * kQ8Scales);
+                                    tma_load_3d(dk, &tmK, 0, 0, (int)(slab * 4), fb);
+                                    tma_load_3d(dk + 1024, &tmV, 0, 0, (int)(slab * 4), fb);
+                                    bulk_load(dk + 2048,
+                                              static_cast<const uint8_t *>(p.v_codes) + slab * 2048,
+                                              2048, fb);
+                                    bulk_load(ds, static_cast<const uint8_t *>(p.k_scales) + slab * 128,
+                                              128, fb);
+                                    bulk_load(ds + 128,
+                                              static_cast<const uint8_t *>(p.v_scales) + slab * 128,
+                                              128, fb);
+                                } else {
+                                    mbar_arrive_expect_tx(fb, 2 * kSlabBytes);
+                                    const uint32_t dv = dk + kSlabBytes;
+                                    const int y = (pid * Hkv + g) * kBlock;
 #pragma unroll
-                                for (int bx = 0; bx < kBoxes; ++bx) {
-                                    tma_load_2d(dk + bx * kBoxBytes, &tmK, bx * kBoxCols, y, fb);
-                                    tma_load_2d(dv + bx * kBoxBytes, &tmV, bx * kBoxCols, y, fb);
+                                    for (int bx = 0; bx < kBoxes; ++bx) {
+                                        tma_load_2d(dk + bx * kBoxBytes, &tmK, bx * kBoxCols, y, fb);
+                                        tma_load_2d(dv + bx * kBoxBytes, &tmV, bx * kBoxCols, y, fb);
+                                    }
                                 }
                                 issued |= 1u << slot;
                                 issued_par = (issued_par & ~(1u << slot)) | (par << slot);
@@ -367,7 +530,47 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const ItemMeta mt = q_ok ? sm_meta[qs] : ItemMeta{0, 0, 0, 0, 0, 1, 0, 0};
         // Q rows of the group as the A operand (rows >= G are zero in shared memory)
         uint32_t qa[KSTEPS][4];
-        {
+        float scale_row = p.scale_log2;
+        if constexpr (Q8) {
+            // fp16 A operand, dimensions permuted inside each 16-wide step to match
+            // the K-code words: k slots 2q4 + e <- 16kk + 4q4 + e and
+            // 8 + 2q4 + e <- 16kk + 4q4 + 2 + e
+            const uint8_t *qrow = qbuf + qs * SM::kQSlotBytes + hrow * (D * 2);
+            uint2 v[KSTEPS];
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk)
+                v[kk] = q_ok ? *reinterpret_cast<const uint2 *>(qrow + (16 * kk + 4 * q4) * 2)
+                             : make_uint2(0u, 0u);
+            if constexpr (BF16) {
+                // bf16 row -> fp16 after scaling by 2^-E, E >= 0 the smallest that
+                // brings the row's largest magnitude below 2^15; exact for every
+                // element in the fp16 normal range.  2^E goes into the row's scale.
+                float amax = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const float2 f0 = E::unpack(v[kk].x), f1 = E::unpack(v[kk].y);
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
+                                             fmaxf(fabsf(f1.x), fabsf(f1.y))));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+                const int e = max(0, ((__float_as_int(amax) >> 23) & 0xff) - 127 - 14);
+                const float down = __int_as_float((127 - e) << 23);
+                scale_row = p.scale_log2 * __int_as_float((127 + e) << 23);
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    const float2 f0 = E::unpack(v[kk].x), f1 = E::unpack(v[kk].y);
+                    qa[kk][0] = Elem<false>::pack(f0.x * down, f0.y * down);
+                    qa[kk][2] = Elem<false>::pack(f1.x * down, f1.y * down);
+                    qa[kk][1] = qa[kk][3] = 0u;
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    qa[kk][0] = v[kk].x; qa[kk][1] = 0u; qa[kk][2] = v[kk].y; qa[kk][3] = 0u;
+                }
+            }
+        } else {
             const uint32_t qb = smem_addr(qbuf + qs * SM::kQSlotBytes);
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -403,6 +606,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const uint32_t vb = kb + kSlabBytes;
             if (dbg_fail(slot < NST && (kb & 1023u) == 0u, p.debug, 7, slot)) continue;
 
+            if constexpr (Q8) {
+                consume_q8_block<BF16>(kb, scl + slot * kQ8Scales, qa, o, m0, l0, valid,
+                                       scale_row, lane);
+            } else {
             // ---- S = Q K^T : two 8-token tiles, two accumulation chains each
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
             float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -508,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     E::mma(o[2 * jj + 1], pb, vr[2], vr[3]);
                 }
             }
+            }   // 16-bit block
             // The stage's next contents arrive through the async proxy (TMA):
             // order this warp's generic-proxy reads of it before the release.
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -537,6 +745,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 wo[(hrow + 8) * OSTRIDE + D + 1] = l1;
             }
         }
+        if constexpr (Q8) {
+            // o[t]: dimensions 16t + hrow (+ 8) of query rows 2q4 and 2q4 + 1
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int d = 16 * t + hrow;
+                wo[(2 * q4) * OSTRIDE + d] = o[t][0];
+                wo[(2 * q4 + 1) * OSTRIDE + d] = o[t][1];
+                wo[(2 * q4) * OSTRIDE + d + 8] = o[t][2];
+                wo[(2 * q4 + 1) * OSTRIDE + d + 8] = o[t][3];
+            }
+        } else
 #pragma unroll
         for (int j = 0; j < NTILES; ++j) {
             const int d0 = 8 * j + 2 * q4;
@@ -719,6 +938,31 @@ static bool make_pool_map(CUtensorMap *map, const void *pool, const PoolGeometry
     return r == CUDA_SUCCESS;
 }
 
+// The two K-code maps of an 8-bit pool: rows of 128 bytes viewed as
+// (byte, c in {0, 1} at stride 128, a at stride 512), box {128, 2, 4} with the
+// 128-byte swizzle.  Map 0 starts at the pool (tokens 4a + c of each slab), map
+// 1 at +256 bytes (tokens 4a + 2 + c); coordinate a = 4 * slab selects a slab.
+static bool make_q8_key_maps(CUtensorMap *m0, CUtensorMap *m1, const void *k_codes,
+                             const PoolGeometry &g)
+{
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t slabs = (cuuint64_t)g.num_blocks * g.num_kv_heads;
+    cuuint64_t dims[3] = {128, 2, slabs * 4};
+    cuuint64_t strides[2] = {128, 512};
+    cuuint32_t box[3] = {128, 2, 4};
+    cuuint32_t estr[3] = {1, 1, 1};
+    for (int b = 0; b < 2; ++b) {
+        CUresult r = enc(b ? m1 : m0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                         const_cast<uint8_t *>(static_cast<const uint8_t *>(k_codes)) + 256 * b,
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return false;
+    }
+    return true;
+}
+
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
 
 struct Variant {
@@ -726,12 +970,16 @@ struct Variant {
     int smem;
 };
 
-template <int D, bool BF16, int GROWS, int NST, int MINB>
+template <int D, bool BF16, int GROWS, int NST, int MINB, bool Q8 = false>
 static Variant variant()
 {
-    return Variant{reinterpret_cast<KernelFn>(&decode_kernel<D, BF16, GROWS, NST, MINB>),
-                   Smem<D, GROWS, NST>::kTotal};
+    return Variant{reinterpret_cast<KernelFn>(&decode_kernel<D, BF16, GROWS, NST, MINB, Q8>),
+                   Smem<D, GROWS, NST, Q8>::kTotal};
 }
+
+// 8-bit variant: 8 stages of 4,352 bytes, three CTAs per SM.
+constexpr int kQ8Stages = 8;
+constexpr int kQ8MinBlocks = 3;
 
 static bool pick_variant(int D, bool bf16, int G, Variant *v)
 {
@@ -783,28 +1031,43 @@ static int persistent_ctas(const Variant &v, int *num_sms_out)
     return -1;
 }
 
-static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
-                  const void *v_pool, const int32_t *block_tables, int32_t maxb,
+// Pool memory of one call: the K and V pools (16-bit), or the K and V codes and
+// the two scale pools (8-bit).
+struct PoolPtrs {
+    const void *k, *v, *ks, *vs;
+};
+
+static int launch(const pkv_pool *pool, void *out, const void *q, const PoolPtrs &pp,
+                  bool want_8bit, const int32_t *block_tables, int32_t maxb,
                   const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
                   int32_t P, void *workspace, size_t workspace_bytes, int32_t *d_status,
                   void *stream)
 {
     PoolGeometry g;
     if (!pool_geometry(pool, &g)) return PKV_ERR_INVALID_ARG;
+    if (want_8bit ? !is_8bit(g) : !is_16bit(g)) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads <= 0 || maxb <= 0 || P <= 0) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % g.num_kv_heads) return PKV_ERR_INVALID_ARG;
     if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_INVALID_ARG;
     const int G = num_q_heads / g.num_kv_heads;
-    if (g.block_size != kBlock || G > 16) return PKV_ERR_UNSUPPORTED;
+    const bool bf = g.dtype == PKV_BF16 || g.dtype == PKV_Q8_BF16;
+    if (g.block_size != kBlock || G > (want_8bit ? 8 : 16)) return PKV_ERR_UNSUPPORTED;
     Variant v;
-    if (!pick_variant(g.head_dim, g.dtype == PKV_BF16, G, &v)) return PKV_ERR_UNSUPPORTED;
+    if (want_8bit) {
+        if (g.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+        v = bf ? variant<128, true, 8, kQ8Stages, kQ8MinBlocks, true>()
+               : variant<128, false, 8, kQ8Stages, kQ8MinBlocks, true>();
+    } else if (!pick_variant(g.head_dim, bf, G, &v)) {
+        return PKV_ERR_UNSUPPORTED;
+    }
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_pool || !v_pool || !block_tables || !context_lens || !workspace ||
-        !d_status)
+    if (!out || !q || !pp.k || !pp.v || !block_tables || !context_lens || !workspace ||
+        !d_status || (want_8bit && (!pp.ks || !pp.vs)))
         return PKV_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+    if (!aligned16(out) || !aligned16(q) || !aligned16(pp.k) || !aligned16(pp.v) ||
         ((uintptr_t)workspace & 255u) || ((uintptr_t)block_tables & 3u) ||
-        ((uintptr_t)context_lens & 3u) || ((uintptr_t)d_status & 3u))
+        ((uintptr_t)context_lens & 3u) || ((uintptr_t)d_status & 3u) ||
+        (want_8bit && (!aligned16(pp.ks) || !aligned16(pp.vs))))
         return PKV_ERR_INVALID_ARG;
     WsLayout w;
     if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, P, &w) ||
@@ -814,7 +1077,9 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
         return PKV_ERR_UNSUPPORTED;   // TMA row coordinate is a signed 32-bit value
 
     CUtensorMap tk, tv;
-    if (!make_pool_map(&tk, k_pool, g) || !make_pool_map(&tv, v_pool, g)) return PKV_ERR_CUDA;
+    if (want_8bit ? !make_q8_key_maps(&tk, &tv, pp.k, g)
+                  : (!make_pool_map(&tk, pp.k, g) || !make_pool_map(&tv, pp.v, g)))
+        return PKV_ERR_CUDA;
 
     char *ws = static_cast<char *>(workspace);
     Params prm;
@@ -836,6 +1101,9 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     prm.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
     prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
     prm.status = d_status;
+    prm.v_codes = want_8bit ? pp.v : nullptr;
+    prm.k_scales = pp.ks;
+    prm.v_scales = pp.vs;
     prm.max_pairs = w.max_pairs;
     prm.debug = prm.header + 1;
 
@@ -864,7 +1132,6 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     if (cudaLaunchKernelEx(&cfg, v.fn, tk, tv, prm) != cudaSuccess) return PKV_ERR_CUDA;
     if (maxb > P) {   // some sequence may have several partitions
         const int64_t pairs = (int64_t)num_seqs * g.num_kv_heads;
-        const bool bf = g.dtype == PKV_BF16;
         void (*merge)(Params) =
             g.head_dim == 128 ? (bf ? decode_merge_kernel<true, 128> : decode_merge_kernel<false, 128>)
                               : (bf ? decode_merge_kernel<true, 64> : decode_merge_kernel<false, 64>);
@@ -912,7 +1179,8 @@ int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
                                  void *workspace, size_t workspace_bytes, int32_t *d_status,
                                  void *stream)
 {
-    return pkv::decode::launch(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+    const pkv::decode::PoolPtrs pp{k_pool, v_pool, nullptr, nullptr};
+    return pkv::decode::launch(pool, out, q, pp, false, block_tables, max_blocks_per_seq,
                                context_lens, num_seqs, num_q_heads, scale, blocks_per_split,
                                workspace, workspace_bytes, d_status, stream);
 }
@@ -923,7 +1191,22 @@ int paged_decode_attention(const pkv_pool *pool, void *out, const void *q, const
                            int32_t num_seqs, int32_t num_q_heads, float scale, void *workspace,
                            size_t workspace_bytes, int32_t *d_status, void *stream)
 {
-    return pkv::decode::launch(pool, out, q, k_pool, v_pool, block_tables, max_blocks_per_seq,
+    const pkv::decode::PoolPtrs pp{k_pool, v_pool, nullptr, nullptr};
+    return pkv::decode::launch(pool, out, q, pp, false, block_tables, max_blocks_per_seq,
+                               context_lens, num_seqs, num_q_heads, scale,
+                               pkv::decode::kDefaultSplit, workspace, workspace_bytes, d_status,
+                               stream);
+}
+
+int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q,
+                              const void *k_codes, const void *v_codes, const void *k_scales,
+                              const void *v_scales, const int32_t *block_tables,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, float scale, void *workspace,
+                              size_t workspace_bytes, int32_t *d_status, void *stream)
+{
+    const pkv::decode::PoolPtrs pp{k_codes, v_codes, k_scales, v_scales};
+    return pkv::decode::launch(pool, out, q, pp, true, block_tables, max_blocks_per_seq,
                                context_lens, num_seqs, num_q_heads, scale,
                                pkv::decode::kDefaultSplit, workspace, workspace_bytes, d_status,
                                stream);
@@ -995,6 +1278,7 @@ extern "C" int paged_decode_attention_noalloc(const pkv_pool *pool, void *out, c
     if (P == 0) return PKV_ERR_INVALID_ARG;   // scratch would exceed PKV_NOALLOC_SCRATCH_BYTES
     void *scratch = noalloc_scratch_address();
     if (!scratch) return PKV_ERR_CUDA;
-    return launch(pool, out, q, k_pool, v_pool, block_tables, maxb, context_lens, num_seqs,
+    const PoolPtrs pp{k_pool, v_pool, nullptr, nullptr};
+    return launch(pool, out, q, pp, false, block_tables, maxb, context_lens, num_seqs,
                   num_q_heads, scale, P, scratch, kNoallocScratchBytes, d_status, stream);
 }

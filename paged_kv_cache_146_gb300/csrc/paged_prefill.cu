@@ -513,7 +513,7 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
 {
     using namespace pkv::prefill;
     pkv::PoolGeometry g;
-    if (!pkv::pool_geometry(pool, &g)) return PKV_ERR_INVALID_ARG;
+    if (!pkv::pool_geometry(pool, &g) || !pkv::is_16bit(g)) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
         return PKV_ERR_INVALID_ARG;
     if (num_q_heads % g.num_kv_heads) return PKV_ERR_INVALID_ARG;

@@ -19,4 +19,10 @@ bool pool_geometry(const pkv_pool *p, PoolGeometry *g);
 
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Element type of the pool is fp16 or bf16 (not an 8-bit cache).
+inline bool is_16bit(const PoolGeometry &g) { return g.dtype == PKV_F16 || g.dtype == PKV_BF16; }
+
+// Pool holds 8-bit codes with fp16 scales.
+inline bool is_8bit(const PoolGeometry &g) { return g.dtype == PKV_Q8_BF16 || g.dtype == PKV_Q8_F16; }
+
 }  // namespace pkv

@@ -7,6 +7,10 @@ GPU, the cache-write kernel stores the new K/V, and the paged attention kernel
 reads every sequence's blocks through its table.  Finished sequences release
 their blocks ("vLLM-and-PagedAttention-KR", "가장 기본적인 decoding", step 5).
 
+The pool may be 16-bit (fp16/bf16 K and V) or an 8-bit cache ("kv-cache-by-model",
+section 1: one-byte codes, one fp16 scale per 32 values); the engine picks the
+matching cache-write and attention calls.
+
 The host side of step k+1 overlaps the kernels of step k: before it touches the
 pinned table again it waits only for step k's host-to-device copy, which runs
 as soon as step k-1's kernels are done.
@@ -15,8 +19,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (KVPool, cache_write, decode_workspace_bytes, paged_decode_attention,
-               status_check)
+from . import (KVPool, cache_write, cache_write_q8, decode_workspace_bytes,
+               paged_decode_attention, paged_decode_attention_q8, status_check)
 
 
 class DecodeEngine:
@@ -29,6 +33,8 @@ class DecodeEngine:
         self.scale = scale
         self.device = device
         self.split = blocks_per_split
+        if pool.is_q8 and blocks_per_split is not None:
+            raise ValueError("the 8-bit path uses the default partition size")
         pin = dict(pin_memory=True)
         self.h_tables = torch.full((num_seqs, max_blocks_per_seq), -1, dtype=torch.int32, **pin)
         self.h_lens = torch.zeros(num_seqs, dtype=torch.int32, **pin)
@@ -43,7 +49,7 @@ class DecodeEngine:
                                         max_blocks_per_seq, blocks_per_split)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        tdt = torch.bfloat16 if pool.dtype == "bf16" else torch.float16
+        tdt = torch.bfloat16 if pool.dtype in ("bf16", "q8_bf16") else torch.float16
         self.out = torch.empty((num_seqs, num_q_heads, pool.head_dim), dtype=tdt, device=device)
         self._ones = np.ones(num_seqs, dtype=np.int32)
         self._copied = None                          # event: last H2D of the pinned ledger
@@ -57,8 +63,7 @@ class DecodeEngine:
         num_new = np.ascontiguousarray(num_new, dtype=np.int32)
         slots = self.pool.append_slots(self.lens, num_new, self.tables)
         if len(slots):
-            d_slots = torch.from_numpy(slots).to(self.device)
-            cache_write(self.pool, k_rows, v_rows, d_slots, self.status)
+            self.write(k_rows, v_rows, torch.from_numpy(slots).to(self.device))
         self.lens += num_new
         return slots
 
@@ -96,13 +101,27 @@ class DecodeEngine:
         self._copied = torch.cuda.Event()
         self._copied.record()
 
+    def write(self, k_new, v_new, d_slots=None) -> None:
+        """a3: cache write of K/V rows into their slots (this step's by default)."""
+        d_slots = self.d_slots if d_slots is None else d_slots
+        if self.pool.is_q8:
+            cache_write_q8(self.pool, k_new, v_new, d_slots, self.status)
+        else:
+            cache_write(self.pool, k_new, v_new, d_slots, self.status)
+
+    def attend(self, q):
+        """a4/a5: paged attention of every sequence over its blocks."""
+        if self.pool.is_q8:
+            return paged_decode_attention_q8(self.pool, q, self.d_tables, self.d_lens, self.scale,
+                                             self.workspace, self.status, out=self.out)
+        return paged_decode_attention(self.pool, q, self.d_tables, self.d_lens, self.scale,
+                                      self.workspace, self.status, out=self.out,
+                                      blocks_per_split=self.split)
+
     def device_step(self, q, k_new, v_new):
         """a3 + a4/a5: cache write of this step's K/V, then paged attention."""
-        cache_write(self.pool, k_new, v_new, self.d_slots, self.status)
-        paged_decode_attention(self.pool, q, self.d_tables, self.d_lens, self.scale,
-                               self.workspace, self.status, out=self.out,
-                               blocks_per_split=self.split)
-        return self.out
+        self.write(k_new, v_new)
+        return self.attend(q)
 
     def decode_step(self, q, k_new, v_new):
         self.host_step()
@@ -124,10 +143,12 @@ class DecodeEngine:
     # --------------------------------------------------------------- accounting
     def step_bytes(self) -> int:
         """Algorithmic bytes one attention call moves at the current lengths:
-        K and V of every context token, q, out, and the table entries read."""
+        K and V of every context token (8-bit pools: codes and scales), q, out,
+        and the table entries read."""
         p = self.pool
         elem = 2
-        kv = int(self.lens.astype(np.int64).sum()) * p.num_kv_heads * p.head_dim * 2 * elem
+        per_head = 2 * (p.head_dim + p.head_dim // 32 * 2) if p.is_q8 else 2 * p.head_dim * elem
+        kv = int(self.lens.astype(np.int64).sum()) * p.num_kv_heads * per_head
         qo = 2 * self.S * self.hq * p.head_dim * elem
         meta = 4 * int(sum(-(-int(n) // p.block_size) for n in self.lens)) + 4 * self.S
         return kv + qo + meta

@@ -1,0 +1,265 @@
+"""GPU parity of the 8-bit KV cache ("kv-cache-by-model", section 1: one-byte
+codes with one fp16 scale per 32 values) against the oracle.
+
+  * quantising cache write: codes and scale bits identical to the oracle's
+    (bit-exact) on ordinary, zero, saturating and subnormal-scale rows; slots
+    outside the pool flagged and skipped, negative slots skipped, every other
+    byte of the pools untouched;
+  * decode attention over the 8-bit pool: |gpu - oracle| <= 2e-3 + 1e-2 |oracle|,
+    the oracle attending in fp64 over code * scale; stale slots past each
+    context (codes -1, NaN scales) never reach the result; repeated launches
+    give the same bits.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import libbuild  # noqa: E402
+import oracle  # noqa: E402
+from decode_case import assert_close, to_np_bits, to_torch  # noqa: E402
+from paged_kv_cache_146_gb300 import (DEV_BAD_SLOT, KVPool, PagedKVError,  # noqa: E402
+                                      cache_write_q8, decode_workspace_bytes,
+                                      paged_decode_attention_q8, status_check, workloads)
+
+libbuild.ensure_built()
+
+D = 128
+
+
+def _fill_sentinel(pool):
+    pool.k_pool.fill_(-1)
+    pool.v_pool.fill_(-1)
+    pool.k_scales.view(torch.int16).fill_(-1)           # fp16 NaN
+    pool.v_scales.view(torch.int16).fill_(-1)
+
+
+def _oracle_pools(nb, hkv):
+    return (np.full((nb, hkv, 16, D), -1, np.int8), np.full((nb, hkv, D, 16), -1, np.int8),
+            np.full((nb, hkv, 16, D // 32), 0xFFFF, np.uint16),
+            np.full((nb, hkv, 16, D // 32), 0xFFFF, np.uint16))
+
+
+def _host_pools(pool):
+    return (pool.k_pool.cpu().numpy(), pool.v_pool.cpu().numpy(),
+            to_np_bits(pool.k_scales), to_np_bits(pool.v_scales))
+
+
+def _assert_pools_equal(pool, ref):
+    got = _host_pools(pool)
+    for name, g, r in zip(("k_codes", "v_codes", "k_scales", "v_scales"), got, ref):
+        assert g.shape == r.shape, name
+        if not np.array_equal(g, r):
+            idx = np.argwhere(g != r)[:5].tolist()
+            raise AssertionError(f"{name}: {int((g != r).sum())} entries differ, first {idx}")
+
+
+class Q8Case:
+    """Sequences of the given lengths in a shuffled pool, every token written by
+    the library's 8-bit cache write and by the oracle's, from the same rows."""
+
+    def __init__(self, lens, hq, hkv, dt, seed, rows=None):
+        rng = np.random.default_rng(seed)
+        self.lens = np.asarray(lens, np.int32)
+        self.hq, self.hkv, self.dt, self.bf = hq, hkv, dt, dt == "bf16"
+        S = len(lens)
+        nbs = [-(-int(n) // 16) for n in lens]
+        self.maxb = max(max(nbs), 1) + 1
+        self.nb = sum(nbs) + 7
+        perm = rng.permutation(self.nb).astype(np.int32)
+        self.tables = np.full((S, self.maxb), -1, np.int32)
+        k = 0
+        for s, n in enumerate(nbs):
+            self.tables[s, :n] = perm[k:k + n]
+            k += n
+        self.slots = np.array([self.tables[s, j // 16] * 16 + j % 16
+                               for s in range(S) for j in range(int(self.lens[s]))], np.int64)
+        T = len(self.slots)
+        self.k_rows = workloads.normal_bits(rng, (T, hkv, D), dt) if rows is None else rows[0]
+        self.v_rows = workloads.normal_bits(rng, (T, hkv, D), dt) if rows is None else rows[1]
+        self.q = workloads.normal_bits(rng, (S, hq, D), dt)
+        self.scale = 1.0 / np.sqrt(D)
+        self.o = oracle.load()
+        self.pool = KVPool(self.nb, hkv, D, "q8_" + dt, device="cuda")
+        _fill_sentinel(self.pool)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.ref = _oracle_pools(self.nb, hkv)
+        if T:
+            cache_write_q8(self.pool, to_torch(self.k_rows, self.bf, "cuda"),
+                           to_torch(self.v_rows, self.bf, "cuda"),
+                           torch.from_numpy(self.slots).cuda(), self.status)
+            assert self.o.cache_write_q8(self.k_rows, self.v_rows, self.slots, self.ref, 16,
+                                         self.bf) == 0
+        assert status_check(self.status) == (0, 0)
+        self.d_tables = torch.from_numpy(self.tables).cuda()
+        self.d_lens = torch.from_numpy(self.lens).cuda()
+        self.ws = torch.empty(decode_workspace_bytes(S, hq, hkv, D, self.maxb),
+                              dtype=torch.uint8, device="cuda")
+
+    def run(self, lens=None):
+        return paged_decode_attention_q8(self.pool, to_torch(self.q, self.bf, "cuda"),
+                                         self.d_tables, self.d_lens if lens is None else lens,
+                                         self.scale, self.ws, self.status)
+
+    def oracle_out(self):
+        out, bad = self.o.paged_decode_q8(self.q, self.ref, self.tables, self.lens, self.scale,
+                                          self.bf, self.o.max_threads())
+        assert bad == 0
+        return out
+
+
+CASES = [
+    # (context lengths, Hq, Hkv, dtype)
+    ([1, 16, 17, 33, 0, 700, 2000], 32, 8, "bf16"),     # empty, exact, ragged, split (G = 4)
+    ([5, 513, 1200], 8, 1, "f16"),                      # G = 8
+    ([300, 64, 1], 16, 16, "bf16"),                     # MHA
+    ([999, 31, 4097], 6, 3, "f16"),                     # G = 2, 257 blocks
+    ([250, 600], 24, 8, "bf16"),                        # G = 3
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c[0][:3]) + c[3] for c in CASES])
+def test_q8_decode_matches_oracle(case):
+    lens, hq, hkv, dt = case
+    c = Q8Case(lens, hq, hkv, dt, seed=len(lens) * 11 + hq)
+    _assert_pools_equal(c.pool, c.ref)               # the cache write, bit for bit
+    out = c.run()
+    assert status_check(c.status) == (0, 0)
+    assert_close(out, c.oracle_out(), f"q8 decode {case}")
+    assert torch.equal(c.run(), out)                 # repeated launches: same bits
+    if 0 in lens:
+        assert not out[list(lens).index(0)].any()
+
+
+def test_q8_cache_write_special_rows():
+    """Zero groups, huge bf16 values (scale saturates at 65504), values whose
+    scale is an fp16 subnormal, mixed magnitudes inside one row; negative slots
+    skipped, a slot past the pool flagged and skipped."""
+    rng = np.random.default_rng(81)
+    for dt in ("bf16", "f16"):
+        bf = dt == "bf16"
+        hkv, nb, T = 2, 6, 40
+        x = rng.standard_normal((2, T, hkv, D)).astype(np.float32)
+        x[:, 0] = 0.0                                           # all-zero rows
+        x[:, 1, 0, :32] = 0.0                                   # one zero group
+        x[:, 2] *= np.float32(3e38 if bf else 6e4) / np.abs(x[:, 2]).max()   # huge
+        x[:, 3] *= np.float32(2.0**-20)                         # subnormal scales
+        x[:, 4, :, ::2] *= np.float32(1e3)                      # mixed in a group
+        x[:, 5, :, :] = np.float32(2.0**-6) * np.round(x[:, 5] * 64)   # ties
+        bits = [workloads._f32_to_bf16_bits(a) if bf else a.astype(np.float16).view(np.uint16)
+                for a in x]
+        slots = rng.permutation(nb * 16)[:T].astype(np.int64)
+        slots[7] = -1
+        slots[9] = nb * 16 + 3                                  # outside the pool
+        pool = KVPool(nb, hkv, D, "q8_" + dt, device="cuda")
+        _fill_sentinel(pool)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        cache_write_q8(pool, to_torch(bits[0], bf, "cuda"), to_torch(bits[1], bf, "cuda"),
+                       torch.from_numpy(slots).cuda(), status)
+        rc, word = status_check(status)
+        assert rc == -5 and word == DEV_BAD_SLOT
+        ref = _oracle_pools(nb, hkv)
+        o = oracle.load()
+        assert o.cache_write_q8(bits[0], bits[1], slots, ref, 16, bf) == 1
+        _assert_pools_equal(pool, ref)
+        ks = ref[2].view(np.float16)
+        assert (ks[np.isfinite(ks)] <= 65504).all()
+
+
+def test_q8_stale_slots_never_read():
+    """Slots past each context hold codes -1 and NaN scales (the sentinel); the
+    result must stay finite and match the oracle, which never reads them."""
+    c = Q8Case([3, 18, 45, 100], 32, 8, "bf16", seed=5)
+    k_codes = c.pool.k_pool.cpu().numpy()
+    for s, n in enumerate(c.lens):
+        last = c.tables[s, (int(n) - 1) // 16]
+        assert (k_codes[last, :, int(n) % 16 or 16:] == -1).all()
+    out = c.run()
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, c.oracle_out(), "stale slots")
+
+
+def test_q8_context_one_is_dequantised_v():
+    """One token: every head of the group returns code * scale of that token's V
+    (to the output's rounding)."""
+    c = Q8Case([1, 1], 16, 4, "f16", seed=9)
+    out = c.run().double().cpu().numpy()
+    vc, vs = c.ref[1], c.ref[3].view(np.float16).astype(np.float64)
+    for s in range(2):
+        b = c.tables[s, 0]
+        for h in range(16):
+            g = h // 4
+            v = vc[b, g, :, 0].astype(np.float64) * np.repeat(vs[b, g, 0], 32)
+            assert np.array_equal(out[s, h], v.astype(np.float16).astype(np.float64))
+
+
+def test_q8_rejects_16bit_pool_and_wide_groups():
+    pool16 = KVPool(4, 2, D, "bf16", device="cuda")
+    q8 = KVPool(4, 1, D, "q8_bf16", device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tables = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    lens = torch.ones(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(decode_workspace_bytes(1, 16, 1, D, 2), dtype=torch.uint8, device="cuda")
+    rows = torch.zeros((1, 2, D), dtype=torch.bfloat16, device="cuda")
+    slots = torch.zeros(1, dtype=torch.int64, device="cuda")
+    with pytest.raises(PagedKVError):
+        cache_write_q8(pool16, rows, rows, slots, status)
+    q = torch.zeros((1, 16, D), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(PagedKVError):                  # G = 16 > 8
+        paged_decode_attention_q8(q8, q, tables, lens, 0.1, ws, status)
+    assert status_check(status) == (0, 0)
+
+
+def test_q8_gqa_long_sampled():
+    """Full-size GQA 32/8 long context (256 sequences, lognormal lengths up to
+    32K) in the bench's launch configuration; a sample of sequences checked
+    against the oracle, the sample's blocks bit for bit after the cache write."""
+    w = workloads.gqa_long(0)
+    lens = (w.prior_lens + w.new_tokens).astype(np.int32)
+    S, hq, hkv = w.num_seqs, w.num_q_heads, w.num_kv_heads
+    pool = KVPool(w.num_blocks, hkv, D, "q8_bf16", free_order=w.free_order, device="cuda")
+    _fill_sentinel(pool)
+    tables = np.full((S, w.max_blocks_per_seq), -1, np.int32)
+    slots = pool.append_slots(np.zeros(S, np.int32), lens, tables)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    T = int(lens.sum())
+    k_rows = torch.randn((T, hkv, D), generator=gen, device="cuda").to(torch.bfloat16)
+    v_rows = torch.randn((T, hkv, D), generator=gen, device="cuda").to(torch.bfloat16)
+    q = torch.randn((S, hq, D), generator=gen, device="cuda").to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache_write_q8(pool, k_rows, v_rows, torch.from_numpy(slots).cuda(), status)
+    ws = torch.empty(decode_workspace_bytes(S, hq, hkv, D, w.max_blocks_per_seq),
+                     dtype=torch.uint8, device="cuda")
+    out = paged_decode_attention_q8(pool, q, torch.from_numpy(tables).cuda(),
+                                    torch.from_numpy(lens).cuda(), w.scale, ws, status)
+    assert status_check(status) == (0, 0)
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(3)
+    sample = sorted({int(np.argmax(lens)), int(np.argmin(lens)),
+                     *rng.choice(S, 4, replace=False).tolist()})
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    o = oracle.load()
+    for s in sample:
+        n = int(lens[s])
+        nbs = -(-n // 16)
+        ids = tables[s, :nbs]
+        kr = to_np_bits(k_rows[starts[s]:starts[s] + n])
+        vr = to_np_bits(v_rows[starts[s]:starts[s] + n])
+        ref = _oracle_pools(nbs, hkv)
+        cslots = np.arange(n, dtype=np.int64)                   # compact pool: block i = id i
+        assert o.cache_write_q8(kr, vr, cslots, ref, 16, True) == 0
+        d_ids = torch.from_numpy(ids.astype(np.int64)).cuda()
+        got = (pool.k_pool[d_ids].cpu().numpy(), pool.v_pool[d_ids].cpu().numpy(),
+               to_np_bits(pool.k_scales[d_ids]), to_np_bits(pool.v_scales[d_ids]))
+        for a, r in zip(got, ref):
+            assert np.array_equal(a, r), f"sequence {s}: pool blocks differ"
+        ctab = np.arange(nbs, dtype=np.int32)[None, :]
+        exp, bad = o.paged_decode_q8(to_np_bits(q[s:s + 1]), ref, ctab, np.array([n], np.int32),
+                                     w.scale, True, o.max_threads())
+        assert bad == 0
+        assert_close(out[s:s + 1], exp, f"q8 gqa_long sequence {s} (context {n})")
