@@ -219,34 +219,40 @@ int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *d
  * Quantisation (a reading; the pages give only the group size and the size):
  * scale = fp16(min(max|x| / 127, 65504)); code = clamp(round-half-even(x /
  * scale), -127, 127) computed in fp32 (codes 0 when the scale is 0); the
- * cached value is code * scale.  Pools of a PKV_Q8_* ledger (head_dim 128):
- *   k_codes  int8 [num_blocks][Hkv][block_size][head_dim]   (token rows)
- *   v_codes  int8 [num_blocks][Hkv][head_dim][block_size]   (dimension rows)
- *   k_scales, v_scales  fp16 [num_blocks][Hkv][block_size][head_dim / 32]
- * kv_pool_scales_bytes gives the size of one scales pool; kv_pool_bytes with a
- * PKV_Q8_* dtype gives one codes pool. */
-size_t kv_pool_scales_bytes(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                            int32_t head_dim);
+ * cached value is code * scale.
+ *
+ * Pool layout (head_dim 128, block_size 16): one record of
+ * PKV_Q8_SLAB_BYTES bytes per (block, kv head), records in the order
+ * [num_blocks][num_kv_heads], so a block's slab is one contiguous copy:
+ *   bytes [0, 2048)     K codes: 16 rows of 128 bytes.  Token t = 4a + 2b + c
+ *                       (a in 0..3, b and c in 0..1) is row r = 8b + 2a + c; its
+ *                       16-byte chunk j (dimensions 16j .. 16j + 15) is stored
+ *                       at byte 128 r + 16 (j XOR (r mod 8)).
+ *   bytes [2048, 4096)  V codes: dimension d's 16 tokens at 2048 + 16 d + t.
+ *   bytes [4096, 4224)  K scales: fp16, token t's group i at 4096 + 8 t + 2 i.
+ *   bytes [4224, 4352)  V scales: fp16, at 4224 + 8 t + 2 i.
+ * kv_pool_bytes with PKV_Q8_BF16 / PKV_Q8_F16 gives the size of the pool. */
+#define PKV_Q8_SLAB_BYTES 4352
 
 /* Quantising cache write: k_new / v_new are bf16 (PKV_Q8_BF16) or fp16
- * (PKV_Q8_F16) rows [num_tokens][Hkv][128]; slots as in kv_cache_write.
- * Errors: PKV_ERR_INVALID_ARG (not an 8-bit pool, alignment), PKV_ERR_UNSUPPORTED
- * (head_dim other than 128), PKV_ERR_CUDA. */
+ * (PKV_Q8_F16) rows [num_tokens][Hkv][128]; slots as in kv_cache_write; kv_q8
+ * is the pool (16-byte aligned).  Errors: PKV_ERR_INVALID_ARG (not an 8-bit
+ * pool, alignment), PKV_ERR_UNSUPPORTED (head_dim other than 128 or block_size
+ * other than 16), PKV_ERR_CUDA.  Slots outside the pool: PKV_DEV_BAD_SLOT. */
 int kv_cache_write_q8(const pkv_pool *pool, const void *k_new, const void *v_new,
-                      const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
-                      void *v_codes, void *k_scales, void *v_scales, int32_t *d_status,
-                      void *stream);
+                      const int64_t *slot_mapping, int32_t num_tokens, void *kv_q8,
+                      int32_t *d_status, void *stream);
 
 /* Paged decode attention over an 8-bit cache: the result of
  * paged_decode_attention with K and V taken as code * scale.  q and out in the
- * pool's query type; workspace as paged_decode_workspace_bytes(...); head_dim
- * 128 and G <= 8.  Errors as paged_decode_attention. */
-int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q,
-                              const void *k_codes, const void *v_codes, const void *k_scales,
-                              const void *v_scales, const int32_t *block_tables,
-                              int32_t max_blocks_per_seq, const int32_t *context_lens,
-                              int32_t num_seqs, int32_t num_q_heads, float scale, void *workspace,
-                              size_t workspace_bytes, int32_t *d_status, void *stream);
+ * pool's query type (bf16 for PKV_Q8_BF16, fp16 for PKV_Q8_F16); workspace as
+ * paged_decode_workspace_bytes(...); head_dim 128, G <= 8 (PKV_ERR_UNSUPPORTED
+ * otherwise).  Errors as paged_decode_attention. */
+int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q, const void *kv_q8,
+                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                              float scale, void *workspace, size_t workspace_bytes,
+                              int32_t *d_status, void *stream);
 
 /* ------------------------------------------------- swap to host (NEXT #4) */
 

@@ -90,9 +90,9 @@ class KVPool:
     (contents uninitialised, as a pool reserved up front).
 
     With ``dtype="q8_bf16"`` or ``"q8_f16"`` (8-bit cache, one fp16 scale per 32
-    values) the device pools are ``k_codes`` int8 [nb][Hkv][bs][D], ``v_codes``
-    int8 [nb][Hkv][D][bs] and ``k_scales``/``v_scales`` fp16 [nb][Hkv][bs][D/32];
-    ``k_pool``/``v_pool`` then name the code pools.
+    values; head_dim 128, block_size 16) the device pool is ``kv`` uint8
+    [num_blocks][num_kv_heads][4352]: one record per slab holding K codes, V codes
+    and both scale runs (layout in include/pagedkv.h).
     """
 
     def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, dtype: str = "bf16",
@@ -112,29 +112,16 @@ class KVPool:
                                    self.dtype_code, _np_ptr(order) if order is not None else None,
                                    ctypes.byref(h)), "kv_pool_create")
         self._h = h
-        self.k_pool = self.v_pool = None
-        self.k_scales = self.v_scales = None
+        self.k_pool = self.v_pool = self.kv = None
         if device is not None:
             import torch
-            shape = (num_blocks, num_kv_heads, block_size, head_dim)
             if self.is_q8:
-                self.k_pool = torch.empty(shape, dtype=torch.int8, device=device)
-                self.v_pool = torch.empty((num_blocks, num_kv_heads, head_dim, block_size),
-                                          dtype=torch.int8, device=device)
-                sshape = (num_blocks, num_kv_heads, block_size, head_dim // 32)
-                self.k_scales = torch.empty(sshape, dtype=torch.float16, device=device)
-                self.v_scales = torch.empty(sshape, dtype=torch.float16, device=device)
+                self.kv = torch.empty((num_blocks, num_kv_heads, _native.PKV_Q8_SLAB_BYTES),
+                                      dtype=torch.uint8, device=device)
             else:
+                shape = (num_blocks, num_kv_heads, block_size, head_dim)
                 self.k_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
                 self.v_pool = torch.empty(shape, dtype=_torch_dtype(self.dtype_code), device=device)
-
-    @property
-    def k_codes(self):
-        return self.k_pool
-
-    @property
-    def v_codes(self):
-        return self.v_pool
 
     @property
     def handle(self):
@@ -371,9 +358,8 @@ def cache_write_q8(pool: KVPool, k_new, v_new, slot_mapping, status, stream=None
     if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
         raise ValueError("inputs must be contiguous")
     check(lib().kv_cache_write_q8(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping),
-                                  T, _t_ptr(pool.k_pool), _t_ptr(pool.v_pool),
-                                  _t_ptr(pool.k_scales), _t_ptr(pool.v_scales), _t_ptr(status),
-                                  _stream(stream)), "kv_cache_write_q8")
+                                  T, _t_ptr(pool.kv), _t_ptr(status), _stream(stream)),
+          "kv_cache_write_q8")
 
 
 def paged_decode_attention_q8(pool: KVPool, q, block_tables, context_lens, scale: float,
@@ -392,18 +378,12 @@ def paged_decode_attention_q8(pool: KVPool, q, block_tables, context_lens, scale
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables and context_lens must be int32")
     nbytes = workspace.numel() * workspace.element_size()
-    check(lib().paged_decode_attention_q8(pool.handle, _t_ptr(out), _t_ptr(q), _t_ptr(pool.k_pool),
-                                          _t_ptr(pool.v_pool), _t_ptr(pool.k_scales),
-                                          _t_ptr(pool.v_scales), _t_ptr(block_tables),
-                                          int(block_tables.shape[1]), _t_ptr(context_lens), S, hq,
-                                          float(scale), _t_ptr(workspace), nbytes, _t_ptr(status),
+    check(lib().paged_decode_attention_q8(pool.handle, _t_ptr(out), _t_ptr(q), _t_ptr(pool.kv),
+                                          _t_ptr(block_tables), int(block_tables.shape[1]),
+                                          _t_ptr(context_lens), S, hq, float(scale),
+                                          _t_ptr(workspace), nbytes, _t_ptr(status),
                                           _stream(stream)), "paged_decode_attention_q8")
     return out
-
-
-def kv_pool_scales_bytes(num_blocks: int, block_size: int, num_kv_heads: int,
-                         head_dim: int) -> int:
-    return lib().kv_pool_scales_bytes(num_blocks, block_size, num_kv_heads, head_dim)
 
 
 def status_check(status, stream=None):

@@ -14,6 +14,7 @@ LIB_PATH = os.environ.get("PKV_LIBRARY") or os.path.join(PKG, "libpagedkv.so")
 
 PKV_F16, PKV_BF16, PKV_Q8_BF16, PKV_Q8_F16 = 0, 1, 2, 3
 PKV_OK = 0
+PKV_Q8_SLAB_BYTES = 4352
 STATUS_NAMES = {
     0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_OUT_OF_BLOCKS",
     -3: "PKV_ERR_BAD_BLOCK", -4: "PKV_ERR_CUDA", -5: "PKV_ERR_DEVICE_BOUNDS",
@@ -57,10 +58,9 @@ SIGNATURES = [
      [_p, _p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _f32, _p, _sz, _p, _p]),
     ("paged_decode_attention_noalloc", ctypes.c_int,
      [_p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _f32, _p, _p]),
-    ("kv_pool_scales_bytes", _sz, [_i32, _i32, _i32, _i32]),
-    ("kv_cache_write_q8", ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _p, _p, _p, _p, _p]),
+    ("kv_cache_write_q8", ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _p, _p]),
     ("paged_decode_attention_q8", ctypes.c_int,
-     [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _f32, _p, _sz, _p, _p]),
+     [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _f32, _p, _sz, _p, _p]),
     ("kv_status_check", ctypes.c_int, [_p, _p, _pi32]),
 ]
 

@@ -133,17 +133,15 @@ __device__ __forceinline__ void q8_quantise4(const uint16_t *src, int lane, uint
     scale_bits = __half_as_ushort(dh);
 }
 
-// One warp per (token, kv head) row, head_dim 128.  K codes go to the token
-// row of the slab, V codes to the dimension rows (byte = slot in the block).
+// One warp per (token, kv head) row, head_dim 128, into the slab's record
+// (layout in pagedkv.h): lane l quantises dimensions 4l .. 4l + 3 (group l / 8).
 template <bool BF16>
 __global__ void __launch_bounds__(256)
 cache_write_q8_kernel(const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
                       const int64_t *__restrict__ slot_mapping, int64_t rows, int32_t num_kv_heads,
-                      int32_t block_size, int64_t num_slots, int8_t *__restrict__ k_codes,
-                      int8_t *__restrict__ v_codes, uint16_t *__restrict__ k_scales,
-                      uint16_t *__restrict__ v_scales, int32_t *__restrict__ status)
+                      int64_t num_slots, uint8_t *__restrict__ kv, int32_t *__restrict__ status)
 {
-    constexpr int D = 128;
+    constexpr int D = 128, BS = 16, SLAB = PKV_Q8_SLAB_BYTES;
     const int lane = threadIdx.x & 31;
     const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
@@ -155,19 +153,23 @@ cache_write_q8_kernel(const uint16_t *__restrict__ k_new, const uint16_t *__rest
             if (lane == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
             continue;
         }
-        const int64_t block = slot / block_size, off = slot - block * block_size;
-        const int64_t slab = block * num_kv_heads + h;
+        const int64_t block = slot / BS;
+        const int off = (int)(slot - block * BS);
+        uint8_t *rec = kv + (block * num_kv_heads + h) * SLAB;
         uint32_t kc, vc;
         uint16_t ks, vs;
         q8_quantise4<BF16>(k_new + r * D, lane, kc, ks);
         q8_quantise4<BF16>(v_new + r * D, lane, vc, vs);
-        *reinterpret_cast<uint32_t *>(k_codes + (slab * block_size + off) * D + 4 * lane) = kc;
+        // K: token off = 4a + 2b + c -> row 8b + 2a + c, chunk (lane / 4) rotated by the row
+        const int row = 8 * ((off >> 1) & 1) + 2 * (off >> 2) + (off & 1);
+        *reinterpret_cast<uint32_t *>(rec + row * 128 + (((lane >> 2) ^ (row & 7)) << 4) +
+                                      4 * (lane & 3)) = kc;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            v_codes[(slab * D + 4 * lane + i) * block_size + off] = (int8_t)((vc >> (8 * i)) & 0xff);
+            rec[2048 + (4 * lane + i) * BS + off] = (uint8_t)((vc >> (8 * i)) & 0xff);
         if ((lane & 7) == 0) {
-            k_scales[(slab * block_size + off) * (D / 32) + lane / 8] = ks;
-            v_scales[(slab * block_size + off) * (D / 32) + lane / 8] = vs;
+            *reinterpret_cast<uint16_t *>(rec + 4096 + off * 8 + 2 * (lane >> 3)) = ks;
+            *reinterpret_cast<uint16_t *>(rec + 4224 + off * 8 + 2 * (lane >> 3)) = vs;
         }
     }
 }
@@ -175,20 +177,16 @@ cache_write_q8_kernel(const uint16_t *__restrict__ k_new, const uint16_t *__rest
 }  // namespace
 
 extern "C" int kv_cache_write_q8(const pkv_pool *pool, const void *k_new, const void *v_new,
-                                 const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
-                                 void *v_codes, void *k_scales, void *v_scales, int32_t *d_status,
-                                 void *stream)
+                                 const int64_t *slot_mapping, int32_t num_tokens, void *kv_q8,
+                                 int32_t *d_status, void *stream)
 {
     pkv::PoolGeometry g;
     if (!pkv::pool_geometry(pool, &g) || num_tokens < 0) return PKV_ERR_INVALID_ARG;
     if (!pkv::is_8bit(g)) return PKV_ERR_INVALID_ARG;
-    if (g.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (g.head_dim != 128 || g.block_size != 16) return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PKV_OK;
-    if (!k_new || !v_new || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales ||
-        !d_status)
-        return PKV_ERR_INVALID_ARG;
-    if (((uintptr_t)k_new & 7u) || ((uintptr_t)v_new & 7u) || ((uintptr_t)k_codes & 15u) ||
-        ((uintptr_t)v_codes & 15u) || ((uintptr_t)k_scales & 15u) || ((uintptr_t)v_scales & 15u) ||
+    if (!k_new || !v_new || !slot_mapping || !kv_q8 || !d_status) return PKV_ERR_INVALID_ARG;
+    if (((uintptr_t)k_new & 7u) || ((uintptr_t)v_new & 7u) || ((uintptr_t)kv_q8 & 15u) ||
         ((uintptr_t)slot_mapping & 7u) || ((uintptr_t)d_status & 3u))
         return PKV_ERR_INVALID_ARG;
     const int64_t rows = (int64_t)num_tokens * g.num_kv_heads;
@@ -200,13 +198,11 @@ extern "C" int kv_cache_write_q8(const pkv_pool *pool, const void *k_new, const 
     if (g.dtype == PKV_Q8_BF16)
         cache_write_q8_kernel<true><<<(unsigned)blocks, threads, 0, st>>>(
             (const uint16_t *)k_new, (const uint16_t *)v_new, slot_mapping, rows, g.num_kv_heads,
-            g.block_size, slots, (int8_t *)k_codes, (int8_t *)v_codes, (uint16_t *)k_scales,
-            (uint16_t *)v_scales, d_status);
+            slots, (uint8_t *)kv_q8, d_status);
     else
         cache_write_q8_kernel<false><<<(unsigned)blocks, threads, 0, st>>>(
             (const uint16_t *)k_new, (const uint16_t *)v_new, slot_mapping, rows, g.num_kv_heads,
-            g.block_size, slots, (int8_t *)k_codes, (int8_t *)v_codes, (uint16_t *)k_scales,
-            (uint16_t *)v_scales, d_status);
+            slots, (uint8_t *)kv_q8, d_status);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -79,19 +79,12 @@ size_t kv_pool_bytes(int32_t num_blocks, int32_t block_size, int32_t num_kv_head
                      int32_t head_dim, pkv_dtype dtype)
 {
     if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
-    if (dtype == PKV_Q8_BF16 || dtype == PKV_Q8_F16)
-        return (size_t)num_blocks * num_kv_heads * block_size * head_dim;   // one-byte codes
+    if (dtype == PKV_Q8_BF16 || dtype == PKV_Q8_F16)   // codes + one fp16 scale per 32, K and V
+        return head_dim % 32 ? 0
+                             : (size_t)num_blocks * num_kv_heads * block_size *
+                                   (head_dim + head_dim / 32 * 2) * 2;
     if (dtype != PKV_F16 && dtype != PKV_BF16) return 0;
     return (size_t)num_blocks * num_kv_heads * block_size * head_dim * 2;
-}
-
-size_t kv_pool_scales_bytes(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
-                            int32_t head_dim)
-{
-    if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        head_dim % 32)
-        return 0;
-    return (size_t)num_blocks * num_kv_heads * block_size * (head_dim / 32) * 2;
 }
 
 int kv_pool_create(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,

@@ -34,14 +34,6 @@
 //   * Every wait is bounded (1 s); on expiry the kernel flags PKV_DEV_TIMEOUT,
 //     stops issuing copies, drains the ones in flight and finishes without
 //     trapping.
-//   * The 8-bit variant ("kv-cache-by-model", section 1: one-byte codes with a
-//     fp16 scale per 32 values) streams 4,352 bytes per block instead of
-//     8,192.  The MMAs take the codes themselves (exact in fp16/bf16); the K
-//     scales multiply the per-group partial scores, the V scales are folded
-//     into the softmax weights of each 32-dimension group.  Tokens are
-//     permuted inside the two 8-column MMA tiles so that each lane's four
-//     scores belong to four adjacent tokens: one 32-bit word of a dimension
-//     row of V codes, and one 32-byte run of scales.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -75,9 +67,7 @@ struct Params {
     float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned
     float *part_o;              // [pairs * Hkv * G * D]: unnormalised partition output
     int32_t *status;
-    const void *v_codes;        // 8-bit variant: V codes and both scale pools (1-D copies)
-    const void *k_scales;
-    const void *v_scales;
+    const uint8_t *kv_q8;       // 8-bit pool: one record of kQ8Slab bytes per (block, kv head)
     int64_t max_pairs;          // capacity of items / partial arrays (checked builds)
     int32_t *debug;             // first failed check: site << 24 | value (checked builds)
 };
@@ -97,31 +87,19 @@ __device__ __forceinline__ bool dbg_fail(bool ok, int32_t *dbg, int site, long l
     return false;
 }
 
-// 8-bit stage: K codes as two 1 KiB TMA boxes (128-byte swizzle), box b holding
-// tokens 4a + 2b + c in row 2a + c, then the 2 KiB of V codes (128 dimension rows
-// of 16 bytes); the scales go to a separate ring of 256 bytes per stage (K
-// scales [16][4] fp16, then V scales).
-constexpr int kQ8Stage = 4096;
-constexpr int kQ8Scales = 256;
-constexpr int kQ8TxBytes = kQ8Stage + kQ8Scales;
-
 // Shared-memory footprint of one kernel variant (without the 1 KiB alignment slack).
-template <int D, int GROWS, int NST, bool Q8 = false>
+template <int D, int GROWS, int NST>
 struct Smem {
-    static constexpr int kStageBytes = Q8 ? kQ8Stage : 2 * (D / kBoxCols) * kBoxBytes;
+    static constexpr int kStageBytes = 2 * (D / kBoxCols) * kBoxBytes;  // K slab + V slab
     static constexpr int kStagesBytes = NST * kStageBytes;
-    static constexpr int kSclBytes = Q8 ? NST * kQ8Scales : 0;
     static constexpr int kQSlotBytes = 16 * D * 2;                      // 16 query rows
     static constexpr int kQBytes = 2 * kQSlotBytes;                     // double buffered
     static constexpr int kBarBytes = (2 * NST + 4) * 8;
     static constexpr int kMetaBytes = 2 * 8 * 4;
-    // scratch row: D sums, the row's max and sum; the 8-bit layout stores
-    // column-wise and pads to 4 mod 32 words to spread the banks
-    static constexpr int kRowStride = Q8 ? D + 4 : D + 2;
     static constexpr int kScratchBytes =
-        kConsumerWarps * GROWS * kRowStride * 4 + NST * 4 + kConsumerWarps * 4 + 16;
+        kConsumerWarps * GROWS * (D + 2) * 4 + NST * 4 + kConsumerWarps * 4 + 16;
     static constexpr int kTotal =
-        1024 + kStagesBytes + kSclBytes + kQBytes + kBarBytes + kMetaBytes + kScratchBytes;
+        1024 + kStagesBytes + kQBytes + kBarBytes + kMetaBytes + kScratchBytes;
 };
 
 // Item metadata the producer hands to the consumers with each item's Q rows.
@@ -204,151 +182,27 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     if (tid == 0) p.header[0] = carry;
 }
 
-// ------------------------------------------------------------ 8-bit block step
-// One 16-token block of an 8-bit slab for the G <= 8 query rows of a warp, all
-// products on fp16 tensor cores (codes are exact in fp16; bf16 queries enter as
-// fp16 after a power-of-two prescale of their row, exact in the fp16 normal range).
-//
-// S = Q K^T: Q rows as A (rows 8-15 zero), K codes as B.  Column c of tile b is
-// token 4 (c >> 1) + 2b + (c & 1), so lane (hrow, q4) holds the scores of tokens
-// 4q4 .. 4q4 + 3 of query row hrow; the K scales multiply the partial score of
-// each 32-dimension group.
-//   S[t] = sum_i ks[t][i] * (q . codes[t]) over group i
-// O^T = V^T P^T: V codes as A (16 dimensions per MMA, k = the 16 tokens), the
-// softmax weights times the V scale of the group as B -- exactly the four weights
-// the lane holds -- so o[t] covers dimensions 16t + r and 16t + r + 8 (r = lane/4)
-// of query rows 2q4 and 2q4 + 1.
-//   O[d][h] += sum_t vcode[d][t] * (p[h][t] * vs[t][d / 32])
-template <bool BF16>
-__device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *scales,
-                                                 const uint32_t (&qa)[8][4], float (&o)[16][4],
-                                                 float &m0, float &l0, int valid,
-                                                 float scale_row, int lane)
-{
-    using H = Elem<false>;
-    const int q4 = lane & 3, r8 = lane & 7;
-    // ldmatrix rows: matrix (lane >> 3) = (tile (lane >> 3) & 1, step 2i + (lane >> 4))
-    const uint32_t krow = kb + ((lane >> 3) & 1) * 1024 + r8 * 128;
-    const int kstep_hi = lane >> 4;
-    const uint32_t vb = kb + 2048;
-
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-        float ks[4][4];        // [token j][group i]
-        const uint4 a = *reinterpret_cast<const uint4 *>(scales + 32 * q4);
-        const uint4 b = *reinterpret_cast<const uint4 *>(scales + 32 * q4 + 16);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
-            ks[k >> 1][2 * (k & 1)] = f.x;
-            ks[k >> 1][2 * (k & 1) + 1] = f.y;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t kr[4];
-            ldsm_x4(kr, krow + (((2 * i + kstep_hi) ^ r8) << 4));
-            float c0[4], c1[4];
-            uint32_t lo, hi;
-            codes_to_pairs<false>(kr[0], lo, hi);
-            H::mma0(c0, qa[2 * i], lo, hi);
-            codes_to_pairs<false>(kr[1], lo, hi);
-            H::mma0(c1, qa[2 * i], lo, hi);
-            codes_to_pairs<false>(kr[2], lo, hi);
-            H::mma(c0, qa[2 * i + 1], lo, hi);
-            codes_to_pairs<false>(kr[3], lo, hi);
-            H::mma(c1, qa[2 * i + 1], lo, hi);
-            sc[0] = fmaf(ks[0][i], c0[0], sc[0]);
-            sc[1] = fmaf(ks[1][i], c0[1], sc[1]);
-            sc[2] = fmaf(ks[2][i], c1[0], sc[2]);
-            sc[3] = fmaf(ks[3][i], c1[1], sc[3]);
-        }
-    }
-    float x[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] = sc[j] * scale_row;
-    float vs[4][4];
-    {
-        const uint4 a = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4);
-        const uint4 b = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4 + 16);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
-            vs[k >> 1][2 * (k & 1)] = f.x;
-            vs[k >> 1][2 * (k & 1) + 1] = f.y;
-        }
-    }
-    if (valid < kBlock) {
-        // tokens past the context: no score, and no scale (a stale one may be NaN)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (4 * q4 + j >= valid) {
-                x[j] = -INFINITY;
-                vs[j][0] = vs[j][1] = vs[j][2] = vs[j][3] = 0.f;
-            }
-    }
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    const float mn = fmaxf(m0, mx);
-    const float a0 = exp2f(m0 - mn);
-    float pj[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) pj[j] = exp2f(x[j] - mn);
-    l0 = l0 * a0 + ((pj[0] + pj[1]) + (pj[2] + pj[3]));
-    m0 = mn;
-    if (__any_sync(kFull, a0 != 1.f)) {
-        // this lane's accumulators belong to query rows 2q4 and 2q4 + 1
-        const float f0 = __shfl_sync(kFull, a0, 8 * q4);
-        const float f1 = __shfl_sync(kFull, a0, 8 * q4 + 4);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            o[t][0] *= f0; o[t][1] *= f1; o[t][2] *= f0; o[t][3] *= f1;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t b0 = H::pack(pj[0] * vs[0][i], pj[1] * vs[1][i]);
-        const uint32_t b1 = H::pack(pj[2] * vs[2][i], pj[3] * vs[3][i]);
-        // matrix m: dimensions 32i + 8m .. 32i + 8m + 7 (lane row r = dimension)
-        uint32_t vr[4];
-        ldsm_x4(vr, vb + (32 * i + lane) * 16);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            uint32_t a[4];
-            codes_to_pairs<false>(vr[2 * t], a[0], a[2]);
-            codes_to_pairs<false>(vr[2 * t + 1], a[1], a[3]);
-            H::mma(o[2 * i + t], a, b0, b1);
-        }
-    }
-}
-
 // ----------------------------------------------------------------- main kernel
-// Q8: tmK / tmV are the two K-code box maps of the 8-bit pool (tokens 4a + c and
-// 4a + 2 + c of every slab); V codes and scales come by 1-D bulk copies.
-template <int D, bool BF16, int GROWS, int NST, int MINB, bool Q8 = false>
+template <int D, bool BF16, int GROWS, int NST, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const Params p)
 {
     using E = Elem<BF16>;
     using T = typename E::T;
-    using SM = Smem<D, GROWS, NST, Q8>;
+    using SM = Smem<D, GROWS, NST>;
     static_assert(NST % kConsumerWarps == 0, "each slot must keep one consumer warp");
-    static_assert(!Q8 || (D == 128 && GROWS == 8), "8-bit variant: head_dim 128, G <= 8");
     constexpr int kBoxes = D / kBoxCols;          // TMA boxes per slab
     constexpr int kSlabBytes = kBoxes * kBoxBytes;
     constexpr int KSTEPS = D / 16;                // QK reduction steps
     constexpr int NTILES = D / 8;                 // PV output tiles of 8 dims
-    constexpr int OSTRIDE = SM::kRowStride;       // padded scratch row
+    constexpr int OSTRIDE = D + 2;                // padded scratch row
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = base;
-    uint8_t *scl = base + SM::kStagesBytes;                                // 8-bit: scale ring
-    uint8_t *qbuf = scl + SM::kSclBytes;                                   // [2][16][D]
+    uint8_t *qbuf = base + SM::kStagesBytes;                               // [2][16][D]
     uint64_t *full_bar = reinterpret_cast<uint64_t *>(qbuf + SM::kQBytes);
     uint64_t *empty_bar = full_bar + NST;
     uint64_t *qfull_bar = empty_bar + NST;
@@ -452,30 +306,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         if (mbar_wait(smem_addr(&empty_bar[slot]), par ^ 1u, sm_abort, p.status)) {
                             if (pid >= 0 && pid < p.num_blocks) {
                                 stage_bad[slot] = 0;
+                                mbar_arrive_expect_tx(fb, 2 * kSlabBytes);
                                 const uint32_t dk = smem_addr(stages + slot * SM::kStageBytes);
-                                if constexpr (Q8) {
-                                    mbar_arrive_expect_tx(fb, kQ8TxBytes);
-                                    const int64_t slab = (int64_t)pid * Hkv + g;
-                                    const uint32_t ds = smem_addr(scl + slot * kQ8Scales);
-                                    tma_load_3d(dk, &tmK, 0, 0, (int)(slab * 4), fb);
-                                    tma_load_3d(dk + 1024, &tmV, 0, 0, (int)(slab * 4), fb);
-                                    bulk_load(dk + 2048,
-                                              static_cast<const uint8_t *>(p.v_codes) + slab * 2048,
-                                              2048, fb);
-                                    bulk_load(ds, static_cast<const uint8_t *>(p.k_scales) + slab * 128,
-                                              128, fb);
-                                    bulk_load(ds + 128,
-                                              static_cast<const uint8_t *>(p.v_scales) + slab * 128,
-                                              128, fb);
-                                } else {
-                                    mbar_arrive_expect_tx(fb, 2 * kSlabBytes);
-                                    const uint32_t dv = dk + kSlabBytes;
-                                    const int y = (pid * Hkv + g) * kBlock;
+                                const uint32_t dv = dk + kSlabBytes;
+                                const int y = (pid * Hkv + g) * kBlock;
 #pragma unroll
-                                    for (int bx = 0; bx < kBoxes; ++bx) {
-                                        tma_load_2d(dk + bx * kBoxBytes, &tmK, bx * kBoxCols, y, fb);
-                                        tma_load_2d(dv + bx * kBoxBytes, &tmV, bx * kBoxCols, y, fb);
-                                    }
+                                for (int bx = 0; bx < kBoxes; ++bx) {
+                                    tma_load_2d(dk + bx * kBoxBytes, &tmK, bx * kBoxCols, y, fb);
+                                    tma_load_2d(dv + bx * kBoxBytes, &tmV, bx * kBoxCols, y, fb);
                                 }
                                 issued |= 1u << slot;
                                 issued_par = (issued_par & ~(1u << slot)) | (par << slot);
@@ -530,47 +368,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const ItemMeta mt = q_ok ? sm_meta[qs] : ItemMeta{0, 0, 0, 0, 0, 1, 0, 0};
         // Q rows of the group as the A operand (rows >= G are zero in shared memory)
         uint32_t qa[KSTEPS][4];
-        float scale_row = p.scale_log2;
-        if constexpr (Q8) {
-            // fp16 A operand, dimensions permuted inside each 16-wide step to match
-            // the K-code words: k slots 2q4 + e <- 16kk + 4q4 + e and
-            // 8 + 2q4 + e <- 16kk + 4q4 + 2 + e
-            const uint8_t *qrow = qbuf + qs * SM::kQSlotBytes + hrow * (D * 2);
-            uint2 v[KSTEPS];
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk)
-                v[kk] = q_ok ? *reinterpret_cast<const uint2 *>(qrow + (16 * kk + 4 * q4) * 2)
-                             : make_uint2(0u, 0u);
-            if constexpr (BF16) {
-                // bf16 row -> fp16 after scaling by 2^-E, E >= 0 the smallest that
-                // brings the row's largest magnitude below 2^15; exact for every
-                // element in the fp16 normal range.  2^E goes into the row's scale.
-                float amax = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk) {
-                    const float2 f0 = E::unpack(v[kk].x), f1 = E::unpack(v[kk].y);
-                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
-                                             fmaxf(fabsf(f1.x), fabsf(f1.y))));
-                }
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-                const int e = max(0, ((__float_as_int(amax) >> 23) & 0xff) - 127 - 14);
-                const float down = __int_as_float((127 - e) << 23);
-                scale_row = p.scale_log2 * __int_as_float((127 + e) << 23);
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk) {
-                    const float2 f0 = E::unpack(v[kk].x), f1 = E::unpack(v[kk].y);
-                    qa[kk][0] = Elem<false>::pack(f0.x * down, f0.y * down);
-                    qa[kk][2] = Elem<false>::pack(f1.x * down, f1.y * down);
-                    qa[kk][1] = qa[kk][3] = 0u;
-                }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk) {
-                    qa[kk][0] = v[kk].x; qa[kk][1] = 0u; qa[kk][2] = v[kk].y; qa[kk][3] = 0u;
-                }
-            }
-        } else {
+        {
             const uint32_t qb = smem_addr(qbuf + qs * SM::kQSlotBytes);
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
@@ -606,10 +404,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const uint32_t vb = kb + kSlabBytes;
             if (dbg_fail(slot < NST && (kb & 1023u) == 0u, p.debug, 7, slot)) continue;
 
-            if constexpr (Q8) {
-                consume_q8_block<BF16>(kb, scl + slot * kQ8Scales, qa, o, m0, l0, valid,
-                                       scale_row, lane);
-            } else {
             // ---- S = Q K^T : two 8-token tiles, two accumulation chains each
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
             float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -715,7 +509,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     E::mma(o[2 * jj + 1], pb, vr[2], vr[3]);
                 }
             }
-            }   // 16-bit block
             // The stage's next contents arrive through the async proxy (TMA):
             // order this warp's generic-proxy reads of it before the release.
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -745,17 +538,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 wo[(hrow + 8) * OSTRIDE + D + 1] = l1;
             }
         }
-        if constexpr (Q8) {
-            // o[t]: dimensions 16t + hrow (+ 8) of query rows 2q4 and 2q4 + 1
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int d = 16 * t + hrow;
-                wo[(2 * q4) * OSTRIDE + d] = o[t][0];
-                wo[(2 * q4 + 1) * OSTRIDE + d] = o[t][1];
-                wo[(2 * q4) * OSTRIDE + d + 8] = o[t][2];
-                wo[(2 * q4 + 1) * OSTRIDE + d + 8] = o[t][3];
-            }
-        } else
 #pragma unroll
         for (int j = 0; j < NTILES; ++j) {
             const int d0 = 8 * j + 2 * q4;
@@ -878,6 +660,425 @@ __global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
     }
 }
 
+// ================================================================== 8-bit path
+// An 8-bit pool ("kv-cache-by-model", section 1: one-byte codes with one fp16
+// scale per 32 values) keeps each (block, kv head) slab as one record of
+// q8::kSlab = 4,352 bytes, so a block costs one bulk copy:
+//   [0, 2048)     K codes, 16 rows of 128 bytes: token t = 4a + 2b + c sits in
+//                 row 8b + 2a + c, its 16-byte chunk j at position j ^ (row & 7)
+//   [2048, 4096)  V codes, 128 dimension rows of 16 bytes (byte = token)
+//   [4096, 4224)  K scales, fp16 [16 tokens][4 groups of 32 dimensions]
+//   [4224, 4352)  V scales, the same
+// The row order puts the tokens of each 8-column MMA tile in rows 0-7 and 8-15,
+// and the chunk rotation lets ldmatrix read them without bank conflicts.
+//
+// Work division: every warp is its own producer.  A warp takes whole items
+// (sequence, kv head, partition of up to 32 blocks) in a fixed stride over the
+// grid, keeps a private ring of kSlots stages and issues the bulk copy of block
+// i + kSlots -- across item boundaries, with the next item's metadata and block
+// ids prefetched into registers -- right after it has consumed block i.  The
+// next item's query rows are copied into the warp's query buffer as soon as the
+// current item's rows have been read out of it.  No producer warp, no cross-warp barriers, no shared-memory merge:
+// the warp writes its rows (or its partition's piece) itself.
+namespace q8 {
+#ifndef PKV_Q8_WARPS
+#define PKV_Q8_WARPS 4
+#endif
+#ifndef PKV_Q8_SLOTS
+#define PKV_Q8_SLOTS 3
+#endif
+#ifndef PKV_Q8_CTAS
+#define PKV_Q8_CTAS 3
+#endif
+constexpr int kSlab = 4352;
+constexpr int kWarps = PKV_Q8_WARPS;             // independent warps per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlots = PKV_Q8_SLOTS;             // ring stages per warp
+constexpr int kMinBlocks = PKV_Q8_CTAS;          // CTAs per SM
+constexpr int kQBytes = 8 * 128 * 2;              // one item's query rows (G <= 8), fp16/bf16
+constexpr int kWarpBytes = kSlots * kSlab + kQBytes + 128;   // stages, query rows, barriers
+constexpr int kSmemBytes = 128 + kWarps * kWarpBytes;
+static_assert(kSlab % 128 == 0 && kWarpBytes % 128 == 0, "stages stay 128-byte aligned");
+}  // namespace q8
+
+// ------------------------------------------------------------ 8-bit block step
+// One 16-token block of an 8-bit slab for the G <= 8 query rows of a warp, all
+// products on fp16 tensor cores (codes are exact in fp16; bf16 queries enter as
+// fp16 after a power-of-two prescale of their row, exact in the fp16 normal range).
+//
+// S = Q K^T: Q rows as A (rows 8-15 zero), K codes as B.  Column c of tile b is
+// token 4 (c >> 1) + 2b + (c & 1), so lane (hrow, q4) holds the scores of tokens
+// 4q4 .. 4q4 + 3 of query row hrow; the K scales multiply the partial score of
+// each 32-dimension group.
+//   S[t] = sum_i ks[t][i] * (q . codes[t]) over group i
+// O^T = V^T P^T: V codes as A (16 dimensions per MMA, k = the 16 tokens), the
+// softmax weights times the V scale of the group as B -- exactly the four weights
+// the lane holds -- so o[t] covers dimensions 16t + r and 16t + r + 8 (r = lane/4)
+// of query rows 2q4 and 2q4 + 1.
+//   O[d][h] += sum_t vcode[d][t] * (p[h][t] * vs[t][d / 32])
+__device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *scales,
+                                                 const uint32_t (&qa)[8][4], float (&o)[8][4],
+                                                 float &m0, float &l0, int valid,
+                                                 float scale_row, int lane)
+{
+    using H = Elem<false>;
+    const int q4 = lane & 3, r8 = lane & 7;
+    // ldmatrix rows: matrix (lane >> 3) = (tile (lane >> 3) & 1, step 2i + (lane >> 4))
+    const uint32_t krow = kb + ((lane >> 3) & 1) * 1024 + r8 * 128;
+    const int kstep_hi = lane >> 4;
+    const uint32_t vb = kb + 2048;
+
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        float ks[4][4];        // [token j][group i]
+        const uint4 a = *reinterpret_cast<const uint4 *>(scales + 32 * q4);
+        const uint4 b = *reinterpret_cast<const uint4 *>(scales + 32 * q4 + 16);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            ks[k >> 1][2 * (k & 1)] = f.x;
+            ks[k >> 1][2 * (k & 1) + 1] = f.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t kr[4];
+            ldsm_x4(kr, krow + (((2 * i + kstep_hi) ^ r8) << 4));
+            float c0[4], c1[4];
+            uint32_t lo, hi;
+            codes_to_pairs<false>(kr[0], lo, hi);
+            H::mma0(c0, qa[2 * i], lo, hi);
+            codes_to_pairs<false>(kr[1], lo, hi);
+            H::mma0(c1, qa[2 * i], lo, hi);
+            codes_to_pairs<false>(kr[2], lo, hi);
+            H::mma(c0, qa[2 * i + 1], lo, hi);
+            codes_to_pairs<false>(kr[3], lo, hi);
+            H::mma(c1, qa[2 * i + 1], lo, hi);
+            sc[0] = fmaf(ks[0][i], c0[0], sc[0]);
+            sc[1] = fmaf(ks[1][i], c0[1], sc[1]);
+            sc[2] = fmaf(ks[2][i], c1[0], sc[2]);
+            sc[3] = fmaf(ks[3][i], c1[1], sc[3]);
+        }
+    }
+    float x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = sc[j] * scale_row;
+    float vs[4][4];
+    {
+        const uint4 a = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4);
+        const uint4 b = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4 + 16);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            vs[k >> 1][2 * (k & 1)] = f.x;
+            vs[k >> 1][2 * (k & 1) + 1] = f.y;
+        }
+    }
+    if (valid < kBlock) {
+        // tokens past the context: no score, and no scale (a stale one may be NaN)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (4 * q4 + j >= valid) {
+                x[j] = -INFINITY;
+                vs[j][0] = vs[j][1] = vs[j][2] = vs[j][3] = 0.f;
+            }
+    }
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float mn = fmaxf(m0, mx);
+    const float a0 = exp2f(m0 - mn);
+    float pj[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pj[j] = exp2f(x[j] - mn);
+    l0 = l0 * a0 + ((pj[0] + pj[1]) + (pj[2] + pj[3]));
+    m0 = mn;
+    if (__any_sync(kFull, a0 != 1.f)) {
+        // this lane's accumulators belong to query rows 2q4 and 2q4 + 1
+        const float f0 = __shfl_sync(kFull, a0, 8 * q4);
+        const float f1 = __shfl_sync(kFull, a0, 8 * q4 + 4);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            o[t][0] *= f0; o[t][1] *= f1; o[t][2] *= f0; o[t][3] *= f1;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b0 = H::pack(pj[0] * vs[0][i], pj[1] * vs[1][i]);
+        const uint32_t b1 = H::pack(pj[2] * vs[2][i], pj[3] * vs[3][i]);
+        // matrix m: dimensions 32i + 8m .. 32i + 8m + 7 (lane row r = dimension)
+        uint32_t vr[4];
+        ldsm_x4(vr, vb + (32 * i + lane) * 16);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            uint32_t a[4];
+            codes_to_pairs<false>(vr[2 * t], a[0], a[2]);
+            codes_to_pairs<false>(vr[2 * t + 1], a[1], a[3]);
+            H::mma(o[2 * i + t], a, b0, b1);
+        }
+    }
+}
+
+// An item as one warp sees it; lane l holds the id of the item's block l.
+struct Q8Item {
+    int item;        // global item index; >= the item count: none
+    int s, g, L, b0, nb, nsplit, pair;
+    int id;
+};
+
+__device__ __forceinline__ void q8_load_item(const Params &p, int it, int total, int lane,
+                                             Q8Item &c)
+{
+    c.item = it;
+    c.nb = 0;
+    if (it >= total) return;
+    const int Hkv = p.num_kv_heads;
+    const int pi = it / Hkv;
+    c.g = it - pi * Hkv;
+    const int2 sp = p.items[pi];
+    c.s = sp.x;
+    c.L = __ldg(p.context_lens + sp.x);
+    const int2 info = __ldg(p.seq_info + sp.x);
+    c.nsplit = info.y;
+    c.pair = info.x + sp.y;
+    c.b0 = sp.y * p.blocks_per_split;
+    c.nb = min(p.blocks_per_split, (c.L + kBlock - 1) / kBlock - c.b0);
+    c.id = lane < c.nb
+               ? __ldg(p.block_tables + (int64_t)c.s * p.max_blocks_per_seq + c.b0 + lane)
+               : 0;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
+    decode_q8_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                     const Params p)
+{
+    using namespace q8;
+    using E = Elem<BF16>;
+    using T = typename E::T;
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    __shared__ int cta_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hrow = lane >> 2, q4 = lane & 3;
+    uint8_t *ring = base + warp * kWarpBytes;
+    uint8_t *qbuf = ring + kSlots * kSlab;                       // [8 rows][128]
+    uint64_t *full = reinterpret_cast<uint64_t *>(qbuf + kQBytes);
+    uint64_t *qfull = full + kSlots;
+    volatile int *abort_flag = &cta_abort;
+    if (threadIdx.x == 0) cta_abort = 0;
+    // query rows >= G stay zero: the copies write G rows only
+    for (int i = lane; i < kQBytes / 16; i += 32)
+        reinterpret_cast<uint4 *>(qbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) {
+        for (int i = 0; i <= kSlots; ++i) mbar_init(smem_addr(&full[i]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    griddep_wait();                // the work list comes from the prep kernel
+
+    const int Hkv = p.num_kv_heads, G = p.group;
+    const int total = p.header[0] * Hkv;
+    const int wstride = gridDim.x * kWarps;
+    Q8Item cur, nxt;
+    q8_load_item(p, blockIdx.x * kWarps + warp, total, lane, cur);
+    q8_load_item(p, cur.item + wstride, total, lane, nxt);
+
+    // copy cursor: block cj of the current item, or of the next one (cnext)
+    int cj = 0;
+    bool cnext = false;
+    uint32_t issued = 0, used = 0, bad_mask = 0;
+    auto issue = [&]() {
+        if (!cnext && cj >= cur.nb) {
+            cnext = true;
+            cj = 0;
+        }
+        const int c_item = cnext ? nxt.item : cur.item;
+        const int c_nb = cnext ? nxt.nb : cur.nb;
+        if (c_item >= total || cj >= c_nb) return;
+        const int id = __shfl_sync(kFull, cnext ? nxt.id : cur.id, cj);
+        const int c_g = cnext ? nxt.g : cur.g;
+        const int slot = (int)(issued % kSlots);
+        const bool ok = id >= 0 && id < p.num_blocks;
+        if (lane == 0) {
+            const uint32_t fb = smem_addr(&full[slot]);
+            if (ok) {
+                mbar_arrive_expect_tx(fb, kSlab);
+                bulk_load(smem_addr(ring + slot * kSlab),
+                          p.kv_q8 + ((int64_t)id * Hkv + c_g) * kSlab, kSlab, fb);
+            } else {
+                atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                mbar_arrive(fb);
+            }
+        }
+        bad_mask = ok ? bad_mask & ~(1u << slot) : bad_mask | (1u << slot);
+        ++issued;
+        ++cj;
+    };
+    // query rows of an item: one bulk copy of G rows into the warp's buffer
+    const uint32_t q_bytes = (uint32_t)(G * D * 2);
+    uint32_t q_issued = 0, q_used = 0;
+    auto issue_q = [&](int s, int g) {
+        if (lane == 0) {
+            const uint32_t qb = smem_addr(qfull);
+            mbar_arrive_expect_tx(qb, q_bytes);
+            bulk_load(smem_addr(qbuf),
+                      static_cast<const T *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)g * G) * D,
+                      q_bytes, qb);
+        }
+        ++q_issued;
+    };
+    if (cur.item < total) issue_q(cur.s, cur.g);
+    for (int k = 0; k < kSlots; ++k) issue();
+
+    bool alive = true;
+    while (alive && cur.item < total) {
+        // this lane's query words: row hrow, dimensions 16kk + 4q4 .. + 3
+        const bool q_landed = mbar_wait(smem_addr(qfull), q_used & 1u, abort_flag, p.status);
+        if (!__all_sync(kFull, q_landed)) break;
+        ++q_used;
+        uint2 qw[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            qw[kk] = *reinterpret_cast<const uint2 *>(qbuf + hrow * (D * 2) + (16 * kk + 4 * q4) * 2);
+        // the buffer is free: the next item's rows may come in (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (nxt.item < total) issue_q(nxt.s, nxt.g);
+        // ---- the item's query rows as fp16 A fragments (rows 8-15 zero);
+        // dimensions permuted inside each 16-wide step to match the K-code words:
+        // k slots 2q4 + e <- 16kk + 4q4 + e, 8 + 2q4 + e <- 16kk + 4q4 + 2 + e
+        uint32_t qa[8][4];
+        float scale_row = p.scale_log2;
+        if constexpr (BF16) {
+            // bf16 row -> fp16 after scaling by 2^-e, e >= 0 the smallest that
+            // brings the row's largest magnitude below 2^15; exact for every
+            // element in the fp16 normal range.  2^e goes into the row's scale.
+            float amax = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const float2 f0 = E::unpack(qw[kk].x), f1 = E::unpack(qw[kk].y);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
+                                         fmaxf(fabsf(f1.x), fabsf(f1.y))));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+            const int e = max(0, ((__float_as_int(amax) >> 23) & 0xff) - 127 - 14);
+            const float down = __int_as_float((127 - e) << 23);
+            scale_row = p.scale_log2 * __int_as_float((127 + e) << 23);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const float2 f0 = E::unpack(qw[kk].x), f1 = E::unpack(qw[kk].y);
+                qa[kk][0] = Elem<false>::pack(f0.x * down, f0.y * down);
+                qa[kk][2] = Elem<false>::pack(f1.x * down, f1.y * down);
+                qa[kk][1] = qa[kk][3] = 0u;
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                qa[kk][0] = qw[kk].x; qa[kk][1] = 0u; qa[kk][2] = qw[kk].y; qa[kk][3] = 0u;
+            }
+        }
+
+        float o[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+        float m0 = -INFINITY, l0 = 0.f;
+        uint32_t bad = 0;
+        for (int j = 0; j < cur.nb; ++j) {
+            const int slot = (int)(used % kSlots);
+            const bool landed = mbar_wait(smem_addr(&full[slot]), (used / kSlots) & 1u,
+                                          abort_flag, p.status);
+            if (!__all_sync(kFull, landed)) {
+                alive = false;
+                break;
+            }
+            const uint32_t b = (bad_mask >> slot) & 1u;
+            bad |= b;
+            if (!b) {
+                const int valid = min(kBlock, cur.L - (cur.b0 + j) * kBlock);
+                uint8_t *st = ring + slot * kSlab;
+                consume_q8_block(smem_addr(st), st + 4096, qa, o, m0, l0, valid, scale_row, lane);
+            }
+            // the next copy into this stage goes through the async proxy: order
+            // this warp's reads of it first
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            ++used;
+            issue();
+        }
+        if (!alive) break;
+
+        // ---- the item's result.  Lane (hrow, q4) holds dimensions 16t + hrow
+        // (+ 8) of query rows 2q4 and 2q4 + 1; row sums come from that row's lanes.
+        float lsum = l0 + __shfl_xor_sync(kFull, l0, 1);
+        lsum += __shfl_xor_sync(kFull, lsum, 2);
+        const float mA = __shfl_sync(kFull, m0, 8 * q4), lA = __shfl_sync(kFull, lsum, 8 * q4);
+        const float mB = __shfl_sync(kFull, m0, 8 * q4 + 4);
+        const float lB = __shfl_sync(kFull, lsum, 8 * q4 + 4);
+        (void)mA; (void)mB;
+        const int hA = 2 * q4, hB = 2 * q4 + 1;
+        if (cur.nsplit == 1) {
+            T *out = static_cast<T *>(p.out) + ((size_t)cur.s * p.num_q_heads + (size_t)cur.g * G) * D;
+            const float iA = 1.f / lA, iB = 1.f / lB;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int d = 16 * t + hrow;
+                if (hA < G) {
+                    out[hA * D + d] = E::from_float(bad ? 0.f : o[t][0] * iA);
+                    out[hA * D + d + 8] = E::from_float(bad ? 0.f : o[t][2] * iA);
+                }
+                if (hB < G) {
+                    out[hB * D + d] = E::from_float(bad ? 0.f : o[t][1] * iB);
+                    out[hB * D + d + 8] = E::from_float(bad ? 0.f : o[t][3] * iB);
+                }
+            }
+        } else {
+            const size_t piece = (size_t)cur.pair * Hkv + cur.g;
+            float *po = p.part_o + piece * G * D;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int d = 16 * t + hrow;
+                if (hA < G) {
+                    po[hA * D + d] = o[t][0];
+                    po[hA * D + d + 8] = o[t][2];
+                }
+                if (hB < G) {
+                    po[hB * D + d] = o[t][1];
+                    po[hB * D + d + 8] = o[t][3];
+                }
+            }
+            if (q4 == 0 && hrow < G)
+                p.part_ml[piece * G + hrow] = make_float2(m0, bad ? -1.f : lsum);
+        }
+
+        // ---- move on: the copy cursor, if already in the next item, stays there
+        cur = nxt;
+        cnext = false;
+        q8_load_item(p, cur.item + wstride, total, lane, nxt);
+    }
+
+    // after a timed-out wait: let the copies still in flight land before exit
+    if (lane == 0) {
+        for (uint32_t k = used; k < issued + (q_issued - q_used); ++k) {
+            const bool is_q = k >= issued;     // the query copy, if one is pending
+            const uint32_t fb = smem_addr(is_q ? qfull : &full[k % kSlots]);
+            const uint32_t par = is_q ? (q_used & 1u) : (k / kSlots) & 1u;
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(fb, par)) {
+                if (globaltimer() - t0 > kTimeoutNs) {
+                    atomicOr(p.status, PKV_DEV_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    }
+}
+
 // --------------------------------------------------------------------- host side
 struct WsLayout {
     size_t header, seq_info, items, part_ml, part_o, total;
@@ -938,48 +1139,28 @@ static bool make_pool_map(CUtensorMap *map, const void *pool, const PoolGeometry
     return r == CUDA_SUCCESS;
 }
 
-// The two K-code maps of an 8-bit pool: rows of 128 bytes viewed as
-// (byte, c in {0, 1} at stride 128, a at stride 512), box {128, 2, 4} with the
-// 128-byte swizzle.  Map 0 starts at the pool (tokens 4a + c of each slab), map
-// 1 at +256 bytes (tokens 4a + 2 + c); coordinate a = 4 * slab selects a slab.
-static bool make_q8_key_maps(CUtensorMap *m0, CUtensorMap *m1, const void *k_codes,
-                             const PoolGeometry &g)
-{
-    EncodeFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t slabs = (cuuint64_t)g.num_blocks * g.num_kv_heads;
-    cuuint64_t dims[3] = {128, 2, slabs * 4};
-    cuuint64_t strides[2] = {128, 512};
-    cuuint32_t box[3] = {128, 2, 4};
-    cuuint32_t estr[3] = {1, 1, 1};
-    for (int b = 0; b < 2; ++b) {
-        CUresult r = enc(b ? m1 : m0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
-                         const_cast<uint8_t *>(static_cast<const uint8_t *>(k_codes)) + 256 * b,
-                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return false;
-    }
-    return true;
-}
-
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
 
 struct Variant {
     KernelFn fn;
     int smem;
+    int threads;
+    int items_per_cta;      // items a CTA works on at once (consumer groups)
 };
 
-template <int D, bool BF16, int GROWS, int NST, int MINB, bool Q8 = false>
+template <int D, bool BF16, int GROWS, int NST, int MINB>
 static Variant variant()
 {
-    return Variant{reinterpret_cast<KernelFn>(&decode_kernel<D, BF16, GROWS, NST, MINB, Q8>),
-                   Smem<D, GROWS, NST, Q8>::kTotal};
+    return Variant{reinterpret_cast<KernelFn>(&decode_kernel<D, BF16, GROWS, NST, MINB>),
+                   Smem<D, GROWS, NST>::kTotal, kThreads, 1};
 }
 
-// 8-bit variant: 8 stages of 4,352 bytes, three CTAs per SM.
-constexpr int kQ8Stages = 8;
-constexpr int kQ8MinBlocks = 3;
+static Variant q8_variant(bool bf16)
+{
+    const KernelFn fn = bf16 ? reinterpret_cast<KernelFn>(&decode_q8_kernel<true>)
+                             : reinterpret_cast<KernelFn>(&decode_q8_kernel<false>);
+    return Variant{fn, q8::kSmemBytes, q8::kThreads, q8::kWarps};
+}
 
 static bool pick_variant(int D, bool bf16, int G, Variant *v)
 {
@@ -1020,7 +1201,7 @@ static int persistent_ctas(const Variant &v, int *num_sms_out)
                 return -1;
             int n = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &n, reinterpret_cast<const void *>(v.fn), kThreads, v.smem) != cudaSuccess ||
+                    &n, reinterpret_cast<const void *>(v.fn), v.threads, v.smem) != cudaSuccess ||
                 n < 1)
                 return -1;
             fns[dev][i] = v.fn;
@@ -1031,14 +1212,9 @@ static int persistent_ctas(const Variant &v, int *num_sms_out)
     return -1;
 }
 
-// Pool memory of one call: the K and V pools (16-bit), or the K and V codes and
-// the two scale pools (8-bit).
-struct PoolPtrs {
-    const void *k, *v, *ks, *vs;
-};
-
-static int launch(const pkv_pool *pool, void *out, const void *q, const PoolPtrs &pp,
-                  bool want_8bit, const int32_t *block_tables, int32_t maxb,
+// 8-bit pool (k_pool = the record pool, v_pool unused) or 16-bit K and V pools.
+static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
+                  const void *v_pool, bool want_8bit, const int32_t *block_tables, int32_t maxb,
                   const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
                   int32_t P, void *workspace, size_t workspace_bytes, int32_t *d_status,
                   void *stream)
@@ -1054,20 +1230,19 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const PoolPtrs
     if (g.block_size != kBlock || G > (want_8bit ? 8 : 16)) return PKV_ERR_UNSUPPORTED;
     Variant v;
     if (want_8bit) {
-        if (g.head_dim != 128) return PKV_ERR_UNSUPPORTED;
-        v = bf ? variant<128, true, 8, kQ8Stages, kQ8MinBlocks, true>()
-               : variant<128, false, 8, kQ8Stages, kQ8MinBlocks, true>();
+        if (g.head_dim != 128 || P > 32) return PKV_ERR_UNSUPPORTED;
+        v = q8_variant(bf);
     } else if (!pick_variant(g.head_dim, bf, G, &v)) {
         return PKV_ERR_UNSUPPORTED;
     }
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !pp.k || !pp.v || !block_tables || !context_lens || !workspace ||
-        !d_status || (want_8bit && (!pp.ks || !pp.vs)))
+    if (!out || !q || !k_pool || (!want_8bit && !v_pool) || !block_tables || !context_lens ||
+        !workspace || !d_status)
         return PKV_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(pp.k) || !aligned16(pp.v) ||
-        ((uintptr_t)workspace & 255u) || ((uintptr_t)block_tables & 3u) ||
-        ((uintptr_t)context_lens & 3u) || ((uintptr_t)d_status & 3u) ||
-        (want_8bit && (!aligned16(pp.ks) || !aligned16(pp.vs))))
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) ||
+        (!want_8bit && !aligned16(v_pool)) || ((uintptr_t)workspace & 255u) ||
+        ((uintptr_t)block_tables & 3u) || ((uintptr_t)context_lens & 3u) ||
+        ((uintptr_t)d_status & 3u))
         return PKV_ERR_INVALID_ARG;
     WsLayout w;
     if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, P, &w) ||
@@ -1076,9 +1251,8 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const PoolPtrs
     if ((int64_t)g.num_blocks * g.num_kv_heads * g.block_size > (int64_t)1 << 31)
         return PKV_ERR_UNSUPPORTED;   // TMA row coordinate is a signed 32-bit value
 
-    CUtensorMap tk, tv;
-    if (want_8bit ? !make_q8_key_maps(&tk, &tv, pp.k, g)
-                  : (!make_pool_map(&tk, pp.k, g) || !make_pool_map(&tv, pp.v, g)))
+    CUtensorMap tk = {}, tv = {};     // the 8-bit kernel copies whole records, without maps
+    if (!want_8bit && (!make_pool_map(&tk, k_pool, g) || !make_pool_map(&tv, v_pool, g)))
         return PKV_ERR_CUDA;
 
     char *ws = static_cast<char *>(workspace);
@@ -1101,9 +1275,7 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const PoolPtrs
     prm.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
     prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
     prm.status = d_status;
-    prm.v_codes = want_8bit ? pp.v : nullptr;
-    prm.k_scales = pp.ks;
-    prm.v_scales = pp.vs;
+    prm.kv_q8 = want_8bit ? static_cast<const uint8_t *>(k_pool) : nullptr;
     prm.max_pairs = w.max_pairs;
     prm.debug = prm.header + 1;
 
@@ -1111,7 +1283,7 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const PoolPtrs
     const int per_sm = persistent_ctas(v, &num_sms);
     if (per_sm < 1) return PKV_ERR_CUDA;
     int64_t grid = (int64_t)per_sm * num_sms;
-    const int64_t upper = w.max_pairs * g.num_kv_heads;
+    const int64_t upper = (w.max_pairs * g.num_kv_heads + v.items_per_cta - 1) / v.items_per_cta;
     if (grid > upper) grid = upper;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 #ifdef PKV_DEBUG_CHECKS
@@ -1124,7 +1296,7 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const PoolPtrs
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(v.threads);
     cfg.dynamicSmemBytes = (size_t)v.smem;
     cfg.stream = st;
     cfg.attrs = pdl;
@@ -1179,10 +1351,9 @@ int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
                                  void *workspace, size_t workspace_bytes, int32_t *d_status,
                                  void *stream)
 {
-    const pkv::decode::PoolPtrs pp{k_pool, v_pool, nullptr, nullptr};
-    return pkv::decode::launch(pool, out, q, pp, false, block_tables, max_blocks_per_seq,
-                               context_lens, num_seqs, num_q_heads, scale, blocks_per_split,
-                               workspace, workspace_bytes, d_status, stream);
+    return pkv::decode::launch(pool, out, q, k_pool, v_pool, false, block_tables,
+                               max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
+                               blocks_per_split, workspace, workspace_bytes, d_status, stream);
 }
 
 int paged_decode_attention(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
@@ -1191,23 +1362,20 @@ int paged_decode_attention(const pkv_pool *pool, void *out, const void *q, const
                            int32_t num_seqs, int32_t num_q_heads, float scale, void *workspace,
                            size_t workspace_bytes, int32_t *d_status, void *stream)
 {
-    const pkv::decode::PoolPtrs pp{k_pool, v_pool, nullptr, nullptr};
-    return pkv::decode::launch(pool, out, q, pp, false, block_tables, max_blocks_per_seq,
-                               context_lens, num_seqs, num_q_heads, scale,
+    return pkv::decode::launch(pool, out, q, k_pool, v_pool, false, block_tables,
+                               max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
                                pkv::decode::kDefaultSplit, workspace, workspace_bytes, d_status,
                                stream);
 }
 
-int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q,
-                              const void *k_codes, const void *v_codes, const void *k_scales,
-                              const void *v_scales, const int32_t *block_tables,
-                              int32_t max_blocks_per_seq, const int32_t *context_lens,
-                              int32_t num_seqs, int32_t num_q_heads, float scale, void *workspace,
-                              size_t workspace_bytes, int32_t *d_status, void *stream)
+int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q, const void *kv_q8,
+                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                              float scale, void *workspace, size_t workspace_bytes,
+                              int32_t *d_status, void *stream)
 {
-    const pkv::decode::PoolPtrs pp{k_codes, v_codes, k_scales, v_scales};
-    return pkv::decode::launch(pool, out, q, pp, true, block_tables, max_blocks_per_seq,
-                               context_lens, num_seqs, num_q_heads, scale,
+    return pkv::decode::launch(pool, out, q, kv_q8, nullptr, true, block_tables,
+                               max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
                                pkv::decode::kDefaultSplit, workspace, workspace_bytes, d_status,
                                stream);
 }
@@ -1278,7 +1446,6 @@ extern "C" int paged_decode_attention_noalloc(const pkv_pool *pool, void *out, c
     if (P == 0) return PKV_ERR_INVALID_ARG;   // scratch would exceed PKV_NOALLOC_SCRATCH_BYTES
     void *scratch = noalloc_scratch_address();
     if (!scratch) return PKV_ERR_CUDA;
-    const PoolPtrs pp{k_pool, v_pool, nullptr, nullptr};
-    return launch(pool, out, q, pp, false, block_tables, maxb, context_lens, num_seqs,
-                  num_q_heads, scale, P, scratch, kNoallocScratchBytes, d_status, stream);
+    return launch(pool, out, q, k_pool, v_pool, false, block_tables, maxb, context_lens,
+                  num_seqs, num_q_heads, scale, P, scratch, kNoallocScratchBytes, d_status, stream);
 }

@@ -4,7 +4,9 @@ codes with one fp16 scale per 32 values) against the oracle.
   * quantising cache write: codes and scale bits identical to the oracle's
     (bit-exact) on ordinary, zero, saturating and subnormal-scale rows; slots
     outside the pool flagged and skipped, negative slots skipped, every other
-    byte of the pools untouched;
+    byte of the pool untouched.  The library keeps each (block, kv head) slab
+    as one record (K codes in its rotated row order, V codes, scales); the test
+    unpacks it by index arithmetic into the oracle's four plain arrays;
   * decode attention over the 8-bit pool: |gpu - oracle| <= 2e-3 + 1e-2 |oracle|,
     the oracle attending in fp64 over code * scale; stale slots past each
     context (codes -1, NaN scales) never reach the result; repeated launches
@@ -32,10 +34,25 @@ D = 128
 
 
 def _fill_sentinel(pool):
-    pool.k_pool.fill_(-1)
-    pool.v_pool.fill_(-1)
-    pool.k_scales.view(torch.int16).fill_(-1)           # fp16 NaN
-    pool.v_scales.view(torch.int16).fill_(-1)
+    pool.kv.fill_(0xFF)                                  # codes -1, scales fp16 NaN
+
+
+def unpack_records(kv: np.ndarray):
+    """Records uint8 [nb][Hkv][4352] -> (k_codes int8 [nb][Hkv][16][128],
+    v_codes int8 [nb][Hkv][128][16], k_scales, v_scales uint16 [nb][Hkv][16][4]).
+    Token t = 4a + 2b + c is K row r = 8b + 2a + c; chunk j of row r sits at
+    chunk position j ^ (r % 8)."""
+    nb, hkv, _ = kv.shape
+    t = np.arange(16)
+    r = 8 * ((t >> 1) & 1) + 2 * (t >> 2) + (t & 1)
+    j = np.arange(8)
+    rows = kv[:, :, :2048].reshape(nb, hkv, 16, 8, 16)
+    k = rows[:, :, r[:, None], j[None, :] ^ (r[:, None] % 8), :]     # [nb][hkv][t][j][16]
+    k_codes = k.reshape(nb, hkv, 16, 128).view(np.int8)
+    v_codes = kv[:, :, 2048:4096].reshape(nb, hkv, 128, 16).view(np.int8)
+    k_scales = np.ascontiguousarray(kv[:, :, 4096:4224]).view(np.uint16).reshape(nb, hkv, 16, 4)
+    v_scales = np.ascontiguousarray(kv[:, :, 4224:4352]).view(np.uint16).reshape(nb, hkv, 16, 4)
+    return k_codes, v_codes, k_scales, v_scales
 
 
 def _oracle_pools(nb, hkv):
@@ -45,8 +62,7 @@ def _oracle_pools(nb, hkv):
 
 
 def _host_pools(pool):
-    return (pool.k_pool.cpu().numpy(), pool.v_pool.cpu().numpy(),
-            to_np_bits(pool.k_scales), to_np_bits(pool.v_scales))
+    return unpack_records(pool.kv.cpu().numpy())
 
 
 def _assert_pools_equal(pool, ref):
@@ -174,7 +190,7 @@ def test_q8_stale_slots_never_read():
     """Slots past each context hold codes -1 and NaN scales (the sentinel); the
     result must stay finite and match the oracle, which never reads them."""
     c = Q8Case([3, 18, 45, 100], 32, 8, "bf16", seed=5)
-    k_codes = c.pool.k_pool.cpu().numpy()
+    k_codes = _host_pools(c.pool)[0]
     for s, n in enumerate(c.lens):
         last = c.tables[s, (int(n) - 1) // 16]
         assert (k_codes[last, :, int(n) % 16 or 16:] == -1).all()
@@ -254,8 +270,7 @@ def test_q8_gqa_long_sampled():
         cslots = np.arange(n, dtype=np.int64)                   # compact pool: block i = id i
         assert o.cache_write_q8(kr, vr, cslots, ref, 16, True) == 0
         d_ids = torch.from_numpy(ids.astype(np.int64)).cuda()
-        got = (pool.k_pool[d_ids].cpu().numpy(), pool.v_pool[d_ids].cpu().numpy(),
-               to_np_bits(pool.k_scales[d_ids]), to_np_bits(pool.v_scales[d_ids]))
+        got = unpack_records(pool.kv[d_ids].cpu().numpy())
         for a, r in zip(got, ref):
             assert np.array_equal(a, r), f"sequence {s}: pool blocks differ"
         ctab = np.arange(nbs, dtype=np.int32)[None, :]
