@@ -107,6 +107,12 @@ struct ItemMeta {
     int s, g, L, b0, b1, nsplit, pair, pad;
 };
 
+// Bring [src, src + bytes) into L2 (bytes a multiple of 16, src 16-byte aligned).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar)
 {
@@ -678,7 +684,9 @@ __global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
 // i + kSlots -- across item boundaries, with the next item's metadata and block
 // ids prefetched into registers -- right after it has consumed block i.  The
 // next item's query rows are copied into the warp's query buffer as soon as the
-// current item's rows have been read out of it.  No producer warp, no cross-warp barriers, no shared-memory merge:
+// current item's rows have been read out of it.  Each copy also prefetches the
+// record kPrefetch blocks further on into L2, which raises the bytes in flight
+// without taking shared memory.  No producer warp, no cross-warp barriers, no shared-memory merge:
 // the warp writes its rows (or its partition's piece) itself.
 namespace q8 {
 #ifndef PKV_Q8_WARPS
@@ -695,6 +703,10 @@ constexpr int kWarps = PKV_Q8_WARPS;             // independent warps per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = PKV_Q8_SLOTS;             // ring stages per warp
 constexpr int kMinBlocks = PKV_Q8_CTAS;          // CTAs per SM
+#ifndef PKV_Q8_PREFETCH
+#define PKV_Q8_PREFETCH 2
+#endif
+constexpr int kPrefetch = PKV_Q8_PREFETCH;       // L2 prefetch this many blocks past the copy
 constexpr int kQBytes = 8 * 128 * 2;              // one item's query rows (G <= 8), fp16/bf16
 constexpr int kWarpBytes = kSlots * kSlab + kQBytes + 128;   // stages, query rows, barriers
 constexpr int kSmemBytes = 128 + kWarps * kWarpBytes;
@@ -900,10 +912,17 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
         const int c_item = cnext ? nxt.item : cur.item;
         const int c_nb = cnext ? nxt.nb : cur.nb;
         if (c_item >= total || cj >= c_nb) return;
-        const int id = __shfl_sync(kFull, cnext ? nxt.id : cur.id, cj);
+        const int c_id = cnext ? nxt.id : cur.id;
+        const int id = __shfl_sync(kFull, c_id, cj);
         const int c_g = cnext ? nxt.g : cur.g;
         const int slot = (int)(issued % kSlots);
         const bool ok = id >= 0 && id < p.num_blocks;
+        // the block kPrefetch further on: in this item, or in the next one
+        const int pj = cj + kPrefetch;
+        const bool in_c = pj < c_nb;
+        const bool in_n = !cnext && !in_c && nxt.item < total && pj - c_nb < nxt.nb;
+        const int pf_id = __shfl_sync(kFull, in_c ? c_id : nxt.id, in_c ? pj : (pj - c_nb) & 31);
+        const int pf_g = in_c ? c_g : nxt.g;
         if (lane == 0) {
             const uint32_t fb = smem_addr(&full[slot]);
             if (ok) {
@@ -914,6 +933,8 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
                 atomicOr(p.status, PKV_DEV_BAD_BLOCK);
                 mbar_arrive(fb);
             }
+            if ((in_c || in_n) && pf_id >= 0 && pf_id < p.num_blocks)
+                bulk_prefetch_l2(p.kv_q8 + ((int64_t)pf_id * Hkv + pf_g) * kSlab, kSlab);
         }
         bad_mask = ok ? bad_mask & ~(1u << slot) : bad_mask | (1u << slot);
         ++issued;
