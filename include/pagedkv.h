@@ -230,7 +230,7 @@ int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *d
  *                       at byte 128 r + 16 (j XOR (r mod 8)).
  *   bytes [2048, 4096)  V codes: dimension d's 16 tokens at 2048 + 16 d + t.
  *   bytes [4096, 4224)  K scales: fp16, token t's group i at 4096 + 8 t + 2 i.
- *   bytes [4224, 4352)  V scales: fp16, at 4224 + 8 t + 2 i.
+ *   bytes [4224, 4352)  V scales: fp16, token t's group i at 4224 + 32 i + 2 t.
  * kv_pool_bytes with PKV_Q8_BF16 / PKV_Q8_F16 gives the size of the pool. */
 #define PKV_Q8_SLAB_BYTES 4352
 

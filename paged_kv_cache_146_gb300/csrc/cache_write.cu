@@ -169,7 +169,7 @@ cache_write_q8_kernel(const uint16_t *__restrict__ k_new, const uint16_t *__rest
             rec[2048 + (4 * lane + i) * BS + off] = (uint8_t)((vc >> (8 * i)) & 0xff);
         if ((lane & 7) == 0) {
             *reinterpret_cast<uint16_t *>(rec + 4096 + off * 8 + 2 * (lane >> 3)) = ks;
-            *reinterpret_cast<uint16_t *>(rec + 4224 + off * 8 + 2 * (lane >> 3)) = vs;
+            *reinterpret_cast<uint16_t *>(rec + 4224 + (lane >> 3) * 32 + off * 2) = vs;
         }
     }
 }

@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
 //                 row 8b + 2a + c, its 16-byte chunk j at position j ^ (row & 7)
 //   [2048, 4096)  V codes, 128 dimension rows of 16 bytes (byte = token)
 //   [4096, 4224)  K scales, fp16 [16 tokens][4 groups of 32 dimensions]
-//   [4224, 4352)  V scales, the same
+//   [4224, 4352)  V scales, fp16 [4 groups][16 tokens]
 // The row order puts the tokens of each 8-column MMA tile in rows 0-7 and 8-15,
 // and the chunk rotation lets ldmatrix read them without bank conflicts.
 //
@@ -775,35 +775,34 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
     float x[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) x[j] = sc[j] * scale_row;
-    float vs[4][4];
-    {
-        const uint4 a = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4);
-        const uint4 b = *reinterpret_cast<const uint4 *>(scales + 128 + 32 * q4 + 16);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    // V scales of this lane's tokens as fp16 pairs: group i -> (4q4, 4q4 + 1),
+    // (4q4 + 2, 4q4 + 3)
+    uint2 vs[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
-            vs[k >> 1][2 * (k & 1)] = f.x;
-            vs[k >> 1][2 * (k & 1) + 1] = f.y;
-        }
-    }
+    for (int i = 0; i < 4; ++i)
+        vs[i] = *reinterpret_cast<const uint2 *>(scales + 128 + 32 * i + 8 * q4);
     if (valid < kBlock) {
         // tokens past the context: no score, and no scale (a stale one may be NaN)
+        const int n = valid - 4 * q4;       // tokens of this lane inside the context
+        const uint32_t m01 = n <= 0 ? 0u : (n == 1 ? 0x0000ffffu : 0xffffffffu);
+        const uint32_t m23 = n <= 2 ? 0u : (n == 3 ? 0x0000ffffu : 0xffffffffu);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            vs[i].x &= m01;
+            vs[i].y &= m23;
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (4 * q4 + j >= valid) {
-                x[j] = -INFINITY;
-                vs[j][0] = vs[j][1] = vs[j][2] = vs[j][3] = 0.f;
-            }
+            if (4 * q4 + j >= valid) x[j] = -INFINITY;
     }
     float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
     const float mn = fmaxf(m0, mx);
-    const float a0 = exp2f(m0 - mn);
+    const float a0 = fast_exp2(m0 - mn);
     float pj[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) pj[j] = exp2f(x[j] - mn);
+    for (int j = 0; j < 4; ++j) pj[j] = fast_exp2(x[j] - mn);
     l0 = l0 * a0 + ((pj[0] + pj[1]) + (pj[2] + pj[3]));
     m0 = mn;
     if (__any_sync(kFull, a0 != 1.f)) {
@@ -815,10 +814,13 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
             o[t][0] *= f0; o[t][1] *= f1; o[t][2] *= f0; o[t][3] *= f1;
         }
     }
+    const uint32_t p01 = H::pack(pj[0], pj[1]), p23 = H::pack(pj[2], pj[3]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t b0 = H::pack(pj[0] * vs[0][i], pj[1] * vs[1][i]);
-        const uint32_t b1 = H::pack(pj[2] * vs[2][i], pj[3] * vs[3][i]);
+        // weights of group i: p * vs, one fp16 product per pair
+        uint32_t b0, b1;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(b0) : "r"(p01), "r"(vs[i].x));
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(b1) : "r"(p23), "r"(vs[i].y));
         // matrix m: dimensions 32i + 8m .. 32i + 8m + 7 (lane row r = dimension)
         uint32_t vr[4];
         ldsm_x4(vr, vb + (32 * i + lane) * 16);
@@ -958,21 +960,14 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
 
     bool alive = true;
     while (alive && cur.item < total) {
-        // this lane's query words: row hrow, dimensions 16kk + 4q4 .. + 3
+        // this lane's query words: row hrow, dimensions 16kk + 4q4 .. + 3, as
+        // fp16 A fragments (rows 8-15 zero), dimensions permuted inside each
+        // 16-wide step to match the K-code words: k slots 2q4 + e <- 16kk + 4q4 + e,
+        // 8 + 2q4 + e <- 16kk + 4q4 + 2 + e
         const bool q_landed = mbar_wait(smem_addr(qfull), q_used & 1u, abort_flag, p.status);
         if (!__all_sync(kFull, q_landed)) break;
         ++q_used;
-        uint2 qw[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            qw[kk] = *reinterpret_cast<const uint2 *>(qbuf + hrow * (D * 2) + (16 * kk + 4 * q4) * 2);
-        // the buffer is free: the next item's rows may come in (async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (nxt.item < total) issue_q(nxt.s, nxt.g);
-        // ---- the item's query rows as fp16 A fragments (rows 8-15 zero);
-        // dimensions permuted inside each 16-wide step to match the K-code words:
-        // k slots 2q4 + e <- 16kk + 4q4 + e, 8 + 2q4 + e <- 16kk + 4q4 + 2 + e
+        const uint2 *qrow = reinterpret_cast<const uint2 *>(qbuf + hrow * (D * 2)) + q4;
         uint32_t qa[8][4];
         float scale_row = p.scale_log2;
         if constexpr (BF16) {
@@ -982,7 +977,8 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
             float amax = 0.f;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const float2 f0 = E::unpack(qw[kk].x), f1 = E::unpack(qw[kk].y);
+                const uint2 w = qrow[4 * kk];
+                const float2 f0 = E::unpack(w.x), f1 = E::unpack(w.y);
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
                                          fmaxf(fabsf(f1.x), fabsf(f1.y))));
             }
@@ -993,7 +989,8 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
             scale_row = p.scale_log2 * __int_as_float((127 + e) << 23);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const float2 f0 = E::unpack(qw[kk].x), f1 = E::unpack(qw[kk].y);
+                const uint2 w = qrow[4 * kk];
+                const float2 f0 = E::unpack(w.x), f1 = E::unpack(w.y);
                 qa[kk][0] = Elem<false>::pack(f0.x * down, f0.y * down);
                 qa[kk][2] = Elem<false>::pack(f1.x * down, f1.y * down);
                 qa[kk][1] = qa[kk][3] = 0u;
@@ -1001,9 +998,14 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
         } else {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                qa[kk][0] = qw[kk].x; qa[kk][1] = 0u; qa[kk][2] = qw[kk].y; qa[kk][3] = 0u;
+                const uint2 w = qrow[4 * kk];
+                qa[kk][0] = w.x; qa[kk][1] = 0u; qa[kk][2] = w.y; qa[kk][3] = 0u;
             }
         }
+        // the buffer is free: the next item's rows may come in (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (nxt.item < total) issue_q(nxt.s, nxt.g);
 
         float o[8][4];
 #pragma unroll

@@ -127,6 +127,15 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// 2^x with the SFU approximation (ex2.approx.ftz: relative error near 2^-22,
+// results below the normal range flushed to 0, 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int NTHREADS>
 __device__ __forceinline__ void named_barrier_sync()
 {

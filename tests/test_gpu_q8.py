@@ -41,7 +41,8 @@ def unpack_records(kv: np.ndarray):
     """Records uint8 [nb][Hkv][4352] -> (k_codes int8 [nb][Hkv][16][128],
     v_codes int8 [nb][Hkv][128][16], k_scales, v_scales uint16 [nb][Hkv][16][4]).
     Token t = 4a + 2b + c is K row r = 8b + 2a + c; chunk j of row r sits at
-    chunk position j ^ (r % 8)."""
+    chunk position j ^ (r % 8).  K scales are stored token-major, V scales
+    group-major."""
     nb, hkv, _ = kv.shape
     t = np.arange(16)
     r = 8 * ((t >> 1) & 1) + 2 * (t >> 2) + (t & 1)
@@ -51,7 +52,8 @@ def unpack_records(kv: np.ndarray):
     k_codes = k.reshape(nb, hkv, 16, 128).view(np.int8)
     v_codes = kv[:, :, 2048:4096].reshape(nb, hkv, 128, 16).view(np.int8)
     k_scales = np.ascontiguousarray(kv[:, :, 4096:4224]).view(np.uint16).reshape(nb, hkv, 16, 4)
-    v_scales = np.ascontiguousarray(kv[:, :, 4224:4352]).view(np.uint16).reshape(nb, hkv, 16, 4)
+    v_scales = np.ascontiguousarray(np.ascontiguousarray(kv[:, :, 4224:4352]).view(np.uint16)
+                                    .reshape(nb, hkv, 4, 16).transpose(0, 1, 3, 2))
     return k_codes, v_codes, k_scales, v_scales
 
 
