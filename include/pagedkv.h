@@ -207,6 +207,8 @@ int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_len
  * device int32 [n]; destinations must differ from each other and from every
  * source (kv_append_slots_cow guarantees it: they are fresh blocks).  A pair
  * naming a block outside the pool is skipped and sets PKV_DEV_BAD_BLOCK.
+ * 8-bit pools: k_pool is the record pool, v_pool is ignored (may be NULL); a
+ * block is its num_kv_heads records.
  * Asynchronous on stream.  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA. */
 int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *dst_ids,
                   int32_t n, void *k_pool, void *v_pool, int32_t *d_status, void *stream);
@@ -262,7 +264,9 @@ int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q, co
  * blocks into one contiguous staging buffer so the host copy is a single
  * transfer, and unpacks a staging buffer into (other) blocks on the way back.
  * staging layout: [n][2 (K, V)][num_kv_heads][block_size][head_dim], pool dtype,
- * device memory, 16-byte aligned, 2 * n * block bytes.  ids: device int32 [n].
+ * device memory, 16-byte aligned, 2 * n * block bytes.  8-bit pools: k_pool is
+ * the record pool, v_pool is ignored (may be NULL), staging is
+ * [n][num_kv_heads][PKV_Q8_SLAB_BYTES] bytes.  ids: device int32 [n].
  * Ids outside the pool are skipped and set PKV_DEV_BAD_BLOCK.  Asynchronous.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA. */
 int kv_gather_blocks(const pkv_pool *pool, const int32_t *ids, int32_t n, const void *k_pool,

@@ -209,11 +209,17 @@ class KVPool:
 
 
 # ------------------------------------------------------------------ device ops
+def _pools(pool: KVPool, k_pool, v_pool):
+    """Device pools of a call: (K, V), or (records, None) for an 8-bit pool."""
+    if pool.is_q8:
+        return (pool.kv if k_pool is None else k_pool), None
+    return (pool.k_pool if k_pool is None else k_pool), (pool.v_pool if v_pool is None else v_pool)
+
+
 def block_copy(pool: KVPool, src_ids, dst_ids, status, k_pool=None, v_pool=None,
                stream=None) -> None:
     """Launch the block-copy kernel (int32 device tensors of block ids)."""
-    k_pool = pool.k_pool if k_pool is None else k_pool
-    v_pool = pool.v_pool if v_pool is None else v_pool
+    k_pool, v_pool = _pools(pool, k_pool, v_pool)
     n = int(src_ids.shape[0])
     if int(dst_ids.shape[0]) != n:
         raise ValueError("src_ids and dst_ids differ in length")
@@ -239,9 +245,9 @@ def cache_write(pool: KVPool, k_new, v_new, slot_mapping, status, k_pool=None, v
 
 def gather_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, stream=None):
     """Pack blocks ``ids`` (int32 device tensor) into ``staging`` (device,
-    [n][2][Hkv][16][D] in the pool dtype) for one host copy (swap out)."""
-    k_pool = pool.k_pool if k_pool is None else k_pool
-    v_pool = pool.v_pool if v_pool is None else v_pool
+    [n][2][Hkv][16][D] in the pool dtype; 8-bit pools [n][Hkv][4352] bytes) for
+    one host copy (swap out)."""
+    k_pool, v_pool = _pools(pool, k_pool, v_pool)
     check(lib().kv_gather_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(k_pool),
                                  _t_ptr(v_pool), _t_ptr(staging), _t_ptr(status),
                                  _stream(stream)), "kv_gather_blocks")
@@ -249,8 +255,7 @@ def gather_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, 
 
 def scatter_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, stream=None):
     """Unpack ``staging`` into blocks ``ids`` (swap in)."""
-    k_pool = pool.k_pool if k_pool is None else k_pool
-    v_pool = pool.v_pool if v_pool is None else v_pool
+    k_pool, v_pool = _pools(pool, k_pool, v_pool)
     check(lib().kv_scatter_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(staging),
                                   _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status),
                                   _stream(stream)), "kv_scatter_blocks")

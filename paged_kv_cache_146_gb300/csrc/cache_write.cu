@@ -64,13 +64,15 @@ block_copy_kernel(const int32_t *__restrict__ src, const int32_t *__restrict__ d
             continue;
         }
         k_pool[(int64_t)b * chunks_per_block + c] = k_pool[(int64_t)a * chunks_per_block + c];
-        v_pool[(int64_t)b * chunks_per_block + c] = v_pool[(int64_t)a * chunks_per_block + c];
+        if (v_pool)     // 8-bit pools: one pool of records
+            v_pool[(int64_t)b * chunks_per_block + c] = v_pool[(int64_t)a * chunks_per_block + c];
     }
 }
 
 // Swap staging: gather blocks ids[0..n) into staging [n][K|V][Hkv][16][D]
-// (to_staging = true) or scatter staging back into blocks ids (false).  One
-// thread per 16-byte chunk; out-of-pool ids are skipped and flagged.
+// (to_staging = true) or scatter staging back into blocks ids (false); an 8-bit
+// pool (v_pool NULL) stages [n][Hkv][record].  One thread per 16-byte chunk;
+// out-of-pool ids are skipped and flagged.
 __global__ void __launch_bounds__(256)
 swap_kernel(const int32_t *__restrict__ ids, int32_t n, int64_t chunks_per_block, int32_t num_blocks,
             uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool, uint4 *__restrict__ staging,
@@ -86,16 +88,16 @@ swap_kernel(const int32_t *__restrict__ ids, int32_t n, int64_t chunks_per_block
             if (c == 0) atomicOr(status, PKV_DEV_BAD_BLOCK);
             continue;
         }
-        uint4 *sk = staging + (2 * i) * chunks_per_block + c;
-        uint4 *sv = sk + chunks_per_block;
+        const int parts = v_pool ? 2 : 1;
+        uint4 *sk = staging + (parts * i) * chunks_per_block + c;
         uint4 *pk = k_pool + (int64_t)b * chunks_per_block + c;
-        uint4 *pv = v_pool + (int64_t)b * chunks_per_block + c;
-        if (to_staging) {
-            *sk = __ldcs(pk);
-            *sv = __ldcs(pv);
-        } else {
-            *pk = __ldcs(sk);
-            *pv = __ldcs(sv);
+        if (to_staging) *sk = __ldcs(pk);
+        else *pk = __ldcs(sk);
+        if (v_pool) {
+            uint4 *sv = sk + chunks_per_block;
+            uint4 *pv = v_pool + (int64_t)b * chunks_per_block + c;
+            if (to_staging) *sv = __ldcs(pv);
+            else *pv = __ldcs(sv);
         }
     }
 }
@@ -211,13 +213,17 @@ static int launch_swap(const pkv_pool *pool, const int32_t *ids, int32_t n, void
                        void *stream)
 {
     pkv::PoolGeometry g;
-    if (!pkv::pool_geometry(pool, &g) || n < 0 || !pkv::is_16bit(g)) return PKV_ERR_INVALID_ARG;
+    if (!pkv::pool_geometry(pool, &g) || n < 0) return PKV_ERR_INVALID_ARG;
+    const bool q8 = pkv::is_8bit(g);
+    if (q8) v_pool = nullptr;
     if (n == 0) return PKV_OK;
-    if (!ids || !k_pool || !v_pool || !staging || !d_status) return PKV_ERR_INVALID_ARG;
-    if (!pkv::aligned16(k_pool) || !pkv::aligned16(v_pool) || !pkv::aligned16(staging) ||
+    if (!ids || !k_pool || (!q8 && !v_pool) || !staging || !d_status) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(k_pool) || (!q8 && !pkv::aligned16(v_pool)) || !pkv::aligned16(staging) ||
         ((uintptr_t)ids & 3u) || ((uintptr_t)d_status & 3u))
         return PKV_ERR_INVALID_ARG;
-    const int64_t block_bytes = (int64_t)g.num_kv_heads * g.block_size * g.head_dim * 2;
+    if (q8 && (g.head_dim != 128 || g.block_size != 16)) return PKV_ERR_UNSUPPORTED;
+    const int64_t block_bytes = q8 ? (int64_t)g.num_kv_heads * PKV_Q8_SLAB_BYTES
+                                   : (int64_t)g.num_kv_heads * g.block_size * g.head_dim * 2;
     if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
     const int64_t chunks = block_bytes / 16;
     const int threads = 256;
@@ -250,13 +256,17 @@ extern "C" int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const
                              void *stream)
 {
     pkv::PoolGeometry g;
-    if (!pkv::pool_geometry(pool, &g) || n < 0 || !pkv::is_16bit(g)) return PKV_ERR_INVALID_ARG;
+    if (!pkv::pool_geometry(pool, &g) || n < 0) return PKV_ERR_INVALID_ARG;
+    const bool q8 = pkv::is_8bit(g);
+    if (q8) v_pool = nullptr;
     if (n == 0) return PKV_OK;
-    if (!src_ids || !dst_ids || !k_pool || !v_pool || !d_status) return PKV_ERR_INVALID_ARG;
-    if (!pkv::aligned16(k_pool) || !pkv::aligned16(v_pool) || ((uintptr_t)src_ids & 3u) ||
+    if (!src_ids || !dst_ids || !k_pool || (!q8 && !v_pool) || !d_status) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(k_pool) || (!q8 && !pkv::aligned16(v_pool)) || ((uintptr_t)src_ids & 3u) ||
         ((uintptr_t)dst_ids & 3u) || ((uintptr_t)d_status & 3u))
         return PKV_ERR_INVALID_ARG;
-    const int64_t block_bytes = (int64_t)g.num_kv_heads * g.block_size * g.head_dim * 2;
+    if (q8 && (g.head_dim != 128 || g.block_size != 16)) return PKV_ERR_UNSUPPORTED;
+    const int64_t block_bytes = q8 ? (int64_t)g.num_kv_heads * PKV_Q8_SLAB_BYTES
+                                   : (int64_t)g.num_kv_heads * g.block_size * g.head_dim * 2;
     if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
     const int64_t chunks = block_bytes / 16;
     const int threads = 256;

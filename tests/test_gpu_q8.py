@@ -25,8 +25,9 @@ import libbuild  # noqa: E402
 import oracle  # noqa: E402
 from decode_case import assert_close, to_np_bits, to_torch  # noqa: E402
 from paged_kv_cache_146_gb300 import (DEV_BAD_SLOT, KVPool, PagedKVError,  # noqa: E402
-                                      cache_write_q8, decode_workspace_bytes,
-                                      paged_decode_attention_q8, status_check, workloads)
+                                      block_copy, cache_write_q8, decode_workspace_bytes,
+                                      gather_blocks, paged_decode_attention_q8,
+                                      scatter_blocks, status_check, workloads)
 
 libbuild.ensure_built()
 
@@ -280,3 +281,40 @@ def test_q8_gqa_long_sampled():
                                      w.scale, True, o.max_threads())
         assert bad == 0
         assert_close(out[s:s + 1], exp, f"q8 gqa_long sequence {s} (context {n})")
+
+
+def test_q8_block_copy_and_swap_round_trip():
+    """Copy-on-write and swap on an 8-bit pool move whole records: a block is its
+    Hkv records, copied bit for bit; a gathered staging buffer holds the
+    records in id order and scatters back into other blocks unchanged."""
+    rng = np.random.default_rng(17)
+    nb, hkv = 30, 4
+    pool = KVPool(nb, hkv, D, "q8_bf16", device="cuda")
+    data = rng.integers(0, 256, (nb, hkv, 4352), dtype=np.uint8)
+    pool.kv.copy_(torch.from_numpy(data).cuda())
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    perm = rng.permutation(nb).astype(np.int32)
+    src, dst = perm[:8], perm[8:16]
+    block_copy(pool, torch.from_numpy(src).cuda(), torch.from_numpy(dst).cuda(), status)
+    assert status_check(status) == (0, 0)
+    expected = data.copy()
+    expected[dst] = data[src]
+    assert np.array_equal(pool.kv.cpu().numpy(), expected)
+    # swap out blocks `out_ids`, back in to `in_ids`
+    out_ids, in_ids = perm[16:22], perm[22:28]
+    staging = torch.empty((len(out_ids), hkv, 4352), dtype=torch.uint8, device="cuda")
+    gather_blocks(pool, torch.from_numpy(out_ids).cuda(), staging, status)
+    assert np.array_equal(staging.cpu().numpy(), expected[out_ids])
+    host = staging.cpu().pin_memory()
+    staging.zero_()
+    staging.copy_(host)
+    scatter_blocks(pool, torch.from_numpy(in_ids).cuda(), staging, status)
+    assert status_check(status) == (0, 0)
+    expected[in_ids] = expected[out_ids]
+    assert np.array_equal(pool.kv.cpu().numpy(), expected)
+    # an id outside the pool is skipped and flagged
+    block_copy(pool, torch.tensor([0], dtype=torch.int32, device="cuda"),
+               torch.tensor([nb], dtype=torch.int32, device="cuda"), status)
+    rc, word = status_check(status)
+    assert rc == -5 and word == 2
+    assert np.array_equal(pool.kv.cpu().numpy(), expected)
