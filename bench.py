@@ -53,16 +53,28 @@ def peaks():
         return 6800.0, "fallback"
 
 
+DECODE_SOURCES = ("decode_params.h", "paged_decode.cu", "pkv_device.cuh")
+
+
+def decode_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the sources the 16-bit decode
+    kernels compile from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_146_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic():
     """DRAM bytes (read + write) per attention call from the committed ncu
-    launch-list summary, or None when the kernel source changed since then."""
-    import hashlib
-    src = os.path.join(ROOT, "paged_kv_cache_146_gb300", "csrc", "paged_decode.cu")
+    launch-list summary, or None when the kernel sources changed since then."""
     prof = os.path.join(ROOT, "profiles", "paged_decode_gqa_long_launches.md")
     try:
         fields = dict(line.split(": ", 1) for line in open(prof).read().splitlines()
                       if line.startswith(("attention_traffic_bytes_per_launch:", "source_sha256_16:")))
-        current = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        current = decode_source_hash()
         if fields.get("source_sha256_16", "").strip() != current:
             return None
         return int(fields["attention_traffic_bytes_per_launch"])

@@ -20,7 +20,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["ledger.cpp", "cache_write.cu", "paged_decode.cu", "paged_prefill.cu"]
+SOURCES = ["ledger.cpp", "cache_write.cu", "paged_decode.cu", "paged_decode_q8.cu",
+           "paged_prefill.cu"]
 
 
 def nvcc() -> str:

@@ -1,0 +1,44 @@
+// Parameters shared by the decode kernels of libpagedkv.so (16-bit kernel,
+// 8-bit kernel, their prep and merge kernels).  Internal to the library.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+#include <vector_types.h>
+
+namespace pkv {
+namespace decode {
+
+constexpr int kDefaultSplit = 32;        // blocks per partition (512 tokens)
+
+struct Params {
+    void *out;
+    const void *q;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
+    int32_t blocks_per_split, num_blocks;
+    float scale_log2;           // softmax scale * log2(e): scores live in the exp2 domain
+    int32_t *header;            // [0] = number of (sequence, partition) pairs
+    int2 *seq_info;             // [S]: first pair index, number of partitions
+    int2 *items;                // [S * ceil(maxb / P)]: (sequence, partition)
+    float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned
+    float *part_o;              // [pairs * Hkv * G * D]: unnormalised partition output
+    int32_t *status;
+    const uint8_t *kv_q8;       // 8-bit pool: one record of kQ8Slab bytes per (block, kv head)
+    int64_t max_pairs;          // capacity of items / partial arrays (checked builds)
+    int32_t *debug;             // first failed check: site << 24 | value (checked builds)
+};
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
+
+// The 8-bit decode kernel (paged_decode_q8.cu) as the launcher sees it.
+struct Q8KernelInfo {
+    KernelFn fn;
+    int smem;          // dynamic shared memory per CTA
+    int threads;       // threads per CTA
+    int warps;         // items a CTA works on at once (one per warp)
+};
+Q8KernelInfo q8_kernel_info(bool bf16_queries);
+
+}  // namespace decode
+}  // namespace pkv
