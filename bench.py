@@ -517,7 +517,8 @@ def prefill_arm(args, world, rank, local):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
                          "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
                          "traffic": None, "peak_kind": tkind,
-                         "note": "mma.sync m16n8k16; 64 query rows per K/V block"},
+                         "note": "tcgen05.mma kind::f16 (TMEM accumulators), 128 query rows x "
+                                 "64-key tiles, P as bf16 high + low parts"},
             "gpu_launches": 2 * args.steps}
     print(json.dumps(line), flush=True)
 

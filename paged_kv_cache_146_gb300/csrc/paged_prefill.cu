@@ -7,20 +7,11 @@
 // its queries, at position p, attends causally over the sequence's tokens 0..p,
 // gathered through the block table exactly like decode.
 //
-// Design (GB300):
-//   * Work items are (sequence, kv head, query tile).  A tile holds 64 / G
-//     query tokens x the G heads of the GQA group = up to 64 rows, 16 per
-//     consumer warp; a persistent grid walks the items in a fixed stride.
-//   * Warp 4 streams every K/V block the tile can see (positions up to the
-//     tile's last query) with 2-D TMA into an mbarrier ring; all four consumer
-//     warps read every stage, each for its own 16 rows, so a stage is released
-//     after four arrivals and no warp ever waits more than one phase ahead.
-//   * Per block and warp: S = Q K^T on tensor cores (mma.sync m16n8k16),
-//     causal mask per row, fp32 online softmax, O += P V with P split into a
-//     high and a low bf16/fp16 part (two MMAs) for fp32-grade weights.  Each
-//     warp owns complete rows: no split-K, no cross-warp merge.
-//   * Waits are bounded (1 s) and report PKV_DEV_TIMEOUT; a slot is released
-//     only after its data is consumed, behind fence.proxy.async.
+// Design (GB300): a tcgen05 kernel (see the section "tcgen05 prefill kernel"):
+// per item, 128 query rows of one kv group against 64-key tiles of the
+// sequence's cache, S and O accumulated in tensor memory by tcgen05.mma from
+// TMA-filled, 128-byte-swizzled shared memory, softmax by four warps that each
+// own 32 tensor-memory lanes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -30,13 +21,10 @@
 #include "pagedkv.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "tc_device.cuh"
 
 namespace pkv {
 namespace prefill {
-
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRows = 16 * kConsumerWarps;      // query rows (token x head) per item
 
 struct Params {
     void *out;
@@ -122,281 +110,381 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
     }
 }
 
-template <int D, int NST>
-struct Smem {
-    static constexpr int kStageBytes = 2 * (D / kBoxCols) * kBoxBytes;
-    static constexpr int kTotal = 1024 + NST * kStageBytes + 2 * NST * 8 + 16;
+// ================================================== tcgen05 prefill kernel
+// Items are (sequence, kv head, query tile of 128 / G tokens): 128 query rows
+// (token-major: row r = token r / G, head r % G) against the sequence's keys
+// 0 .. last position of the tile, in KV tiles of 64 keys (4 blocks).
+//   warp 4 (producer): TMA of the item's Q rows (one 4-D box per 64 columns)
+//     and of each KV tile's 4 K and 4 V blocks into a 2-stage ring.
+//   warp 5 lane 0 (MMA issuer): S = Q K^T into one of two tensor-memory
+//     buffers (M 128, N 64), then O += P V for the previous tile (M 128, N D,
+//     V as an MN-major operand), P as a high and a low bf16/fp16 part.
+//   warps 0-3 (softmax): thread r owns row r = tensor-memory lane r.  Running
+//     maximum with lazy rescaling: the reference maximum moves only when a
+//     tile's maximum exceeds it by more than 8 (log2 units), so weights stay
+//     <= 2^8 and O in tensor memory is rescaled rarely.  V rows past the last
+//     visible key are zeroed in shared memory before the P V product (stale
+//     pool rows may hold anything, and 0 * NaN is NaN).
+// Every wait is bounded; on expiry the kernel flags PKV_DEV_TIMEOUT and stops.
+namespace tcp {
+
+constexpr int kRows = 128;             // M: query rows per item
+constexpr int kKeys = 64;              // keys per KV tile
+constexpr int kThreads = 6 * 32;       // softmax warps 0-3, producer 4, MMA 5
+constexpr int kProducer = 4, kIssuer = 5;
+constexpr float kLazy = 8.f;           // rescale threshold (log2 units)
+
+template <int D>
+struct Layout {
+    static constexpr int kRegions = D / 64;
+    static constexpr int kQBytes = kRegions * kRows * 128;     // [region][row][128 B]
+    static constexpr int kKVBytes = kRegions * kKeys * 128;    // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kKVBytes;           // K tile, then V tile
+    static constexpr int kPBytes = kRows * 128;                // [row][64 keys]
+    static constexpr int kStage0 = kQBytes;
+    static constexpr int kP = kStage0 + 2 * kStageBytes;       // P high, then P low
+    static constexpr int kMisc = kP + 2 * kPBytes;             // barriers and flags
+    static constexpr int kTotal = 1024 + kMisc + 256;
+    static constexpr uint32_t kTmemCols = 256;                 // S0 [0,64) S1 [64,128) O [128, 128 + D)
 };
 
-template <int D, bool BF16, int NST, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const Params p)
+struct Item {
+    int s, g, r0, C, L, t0, t1, nkeys, ntiles;
+};
+
+__device__ __forceinline__ Item load_item(const Params &p, int i, int total, int QT)
+{
+    Item it;
+    const int id = total - 1 - i;          // longest tiles first
+    const int Hkv = p.num_kv_heads;
+    const int sj = id / Hkv;
+    it.g = id - sj * Hkv;
+    const int2 e = p.items[sj];
+    it.s = e.x;
+    it.r0 = __ldg(p.query_start + e.x);
+    it.C = __ldg(p.query_start + e.x + 1) - it.r0;
+    it.L = __ldg(p.context_lens + e.x);
+    it.t0 = e.y * QT;
+    it.t1 = min(it.t0 + QT, it.C);
+    it.nkeys = it.L - it.C + it.t1;
+    it.ntiles = (it.nkeys + kKeys - 1) / kKeys;
+    return it;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmQ, const Params p)
 {
     using E = Elem<BF16>;
     using T = typename E::T;
-    using SM = Smem<D, NST>;
-    constexpr int kBoxes = D / kBoxCols;
-    constexpr int kSlabBytes = kBoxes * kBoxBytes;
-    constexpr int KSTEPS = D / 16;
-    constexpr int NTILES = D / 8;
-
+    using LY = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *stages = base;
-    uint64_t *full_bar = reinterpret_cast<uint64_t *>(base + NST * SM::kStageBytes);
-    uint64_t *empty_bar = full_bar + NST;
-    volatile int *sm_abort = reinterpret_cast<int *>(empty_bar + NST);
+    uint8_t *q_s = base;
+    uint8_t *stage_s = base + LY::kStage0;
+    uint8_t *p_s = base + LY::kP;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + LY::kMisc);
+    uint64_t *q_full = bars + 0, *q_empty = bars + 1;
+    uint64_t *kv_full = bars + 2, *kv_empty = bars + 4;       // [2] each
+    uint64_t *s_full = bars + 6;                              // [2]
+    uint64_t *p_full = bars + 8, *o_full = bars + 9, *done = bars + 10;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 11);
+    int *stage_bad = reinterpret_cast<int *>(tslot + 1);      // [2]
+    volatile int *abort_flag = stage_bad + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(smem_addr(&full_bar[i]), 1);
-            mbar_init(smem_addr(&empty_bar[i]), kConsumerWarps);
+        mbar_init(smem_addr(q_full), 1);
+        mbar_init(smem_addr(q_empty), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&kv_full[i]), 1);
+            mbar_init(smem_addr(&kv_empty[i]), 1);
+            mbar_init(smem_addr(&s_full[i]), 1);
         }
-        *sm_abort = 0;
+        mbar_init(smem_addr(p_full), 4);
+        mbar_init(smem_addr(o_full), 1);
+        mbar_init(smem_addr(done), 1);
+        *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 0) tc::tmem_alloc(tslot, LY::kTmemCols);
+    tc::fence_before_sync();
     __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
     griddep_wait();
 
     const int Hkv = p.num_kv_heads, G = p.group, QT = p.tile_tokens;
-    const int total_items = p.header[0] * Hkv;
+    const int total = p.header[0] * Hkv;
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer
-        uint32_t cnt = 0, issued = 0, issued_par = 0;
-        for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-            const int sj = item / Hkv, g = item - sj * Hkv;
-            const int2 it = p.items[sj];
-            const int s = it.x;
-            const int r0 = __ldg(p.query_start + s), C = __ldg(p.query_start + s + 1) - r0;
-            const int L = __ldg(p.context_lens + s);
-            const int t1 = min((it.y + 1) * QT, C);
-            const int nb = (L - C + t1 - 1) / kBlock + 1;        // blocks up to the last query
-            const int32_t *row = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
-            for (int cb = 0; cb < nb; cb += 32) {
-                const int n = min(32, nb - cb);
-                const int my_id = lane < n ? __ldg(row + cb + lane) : 0;
-                for (int j = 0; j < n; ++j) {
-                    const int pid = __shfl_sync(kFull, my_id, j);
-                    if (lane == 0) {
-                        const int slot = (int)(cnt % NST);
-                        const uint32_t par = (cnt / NST) & 1u;
-                        const uint32_t fb = smem_addr(&full_bar[slot]);
-                        if (mbar_wait(smem_addr(&empty_bar[slot]), par ^ 1u, sm_abort, p.status)) {
-                            if (pid >= 0 && pid < p.num_blocks) {
-                                mbar_arrive_expect_tx(fb, 2 * kSlabBytes);
-                                const uint32_t dk = smem_addr(stages + slot * SM::kStageBytes);
-                                const int y = (pid * Hkv + g) * kBlock;
+    if (warp == kProducer) {
+        if (lane == 0) {
+            uint32_t kv_cnt = 0, it_cnt = 0;
+            int last_par[2] = {-1, -1}, last_q = -1;   // phases of the last copies issued
+            for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++it_cnt) {
+                const Item it = load_item(p, i, total, QT);
+                if (it_cnt > 0 &&
+                    !mbar_wait(smem_addr(q_empty), (it_cnt - 1) & 1u, abort_flag, p.status))
+                    break;
+                const uint32_t qb = smem_addr(q_full);
+                last_q = (int)(it_cnt & 1u);
+                mbar_arrive_expect_tx(qb, (uint32_t)(LY::kRegions * QT * G * 128));
+                for (int rg = 0; rg < LY::kRegions; ++rg)
+                    tc::tma_load_4d(smem_addr(q_s + rg * kRows * 128), &tmQ, rg * 64, 0, it.g,
+                                    it.r0 + it.t0, qb);
+                const int32_t *row = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq;
+                const int nb = (it.nkeys + kBlock - 1) / kBlock;
+                for (int t = 0; t < it.ntiles; ++t, ++kv_cnt) {
+                    const int st = (int)(kv_cnt & 1u);
+                    if (kv_cnt >= 2 && !mbar_wait(smem_addr(&kv_empty[st]),
+                                                  ((kv_cnt >> 1) - 1) & 1u, abort_flag, p.status))
+                        break;
+                    int ids[4];
+                    int bad = 0;
 #pragma unroll
-                                for (int bx = 0; bx < kBoxes; ++bx) {
-                                    tma_load_2d(dk + bx * kBoxBytes, &tmK, bx * kBoxCols, y, fb);
-                                    tma_load_2d(dk + kSlabBytes + bx * kBoxBytes, &tmV,
-                                                bx * kBoxCols, y, fb);
-                                }
-                                issued |= 1u << slot;
-                                issued_par = (issued_par & ~(1u << slot)) | (par << slot);
-                            } else {
-                                atomicOr(p.status, PKV_DEV_BAD_BLOCK);
-                                mbar_arrive(fb);
-                            }
+                    for (int b = 0; b < 4; ++b) {
+                        const int id = __ldg(row + min(4 * t + b, nb - 1));
+                        const bool ok = id >= 0 && id < p.num_blocks;
+                        bad |= !ok;
+                        ids[b] = ok ? id : 0;
+                    }
+                    if (bad) atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                    stage_bad[st] = bad;
+                    last_par[st] = (int)((kv_cnt >> 1) & 1u);
+                    const uint32_t fb = smem_addr(&kv_full[st]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)(2 * LY::kKVBytes));
+                    const uint32_t ks = smem_addr(stage_s + st * LY::kStageBytes);
+                    const uint32_t vs = ks + LY::kKVBytes;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int y = (ids[b] * Hkv + it.g) * kBlock;
+#pragma unroll
+                        for (int rg = 0; rg < LY::kRegions; ++rg) {
+                            const uint32_t off = rg * kKeys * 128 + b * kBlock * 128;
+                            tma_load_2d(ks + off, &tmK, rg * 64, y, fb);
+                            tma_load_2d(vs + off, &tmV, rg * 64, y, fb);
                         }
                     }
-                    ++cnt;
                 }
             }
-        }
-        if (lane == 0) {
-            for (int slot = 0; slot < NST; ++slot) {
-                if (!(issued & (1u << slot))) continue;
-                const uint32_t fb = smem_addr(&full_bar[slot]);
-                const uint32_t par = (issued_par >> slot) & 1u;
-                const unsigned long long t0 = globaltimer();
-                while (!mbar_try_wait(fb, par)) {
-                    if (globaltimer() - t0 > kTimeoutNs) {
-                        atomicOr(p.status, PKV_DEV_TIMEOUT);
-                        break;
+            // after a timed-out wait: let the copies still in flight land first
+            if (*abort_flag) {
+                for (int k = 0; k < 3; ++k) {
+                    const int par = k < 2 ? last_par[k] : last_q;
+                    if (par < 0) continue;
+                    const uint32_t fb = smem_addr(k < 2 ? &kv_full[k] : q_full);
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(fb, (uint32_t)par)) {
+                        if (globaltimer() - t0 > kTimeoutNs) break;
                     }
                 }
             }
         }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
-    const int hrow = lane >> 2, q4 = lane & 3;
-    const int mi = lane >> 3, r8 = lane & 7;
-    const int k_tok = ((mi >> 1) << 3) + r8, k_chunk = mi & 1;
-    const int v_tok = ((mi & 1) << 3) + r8, v_chunk = mi >> 1;
-    uint32_t cnt = 0;
-
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int sj = item / Hkv, g = item - sj * Hkv;
-        const int2 it = p.items[sj];
-        const int s = it.x;
-        const int r0 = __ldg(p.query_start + s), C = __ldg(p.query_start + s + 1) - r0;
-        const int L = __ldg(p.context_lens + s);
-        const int t0 = it.y * QT, t1 = min(t0 + QT, C);
-        const int max_pos = L - C + t1 - 1;
-        const int nb = max_pos / kBlock + 1;
-        // this thread's two rows: a = warp*16 + hrow, b = a + 8
-        const int ra = warp * 16 + hrow, rb = ra + 8;
-        const int ta = ra / G, tb = rb / G;
-        const bool va = t0 + ta < t1, vb = t0 + tb < t1;
-        // positions: invalid rows see the tile's last position (finite, never written)
-        const int pa_pos = va ? L - C + t0 + ta : max_pos;
-        const int pb_pos = vb ? L - C + t0 + tb : max_pos;
-        const size_t qrow_a = ((size_t)(r0 + t0 + ta) * p.num_q_heads + (size_t)g * G + ra % G);
-        const size_t qrow_b = ((size_t)(r0 + t0 + tb) * p.num_q_heads + (size_t)g * G + rb % G);
-        uint32_t qa[KSTEPS][4];
-        {
-            const uint32_t *qw = static_cast<const uint32_t *>(p.q);
+    } else if (warp == kIssuer) {
+        if (lane == 0) {
+            const uint32_t id_qk = tc::idesc_f16(BF16, kRows, kKeys, 0, 0);
+            const uint32_t id_pv = tc::idesc_f16(BF16, kRows, D, 0, 1);
+            const uint32_t q_a = smem_addr(q_s), st_a = smem_addr(stage_s), p_a = smem_addr(p_s);
+            uint32_t tg = 0, it_cnt = 0;
+            bool ok = true;
+            auto issue_pv = [&](uint32_t t, bool first) {
+                if (!mbar_wait(smem_addr(p_full), t & 1u, abort_flag, p.status)) { ok = false; return; }
+                tc::fence_after_sync();
+                const uint32_t vs = st_a + (t & 1u) * LY::kStageBytes + LY::kKVBytes;
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int c = (kk * 16 + 2 * q4) >> 1;
-                qa[kk][0] = va ? __ldg(qw + qrow_a * (D / 2) + c) : 0u;
-                qa[kk][2] = va ? __ldg(qw + qrow_a * (D / 2) + c + 4) : 0u;
-                qa[kk][1] = vb ? __ldg(qw + qrow_b * (D / 2) + c) : 0u;
-                qa[kk][3] = vb ? __ldg(qw + qrow_b * (D / 2) + c + 4) : 0u;
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk) {
+                        const uint64_t a = tc::desc_sw128(p_a + part * LY::kPBytes + kk * 32, 16, 1024);
+                        const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
+                        tc::mma_f16(tmem + 128, a, b, id_pv, !(first && part == 0 && kk == 0));
+                    }
+                tc::mma_commit(smem_addr(o_full));
+                tc::mma_commit(smem_addr(&kv_empty[t & 1u]));
+            };
+            for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it_cnt) {
+                const Item it = load_item(p, i, total, QT);
+                if (!mbar_wait(smem_addr(q_full), it_cnt & 1u, abort_flag, p.status)) break;
+                for (int t = 0; t < it.ntiles && ok; ++t, ++tg) {
+                    const uint32_t st = tg & 1u;
+                    if (!mbar_wait(smem_addr(&kv_full[st]), (tg >> 1) & 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t ks = st_a + st * LY::kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
+                        const uint64_t a = tc::desc_sw128(q_a + (kk >> 2) * kRows * 128 + off, 16, 1024);
+                        const uint64_t b = tc::desc_sw128(ks + (kk >> 2) * kKeys * 128 + off, 16, 1024);
+                        tc::mma_f16(tmem + 64 * st, a, b, id_qk, kk > 0);
+                    }
+                    tc::mma_commit(smem_addr(&s_full[st]));
+                    if (t == it.ntiles - 1) tc::mma_commit(smem_addr(q_empty));
+                    if (t >= 1) issue_pv(tg - 1, t == 1);
+                }
+                if (ok) issue_pv(tg - 1, it.ntiles == 1);
             }
-        }
-        float o[NTILES][4];
-#pragma unroll
-        for (int j = 0; j < NTILES; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-        for (int b = 0; b < nb; ++b, ++cnt) {
-            const int slot = (int)(cnt % NST);
-            const uint32_t par = (cnt / NST) & 1u;
-            const bool landed = mbar_wait(smem_addr(&full_bar[slot]), par, sm_abort, p.status);
-            if (!__all_sync(kFull, landed)) continue;
-            const uint32_t kb = smem_addr(stages + slot * SM::kStageBytes);
-            const uint32_t vbase = kb + kSlabBytes;
-            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-            float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int chunk = 2 * kk + k_chunk;
-                const uint32_t addr = kb + (chunk >> 3) * kBoxBytes + k_tok * 128 +
-                                      (((chunk & 7) ^ r8) << 4);
-                uint32_t kr[4];
-                ldsm_x4(kr, addr);
-                if (kk & 1) {
-                    E::mma(u0, qa[kk], kr[0], kr[1]);
-                    E::mma(u1, qa[kk], kr[2], kr[3]);
-                } else {
-                    E::mma(s0, qa[kk], kr[0], kr[1]);
-                    E::mma(s1, qa[kk], kr[2], kr[3]);
+            // every MMA issued has completed before the columns are freed
+            tc::mma_commit(smem_addr(done));
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(smem_addr(done), 0)) {
+                if (globaltimer() - t0 > kTimeoutNs) {
+                    atomicOr(p.status, PKV_DEV_TIMEOUT);
+                    break;
                 }
             }
+        }
+    } else {
+        // ---------------------------------------------------------- softmax
+        const int r = threadIdx.x;                  // row = tensor-memory lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        uint32_t tg = 0, it_cnt = 0;
+        bool alive = true;
+        for (int i = blockIdx.x; i < total && alive; i += gridDim.x, ++it_cnt) {
+            const Item it = load_item(p, i, total, QT);
+            const int jj = r / G, h = r - (r / G) * G;
+            const bool valid = r < QT * G && it.t0 + jj < it.t1;
+            const int pos = valid ? it.L - it.C + it.t0 + jj : it.nkeys - 1;
+            float m_ref = -INFINITY, l = 0.f;
+            int bad = 0;
+            for (int t = 0; t < it.ntiles; ++t, ++tg) {
+                const uint32_t sb = tg & 1u;
+                const bool ok1 = mbar_wait(smem_addr(&kv_full[sb]), (tg >> 1) & 1u, abort_flag, p.status);
+                const bool ok2 = ok1 && mbar_wait(smem_addr(&s_full[sb]), (tg >> 1) & 1u, abort_flag, p.status);
+                if (!__all_sync(kFull, ok2)) { alive = false; break; }
+                tc::fence_after_sync();
+                bad |= stage_bad[sb];
+                float x[kKeys];
+                {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lane_base + 64 * sb, v);
+                    tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { s0[i] += u0[i]; s1[i] += u1[i]; }
-            // causal mask: key position k is visible to a row at position p iff k <= p
-            const int kbase = b * kBlock + 2 * q4;
-            float x0 = s0[0] * p.scale_log2, x1 = s0[1] * p.scale_log2;
-            float x2 = s1[0] * p.scale_log2, x3 = s1[1] * p.scale_log2;
-            float y0 = s0[2] * p.scale_log2, y1 = s0[3] * p.scale_log2;
-            float y2 = s1[2] * p.scale_log2, y3 = s1[3] * p.scale_log2;
-            if (kbase > pa_pos) x0 = -INFINITY;
-            if (kbase + 1 > pa_pos) x1 = -INFINITY;
-            if (kbase + 8 > pa_pos) x2 = -INFINITY;
-            if (kbase + 9 > pa_pos) x3 = -INFINITY;
-            if (kbase > pb_pos) y0 = -INFINITY;
-            if (kbase + 1 > pb_pos) y1 = -INFINITY;
-            if (kbase + 8 > pb_pos) y2 = -INFINITY;
-            if (kbase + 9 > pb_pos) y3 = -INFINITY;
-            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-            float my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
-            my = fmaxf(my, __shfl_xor_sync(kFull, my, 1));
-            my = fmaxf(my, __shfl_xor_sync(kFull, my, 2));
-            // a row whose keys of this block are all hidden keeps its state
-            const float mn0 = fmaxf(m0, mx), mn1 = fmaxf(m1, my);
-            const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-            const float a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-            const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn0);
-            const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn0);
-            const float e0 = exp2f(y0 - mn1), e1 = exp2f(y1 - mn1);
-            const float e2 = exp2f(y2 - mn1), e3 = exp2f(y3 - mn1);
-            l0 = l0 * a0 + ((p0 + p1) + (p2 + p3));
-            l1 = l1 * a1 + ((e0 + e1) + (e2 + e3));
-            m0 = mn0;
-            m1 = mn1;
-            if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
+                    for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]);
+                    tc::tmem_ld32(lane_base + 64 * sb + 32, v);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < NTILES; ++j) {
-                    o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
+                    for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]);
+                }
+                const int k0 = t * kKeys;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c) {
+                    x[c] = k0 + c <= pos ? x[c] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
+                float f = 1.f;
+                bool resc = false;
+                if (mx > m_ref + kLazy) {          // also the first tile: m_ref = -inf
+                    if (m_ref != -INFINITY) {
+                        f = fast_exp2(m_ref - mx);
+                        resc = true;
+                    }
+                    m_ref = mx;
+                }
+                float lsum = 0.f;
+                uint32_t hi[kKeys / 2], lo[kKeys / 2];
+#pragma unroll
+                for (int c = 0; c < kKeys; c += 2) {
+                    const float p0 = fast_exp2(x[c] - m_ref), p1 = fast_exp2(x[c + 1] - m_ref);
+                    lsum += p0 + p1;
+                    hi[c / 2] = E::pack(p0, p1);
+                    const float2 hh = E::unpack(hi[c / 2]);
+                    lo[c / 2] = E::pack(p0 - hh.x, p1 - hh.y);
+                }
+                l = l * f + lsum;
+                // P V of the previous tile must be done: it reads the P buffer and
+                // writes O
+                if (t >= 1) {
+                    const bool okp = mbar_wait(smem_addr(o_full), (tg - 1) & 1u, abort_flag, p.status);
+                    if (!__all_sync(kFull, okp)) { alive = false; break; }
+                    tc::fence_after_sync();
+                }
+                if (__any_sync(kFull, resc)) {
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t v[32];
+                        tc::tmem_ld32(lane_base + 128 + c0, v);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
+                        tc::tmem_st32(lane_base + 128 + c0, v);
+                    }
+                    tc::tmem_wait_st();
+                }
+                // this row of P (high and low), 128-byte swizzle
+                uint8_t *ph = p_s + r * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int pos16 = (j ^ (r & 7)) << 4;
+                    *reinterpret_cast<uint4 *>(ph + pos16) =
+                        make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                    *reinterpret_cast<uint4 *>(ph + LY::kPBytes + pos16) =
+                        make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+                }
+                // zero the V rows of keys past the last visible one (last tile only)
+                const int nvis = it.nkeys - k0;
+                if (nvis < kKeys) {
+                    uint8_t *vs = stage_s + sb * LY::kStageBytes + LY::kKVBytes;
+                    const int nrows = kKeys - nvis;
+                    for (int e = r; e < nrows * LY::kRegions * 8; e += kRows) {
+                        const int row = nvis + e / (LY::kRegions * 8);
+                        const int rem = e % (LY::kRegions * 8);
+                        *reinterpret_cast<uint4 *>(vs + (rem >> 3) * kKeys * 128 + row * 128 +
+                                                   (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(p_full));
+            }
+            if (!alive) break;
+            // ---- the item's result: O / l once the last P V is done
+            const bool oko = mbar_wait(smem_addr(o_full), (tg - 1) & 1u, abort_flag, p.status);
+            if (!__all_sync(kFull, oko)) break;
+            tc::fence_after_sync();
+            const float inv = 1.f / l;
+            T *out = static_cast<T *>(p.out) +
+                     ((size_t)(it.r0 + it.t0 + jj) * p.num_q_heads + (size_t)it.g * G + h) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tc::tmem_ld32(lane_base + 128 + c0, v);
+                tc::tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 w;
+                        w.x = bad ? 0u : E::pack(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
+                        w.y = bad ? 0u : E::pack(__uint_as_float(v[c + 2]) * inv, __uint_as_float(v[c + 3]) * inv);
+                        w.z = bad ? 0u : E::pack(__uint_as_float(v[c + 4]) * inv, __uint_as_float(v[c + 5]) * inv);
+                        w.w = bad ? 0u : E::pack(__uint_as_float(v[c + 6]) * inv, __uint_as_float(v[c + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(out + c0 + c) = w;
+                    }
                 }
             }
-            uint32_t ph[4], pl[4];
-            ph[0] = E::pack(p0, p1);
-            ph[1] = E::pack(e0, e1);
-            ph[2] = E::pack(p2, p3);
-            ph[3] = E::pack(e2, e3);
-            {
-                const float2 h0 = E::unpack(ph[0]), h1 = E::unpack(ph[1]);
-                const float2 h2 = E::unpack(ph[2]), h3 = E::unpack(ph[3]);
-                pl[0] = E::pack(p0 - h0.x, p1 - h0.y);
-                pl[1] = E::pack(e0 - h1.x, e1 - h1.y);
-                pl[2] = E::pack(p2 - h2.x, p3 - h2.y);
-                pl[3] = E::pack(e2 - h3.x, e3 - h3.y);
-            }
-            // V rows past the tile's last position may hold stale data: zero them
-            const int valid = min(kBlock, max_pos + 1 - b * kBlock);
-            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-            if (valid < kBlock) {
-                const int t0r = 2 * q4;
-                mlo = (t0r < valid ? 0x0000ffffu : 0u) | (t0r + 1 < valid ? 0xffff0000u : 0u);
-                mhi = (t0r + 8 < valid ? 0x0000ffffu : 0u) | (t0r + 9 < valid ? 0xffff0000u : 0u);
-            }
-#pragma unroll
-            for (int jj = 0; jj < NTILES / 2; ++jj) {
-                const int chunk = 2 * jj + v_chunk;
-                const uint32_t addr = vbase + (chunk >> 3) * kBoxBytes + v_tok * 128 +
-                                      (((chunk & 7) ^ r8) << 4);
-                uint32_t vr[4];
-                ldsm_x4_trans(vr, addr);
-                vr[0] &= mlo; vr[2] &= mlo;
-                vr[1] &= mhi; vr[3] &= mhi;
-                E::mma(o[2 * jj], ph, vr[0], vr[1]);
-                E::mma(o[2 * jj + 1], ph, vr[2], vr[3]);
-                E::mma(o[2 * jj], pl, vr[0], vr[1]);
-                E::mma(o[2 * jj + 1], pl, vr[2], vr[3]);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
-        }
-        // rows are complete: normalise and store
-        l0 += __shfl_xor_sync(kFull, l0, 1);
-        l0 += __shfl_xor_sync(kFull, l0, 2);
-        l1 += __shfl_xor_sync(kFull, l1, 1);
-        l1 += __shfl_xor_sync(kFull, l1, 2);
-        if (*sm_abort) continue;
-        T *out = static_cast<T *>(p.out);
-        const float ia = 1.f / l0, ib = 1.f / l1;
-#pragma unroll
-        for (int j = 0; j < NTILES; ++j) {
-            const int d0 = 8 * j + 2 * q4;
-            if (va)
-                *reinterpret_cast<uint32_t *>(out + qrow_a * D + d0) =
-                    E::pack(o[j][0] * ia, o[j][1] * ia);
-            if (vb)
-                *reinterpret_cast<uint32_t *>(out + qrow_b * D + d0) =
-                    E::pack(o[j][2] * ib, o[j][3] * ib);
+            tc::fence_before_sync();
         }
     }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, LY::kTmemCols);
 }
+
+}  // namespace tcp
 
 // --------------------------------------------------------------------- host side
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 static int64_t max_items(int64_t S, int64_t T, int64_t QT) { return T / QT + S + 1; }
 
-static int tile_tokens(int G) { return kRows / G; }
+static int tile_tokens(int G) { return tcp::kRows / G; }
 
 static size_t ws_bytes(int64_t S, int64_t T, int64_t G)
 {
@@ -437,31 +525,46 @@ static bool make_pool_map(CUtensorMap *map, const void *pool, const PoolGeometry
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
+// Query rows [T][Hq][D] as a 4-D view (D, G, Hkv, T): a box (64, G, 1, QT)
+// brings the QT x G rows of one kv group's query tile, token-major, into one
+// 128-byte-swizzled region.
+static bool make_q_map(CUtensorMap *map, const void *q, int64_t T, int Hkv, int G, int D, int QT,
+                       bool bf16)
+{
+    EncodeFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)Hkv, (cuuint64_t)T};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)G * D * 2, (cuuint64_t)Hkv * G * D * 2};
+    cuuint32_t box[4] = {64u, (cuuint32_t)G, 1u, (cuuint32_t)QT};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+               const_cast<void *>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
-template <int D, bool BF16, int NST, int MINB>
-static KernelFn kernel_of() { return &prefill_kernel<D, BF16, NST, MINB>; }
+using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
 
-static bool pick(int D, bool bf16, KernelFn *fn, int *smem)
+static bool pick_tc(int D, bool bf16, TcKernelFn *fn, int *smem)
 {
     if (D == 128) {
-        *fn = bf16 ? kernel_of<128, true, 8, 2>() : kernel_of<128, false, 8, 2>();
-        *smem = Smem<128, 8>::kTotal;
+        *fn = bf16 ? &tcp::prefill_tc_kernel<128, true> : &tcp::prefill_tc_kernel<128, false>;
+        *smem = tcp::Layout<128>::kTotal;
         return true;
     }
     if (D == 64) {
-        *fn = bf16 ? kernel_of<64, true, 16, 2>() : kernel_of<64, false, 16, 2>();
-        *smem = Smem<64, 16>::kTotal;
+        *fn = bf16 ? &tcp::prefill_tc_kernel<64, true> : &tcp::prefill_tc_kernel<64, false>;
+        *smem = tcp::Layout<64>::kTotal;
         return true;
     }
     return false;
 }
 
-static int resident(KernelFn fn, int smem, int *sms_out)
+static int resident(const void *fn, int smem, int threads, int *sms_out)
 {
     constexpr int kMaxDev = 64, kMaxVar = 8;
     static std::mutex mu;
-    static KernelFn fns[kMaxDev][kMaxVar];
+    static const void *fns[kMaxDev][kMaxVar];
     static int ctas[kMaxDev][kMaxVar];
     static int sms[kMaxDev];
     int dev = 0;
@@ -474,13 +577,11 @@ static int resident(KernelFn fn, int smem, int *sms_out)
     for (int i = 0; i < kMaxVar; ++i) {
         if (fns[dev][i] == fn) return ctas[dev][i];
         if (fns[dev][i] == nullptr) {
-            if (cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                 cudaSuccess)
                 return -1;
             int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &n, reinterpret_cast<const void *>(fn), kThreads, smem) != cudaSuccess ||
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess ||
                 n < 1)
                 return -1;
             fns[dev][i] = fn;
@@ -520,9 +621,9 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_INVALID_ARG;
     const int G = num_q_heads / g.num_kv_heads;
     if (g.block_size != pkv::kBlock || G > 16) return PKV_ERR_UNSUPPORTED;
-    KernelFn fn;
+    TcKernelFn fn;
     int smem = 0;
-    if (!pick(g.head_dim, g.dtype == PKV_BF16, &fn, &smem)) return PKV_ERR_UNSUPPORTED;
+    if (!pick_tc(g.head_dim, g.dtype == PKV_BF16, &fn, &smem)) return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
     if (!out || !q || !k_pool || !v_pool || !block_tables || !query_start || !context_lens ||
         !workspace || !d_status)
@@ -535,8 +636,11 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     if (workspace_bytes < ws_bytes(num_seqs, num_tokens, G)) return PKV_ERR_INVALID_ARG;
     if ((int64_t)g.num_blocks * g.num_kv_heads * g.block_size > (int64_t)1 << 31)
         return PKV_ERR_UNSUPPORTED;
-    CUtensorMap tk, tv;
-    if (!make_pool_map(&tk, k_pool, g) || !make_pool_map(&tv, v_pool, g)) return PKV_ERR_CUDA;
+    CUtensorMap tk, tv, tq;
+    if (!make_pool_map(&tk, k_pool, g) || !make_pool_map(&tv, v_pool, g) ||
+        !make_q_map(&tq, q, num_tokens, g.num_kv_heads, G, g.head_dim, tcp::kRows / G,
+                    g.dtype == PKV_BF16))
+        return PKV_ERR_CUDA;
 
     Params prm;
     prm.out = out;
@@ -559,7 +663,7 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     prm.status = d_status;
 
     int sms = 0;
-    const int per_sm = resident(fn, smem, &sms);
+    const int per_sm = resident(reinterpret_cast<const void *>(fn), smem, tcp::kThreads, &sms);
     if (per_sm < 1) return PKV_ERR_CUDA;
     int64_t grid = (int64_t)per_sm * sms;
     const int64_t upper = prm.max_items * g.num_kv_heads;
@@ -572,10 +676,10 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(tcp::kThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, tk, tv, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, fn, tk, tv, tq, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
