@@ -137,12 +137,13 @@ constexpr float kLazy = 8.f;           // rescale threshold (log2 units)
 template <int D>
 struct Layout {
     static constexpr int kRegions = D / 64;
+    static constexpr int kStages = D == 128 ? 4 : 3;           // K/V tiles in flight (D 64: 2 CTAs/SM)
     static constexpr int kQBytes = kRegions * kRows * 128;     // [region][row][128 B]
     static constexpr int kKVBytes = kRegions * kKeys * 128;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kKVBytes;           // K tile, then V tile
     static constexpr int kPBytes = kRows * 128;                // [row][64 keys]
     static constexpr int kStage0 = kQBytes;
-    static constexpr int kP = kStage0 + 2 * kStageBytes;       // P high, then P low
+    static constexpr int kP = kStage0 + kStages * kStageBytes; // P high, then P low
     static constexpr int kMisc = kP + 2 * kPBytes;             // barriers and flags
     static constexpr int kTotal = 1024 + kMisc + 256;
     static constexpr uint32_t kTmemCols = 256;                 // S0 [0,64) S1 [64,128) O [128, 128 + D)
@@ -187,22 +188,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *p_s = base + LY::kP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + LY::kMisc);
     uint64_t *q_full = bars + 0, *q_empty = bars + 1;
-    uint64_t *kv_full = bars + 2, *kv_empty = bars + 4;       // [2] each
-    uint64_t *s_full = bars + 6;                              // [2]
-    uint64_t *p_full = bars + 8, *o_full = bars + 9, *done = bars + 10;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + 11);
-    int *stage_bad = reinterpret_cast<int *>(tslot + 1);      // [2]
-    volatile int *abort_flag = stage_bad + 2;
+    uint64_t *kv_full = bars + 2, *kv_empty = kv_full + LY::kStages;   // [LY::kStages] each
+    uint64_t *s_full = kv_empty + LY::kStages;                          // [2]
+    uint64_t *p_full = s_full + 2, *o_full = p_full + 1, *done = o_full + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    int *stage_bad = reinterpret_cast<int *>(tslot + 1);            // [LY::kStages]
+    volatile int *abort_flag = stage_bad + LY::kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(q_full), 1);
         mbar_init(smem_addr(q_empty), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < LY::kStages; ++i) {
             mbar_init(smem_addr(&kv_full[i]), 1);
             mbar_init(smem_addr(&kv_empty[i]), 1);
-            mbar_init(smem_addr(&s_full[i]), 1);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(smem_addr(&s_full[i]), 1);
         mbar_init(smem_addr(p_full), 4);
         mbar_init(smem_addr(o_full), 1);
         mbar_init(smem_addr(done), 1);
@@ -222,7 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducer) {
         if (lane == 0) {
             uint32_t kv_cnt = 0, it_cnt = 0;
-            int last_par[2] = {-1, -1}, last_q = -1;   // phases of the last copies issued
+            int last_par[LY::kStages], last_q = -1;          // phases of the last copies issued
+            for (int k = 0; k < LY::kStages; ++k) last_par[k] = -1;
             for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++it_cnt) {
                 const Item it = load_item(p, i, total, QT);
                 if (it_cnt > 0 &&
@@ -237,9 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t *row = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq;
                 const int nb = (it.nkeys + kBlock - 1) / kBlock;
                 for (int t = 0; t < it.ntiles; ++t, ++kv_cnt) {
-                    const int st = (int)(kv_cnt & 1u);
-                    if (kv_cnt >= 2 && !mbar_wait(smem_addr(&kv_empty[st]),
-                                                  ((kv_cnt >> 1) - 1) & 1u, abort_flag, p.status))
+                    const int st = (int)(kv_cnt % LY::kStages);
+                    const uint32_t fill = kv_cnt / LY::kStages;
+                    if (fill >= 1 && !mbar_wait(smem_addr(&kv_empty[st]), (fill - 1) & 1u,
+                                                abort_flag, p.status))
                         break;
                     int ids[4];
                     int bad = 0;
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (bad) atomicOr(p.status, PKV_DEV_BAD_BLOCK);
                     stage_bad[st] = bad;
-                    last_par[st] = (int)((kv_cnt >> 1) & 1u);
+                    last_par[st] = (int)(fill & 1u);
                     const uint32_t fb = smem_addr(&kv_full[st]);
                     mbar_arrive_expect_tx(fb, (uint32_t)(2 * LY::kKVBytes));
                     const uint32_t ks = smem_addr(stage_s + st * LY::kStageBytes);
@@ -271,10 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // after a timed-out wait: let the copies still in flight land first
             if (*abort_flag) {
-                for (int k = 0; k < 3; ++k) {
-                    const int par = k < 2 ? last_par[k] : last_q;
+                for (int k = 0; k <= LY::kStages; ++k) {
+                    const int par = k < LY::kStages ? last_par[k] : last_q;
                     if (par < 0) continue;
-                    const uint32_t fb = smem_addr(k < 2 ? &kv_full[k] : q_full);
+                    const uint32_t fb = smem_addr(k < LY::kStages ? &kv_full[k] : q_full);
                     const unsigned long long t0 = globaltimer();
                     while (!mbar_try_wait(fb, (uint32_t)par)) {
                         if (globaltimer() - t0 > kTimeoutNs) break;
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv = [&](uint32_t t, bool first) {
                 if (!mbar_wait(smem_addr(p_full), t & 1u, abort_flag, p.status)) { ok = false; return; }
                 tc::fence_after_sync();
-                const uint32_t vs = st_a + (t & 1u) * LY::kStageBytes + LY::kKVBytes;
+                const uint32_t vs = st_a + (t % LY::kStages) * LY::kStageBytes + LY::kKVBytes;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -302,14 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::mma_f16(tmem + 128, a, b, id_pv, !(first && part == 0 && kk == 0));
                     }
                 tc::mma_commit(smem_addr(o_full));
-                tc::mma_commit(smem_addr(&kv_empty[t & 1u]));
+                tc::mma_commit(smem_addr(&kv_empty[t % LY::kStages]));
             };
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it_cnt) {
                 const Item it = load_item(p, i, total, QT);
                 if (!mbar_wait(smem_addr(q_full), it_cnt & 1u, abort_flag, p.status)) break;
                 for (int t = 0; t < it.ntiles && ok; ++t, ++tg) {
-                    const uint32_t st = tg & 1u;
-                    if (!mbar_wait(smem_addr(&kv_full[st]), (tg >> 1) & 1u, abort_flag, p.status)) {
+                    const uint32_t st = tg % LY::kStages, sb = tg & 1u;
+                    if (!mbar_wait(smem_addr(&kv_full[st]), (tg / LY::kStages) & 1u, abort_flag,
+                                   p.status)) {
                         ok = false;
                         break;
                     }
@@ -320,9 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
                         const uint64_t a = tc::desc_sw128(q_a + (kk >> 2) * kRows * 128 + off, 16, 1024);
                         const uint64_t b = tc::desc_sw128(ks + (kk >> 2) * kKeys * 128 + off, 16, 1024);
-                        tc::mma_f16(tmem + 64 * st, a, b, id_qk, kk > 0);
+                        tc::mma_f16(tmem + 64 * sb, a, b, id_qk, kk > 0);
                     }
-                    tc::mma_commit(smem_addr(&s_full[st]));
+                    tc::mma_commit(smem_addr(&s_full[sb]));
                     if (t == it.ntiles - 1) tc::mma_commit(smem_addr(q_empty));
                     if (t >= 1) issue_pv(tg - 1, t == 1);
                 }
@@ -352,12 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_ref = -INFINITY, l = 0.f;
             int bad = 0;
             for (int t = 0; t < it.ntiles; ++t, ++tg) {
-                const uint32_t sb = tg & 1u;
-                const bool ok1 = mbar_wait(smem_addr(&kv_full[sb]), (tg >> 1) & 1u, abort_flag, p.status);
-                const bool ok2 = ok1 && mbar_wait(smem_addr(&s_full[sb]), (tg >> 1) & 1u, abort_flag, p.status);
+                const uint32_t st = tg % LY::kStages, sb = tg & 1u;
+                const bool ok1 = mbar_wait(smem_addr(&kv_full[st]), (tg / LY::kStages) & 1u, abort_flag,
+                                           p.status);
+                const bool ok2 = ok1 && mbar_wait(smem_addr(&s_full[sb]), (tg >> 1) & 1u, abort_flag,
+                                                  p.status);
                 if (!__all_sync(kFull, ok2)) { alive = false; break; }
                 tc::fence_after_sync();
-                bad |= stage_bad[sb];
+                bad |= stage_bad[st];
                 float x[kKeys];
                 {
                     uint32_t v[32];
@@ -370,13 +376,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]);
                 }
+                // raw scores; the scale enters inside the exponent (one FFMA each).
+                // Hidden keys are kept out of the maximum here and get weight 0 below.
                 const int k0 = t * kKeys;
+                const bool cross = k0 + kKeys - 1 > pos;   // the tile crosses this row's position
+                if (cross) {
+                    const float hide = p.scale_log2 < 0.f ? INFINITY : -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < kKeys; ++c)
+                        if (k0 + c > pos) x[c] = hide;
+                }
                 float mx = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
-                    x[c] = k0 + c <= pos ? x[c] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
+                for (int c = 0; c < kKeys; ++c) mx = fmaxf(mx, x[c]);
+                if (p.scale_log2 < 0.f) {          // the largest scaled score is the smallest raw one
+                    mx = INFINITY;
+#pragma unroll
+                    for (int c = 0; c < kKeys; ++c) mx = fminf(mx, x[c]);
                 }
+                mx *= p.scale_log2;
                 float f = 1.f;
                 bool resc = false;
                 if (mx > m_ref + kLazy) {          // also the first tile: m_ref = -inf
@@ -388,9 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float lsum = 0.f;
                 uint32_t hi[kKeys / 2], lo[kKeys / 2];
+                const float nm = -m_ref;
 #pragma unroll
                 for (int c = 0; c < kKeys; c += 2) {
-                    const float p0 = fast_exp2(x[c] - m_ref), p1 = fast_exp2(x[c + 1] - m_ref);
+                    float p0 = fast_exp2(fmaf(x[c], p.scale_log2, nm));
+                    float p1 = fast_exp2(fmaf(x[c + 1], p.scale_log2, nm));
+                    if (cross) {
+                        if (k0 + c > pos) p0 = 0.f;
+                        if (k0 + c + 1 > pos) p1 = 0.f;
+                    }
                     lsum += p0 + p1;
                     hi[c / 2] = E::pack(p0, p1);
                     const float2 hh = E::unpack(hi[c / 2]);
@@ -429,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // zero the V rows of keys past the last visible one (last tile only)
                 const int nvis = it.nkeys - k0;
                 if (nvis < kKeys) {
-                    uint8_t *vs = stage_s + sb * LY::kStageBytes + LY::kKVBytes;
+                    uint8_t *vs = stage_s + st * LY::kStageBytes + LY::kKVBytes;
                     const int nrows = kKeys - nvis;
                     for (int e = r; e < nrows * LY::kRegions * 8; e += kRows) {
                         const int row = nvis + e / (LY::kRegions * 8);
