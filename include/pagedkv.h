@@ -225,7 +225,8 @@ int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *d
  *
  * Pool layout (head_dim 128, block_size 16): one record of
  * PKV_Q8_SLAB_BYTES bytes per (block, kv head), records in the order
- * [num_blocks][num_kv_heads], so a block's slab is one contiguous copy:
+ * [num_blocks][num_kv_heads], so a block's slab is one contiguous copy.  A
+ * code c is stored as the byte c + 128 (c XOR 0x80):
  *   bytes [0, 2048)     K codes: 16 rows of 128 bytes.  Token t = 4a + 2b + c
  *                       (a in 0..3, b and c in 0..1) is row r = 8b + 2a + c; its
  *                       16-byte chunk j (dimensions 16j .. 16j + 15) is stored

@@ -164,11 +164,12 @@ cache_write_q8_kernel(const uint16_t *__restrict__ k_new, const uint16_t *__rest
         q8_quantise4<BF16>(v_new + r * D, lane, vc, vs);
         // K: token off = 4a + 2b + c -> row 8b + 2a + c, chunk (lane / 4) rotated by the row
         const int row = 8 * ((off >> 1) & 1) + 2 * (off >> 2) + (off & 1);
+        // codes are stored biased: byte = code + 128 (code XOR 0x80)
         *reinterpret_cast<uint32_t *>(rec + row * 128 + (((lane >> 2) ^ (row & 7)) << 4) +
-                                      4 * (lane & 3)) = kc;
+                                      4 * (lane & 3)) = kc ^ 0x80808080u;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            rec[2048 + (4 * lane + i) * BS + off] = (uint8_t)((vc >> (8 * i)) & 0xff);
+            rec[2048 + (4 * lane + i) * BS + off] = (uint8_t)(((vc >> (8 * i)) & 0xff) ^ 0x80u);
         if ((lane & 7) == 0) {
             *reinterpret_cast<uint16_t *>(rec + 4096 + off * 8 + 2 * (lane >> 3)) = ks;
             *reinterpret_cast<uint16_t *>(rec + 4224 + (lane >> 3) * 32 + off * 2) = vs;

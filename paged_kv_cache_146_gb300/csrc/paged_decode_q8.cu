@@ -13,9 +13,25 @@
 namespace pkv {
 namespace decode {
 
+// Four stored bytes (byte i = code i + 128) -> fp16 pairs lo = (code0, code1),
+// hi = (code2, code3), exact: the byte u is the low mantissa of 1024 (fp16 bits
+// 0x6400 | u = 1024 + u) and one packed subtraction of 1152 leaves the code.
+__device__ __forceinline__ void biased_to_pairs(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    uint32_t a = __byte_perm(w, 0x64646464u, 0x4140);     // (0x64, u0), (0x64, u1)
+    uint32_t b = __byte_perm(w, 0x64646464u, 0x4342);     // (0x64, u2), (0x64, u3)
+    const uint32_t bias = 0x64806480u;                    // (1152, 1152)
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(a) : "r"(bias));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(b) : "r"(bias));
+    lo = a;
+    hi = b;
+}
+
 // An 8-bit pool ("kv-cache-by-model", section 1: one-byte codes with one fp16
 // scale per 32 values) keeps each (block, kv head) slab as one record of
 // q8::kSlab = 4,352 bytes, so a block costs one bulk copy:
+// Codes are stored biased (byte = code + 128), which saves the decode kernel a
+// bias step per code word.
 //   [0, 2048)     K codes, 16 rows of 128 bytes: token t = 4a + 2b + c sits in
 //                 row 8b + 2a + c, its 16-byte chunk j at position j ^ (row & 7)
 //   [2048, 4096)  V codes, 128 dimension rows of 16 bytes (byte = token)
@@ -104,13 +120,13 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
             ldsm_x4(kr, krow + (((2 * i + kstep_hi) ^ r8) << 4));
             float c0[4], c1[4];
             uint32_t lo, hi;
-            codes_to_pairs<false>(kr[0], lo, hi);
+            biased_to_pairs(kr[0], lo, hi);
             H::mma0(c0, qa[2 * i], lo, hi);
-            codes_to_pairs<false>(kr[1], lo, hi);
+            biased_to_pairs(kr[1], lo, hi);
             H::mma0(c1, qa[2 * i], lo, hi);
-            codes_to_pairs<false>(kr[2], lo, hi);
+            biased_to_pairs(kr[2], lo, hi);
             H::mma(c0, qa[2 * i + 1], lo, hi);
-            codes_to_pairs<false>(kr[3], lo, hi);
+            biased_to_pairs(kr[3], lo, hi);
             H::mma(c1, qa[2 * i + 1], lo, hi);
             sc[0] = fmaf(ks[0][i], c0[0], sc[0]);
             sc[1] = fmaf(ks[1][i], c0[1], sc[1]);
@@ -173,8 +189,8 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             uint32_t a[4];
-            codes_to_pairs<false>(vr[2 * t], a[0], a[2]);
-            codes_to_pairs<false>(vr[2 * t + 1], a[1], a[3]);
+            biased_to_pairs(vr[2 * t], a[0], a[2]);
+            biased_to_pairs(vr[2 * t + 1], a[1], a[3]);
             H::mma(o[2 * i + t], a, b0, b1);
         }
     }

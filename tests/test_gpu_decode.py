@@ -285,3 +285,17 @@ def test_repeated_launches_are_identical(split):
     for o in outs:
         assert torch.equal(o, outs[0])
     assert_close(outs[0], exp, f"split={split}")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0883883])
+def test_zero_and_negative_scale(scale):
+    """A zero scale gives the plain mean of V over the context; a negative one
+    weights the smallest scores most: both against the oracle, split and not."""
+    w = workloads.small_random(31, 6, 900, 32, 8, 128, "bf16")
+    w.scale = scale
+    c = _case(w)
+    exp = c.oracle_out()
+    for split in (None, 3):
+        out = c.run_gpu(blocks_per_split=split)
+        assert status_check(c.status) == (0, 0)
+        assert_close(out, exp, f"decode scale {scale} split {split}")

@@ -105,3 +105,15 @@ def test_bad_chunk_is_rejected():
     assert rc == -5 and word & 4
     assert not out[50:].any()
     assert_close(out[:50], _oracle(c, qb, qs)[:50], "other sequence unaffected")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0883883])
+def test_zero_and_negative_scale(scale):
+    """A zero scale gives uniform weights over the visible keys; a negative one
+    makes the smallest score the largest weight: both against the oracle."""
+    c, qb, qs = _case(13, [300, 70], [120, 70], 32, 8, 128, "bf16")
+    c.w.scale = scale
+    out = _run(c, qb, qs)
+    assert status_check(c.status) == (0, 0)
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, _oracle(c, qb, qs), f"prefill scale {scale}")

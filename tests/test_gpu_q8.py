@@ -9,7 +9,7 @@ codes with one fp16 scale per 32 values) against the oracle.
     unpacks it by index arithmetic into the oracle's four plain arrays;
   * decode attention over the 8-bit pool: |gpu - oracle| <= 2e-3 + 1e-2 |oracle|,
     the oracle attending in fp64 over code * scale; stale slots past each
-    context (codes -1, NaN scales) never reach the result; repeated launches
+    context (stored bytes 0xFF, NaN scales) never reach the result; repeated launches
     give the same bits.
 """
 import numpy as np
@@ -35,23 +35,23 @@ D = 128
 
 
 def _fill_sentinel(pool):
-    pool.kv.fill_(0xFF)                                  # codes -1, scales fp16 NaN
+    pool.kv.fill_(0xFF)                                  # codes 127, scales fp16 NaN
 
 
 def unpack_records(kv: np.ndarray):
     """Records uint8 [nb][Hkv][4352] -> (k_codes int8 [nb][Hkv][16][128],
     v_codes int8 [nb][Hkv][128][16], k_scales, v_scales uint16 [nb][Hkv][16][4]).
     Token t = 4a + 2b + c is K row r = 8b + 2a + c; chunk j of row r sits at
-    chunk position j ^ (r % 8).  K scales are stored token-major, V scales
-    group-major."""
+    chunk position j ^ (r % 8); codes are stored biased (byte = code + 128).
+    K scales are stored token-major, V scales group-major."""
     nb, hkv, _ = kv.shape
     t = np.arange(16)
     r = 8 * ((t >> 1) & 1) + 2 * (t >> 2) + (t & 1)
     j = np.arange(8)
     rows = kv[:, :, :2048].reshape(nb, hkv, 16, 8, 16)
     k = rows[:, :, r[:, None], j[None, :] ^ (r[:, None] % 8), :]     # [nb][hkv][t][j][16]
-    k_codes = k.reshape(nb, hkv, 16, 128).view(np.int8)
-    v_codes = kv[:, :, 2048:4096].reshape(nb, hkv, 128, 16).view(np.int8)
+    k_codes = (k.reshape(nb, hkv, 16, 128) ^ 0x80).view(np.int8)         # stored as code + 128
+    v_codes = (kv[:, :, 2048:4096].reshape(nb, hkv, 128, 16) ^ 0x80).view(np.int8)
     k_scales = np.ascontiguousarray(kv[:, :, 4096:4224]).view(np.uint16).reshape(nb, hkv, 16, 4)
     v_scales = np.ascontiguousarray(np.ascontiguousarray(kv[:, :, 4224:4352]).view(np.uint16)
                                     .reshape(nb, hkv, 4, 16).transpose(0, 1, 3, 2))
@@ -59,7 +59,8 @@ def unpack_records(kv: np.ndarray):
 
 
 def _oracle_pools(nb, hkv):
-    return (np.full((nb, hkv, 16, D), -1, np.int8), np.full((nb, hkv, D, 16), -1, np.int8),
+    # the library pool starts as 0xFF bytes: stored 0xFF is the code 127
+    return (np.full((nb, hkv, 16, D), 127, np.int8), np.full((nb, hkv, D, 16), 127, np.int8),
             np.full((nb, hkv, 16, D // 32), 0xFFFF, np.uint16),
             np.full((nb, hkv, 16, D // 32), 0xFFFF, np.uint16))
 
@@ -190,13 +191,13 @@ def test_q8_cache_write_special_rows():
 
 
 def test_q8_stale_slots_never_read():
-    """Slots past each context hold codes -1 and NaN scales (the sentinel); the
+    """Slots past each context hold codes 127 and NaN scales (the sentinel); the
     result must stay finite and match the oracle, which never reads them."""
     c = Q8Case([3, 18, 45, 100], 32, 8, "bf16", seed=5)
     k_codes = _host_pools(c.pool)[0]
     for s, n in enumerate(c.lens):
         last = c.tables[s, (int(n) - 1) // 16]
-        assert (k_codes[last, :, int(n) % 16 or 16:] == -1).all()
+        assert (k_codes[last, :, int(n) % 16 or 16:] == 127).all()
     out = c.run()
     assert torch.isfinite(out.float()).all()
     assert_close(out, c.oracle_out(), "stale slots")
@@ -318,3 +319,12 @@ def test_q8_block_copy_and_swap_round_trip():
     rc, word = status_check(status)
     assert rc == -5 and word == 2
     assert np.array_equal(pool.kv.cpu().numpy(), expected)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0883883])
+def test_q8_zero_and_negative_scale(scale):
+    c = Q8Case([40, 700, 1500], 32, 8, "bf16", seed=23)
+    c.scale = scale
+    out = c.run()
+    assert status_check(c.status) == (0, 0)
+    assert_close(out, c.oracle_out(), f"q8 scale {scale}")
