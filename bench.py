@@ -518,7 +518,7 @@ def prefill_arm(args, world, rank, local):
                          "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
                          "traffic": None, "peak_kind": tkind,
                          "note": "tcgen05.mma kind::f16 (TMEM accumulators), 128 query rows x "
-                                 "64-key tiles, P as bf16 high + low parts"},
+                                 "64-key tiles, two query tiles per CTA, P as bf16 high + low parts"},
             "gpu_launches": 2 * args.steps}
     print(json.dumps(line), flush=True)
 

@@ -111,15 +111,17 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
 }
 
 // ================================================== tcgen05 prefill kernel
-// Items are (sequence, kv head, query tile of 128 / G tokens): 128 query rows
-// (token-major: row r = token r / G, head r % G) against the sequence's keys
-// 0 .. last position of the tile, in KV tiles of 64 keys (4 blocks).
-//   warp 4 (producer): TMA of the item's Q rows (one 4-D box per 64 columns)
+// Items are (sequence, kv head, two query tiles of 128 / G tokens): per tile
+// 128 query rows (token-major: row r = token r / G, head r % G), both tiles
+// against the same KV tiles of 64 keys (4 blocks) up to the second tile's last
+// position, so each K/V tile is loaded once for 256 rows.
+//   warp 8 (producer): TMA of the item's Q rows (one 4-D box per 64 columns)
 //     and of each KV tile's 4 K and 4 V blocks into a 2-stage ring.
-//   warp 5 lane 0 (MMA issuer): S = Q K^T into one of two tensor-memory
+//   warp 9 lane 0 (MMA issuer): per group S = Q K^T into one of two tensor-memory
 //     buffers (M 128, N 64), then O += P V for the previous tile (M 128, N D,
 //     V as an MN-major operand), P as a high and a low bf16/fp16 part.
-//   warps 0-3 (softmax): thread r owns row r = tensor-memory lane r.  Running
+//   warps 0-3 and 4-7 (softmax, one warpgroup per query tile, ping-pong on the
+//     tensor pipe): thread r of a group owns row r = tensor-memory lane r.  Running
 //     maximum with lazy rescaling: the reference maximum moves only when a
 //     tile's maximum exceeds it by more than 8 (log2 units), so weights stay
 //     <= 2^8 and O in tensor memory is rescaled rarely.  V rows past the last
@@ -128,27 +130,31 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
 // Every wait is bounded; on expiry the kernel flags PKV_DEV_TIMEOUT and stops.
 namespace tcp {
 
-constexpr int kRows = 128;             // M: query rows per item
+constexpr int kRows = 128;             // M: query rows per query tile
+constexpr int kGroups = 2;             // query tiles per item, sharing every K/V tile
 constexpr int kKeys = 64;              // keys per KV tile
-constexpr int kThreads = 6 * 32;       // softmax warps 0-3, producer 4, MMA 5
-constexpr int kProducer = 4, kIssuer = 5;
+constexpr int kThreads = (4 * kGroups + 2) * 32;   // softmax warps 0-7, producer 8, MMA 9
+constexpr int kProducer = 4 * kGroups, kIssuer = 4 * kGroups + 1;
 constexpr float kLazy = 8.f;           // rescale threshold (log2 units)
 
 template <int D>
 struct Layout {
     static constexpr int kRegions = D / 64;
-    static constexpr int kStages = D == 128 ? 4 : 3;           // K/V tiles in flight (D 64: 2 CTAs/SM)
-    static constexpr int kQBytes = kRegions * kRows * 128;     // [region][row][128 B]
+    static constexpr int kStages = D == 128 ? 3 : 4;           // K/V tiles in flight
+    static constexpr int kQBytes = kRegions * kRows * 128;     // one query tile: [region][row][128 B]
     static constexpr int kKVBytes = kRegions * kKeys * 128;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kKVBytes;           // K tile, then V tile
     static constexpr int kPBytes = kRows * 128;                // [row][64 keys]
-    static constexpr int kStage0 = kQBytes;
-    static constexpr int kP = kStage0 + kStages * kStageBytes; // P high, then P low
-    static constexpr int kMisc = kP + 2 * kPBytes;             // barriers and flags
+    static constexpr int kStage0 = kGroups * kQBytes;
+    static constexpr int kP = kStage0 + kStages * kStageBytes; // per group: P high, then P low
+    static constexpr int kMisc = kP + kGroups * 2 * kPBytes;   // barriers and flags
     static constexpr int kTotal = 1024 + kMisc + 256;
-    static constexpr uint32_t kTmemCols = 256;                 // S0 [0,64) S1 [64,128) O [128, 128 + D)
+    // S of group g, buffer b at 64 (2g + b); O of group g at 256 + 128 g
+    static constexpr uint32_t kTmemCols = 512;
 };
 
+// An item: the query tiles [t0, t0 + QT) (group 0) and [t0 + QT, t0 + 2 QT)
+// (group 1) of one sequence's chunk and one kv head; keys 0 .. nkeys - 1.
 struct Item {
     int s, g, r0, C, L, t0, t1, nkeys, ntiles;
 };
@@ -165,15 +171,15 @@ __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int
     it.r0 = __ldg(p.query_start + e.x);
     it.C = __ldg(p.query_start + e.x + 1) - it.r0;
     it.L = __ldg(p.context_lens + e.x);
-    it.t0 = e.y * QT;
-    it.t1 = min(it.t0 + QT, it.C);
+    it.t0 = e.y * kGroups * QT;
+    it.t1 = min(it.t0 + kGroups * QT, it.C);
     it.nkeys = it.L - it.C + it.t1;
     it.ntiles = (it.nkeys + kKeys - 1) / kKeys;
     return it;
 }
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmQ, const Params p)
 {
@@ -189,8 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + LY::kMisc);
     uint64_t *q_full = bars + 0, *q_empty = bars + 1;
     uint64_t *kv_full = bars + 2, *kv_empty = kv_full + LY::kStages;   // [LY::kStages] each
-    uint64_t *s_full = kv_empty + LY::kStages;                          // [2]
-    uint64_t *p_full = s_full + 2, *o_full = p_full + 1, *done = o_full + 1;
+    uint64_t *s_full = kv_empty + LY::kStages;                 // [group][buffer]
+    uint64_t *p_full = s_full + 2 * kGroups;                   // [group]
+    uint64_t *o_full = p_full + kGroups;                       // [group]
+    uint64_t *done = o_full + kGroups;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
     int *stage_bad = reinterpret_cast<int *>(tslot + 1);            // [LY::kStages]
     volatile int *abort_flag = stage_bad + LY::kStages;
@@ -203,9 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&kv_full[i]), 1);
             mbar_init(smem_addr(&kv_empty[i]), 1);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(smem_addr(&s_full[i]), 1);
-        mbar_init(smem_addr(p_full), 4);
-        mbar_init(smem_addr(o_full), 1);
+        for (int i = 0; i < 2 * kGroups; ++i) mbar_init(smem_addr(&s_full[i]), 1);
+        for (int i = 0; i < kGroups; ++i) {
+            mbar_init(smem_addr(&p_full[i]), 4);
+            mbar_init(smem_addr(&o_full[i]), 1);
+        }
         mbar_init(smem_addr(done), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -217,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tslot;
     griddep_wait();
 
-    const int Hkv = p.num_kv_heads, G = p.group, QT = p.tile_tokens;
+    const int Hkv = p.num_kv_heads, G = p.group, QT = p.tile_tokens / kGroups;   // one query tile
     const int total = p.header[0] * Hkv;
 
     if (warp == kProducer) {
@@ -232,10 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 const uint32_t qb = smem_addr(q_full);
                 last_q = (int)(it_cnt & 1u);
-                mbar_arrive_expect_tx(qb, (uint32_t)(LY::kRegions * QT * G * 128));
-                for (int rg = 0; rg < LY::kRegions; ++rg)
-                    tc::tma_load_4d(smem_addr(q_s + rg * kRows * 128), &tmQ, rg * 64, 0, it.g,
-                                    it.r0 + it.t0, qb);
+                mbar_arrive_expect_tx(qb, (uint32_t)(kGroups * LY::kRegions * QT * G * 128));
+                for (int gr = 0; gr < kGroups; ++gr)
+                    for (int rg = 0; rg < LY::kRegions; ++rg)
+                        tc::tma_load_4d(smem_addr(q_s + gr * LY::kQBytes + rg * kRows * 128), &tmQ,
+                                        rg * 64, 0, it.g, it.r0 + it.t0 + gr * QT, qb);
                 const int32_t *row = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq;
                 const int nb = (it.nkeys + kBlock - 1) / kBlock;
                 for (int t = 0; t < it.ntiles; ++t, ++kv_cnt) {
@@ -292,19 +303,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t q_a = smem_addr(q_s), st_a = smem_addr(stage_s), p_a = smem_addr(p_s);
             uint32_t tg = 0, it_cnt = 0;
             bool ok = true;
+            // P V of tile t for both groups, then the stage is free
             auto issue_pv = [&](uint32_t t, bool first) {
-                if (!mbar_wait(smem_addr(p_full), t & 1u, abort_flag, p.status)) { ok = false; return; }
-                tc::fence_after_sync();
                 const uint32_t vs = st_a + (t % LY::kStages) * LY::kStageBytes + LY::kKVBytes;
-#pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int kk = 0; kk < kKeys / 16; ++kk) {
-                        const uint64_t a = tc::desc_sw128(p_a + part * LY::kPBytes + kk * 32, 16, 1024);
-                        const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
-                        tc::mma_f16(tmem + 128, a, b, id_pv, !(first && part == 0 && kk == 0));
+                for (int gr = 0; gr < kGroups && ok; ++gr) {
+                    if (!mbar_wait(smem_addr(&p_full[gr]), t & 1u, abort_flag, p.status)) {
+                        ok = false;
+                        return;
                     }
-                tc::mma_commit(smem_addr(o_full));
+                    tc::fence_after_sync();
+                    const uint32_t pg = p_a + gr * 2 * LY::kPBytes;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < kKeys / 16; ++kk) {
+                            const uint64_t a = tc::desc_sw128(pg + part * LY::kPBytes + kk * 32, 16, 1024);
+                            const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
+                            tc::mma_f16(tmem + 256 + 128 * gr, a, b, id_pv,
+                                        !(first && part == 0 && kk == 0));
+                        }
+                    tc::mma_commit(smem_addr(&o_full[gr]));
+                }
                 tc::mma_commit(smem_addr(&kv_empty[t % LY::kStages]));
             };
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it_cnt) {
@@ -319,14 +338,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::fence_after_sync();
                     const uint32_t ks = st_a + st * LY::kStageBytes;
+                    for (int gr = 0; gr < kGroups; ++gr) {
+                        const uint32_t qg = q_a + gr * LY::kQBytes;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
-                        const uint64_t a = tc::desc_sw128(q_a + (kk >> 2) * kRows * 128 + off, 16, 1024);
-                        const uint64_t b = tc::desc_sw128(ks + (kk >> 2) * kKeys * 128 + off, 16, 1024);
-                        tc::mma_f16(tmem + 64 * sb, a, b, id_qk, kk > 0);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
+                            const uint64_t a = tc::desc_sw128(qg + (kk >> 2) * kRows * 128 + off, 16, 1024);
+                            const uint64_t b = tc::desc_sw128(ks + (kk >> 2) * kKeys * 128 + off, 16, 1024);
+                            tc::mma_f16(tmem + 64 * (2 * gr + sb), a, b, id_qk, kk > 0);
+                        }
+                        tc::mma_commit(smem_addr(&s_full[2 * gr + sb]));
                     }
-                    tc::mma_commit(smem_addr(&s_full[sb]));
                     if (t == it.ntiles - 1) tc::mma_commit(smem_addr(q_empty));
                     if (t >= 1) issue_pv(tg - 1, t == 1);
                 }
@@ -344,34 +366,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- softmax
-        const int r = threadIdx.x;                  // row = tensor-memory lane
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+        const int gr = warp >> 2;                   // query tile of this warpgroup
+        const int r = threadIdx.x - kRows * gr;     // row = tensor-memory lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const uint32_t s_col = 64 * 2 * gr, o_col = 256 + 128 * gr;
+        uint8_t *p_g = p_s + gr * 2 * LY::kPBytes;
         uint32_t tg = 0, it_cnt = 0;
         bool alive = true;
         for (int i = blockIdx.x; i < total && alive; i += gridDim.x, ++it_cnt) {
             const Item it = load_item(p, i, total, QT);
             const int jj = r / G, h = r - (r / G) * G;
-            const bool valid = r < QT * G && it.t0 + jj < it.t1;
-            const int pos = valid ? it.L - it.C + it.t0 + jj : it.nkeys - 1;
+            const int tg0 = it.t0 + gr * QT;            // this group's first token
+            const bool valid = r < QT * G && tg0 + jj < it.t1;
+            const int pos = valid ? it.L - it.C + tg0 + jj : it.nkeys - 1;
             float m_ref = -INFINITY, l = 0.f;
             int bad = 0;
             for (int t = 0; t < it.ntiles; ++t, ++tg) {
                 const uint32_t st = tg % LY::kStages, sb = tg & 1u;
                 const bool ok1 = mbar_wait(smem_addr(&kv_full[st]), (tg / LY::kStages) & 1u, abort_flag,
                                            p.status);
-                const bool ok2 = ok1 && mbar_wait(smem_addr(&s_full[sb]), (tg >> 1) & 1u, abort_flag,
-                                                  p.status);
+                const bool ok2 = ok1 && mbar_wait(smem_addr(&s_full[2 * gr + sb]), (tg >> 1) & 1u,
+                                                  abort_flag, p.status);
                 if (!__all_sync(kFull, ok2)) { alive = false; break; }
                 tc::fence_after_sync();
                 bad |= stage_bad[st];
                 float x[kKeys];
                 {
                     uint32_t v[32];
-                    tc::tmem_ld32(lane_base + 64 * sb, v);
+                    tc::tmem_ld32(lane_base + s_col + 64 * sb, v);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]);
-                    tc::tmem_ld32(lane_base + 64 * sb + 32, v);
+                    tc::tmem_ld32(lane_base + s_col + 64 * sb + 32, v);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]);
@@ -424,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P V of the previous tile must be done: it reads the P buffer and
                 // writes O
                 if (t >= 1) {
-                    const bool okp = mbar_wait(smem_addr(o_full), (tg - 1) & 1u, abort_flag, p.status);
+                    const bool okp = mbar_wait(smem_addr(&o_full[gr]), (tg - 1) & 1u, abort_flag, p.status);
                     if (!__all_sync(kFull, okp)) { alive = false; break; }
                     tc::fence_after_sync();
                 }
@@ -432,16 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t v[32];
-                        tc::tmem_ld32(lane_base + 128 + c0, v);
+                        tc::tmem_ld32(lane_base + o_col + c0, v);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
-                        tc::tmem_st32(lane_base + 128 + c0, v);
+                        tc::tmem_st32(lane_base + o_col + c0, v);
                     }
                     tc::tmem_wait_st();
                 }
                 // this row of P (high and low), 128-byte swizzle
-                uint8_t *ph = p_s + r * 128;
+                uint8_t *ph = p_g + r * 128;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int pos16 = (j ^ (r & 7)) << 4;
@@ -452,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // zero the V rows of keys past the last visible one (last tile only)
                 const int nvis = it.nkeys - k0;
-                if (nvis < kKeys) {
+                if (gr == 0 && nvis < kKeys) {           // one group does it for both
                     uint8_t *vs = stage_s + st * LY::kStageBytes + LY::kKVBytes;
                     const int nrows = kKeys - nvis;
                     for (int e = r; e < nrows * LY::kRegions * 8; e += kRows) {
@@ -465,20 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(p_full));
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[gr]));
             }
             if (!alive) break;
             // ---- the item's result: O / l once the last P V is done
-            const bool oko = mbar_wait(smem_addr(o_full), (tg - 1) & 1u, abort_flag, p.status);
+            const bool oko = mbar_wait(smem_addr(&o_full[gr]), (tg - 1) & 1u, abort_flag, p.status);
             if (!__all_sync(kFull, oko)) break;
             tc::fence_after_sync();
             const float inv = 1.f / l;
             T *out = static_cast<T *>(p.out) +
-                     ((size_t)(it.r0 + it.t0 + jj) * p.num_q_heads + (size_t)it.g * G + h) * D;
+                     ((size_t)(it.r0 + tg0 + jj) * p.num_q_heads + (size_t)it.g * G + h) * D;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t v[32];
-                tc::tmem_ld32(lane_base + 128 + c0, v);
+                tc::tmem_ld32(lane_base + o_col + c0, v);
                 tc::tmem_wait_ld();
                 if (valid) {
 #pragma unroll
@@ -508,7 +534,8 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 static int64_t max_items(int64_t S, int64_t T, int64_t QT) { return T / QT + S + 1; }
 
-static int tile_tokens(int G) { return tcp::kRows / G; }
+// tokens of one item: kGroups query tiles of kRows / G tokens each
+static int tile_tokens(int G) { return tcp::kGroups * (tcp::kRows / G); }
 
 static size_t ws_bytes(int64_t S, int64_t T, int64_t G)
 {
