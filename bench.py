@@ -443,7 +443,8 @@ def our_arm(args, world, rank, local):
                      "launch_ms": round(attn_avg_ms, 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (4 if eng.maxb > default_split() else 3) * args.steps,
+        "gpu_launches": (4 if eng.maxb > (eng.split_for_step() or default_split()) else 3)
+        * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
