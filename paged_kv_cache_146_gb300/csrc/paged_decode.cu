@@ -91,18 +91,61 @@ struct ItemMeta {
 // ----------------------------------------------------------------- prep kernel
 // One CTA: partitions per sequence, their prefix sum, the item list, and zero
 // rows for empty or invalid sequences.
+//
+// Item order: the persistent grid takes items in a fixed stride, so the list
+// ends with the smallest ones and every CTA's last item is short.  Full
+// partitions (P blocks) come first, in sequence order; then each sequence's
+// partial last partition, by size from large to small (kOrderBins size bins,
+// sequence order inside a bin).  The list must not vary between launches with
+// equal inputs: a CTA hands its blocks to its consumer warps by their position
+// in its own stream, so which CTA takes an item decides how the item's sum is
+// split between warps, and with it the last bits of the result.
+constexpr int kOrderBins = 64;
+
+// Inclusive scan of two counters over the 1024 threads of the prep CTA.
+__device__ __forceinline__ int2 prep_scan2(int2 x, int2 (&warp_tot)[32], int lane, int warp)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(kFull, x.x, o), b = __shfl_up_sync(kFull, x.y, o);
+        if (lane >= o) { x.x += a; x.y += b; }
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int2 t = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(kFull, t.x, o), b = __shfl_up_sync(kFull, t.y, o);
+            if (lane >= o) { t.x += a; t.y += b; }
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    if (warp > 0) { x.x += warp_tot[warp - 1].x; x.y += warp_tot[warp - 1].y; }
+    return x;
+}
+
 __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t head_dim)
 {
-    __shared__ int warp_tot[32];
-    __shared__ int carry;
+    __shared__ int2 warp_tot[32];
+    __shared__ int2 carry;               // (pairs, full partitions) of earlier chunks
+    __shared__ int bin_next[kOrderBins];
+    __shared__ int warp_bin[32][kOrderBins];   // pass 2: per-warp counts, then offsets
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = p.blocks_per_split;
     griddep_launch_dependents();   // the main kernel may set up its CTAs meanwhile
-    if (tid == 0) carry = 0;
+    if (tid == 0) carry = make_int2(0, 0);
+    for (int i = tid; i < kOrderBins; i += 1024) bin_next[i] = 0;
+    for (int i = tid; i < 32 * kOrderBins; i += 1024) (&warp_bin[0][0])[i] = 0;
     __syncthreads();
+    // bin of a partial last partition of r blocks, 0 < r < P: larger r, lower bin
+    auto bin_of = [P](int r) { return (int)((int64_t)(P - 1 - r) * kOrderBins / P); };
     const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
+    // pass 1: partitions, pair offsets, full partitions, size histogram, zero rows
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int s = base + tid;
-        int nsplit = 0;
+        int nsplit = 0, partial = 0, r = 0;
         bool zero_row = false;
         if (s < p.num_seqs) {
             const int L = p.context_lens[s];
@@ -113,33 +156,23 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
                 zero_row = true;
             } else {
                 const int nb = (L + kBlock - 1) / kBlock;
-                nsplit = (nb + p.blocks_per_split - 1) / p.blocks_per_split;
+                nsplit = (nb + P - 1) / P;
+                r = nb - (nsplit - 1) * P;
+                partial = r < P;
             }
         }
-        int x = nsplit;   // inclusive scan over the CTA
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) warp_tot[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int t = warp_tot[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, t, o);
-                if (lane >= o) t += y;
-            }
-            warp_tot[lane] = t;
-        }
-        __syncthreads();
-        const int excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - nsplit;
-        if (s < p.num_seqs && dbg_fail((int64_t)excl + nsplit <= p.max_pairs, p.debug, 12, excl))
+        const int2 inc = prep_scan2(make_int2(nsplit, nsplit - partial), warp_tot, lane, warp);
+        const int2 c0 = carry;
+        const int excl = c0.x + inc.x - nsplit;
+        const int excl_full = c0.y + inc.y - (nsplit - partial);
+        if (s < p.num_seqs && dbg_fail((int64_t)excl + nsplit <= p.max_pairs, p.debug, 12, excl)) {
             nsplit = 0;
+            partial = 0;
+        }
         if (s < p.num_seqs) {
             p.seq_info[s] = make_int2(excl, nsplit);
-            for (int k = 0; k < nsplit; ++k) p.items[excl + k] = make_int2(s, k);
+            for (int k = 0; k < nsplit - partial; ++k) p.items[excl_full + k] = make_int2(s, k);
+            if (partial) atomicAdd(&bin_next[bin_of(r)], 1);
             if (zero_row) {
                 uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(p.out) +
                                                      (size_t)s * p.num_q_heads * head_dim * 2);
@@ -148,10 +181,63 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
             }
         }
         __syncthreads();
-        if (tid == 0) carry += warp_tot[31];
+        if (tid == 0) carry = make_int2(c0.x + warp_tot[31].x, c0.y + warp_tot[31].y);
         __syncthreads();
     }
-    if (tid == 0) p.header[0] = carry;
+    // bin counts -> first item index of each bin (after the full partitions)
+    if (warp == 0) {
+        constexpr int kPer = kOrderBins / 32;
+        int c[kPer], sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) { c[i] = bin_next[lane * kPer + i]; sum += c[i]; }
+        int x = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        int at = carry.y + x - sum;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) { bin_next[lane * kPer + i] = at; at += c[i]; }
+    }
+    __syncthreads();
+    // pass 2: partial last partitions into their bins, a stable counting sort:
+    // within a chunk, rank among the warp's lanes of the same bin, then the
+    // counts of lower warps, then the earlier chunks (bin_next)
+    for (int base = 0; base < p.num_seqs; base += 1024) {
+        const int s = base + tid;
+        int bin = -1, nsplit = 0;
+        if (s < p.num_seqs) {
+            nsplit = p.seq_info[s].y;
+            if (nsplit > 0) {
+                const int nb = (p.context_lens[s] + kBlock - 1) / kBlock;
+                const int r = nb - (nsplit - 1) * P;
+                if (r < P) bin = bin_of(r);
+            }
+        }
+        const unsigned peers = __match_any_sync(kFull, bin);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (bin >= 0 && rank == 0) warp_bin[warp][bin] = __popc(peers);
+        __syncthreads();
+        if (tid < kOrderBins) {
+            int at = bin_next[tid];
+            for (int w = 0; w < 32; ++w) {
+                const int c = warp_bin[w][tid];
+                warp_bin[w][tid] = at;
+                at += c;
+            }
+            bin_next[tid] = at;
+        }
+        __syncthreads();
+        if (bin >= 0) {
+            const int at = warp_bin[warp][bin] + rank;
+            if (!dbg_fail(at < p.max_pairs, p.debug, 13, at)) p.items[at] = make_int2(s, nsplit - 1);
+        }
+        __syncthreads();
+        for (int i = tid; i < 32 * kOrderBins; i += 1024) (&warp_bin[0][0])[i] = 0;
+        __syncthreads();
+    }
+    if (tid == 0) p.header[0] = carry.x;
 }
 
 // ----------------------------------------------------------------- main kernel

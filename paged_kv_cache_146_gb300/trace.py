@@ -81,6 +81,31 @@ class TraceRunner:
         self.swapped_bytes = 0
         self.staging = torch.empty((self.maxb, 2, sched.num_kv_heads, bs, sched.head_dim),
                                    dtype=tdt, device=device)
+        # Pinned copies of the step's ledger output: the host hands them to the
+        # GPU without waiting, and rewrites them only after the previous step's
+        # copies have landed (self._copied).
+        self.h_tables = torch.full((S, self.maxb), -1, dtype=torch.int32, pin_memory=True)
+        self.h_ctx = torch.zeros(S, dtype=torch.int32, pin_memory=True)
+        self.h_slots = torch.zeros(S, dtype=torch.int64, pin_memory=True)
+        self.d_slots = torch.zeros(S, dtype=torch.int64, device=device)
+        self._copied = None
+
+    def _stage_slots(self, slots: np.ndarray):
+        """Device copy of this step's slot mapping, through pinned memory."""
+        torch, n = self.torch, len(slots)
+        if n > self.h_slots.numel():
+            cap = max(n, 2 * self.h_slots.numel())
+            self.h_slots = torch.zeros(cap, dtype=torch.int64, pin_memory=True)
+            self.d_slots = torch.zeros(cap, dtype=torch.int64, device=self.device)
+        self.h_slots.numpy()[:n] = slots
+        d = self.d_slots[:n]
+        d.copy_(self.h_slots[:n], non_blocking=True)
+        return d
+
+    def _wait_copied(self):
+        if self._copied is not None:
+            self._copied.synchronize()
+            self._copied = None
 
     def _draw(self, *shape):
         t = self.torch
@@ -181,11 +206,15 @@ class TraceRunner:
         k_new = self._draw(n_tok, sc.num_kv_heads, sc.head_dim)
         v_new = self._draw(n_tok, sc.num_kv_heads, sc.head_dim)
         q = self._draw(self.S, sc.num_q_heads, sc.head_dim)
+        self._wait_copied()
         if n_tok:
-            d_slots = torch.from_numpy(slots).to(self.device, non_blocking=False)
-            cache_write(self.pool, k_new, v_new, d_slots, self.status)
-        self.d_tables.copy_(torch.from_numpy(self.tables))
-        self.d_ctx.copy_(torch.from_numpy(ctx))
+            cache_write(self.pool, k_new, v_new, self._stage_slots(slots), self.status)
+        self.h_tables.numpy()[:] = self.tables
+        self.h_ctx.numpy()[:] = ctx
+        self.d_tables.copy_(self.h_tables, non_blocking=True)
+        self.d_ctx.copy_(self.h_ctx, non_blocking=True)
+        self._copied = torch.cuda.Event()
+        self._copied.record()
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev0.record()

@@ -299,3 +299,50 @@ def test_zero_and_negative_scale(scale):
         out = c.run_gpu(blocks_per_split=split)
         assert status_check(c.status) == (0, 0)
         assert_close(out, exp, f"decode scale {scale} split {split}")
+
+
+@pytest.mark.parametrize("seqs,max_len", [(200, 5000), (2500, 400)])
+@pytest.mark.parametrize("split", [3, None, 300])
+def test_work_list_order(split, seqs, max_len):
+    """The prep kernel's work list (read back from the workspace: pair count at
+    byte 0, per-sequence (first pair, partitions) at byte 256, the items after
+    them at the next 256-byte boundary) holds every (sequence, partition) once:
+    the full partitions first in sequence order, then the partial last
+    partitions from the largest to the smallest."""
+    from paged_kv_cache_146_gb300 import default_split, paged_decode_attention
+    w = workloads.small_random(91, seqs, max_len, 32, 8, 128, "bf16")
+    c = _case(w)
+    lens = c.context_lens.copy()
+    lens[::17] = 0                                   # idle rows
+    d_lens = torch.from_numpy(lens).cuda()
+    ws = c.workspace(split)
+    paged_decode_attention(c.pool, c.dev["q"], c.d_tables, d_lens, w.scale, ws, c.status,
+                           blocks_per_split=split)
+    assert status_check(c.status) == (0, 0)
+    P = split or default_split()
+    S = w.num_seqs
+    raw = ws.cpu().numpy()
+    nb = -(-lens.astype(np.int64) // 16)
+    nsplit = -(-nb // P)
+    T = int(nsplit.sum())
+    assert int(raw[:4].view(np.int32)[0]) == T
+    info = raw[256:256 + 8 * S].view(np.int32).reshape(S, 2)
+    assert info[:, 1].tolist() == nsplit.tolist()
+    assert info[:, 0].tolist() == (np.cumsum(nsplit) - nsplit).tolist()
+    at = 256 + -(-(8 * S) // 256) * 256
+    items = raw[at:at + 8 * T].view(np.int32).reshape(T, 2)
+    pairs = sorted((s, k) for s in range(S) for k in range(int(nsplit[s])))
+    assert sorted(map(tuple, items.tolist())) == pairs
+    size = np.minimum(P, nb[items[:, 0]] - items[:, 1].astype(np.int64) * P)
+    full = [(s, k) for s, k in pairs if min(P, nb[s] - k * P) == P]
+    F = len(full)
+    assert list(map(tuple, items[:F].tolist())) == full
+    assert (size[:F] == P).all() and (size[F:] < P).all()
+    bins = (P - 1 - size[F:]) * 64 // P
+    assert (np.diff(bins) >= 0).all()
+    # sequence order inside a bin (the list is the same on every launch)
+    rest = items[F:]
+    for b in np.unique(bins):
+        seqs = rest[bins == b, 0]
+        assert (np.diff(seqs) > 0).all()
+    assert_close(c.run_gpu(blocks_per_split=split), c.oracle_out(), f"split={split}")
