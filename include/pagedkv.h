@@ -307,7 +307,11 @@ size_t paged_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * where K_s[j] lives in block block_tables[s][j / bs] at row j % bs (R1).
  * Work is split along the context into partitions whose (o, max, sum) pieces are
  * merged with the log-sum-exp rule; accumulation is fp32; out is rounded to the
- * pool dtype.  Requirements: pool block_size 16; head_dim 64 or 128;
+ * pool dtype.  The partition size is chosen on the device from the context
+ * lengths: 32, 64 or 128 blocks, the largest that still leaves every resident
+ * CTA about five work items (paged_decode_default_split() is the smallest
+ * candidate, the one the workspace is sized for).  Requirements: pool
+ * block_size 16; head_dim 64 or 128;
  * num_q_heads a multiple of num_kv_heads with G <= 16; q/out/pools 16-byte
  * aligned; workspace of at least paged_decode_workspace_bytes(...) bytes,
  * 256-byte aligned, contents need not be initialised.  d_status: see the bits.
@@ -324,8 +328,8 @@ int paged_decode_attention(const pkv_pool *pool, void *out, const void *q,
 
 /* Same operation with an explicit partition size: each (sequence, kv head) is
  * cut into partitions of blocks_per_split blocks (>= 1) that run as separate
- * work items and are merged by log-sum-exp.  paged_decode_attention uses a
- * default size; results agree within rounding for any size. */
+ * work items and are merged by log-sum-exp.  paged_decode_attention chooses
+ * the size itself; results agree within rounding for any size. */
 size_t paged_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
                                           int32_t num_kv_heads, int32_t head_dim,
                                           int32_t max_blocks_per_seq,
@@ -367,7 +371,8 @@ int paged_prefill_attention(const pkv_pool *pool, void *out, const void *q, cons
                             int32_t num_q_heads, float scale, void *workspace,
                             size_t workspace_bytes, int32_t *d_status, void *stream);
 
-/* Default partition size (blocks) paged_decode_attention uses. */
+/* Smallest partition size (blocks) paged_decode_attention considers, the one
+ * its workspace is laid out for; the 8-bit decode uses exactly this size. */
 int32_t paged_decode_default_split(void);
 
 /* Paged decode attention that allocates nothing and takes no workspace.

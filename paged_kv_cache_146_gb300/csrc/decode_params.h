@@ -16,9 +16,11 @@ struct Params {
     const int32_t *block_tables;
     const int32_t *context_lens;
     int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
-    int32_t blocks_per_split, num_blocks;
+    int32_t blocks_per_split;   // fixed size, or the smallest candidate (automatic)
+    int32_t num_blocks;
+    int32_t auto_split_pairs;   // > 0: the prep kernel picks the size (header[2])
     float scale_log2;           // softmax scale * log2(e): scores live in the exp2 domain
-    int32_t *header;            // [0] = number of (sequence, partition) pairs
+    int32_t *header;            // [0] pairs, [1] debug word, [2] blocks per partition
     int2 *seq_info;             // [S]: first pair index, number of partitions
     int2 *items;                // [S * ceil(maxb / P)]: (sequence, partition)
     float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned

@@ -102,6 +102,14 @@ struct ItemMeta {
 // split between warps, and with it the last bits of the result.
 constexpr int kOrderBins = 64;
 
+// Automatic partition size: the candidates are P0, 2 P0 and 4 P0 blocks (P0 =
+// the size the workspace was laid out for, so every candidate fits it).  Larger
+// partitions mean fewer pieces to merge and less per-item work; the size stops
+// growing once it would leave fewer than kAutoItemsPerCta items per resident
+// CTA, below which the grid runs out of parallel work.
+constexpr int kAutoSizes = 3;
+constexpr int kAutoItemsPerCta = 5;
+
 // Inclusive scan of two counters over the 1024 threads of the prep CTA.
 __device__ __forceinline__ int2 prep_scan2(int2 x, int2 (&warp_tot)[32], int lane, int warp)
 {
@@ -132,16 +140,51 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     __shared__ int2 carry;               // (pairs, full partitions) of earlier chunks
     __shared__ int bin_next[kOrderBins];
     __shared__ int warp_bin[32][kOrderBins];   // pass 2: per-warp counts, then offsets
+    __shared__ long long auto_tot[32][kAutoSizes];
+    __shared__ int chosen_split;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int P = p.blocks_per_split;
     griddep_launch_dependents();   // the main kernel may set up its CTAs meanwhile
     if (tid == 0) carry = make_int2(0, 0);
     for (int i = tid; i < kOrderBins; i += 1024) bin_next[i] = 0;
     for (int i = tid; i < 32 * kOrderBins; i += 1024) (&warp_bin[0][0])[i] = 0;
+    const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
+    // pass 0 (automatic partition size): pairs at P0, 2 P0, 4 P0 blocks per
+    // partition; the largest size that still gives auto_split_pairs pairs wins
+    if (p.auto_split_pairs > 0) {
+        long long n[kAutoSizes] = {};
+        for (int s = tid; s < p.num_seqs; s += 1024) {
+            const int L = p.context_lens[s];
+            if (L <= 0 || (int64_t)L > max_tokens) continue;
+            const int nb = (L + kBlock - 1) / kBlock;
+#pragma unroll
+            for (int k = 0; k < kAutoSizes; ++k) {
+                const int Pk = p.blocks_per_split << k;
+                n[k] += (nb + Pk - 1) / Pk;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kAutoSizes; ++k) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) n[k] += __shfl_xor_sync(kFull, n[k], o);
+            if (lane == 0) auto_tot[warp][k] = n[k];
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int pick = 0;
+            for (int k = 1; k < kAutoSizes; ++k) {
+                long long t = 0;
+                for (int w = 0; w < 32; ++w) t += auto_tot[w][k];
+                if (t >= p.auto_split_pairs) pick = k;
+            }
+            chosen_split = p.blocks_per_split << pick;
+        }
+    } else if (tid == 0) {
+        chosen_split = p.blocks_per_split;
+    }
     __syncthreads();
+    const int P = chosen_split;
     // bin of a partial last partition of r blocks, 0 < r < P: larger r, lower bin
     auto bin_of = [P](int r) { return (int)((int64_t)(P - 1 - r) * kOrderBins / P); };
-    const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
     // pass 1: partitions, pair offsets, full partitions, size histogram, zero rows
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int s = base + tid;
@@ -237,7 +280,10 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
         for (int i = tid; i < 32 * kOrderBins; i += 1024) (&warp_bin[0][0])[i] = 0;
         __syncthreads();
     }
-    if (tid == 0) p.header[0] = carry.x;
+    if (tid == 0) {
+        p.header[0] = carry.x;
+        p.header[2] = P;
+    }
 }
 
 // ----------------------------------------------------------------- main kernel
@@ -292,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     __syncthreads();
     griddep_wait();                // the work list comes from the prep kernel
 
-    const int Hkv = p.num_kv_heads, G = p.group, P = p.blocks_per_split;
+    const int Hkv = p.num_kv_heads, G = p.group, P = p.header[2];   // chosen by the prep kernel
     const int total_items = p.header[0] * Hkv;
     const int stride = gridDim.x;
 
@@ -853,8 +899,8 @@ static int persistent_ctas(const Variant &v, int *num_sms_out)
 static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
                   const void *v_pool, bool want_8bit, const int32_t *block_tables, int32_t maxb,
                   const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
-                  int32_t P, void *workspace, size_t workspace_bytes, int32_t *d_status,
-                  void *stream)
+                  int32_t P, bool auto_split, void *workspace, size_t workspace_bytes,
+                  int32_t *d_status, void *stream)
 {
     PoolGeometry g;
     if (!pool_geometry(pool, &g)) return PKV_ERR_INVALID_ARG;
@@ -920,6 +966,8 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     const int per_sm = persistent_ctas(v, &num_sms);
     if (per_sm < 1) return PKV_ERR_CUDA;
     int64_t grid = (int64_t)per_sm * num_sms;
+    prm.auto_split_pairs =
+        auto_split ? (int32_t)((kAutoItemsPerCta * grid + g.num_kv_heads - 1) / g.num_kv_heads) : 0;
     const int64_t upper = (w.max_pairs * g.num_kv_heads + v.items_per_cta - 1) / v.items_per_cta;
     if (grid > upper) grid = upper;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -990,7 +1038,8 @@ int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
 {
     return pkv::decode::launch(pool, out, q, k_pool, v_pool, false, block_tables,
                                max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
-                               blocks_per_split, workspace, workspace_bytes, d_status, stream);
+                               blocks_per_split, false, workspace, workspace_bytes, d_status,
+                               stream);
 }
 
 int paged_decode_attention(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
@@ -1001,8 +1050,8 @@ int paged_decode_attention(const pkv_pool *pool, void *out, const void *q, const
 {
     return pkv::decode::launch(pool, out, q, k_pool, v_pool, false, block_tables,
                                max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
-                               pkv::decode::kDefaultSplit, workspace, workspace_bytes, d_status,
-                               stream);
+                               pkv::decode::kDefaultSplit, true, workspace, workspace_bytes,
+                               d_status, stream);
 }
 
 int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q, const void *kv_q8,
@@ -1013,8 +1062,8 @@ int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q, co
 {
     return pkv::decode::launch(pool, out, q, kv_q8, nullptr, true, block_tables,
                                max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
-                               pkv::decode::kDefaultSplit, workspace, workspace_bytes, d_status,
-                               stream);
+                               pkv::decode::kDefaultSplit, false, workspace, workspace_bytes,
+                               d_status, stream);
 }
 
 }  // extern "C"
@@ -1084,5 +1133,6 @@ extern "C" int paged_decode_attention_noalloc(const pkv_pool *pool, void *out, c
     void *scratch = noalloc_scratch_address();
     if (!scratch) return PKV_ERR_CUDA;
     return launch(pool, out, q, k_pool, v_pool, false, block_tables, maxb, context_lens,
-                  num_seqs, num_q_heads, scale, P, scratch, kNoallocScratchBytes, d_status, stream);
+                  num_seqs, num_q_heads, scale, P, false, scratch, kNoallocScratchBytes, d_status,
+                  stream);
 }

@@ -23,16 +23,6 @@ from . import (KVPool, cache_write, cache_write_q8, decode_workspace_bytes,
                paged_decode_attention, paged_decode_attention_q8, status_check)
 
 
-# Partition size (blocks per split-K piece) for 16-bit pools when the caller
-# gives none: the library default (32 blocks) unless the batch's contexts are
-# long (mean >= 256 blocks), where 128-block pieces measured faster (GQA 32/8,
-# 256 sequences of LogNormal(4096) tokens: 6.19 -> 6.38 TB/s with L2 flushed;
-# fewer pieces to merge, still many items per SM).  Shorter mixes and MHA
-# batches measured best at the default.
-LONG_CONTEXT_BLOCKS = 256
-LONG_CONTEXT_SPLIT = 128
-
-
 class DecodeEngine:
     def __init__(self, pool: KVPool, num_seqs: int, num_q_heads: int, max_blocks_per_seq: int,
                  scale: float, device, blocks_per_split: int | None = None):
@@ -129,18 +119,9 @@ class DecodeEngine:
                                       blocks_per_split=self.split_for_step())
 
     def split_for_step(self):
-        """Blocks per partition of this step's attention call (None: the library
-        default).  The workspace, sized for the default, fits every larger one."""
-        if self.split is not None:
-            return self.split
-        if self.pool.is_q8:
-            return None
-        bs = self.pool.block_size
-        active = self.lens[self.lens > 0]
-        if len(active) and (active.astype(np.int64) + bs - 1).sum() // bs >= \
-                LONG_CONTEXT_BLOCKS * len(active):
-            return LONG_CONTEXT_SPLIT
-        return None
+        """Blocks per partition the caller fixed, or None: the library picks the
+        size on the device from the context lengths (16-bit pools)."""
+        return self.split
 
     def device_step(self, q, k_new, v_new):
         """a3 + a4/a5: cache write of this step's K/V, then paged attention."""

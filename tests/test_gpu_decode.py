@@ -301,14 +301,17 @@ def test_zero_and_negative_scale(scale):
         assert_close(out, exp, f"decode scale {scale} split {split}")
 
 
-@pytest.mark.parametrize("seqs,max_len", [(200, 5000), (2500, 400)])
+@pytest.mark.parametrize("seqs,max_len,auto_split", [(4, 5000, 32), (200, 5000, 128),
+                                                      (2500, 400, 128)])
 @pytest.mark.parametrize("split", [3, None, 300])
-def test_work_list_order(split, seqs, max_len):
+def test_work_list_order(split, seqs, max_len, auto_split):
     """The prep kernel's work list (read back from the workspace: pair count at
-    byte 0, per-sequence (first pair, partitions) at byte 256, the items after
-    them at the next 256-byte boundary) holds every (sequence, partition) once:
-    the full partitions first in sequence order, then the partial last
-    partitions from the largest to the smallest."""
+    byte 0, the partition size at byte 8, per-sequence (first pair, partitions)
+    at byte 256, the items after them at the next 256-byte boundary) holds every
+    (sequence, partition) once: the full partitions first in sequence order,
+    then the partial last partitions from the largest to the smallest.  Without
+    an explicit size the library picks 32, 64 or 128 blocks: 4 sequences give
+    too few items for more than 32; the larger batches give enough at 128."""
     from paged_kv_cache_146_gb300 import default_split, paged_decode_attention
     w = workloads.small_random(91, seqs, max_len, 32, 8, 128, "bf16")
     c = _case(w)
@@ -319,9 +322,11 @@ def test_work_list_order(split, seqs, max_len):
     paged_decode_attention(c.pool, c.dev["q"], c.d_tables, d_lens, w.scale, ws, c.status,
                            blocks_per_split=split)
     assert status_check(c.status) == (0, 0)
-    P = split or default_split()
     S = w.num_seqs
     raw = ws.cpu().numpy()
+    P = int(raw[8:12].view(np.int32)[0])
+    assert P == (split or auto_split)
+    assert default_split() == 32
     nb = -(-lens.astype(np.int64) // 16)
     nsplit = -(-nb // P)
     T = int(nsplit.sum())
