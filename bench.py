@@ -281,7 +281,8 @@ def our_arm(args, world, rank, local):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     e2e_steps = args.e2e_steps
-    n_steps = args.warmup + args.steps + e2e_steps
+    e2e_warmup = 3 if e2e_steps > 0 else 0
+    n_steps = args.warmup + args.steps + e2e_warmup + e2e_steps
     q8 = args.workload == "gqa_long_q8"
     if args.workload in ("gqa_long", "gqa_long_q8"):
         w = rank_workload(args.seed, rank, args.num_seqs, n_steps + 16)
@@ -377,31 +378,35 @@ def our_arm(args, world, rank, local):
     # ---- end to end through the public API with host buffers
     e2e = None
     if e2e_steps > 0:
-        hq_h = [qs[i % len(qs)].cpu().pin_memory() for i in range(e2e_steps)]
-        hk_h = [ks[i % len(ks)].cpu().pin_memory() for i in range(e2e_steps)]
-        hv_h = [vs[i % len(vs)].cpu().pin_memory() for i in range(e2e_steps)]
-        out_h = torch.empty_like(eng.out, device="cpu").pin_memory()
-        dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(ks[0]), torch.empty_like(vs[0])
+        n_e = e2e_warmup + e2e_steps
+        hq_h = [qs[i % len(qs)].cpu().pin_memory() for i in range(n_e)]
+        hk_h = [ks[i % len(ks)].cpu().pin_memory() for i in range(n_e)]
+        hv_h = [vs[i % len(vs)].cpu().pin_memory() for i in range(n_e)]
+        out_h = [torch.empty_like(eng.out, device="cpu").pin_memory() for _ in range(n_e)]
+        for i in range(e2e_warmup):      # untimed: copy streams and buffers come up here
+            eng.decode_step_host(hq_h[i], hk_h[i], hv_h[i], out_h[i])
+        eng.join_copies()
+        hq_h, hk_h, hv_h, out_h = (x[e2e_warmup:] for x in (hq_h, hk_h, hv_h, out_h))
         e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_bytes = 0
         barrier(world)
         torch.cuda.synchronize()
         e_start.record(stream)
+        eng.copies_after(e_start)
         for i in range(e2e_steps):
-            dq.copy_(hq_h[i], non_blocking=True)
-            dk.copy_(hk_h[i], non_blocking=True)
-            dv.copy_(hv_h[i], non_blocking=True)
-            eng.decode_step(dq, dk, dv)
-            out_h.copy_(eng.out, non_blocking=True)
+            # inputs from pinned host memory, output back to it: transfers overlap
+            # the neighbouring steps' kernels and stay inside the timed region
+            eng.decode_step_host(hq_h[i], hk_h[i], hv_h[i], out_h[i])
             e_bytes += eng.step_bytes()
+        eng.join_copies()
         e_stop.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         e_ms = max_over_ranks(e_start.elapsed_time(e_stop), world)
-        h2d = (dq.numel() + dk.numel() + dv.numel()) * 2 + eng.h_tables.numel() * 4 + \
-            eng.h_lens.numel() * 4 + eng.h_slots.numel() * 8
+        h2d = (hq_h[0].numel() + hk_h[0].numel() + hv_h[0].numel()) * 2 + \
+            eng.h_tables.numel() * 4 + eng.h_lens.numel() * 4 + eng.h_slots.numel() * 8
         e2e = {"value": round(e_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h.numel() * 2),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h[0].numel() * 2),
                "ms_per_step": round(e_ms / e2e_steps, 4)}
         rc, word = eng.check()
         if rc != 0:

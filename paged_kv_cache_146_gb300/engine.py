@@ -11,9 +11,13 @@ The pool may be 16-bit (fp16/bf16 K and V) or an 8-bit cache ("kv-cache-by-model
 section 1: one-byte codes, one fp16 scale per 32 values); the engine picks the
 matching cache-write and attention calls.
 
-The host side of step k+1 overlaps the kernels of step k: before it touches the
-pinned table again it waits only for step k's host-to-device copy, which runs
-as soon as step k-1's kernels are done.
+Hand-off to the GPU: the device copies of the ledger arrays (table, lengths,
+slots) come in two sets.  Step t's arrays are copied on a copy stream into the
+set step t-1 is not reading, while step t-1's kernels run; the compute stream
+waits for that copy and carries kernels only.  The host side of step t+1
+overlaps the kernels of step t: before it rewrites the pinned arrays it waits
+only for step t's copy, which starts once step t-2's kernels are done.
+``decode_step_host`` moves the step's q/k/v in and its output out the same way.
 """
 from __future__ import annotations
 
@@ -41,10 +45,21 @@ class DecodeEngine:
         self.h_slots = torch.zeros(num_seqs, dtype=torch.int64, **pin)
         self.tables = self.h_tables.numpy()      # ledger writes here directly
         self.lens = self.h_lens.numpy()
-        self.d_tables = torch.full((num_seqs, max_blocks_per_seq), -1, dtype=torch.int32,
-                                   device=device)
-        self.d_lens = torch.zeros(num_seqs, dtype=torch.int32, device=device)
-        self.d_slots = torch.zeros(num_seqs, dtype=torch.int64, device=device)
+        # two device sets of the ledger arrays (see the module docstring)
+        self._sets = [{"tables": torch.full((num_seqs, max_blocks_per_seq), -1,
+                                            dtype=torch.int32, device=device),
+                       "lens": torch.zeros(num_seqs, dtype=torch.int32, device=device),
+                       "slots": torch.zeros(num_seqs, dtype=torch.int64, device=device)}
+                      for _ in range(2)]
+        self._set = 0
+        self._h2d = torch.cuda.Stream(device=device)
+        self._d2h = torch.cuda.Stream(device=device)
+        # loaded[b]: set b's copy has landed; used[b]: recorded after the last
+        # kernel that reads set b was enqueued.  Events never recorded count as
+        # complete, so the first waits pass at once.
+        self._loaded = [torch.cuda.Event() for _ in range(2)]
+        self._used = [torch.cuda.Event() for _ in range(2)]
+        self._io = None                              # q/k/v/out sets of decode_step_host
         nbytes = decode_workspace_bytes(num_seqs, num_q_heads, pool.num_kv_heads, pool.head_dim,
                                         max_blocks_per_seq, blocks_per_split)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -53,6 +68,19 @@ class DecodeEngine:
         self.out = torch.empty((num_seqs, num_q_heads, pool.head_dim), dtype=tdt, device=device)
         self._ones = np.ones(num_seqs, dtype=np.int32)
         self._copied = None                          # event: last H2D of the pinned ledger
+
+    # the device ledger arrays of the current step
+    @property
+    def d_tables(self):
+        return self._sets[self._set]["tables"]
+
+    @property
+    def d_lens(self):
+        return self._sets[self._set]["lens"]
+
+    @property
+    def d_slots(self):
+        return self._sets[self._set]["slots"]
 
     # ------------------------------------------------------------------ prompt
     def prefill(self, k_rows, v_rows, num_new) -> np.ndarray:
@@ -75,6 +103,7 @@ class DecodeEngine:
         bs = self.pool.block_size
         if num_tokens % bs or self.lens[0] < num_tokens or (self.lens[1:] != 0).any():
             raise ValueError("prefix must be whole blocks of sequence 0; others empty")
+        self._wait_copy()
         ids = self.tables[0, :num_tokens // bs].copy()
         for _ in range(self.S - 1):
             self.pool.ref(ids)
@@ -88,18 +117,40 @@ class DecodeEngine:
             self._copied.synchronize()
             self._copied = None
 
-    def host_step(self) -> None:
-        """a1 + a2: on-demand blocks for one new token per sequence, block table,
-        context lengths and slot mapping, then their copy to the device."""
-        torch = self.torch
+    def _ledger_step(self) -> None:
+        """a1 + a2 on the host: on-demand blocks for one new token per sequence;
+        block table, context lengths and slot mapping in the pinned buffers."""
         self._wait_copy()
         self.h_slots.numpy()[:] = self.pool.append_slots(self.lens, self._ones, self.tables)
         self.lens += 1
-        self.d_tables.copy_(self.h_tables, non_blocking=True)
-        self.d_lens.copy_(self.h_lens, non_blocking=True)
-        self.d_slots.copy_(self.h_slots, non_blocking=True)
-        self._copied = torch.cuda.Event()
-        self._copied.record()
+
+    def _stage(self, extra=()) -> int:
+        """The ledger step, then the copy of its arrays (and of the ``extra``
+        (device, host) pairs) into the other device set on the copy stream; the
+        compute stream waits for it.  Returns the set now current."""
+        torch = self.torch
+        self._ledger_step()
+        b = self._set ^ 1
+        dst = self._sets[b]
+        self._h2d.wait_event(self._used[b])     # set b's last readers were enqueued
+        with torch.cuda.stream(self._h2d):
+            dst["tables"].copy_(self.h_tables, non_blocking=True)
+            dst["lens"].copy_(self.h_lens, non_blocking=True)
+            dst["slots"].copy_(self.h_slots, non_blocking=True)
+            for d, h in extra:
+                d.copy_(h, non_blocking=True)
+            self._loaded[b].record(self._h2d)
+        self._copied = self._loaded[b]
+        torch.cuda.current_stream().wait_event(self._loaded[b])
+        self._set = b
+        return b
+
+    def _mark_used(self) -> None:
+        self._used[self._set].record(self.torch.cuda.current_stream())
+
+    def host_step(self) -> None:
+        """a1 + a2: the ledger step and the hand-off of its arrays to the device."""
+        self._stage()
 
     def write(self, k_new, v_new, d_slots=None) -> None:
         """a3: cache write of K/V rows into their slots (this step's by default)."""
@@ -108,15 +159,22 @@ class DecodeEngine:
             cache_write_q8(self.pool, k_new, v_new, d_slots, self.status)
         else:
             cache_write(self.pool, k_new, v_new, d_slots, self.status)
+        self._mark_used()
 
     def attend(self, q):
         """a4/a5: paged attention of every sequence over its blocks."""
+        return self._attend_into(q, self.out)
+
+    def _attend_into(self, q, out):
         if self.pool.is_q8:
-            return paged_decode_attention_q8(self.pool, q, self.d_tables, self.d_lens, self.scale,
-                                             self.workspace, self.status, out=self.out)
-        return paged_decode_attention(self.pool, q, self.d_tables, self.d_lens, self.scale,
-                                      self.workspace, self.status, out=self.out,
-                                      blocks_per_split=self.split_for_step())
+            r = paged_decode_attention_q8(self.pool, q, self.d_tables, self.d_lens, self.scale,
+                                          self.workspace, self.status, out=out)
+        else:
+            r = paged_decode_attention(self.pool, q, self.d_tables, self.d_lens, self.scale,
+                                       self.workspace, self.status, out=out,
+                                       blocks_per_split=self.split_for_step())
+        self._mark_used()
+        return r
 
     def split_for_step(self):
         """Blocks per partition the caller fixed, or None: the library picks the
@@ -131,6 +189,62 @@ class DecodeEngine:
     def decode_step(self, q, k_new, v_new):
         self.host_step()
         return self.device_step(q, k_new, v_new)
+
+    # ------------------------------------------------------- host-buffer steps
+    def decode_step_host(self, q_h, k_h, v_h, out_h):
+        """One decode step from pinned host tensors (q [S][Hq][D], k/v
+        [S][Hkv][D]) into a pinned host ``out_h`` [S][Hq][D], asynchronously.
+
+        The step's inputs travel with its ledger arrays on the copy stream,
+        into the device set the previous step is not reading; its output goes
+        back on a second copy stream while the next step computes.  The call
+        returns once everything is enqueued: ``q_h``/``k_h``/``v_h`` must stay
+        unchanged, and ``out_h`` unread, until ``join_copies()`` (or a device
+        synchronisation) has passed."""
+        torch = self.torch
+        io = self._io_state()
+        if q_h.shape != io["q"][0].shape or k_h.shape != io["k"][0].shape or \
+                v_h.shape != io["v"][0].shape or out_h.shape != io["out"][0].shape:
+            raise ValueError("host tensors must be q/out [S][Hq][D] and k/v [S][Hkv][D]")
+        nb = self._set ^ 1
+        b = self._stage([(io["q"][nb], q_h), (io["k"][nb], k_h), (io["v"][nb], v_h)])
+        cur = torch.cuda.current_stream()
+        cur.wait_event(io["sent"][b])           # out set b's previous contents have left
+        self.write(io["k"][b], io["v"][b])
+        self._attend_into(io["q"][b], io["out"][b])
+        self._d2h.wait_event(self._used[b])
+        with torch.cuda.stream(self._d2h):
+            out_h.copy_(io["out"][b], non_blocking=True)
+            io["sent"][b].record(self._d2h)
+        return out_h
+
+    def join_copies(self) -> None:
+        """Make the current stream wait for every transfer the engine enqueued
+        (after this, a synchronisation makes ``out_h`` readable)."""
+        cur = self.torch.cuda.current_stream()
+        for b in (0, 1):
+            cur.wait_event(self._loaded[b])
+            if self._io is not None:
+                cur.wait_event(self._io["sent"][b])
+
+    def copies_after(self, event) -> None:
+        """Later transfers start only after ``event`` (e.g. the start event of a
+        timed region recorded on the compute stream)."""
+        self._h2d.wait_event(event)
+        self._d2h.wait_event(event)
+
+    def _io_state(self) -> dict:
+        if self._io is None:
+            torch, dev, p = self.torch, self.device, self.pool
+            kshape = (self.S, p.num_kv_heads, p.head_dim)
+            self._io = {
+                "q": [torch.empty_like(self.out) for _ in range(2)],
+                "k": [torch.empty(kshape, dtype=self.out.dtype, device=dev) for _ in range(2)],
+                "v": [torch.empty(kshape, dtype=self.out.dtype, device=dev) for _ in range(2)],
+                "out": [torch.empty_like(self.out) for _ in range(2)],
+                "sent": [torch.cuda.Event() for _ in range(2)],
+            }
+        return self._io
 
     def release(self, seqs) -> None:
         """a6: finished sequences give back their blocks."""
