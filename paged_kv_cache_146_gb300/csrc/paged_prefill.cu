@@ -117,9 +117,12 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
 // position, so each K/V tile is loaded once for 256 rows.
 //   warp 8 (producer): TMA of the item's Q rows (one 4-D box per 64 columns)
 //     and of each KV tile's 4 K and 4 V blocks into a 2-stage ring.
-//   warp 9 lane 0 (MMA issuer): per group S = Q K^T into one of two tensor-memory
-//     buffers (M 128, N 64), then O += P V for the previous tile (M 128, N D,
-//     V as an MN-major operand), P as a high and a low bf16/fp16 part.
+//   warps 9 and 10, lane 0 (MMA issuers, one per query tile): S = Q K^T into
+//     one of two tensor-memory buffers (M 128, N 64), then O += P V for the
+//     previous tile (M 128, N D, V as an MN-major operand), P as a high and a
+//     low bf16/fp16 part.  A thread gets a new tcgen05.mma accepted only about
+//     110 cycles after its previous one (measured, whatever N <= 128), so one
+//     issuer for both tiles left the tensor pipe idle most of the time.
 //   warps 0-3 and 4-7 (softmax, one warpgroup per query tile, ping-pong on the
 //     tensor pipe): thread r of a group owns row r = tensor-memory lane r.  Running
 //     maximum with lazy rescaling: the reference maximum moves only when a
@@ -133,23 +136,92 @@ namespace tcp {
 constexpr int kRows = 128;             // M: query rows per query tile
 constexpr int kGroups = 2;             // query tiles per item, sharing every K/V tile
 constexpr int kKeys = 64;              // keys per KV tile
-constexpr int kThreads = (4 * kGroups + 2) * 32;   // softmax warps 0-7, producer 8, MMA 9
+// softmax warps 0-7, producer 8, MMA issuers 9 (query tile 0) and 10 (query tile 1)
+constexpr int kThreads = (5 * kGroups + 1) * 32;
 constexpr int kProducer = 4 * kGroups, kIssuer = 4 * kGroups + 1;
 constexpr float kLazy = 8.f;           // rescale threshold (log2 units)
+
+// ---- softmax arithmetic helpers: three-input max/min, packed fp32 pairs
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack2f(float a, float b)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ float2 unpack2f(uint64_t v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2f(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2f(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2f(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Weights (p0, p1) (pp = the same pair packed) as a high and a low 16-bit part
+// each, the even index in the low half of each word.  bf16: the high part is
+// the weight truncated to bf16 (its upper 16 bits, exact), the low part the
+// remainder rounded to bf16, so high + low carries the weight to ~2^-16.
+// fp16: high = the rounded weight, low = the rounded remainder.
+template <bool BF16>
+__device__ __forceinline__ void split_hi_lo(float p0, float p1, uint64_t pp, uint32_t &hi,
+                                            uint32_t &lo)
+{
+    using E = Elem<BF16>;
+    if constexpr (BF16) {
+        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+        hi = __byte_perm(b0, b1, 0x7632);
+        const float2 d = unpack2f(sub2f(pp, pack2f(__uint_as_float(b0 & 0xffff0000u),
+                                                   __uint_as_float(b1 & 0xffff0000u))));
+        lo = E::pack(d.x, d.y);
+    } else {
+        hi = E::pack(p0, p1);
+        const float2 h = E::unpack(hi);
+        const float2 d = unpack2f(sub2f(pp, pack2f(h.x, h.y)));
+        lo = E::pack(d.x, d.y);
+    }
+}
 
 template <int D>
 struct Layout {
     static constexpr int kRegions = D / 64;
-    static constexpr int kStages = D == 128 ? 3 : 4;           // K/V tiles in flight
+    static constexpr int kStages = D == 128 ? 5 : 8;           // K/V tiles in flight
     static constexpr int kQBytes = kRegions * kRows * 128;     // one query tile: [region][row][128 B]
     static constexpr int kKVBytes = kRegions * kKeys * 128;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kKVBytes;           // K tile, then V tile
-    static constexpr int kPBytes = kRows * 128;                // [row][64 keys]
     static constexpr int kStage0 = kGroups * kQBytes;
-    static constexpr int kP = kStage0 + kStages * kStageBytes; // per group: P high, then P low
-    static constexpr int kMisc = kP + kGroups * 2 * kPBytes;   // barriers and flags
-    static constexpr int kTotal = 1024 + kMisc + 256;
-    // S of group g, buffer b at 64 (2g + b); O of group g at 256 + 128 g
+    static constexpr int kMisc = kStage0 + kStages * kStageBytes;   // barriers and flags
+    static constexpr int kTotal = 1024 + kMisc + 512;
+    // S of group g, buffer b at 64 (2g + b), overwritten by that tile's P (high
+    // part in its first 32 columns, low part in the next 32); O of group g at
+    // 256 + 128 g
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -191,32 +263,31 @@ __global__ void __launch_bounds__(kThreads)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *q_s = base;
     uint8_t *stage_s = base + LY::kStage0;
-    uint8_t *p_s = base + LY::kP;
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + LY::kMisc);
     uint64_t *q_full = bars + 0, *q_empty = bars + 1;
     uint64_t *kv_full = bars + 2, *kv_empty = kv_full + LY::kStages;   // [LY::kStages] each
     uint64_t *s_full = kv_empty + LY::kStages;                 // [group][buffer]
     uint64_t *p_full = s_full + 2 * kGroups;                   // [group]
     uint64_t *o_full = p_full + kGroups;                       // [group]
-    uint64_t *done = o_full + kGroups;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *done = o_full + kGroups;                         // [group]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(done + kGroups);
     int *stage_bad = reinterpret_cast<int *>(tslot + 1);            // [LY::kStages]
     volatile int *abort_flag = stage_bad + LY::kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(q_full), 1);
-        mbar_init(smem_addr(q_empty), 1);
+        mbar_init(smem_addr(q_empty), kGroups);     // one commit per issuer
         for (int i = 0; i < LY::kStages; ++i) {
             mbar_init(smem_addr(&kv_full[i]), 1);
-            mbar_init(smem_addr(&kv_empty[i]), 1);
+            mbar_init(smem_addr(&kv_empty[i]), kGroups);
         }
         for (int i = 0; i < 2 * kGroups; ++i) mbar_init(smem_addr(&s_full[i]), 1);
         for (int i = 0; i < kGroups; ++i) {
             mbar_init(smem_addr(&p_full[i]), 4);
             mbar_init(smem_addr(&o_full[i]), 1);
         }
-        mbar_init(smem_addr(done), 1);
+        for (int i = 0; i < kGroups; ++i) mbar_init(smem_addr(&done[i]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -296,34 +367,36 @@ __global__ void __launch_bounds__(kThreads)
                 }
             }
         }
-    } else if (warp == kIssuer) {
+    } else if (warp == kIssuer || warp == kIssuer + 1) {
+        // one issuer per query tile: the tensor pipe takes a new tcgen05.mma from
+        // a thread only ~110 cycles after its previous one, so two threads keep it
+        // fed where one could not
         if (lane == 0) {
+            const int gr = warp - kIssuer;
             const uint32_t id_qk = tc::idesc_f16(BF16, kRows, kKeys, 0, 0);
             const uint32_t id_pv = tc::idesc_f16(BF16, kRows, D, 0, 1);
-            const uint32_t q_a = smem_addr(q_s), st_a = smem_addr(stage_s), p_a = smem_addr(p_s);
+            const uint32_t q_a = smem_addr(q_s) + gr * LY::kQBytes, st_a = smem_addr(stage_s);
+            const uint32_t o_t = tmem + 256 + 128 * gr;
             uint32_t tg = 0, it_cnt = 0;
             bool ok = true;
-            // P V of tile t for both groups, then the stage is free
+            // P V of tile t for this group, then its share of freeing the stage
             auto issue_pv = [&](uint32_t t, bool first) {
                 const uint32_t vs = st_a + (t % LY::kStages) * LY::kStageBytes + LY::kKVBytes;
-                for (int gr = 0; gr < kGroups && ok; ++gr) {
-                    if (!mbar_wait(smem_addr(&p_full[gr]), t & 1u, abort_flag, p.status)) {
-                        ok = false;
-                        return;
-                    }
-                    tc::fence_after_sync();
-                    const uint32_t pg = p_a + gr * 2 * LY::kPBytes;
-#pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < kKeys / 16; ++kk) {
-                            const uint64_t a = tc::desc_sw128(pg + part * LY::kPBytes + kk * 32, 16, 1024);
-                            const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
-                            tc::mma_f16(tmem + 256 + 128 * gr, a, b, id_pv,
-                                        !(first && part == 0 && kk == 0));
-                        }
-                    tc::mma_commit(smem_addr(&o_full[gr]));
+                if (!mbar_wait(smem_addr(&p_full[gr]), t & 1u, abort_flag, p.status)) {
+                    ok = false;
+                    return;
                 }
+                tc::fence_after_sync();
+                const uint32_t pt = tmem + 64 * (2 * gr + (t & 1u));   // P of tile t
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk) {
+                        const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
+                        tc::mma_f16_ts(o_t, pt + part * 32 + kk * 8, b, id_pv,
+                                       !(first && part == 0 && kk == 0));
+                    }
+                tc::mma_commit(smem_addr(&o_full[gr]));
                 tc::mma_commit(smem_addr(&kv_empty[t % LY::kStages]));
             };
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it_cnt) {
@@ -338,26 +411,23 @@ __global__ void __launch_bounds__(kThreads)
                     }
                     tc::fence_after_sync();
                     const uint32_t ks = st_a + st * LY::kStageBytes;
-                    for (int gr = 0; gr < kGroups; ++gr) {
-                        const uint32_t qg = q_a + gr * LY::kQBytes;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
-                            const uint64_t a = tc::desc_sw128(qg + (kk >> 2) * kRows * 128 + off, 16, 1024);
-                            const uint64_t b = tc::desc_sw128(ks + (kk >> 2) * kKeys * 128 + off, 16, 1024);
-                            tc::mma_f16(tmem + 64 * (2 * gr + sb), a, b, id_qk, kk > 0);
-                        }
-                        tc::mma_commit(smem_addr(&s_full[2 * gr + sb]));
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
+                        const uint64_t a = tc::desc_sw128(q_a + (kk >> 2) * kRows * 128 + off, 16, 1024);
+                        const uint64_t b = tc::desc_sw128(ks + (kk >> 2) * kKeys * 128 + off, 16, 1024);
+                        tc::mma_f16(tmem + 64 * (2 * gr + sb), a, b, id_qk, kk > 0);
                     }
+                    tc::mma_commit(smem_addr(&s_full[2 * gr + sb]));
                     if (t == it.ntiles - 1) tc::mma_commit(smem_addr(q_empty));
                     if (t >= 1) issue_pv(tg - 1, t == 1);
                 }
                 if (ok) issue_pv(tg - 1, it.ntiles == 1);
             }
-            // every MMA issued has completed before the columns are freed
-            tc::mma_commit(smem_addr(done));
+            // every MMA this thread issued has completed before the columns are freed
+            tc::mma_commit(smem_addr(&done[gr]));
             const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait(smem_addr(done), 0)) {
+            while (!mbar_try_wait(smem_addr(&done[gr]), 0)) {
                 if (globaltimer() - t0 > kTimeoutNs) {
                     atomicOr(p.status, PKV_DEV_TIMEOUT);
                     break;
@@ -370,7 +440,6 @@ __global__ void __launch_bounds__(kThreads)
         const int r = threadIdx.x - kRows * gr;     // row = tensor-memory lane
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const uint32_t s_col = 64 * 2 * gr, o_col = 256 + 128 * gr;
-        uint8_t *p_g = p_s + gr * 2 * LY::kPBytes;
         uint32_t tg = 0, it_cnt = 0;
         bool alive = true;
         for (int i = blockIdx.x; i < total && alive; i += gridDim.x, ++it_cnt) {
@@ -392,15 +461,15 @@ __global__ void __launch_bounds__(kThreads)
                 bad |= stage_bad[st];
                 float x[kKeys];
                 {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lane_base + s_col + 64 * sb, v);
+                    uint32_t v[2][32];
+                    tc::tmem_ld32(lane_base + s_col + 64 * sb, v[0]);
+                    tc::tmem_ld32(lane_base + s_col + 64 * sb + 32, v[1]);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]);
-                    tc::tmem_ld32(lane_base + s_col + 64 * sb + 32, v);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]);
+                    for (int c = 0; c < 32; ++c) {
+                        x[c] = __uint_as_float(v[0][c]);
+                        x[32 + c] = __uint_as_float(v[1][c]);
+                    }
                 }
                 // raw scores; the scale enters inside the exponent (one FFMA each).
                 // Hidden keys are kept out of the maximum here and get weight 0 below.
@@ -412,13 +481,15 @@ __global__ void __launch_bounds__(kThreads)
                     for (int c = 0; c < kKeys; ++c)
                         if (k0 + c > pos) x[c] = hide;
                 }
-                float mx = -INFINITY;
+                float mx;
+                if (p.scale_log2 >= 0.f) {
+                    mx = fmaxf(x[0], x[1]);
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) mx = fmaxf(mx, x[c]);
-                if (p.scale_log2 < 0.f) {          // the largest scaled score is the smallest raw one
-                    mx = INFINITY;
+                    for (int c = 2; c < kKeys; c += 2) mx = max3f(mx, x[c], x[c + 1]);
+                } else {                           // the largest scaled score is the smallest raw one
+                    mx = fminf(x[0], x[1]);
 #pragma unroll
-                    for (int c = 0; c < kKeys; ++c) mx = fminf(mx, x[c]);
+                    for (int c = 2; c < kKeys; c += 2) mx = min3f(mx, x[c], x[c + 1]);
                 }
                 mx *= p.scale_log2;
                 float f = 1.f;
@@ -430,31 +501,33 @@ __global__ void __launch_bounds__(kThreads)
                     }
                     m_ref = mx;
                 }
-                float lsum = 0.f;
+                // weights in pairs: packed fp32 arithmetic (f32x2), then a high and a
+                // low 16-bit part per weight
                 uint32_t hi[kKeys / 2], lo[kKeys / 2];
-                const float nm = -m_ref;
+                const uint64_t sc2 = pack2f(p.scale_log2, p.scale_log2), nm2 = pack2f(-m_ref, -m_ref);
+                uint64_t lsum2 = pack2f(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < kKeys; c += 2) {
-                    float p0 = fast_exp2(fmaf(x[c], p.scale_log2, nm));
-                    float p1 = fast_exp2(fmaf(x[c + 1], p.scale_log2, nm));
+                    const float2 e = unpack2f(fma2f(pack2f(x[c], x[c + 1]), sc2, nm2));
+                    float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
                     if (cross) {
                         if (k0 + c > pos) p0 = 0.f;
                         if (k0 + c + 1 > pos) p1 = 0.f;
                     }
-                    lsum += p0 + p1;
-                    hi[c / 2] = E::pack(p0, p1);
-                    const float2 hh = E::unpack(hi[c / 2]);
-                    lo[c / 2] = E::pack(p0 - hh.x, p1 - hh.y);
+                    const uint64_t pp = pack2f(p0, p1);
+                    lsum2 = add2f(lsum2, pp);
+                    split_hi_lo<BF16>(p0, p1, pp, hi[c / 2], lo[c / 2]);
                 }
-                l = l * f + lsum;
-                // P V of the previous tile must be done: it reads the P buffer and
-                // writes O
-                if (t >= 1) {
+                const float2 ls = unpack2f(lsum2);
+                l = l * f + (ls.x + ls.y);
+                // O is rescaled before P V of this tile, once P V of the previous
+                // tile has finished writing it; the wait for that P V consumes the
+                // o_full phase of the previous tile either here or after P is out
+                const bool any_resc = __any_sync(kFull, resc);
+                if (t >= 1 && any_resc) {
                     const bool okp = mbar_wait(smem_addr(&o_full[gr]), (tg - 1) & 1u, abort_flag, p.status);
                     if (!__all_sync(kFull, okp)) { alive = false; break; }
                     tc::fence_after_sync();
-                }
-                if (__any_sync(kFull, resc)) {
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t v[32];
@@ -464,21 +537,14 @@ __global__ void __launch_bounds__(kThreads)
                         for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
                         tc::tmem_st32(lane_base + o_col + c0, v);
                     }
-                    tc::tmem_wait_st();
                 }
-                // this row of P (high and low), 128-byte swizzle
-                uint8_t *ph = p_g + r * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int pos16 = (j ^ (r & 7)) << 4;
-                    *reinterpret_cast<uint4 *>(ph + pos16) =
-                        make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
-                    *reinterpret_cast<uint4 *>(ph + LY::kPBytes + pos16) =
-                        make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
-                }
+                // P of this tile over its own S columns (already read): high part
+                // in the first 32, low part in the next 32
+                tc::tmem_st32(lane_base + s_col + 64 * sb, hi);
+                tc::tmem_st32(lane_base + s_col + 64 * sb + 32, lo);
                 // zero the V rows of keys past the last visible one (last tile only)
                 const int nvis = it.nkeys - k0;
-                if (gr == 0 && nvis < kKeys) {           // one group does it for both
+                if (nvis < kKeys) {      // both groups write the same zeros, each before its P
                     uint8_t *vs = stage_s + st * LY::kStageBytes + LY::kKVBytes;
                     const int nrows = kKeys - nvis;
                     for (int e = r; e < nrows * LY::kRegions * 8; e += kRows) {
@@ -487,11 +553,16 @@ __global__ void __launch_bounds__(kThreads)
                         *reinterpret_cast<uint4 *>(vs + (rem >> 3) * kKeys * 128 + row * 128 +
                                                    (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&p_full[gr]));
+                if (t >= 1 && !any_resc) {
+                    const bool okp = mbar_wait(smem_addr(&o_full[gr]), (tg - 1) & 1u, abort_flag, p.status);
+                    if (!__all_sync(kFull, okp)) { alive = false; break; }
+                }
             }
             if (!alive) break;
             // ---- the item's result: O / l once the last P V is done

@@ -65,6 +65,19 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.  A is M rows in lanes
+// 0..M-1, two 16-bit values per 32-bit column (the even reduction index in the
+// low half), 8 columns per 16 reduction indices.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
 // The mbarrier receives one arrival when every MMA this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
