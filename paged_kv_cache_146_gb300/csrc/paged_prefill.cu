@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "pagedkv.h"
 #include "pkv_device.cuh"
@@ -506,18 +507,24 @@ __global__ void __launch_bounds__(kThreads)
                 uint32_t hi[kKeys / 2], lo[kKeys / 2];
                 const uint64_t sc2 = pack2f(p.scale_log2, p.scale_log2), nm2 = pack2f(-m_ref, -m_ref);
                 uint64_t lsum2 = pack2f(0.f, 0.f);
+                // two copies of the loop: only a tile that crosses the row's
+                // position pays for the per-key causal test
+                auto weights = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < kKeys; c += 2) {
-                    const float2 e = unpack2f(fma2f(pack2f(x[c], x[c + 1]), sc2, nm2));
-                    float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
-                    if (cross) {
-                        if (k0 + c > pos) p0 = 0.f;
-                        if (k0 + c + 1 > pos) p1 = 0.f;
+                    for (int c = 0; c < kKeys; c += 2) {
+                        const float2 e = unpack2f(fma2f(pack2f(x[c], x[c + 1]), sc2, nm2));
+                        float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+                        if constexpr (decltype(masked)::value) {
+                            if (k0 + c > pos) p0 = 0.f;
+                            if (k0 + c + 1 > pos) p1 = 0.f;
+                        }
+                        const uint64_t pp = pack2f(p0, p1);
+                        lsum2 = add2f(lsum2, pp);
+                        split_hi_lo<BF16>(p0, p1, pp, hi[c / 2], lo[c / 2]);
                     }
-                    const uint64_t pp = pack2f(p0, p1);
-                    lsum2 = add2f(lsum2, pp);
-                    split_hi_lo<BF16>(p0, p1, pp, hi[c / 2], lo[c / 2]);
-                }
+                };
+                if (cross) weights(std::true_type{});
+                else weights(std::false_type{});
                 const float2 ls = unpack2f(lsum2);
                 l = l * f + (ls.x + ls.y);
                 // O is rescaled before P V of this tile, once P V of the previous
