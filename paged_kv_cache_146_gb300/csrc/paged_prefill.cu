@@ -121,9 +121,10 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
 //   warps 9 and 10, lane 0 (MMA issuers, one per query tile): S = Q K^T into
 //     one of two tensor-memory buffers (M 128, N 64), then O += P V for the
 //     previous tile (M 128, N D, V as an MN-major operand), P as a high and a
-//     low bf16/fp16 part.  A thread gets a new tcgen05.mma accepted only about
-//     110 cycles after its previous one (measured, whatever N <= 128), so one
-//     issuer for both tiles left the tensor pipe idle most of the time.
+//     low bf16 part (bf16 pools) or one fp16 part (fp16 pools).  A thread gets
+//     a new tcgen05.mma accepted only about 110 cycles after its previous one
+//     (measured, whatever N <= 128), so one issuer for both tiles left the
+//     tensor pipe idle most of the time.
 //   warps 0-3 and 4-7 (softmax, one warpgroup per query tile, ping-pong on the
 //     tensor pipe): thread r of a group owns row r = tensor-memory lane r.  Running
 //     maximum with lazy rescaling: the reference maximum moves only when a
@@ -186,28 +187,22 @@ __device__ __forceinline__ uint64_t sub2f(uint64_t a, uint64_t b)
     return d;
 }
 
-// Weights (p0, p1) (pp = the same pair packed) as a high and a low 16-bit part
-// each, the even index in the low half of each word.  bf16: the high part is
-// the weight truncated to bf16 (its upper 16 bits, exact), the low part the
-// remainder rounded to bf16, so high + low carries the weight to ~2^-16.
-// fp16: high = the rounded weight, low = the rounded remainder.
+// bf16 weights (p0, p1) (pp = the same pair packed) as a high and a low part,
+// the even index in the low half of each word: the high part is the weight
+// truncated to bf16 (its upper 16 bits, exact), the low part the remainder
+// rounded to bf16, so high + low carries the weight to ~2^-16.  (fp16 pools
+// keep a single fp16 part: its relative error, <= 2^-11, is inside the
+// tolerance, where a single bf16 part's 2^-9 is not.)
 template <bool BF16>
 __device__ __forceinline__ void split_hi_lo(float p0, float p1, uint64_t pp, uint32_t &hi,
                                             uint32_t &lo)
 {
-    using E = Elem<BF16>;
-    if constexpr (BF16) {
-        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-        hi = __byte_perm(b0, b1, 0x7632);
-        const float2 d = unpack2f(sub2f(pp, pack2f(__uint_as_float(b0 & 0xffff0000u),
-                                                   __uint_as_float(b1 & 0xffff0000u))));
-        lo = E::pack(d.x, d.y);
-    } else {
-        hi = E::pack(p0, p1);
-        const float2 h = E::unpack(hi);
-        const float2 d = unpack2f(sub2f(pp, pack2f(h.x, h.y)));
-        lo = E::pack(d.x, d.y);
-    }
+    static_assert(BF16, "fp16 weights take one part");
+    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+    hi = __byte_perm(b0, b1, 0x7632);
+    const float2 d = unpack2f(sub2f(pp, pack2f(__uint_as_float(b0 & 0xffff0000u),
+                                               __uint_as_float(b1 & 0xffff0000u))));
+    lo = Elem<true>::pack(d.x, d.y);
 }
 
 template <int D>
@@ -268,9 +263,14 @@ __global__ void __launch_bounds__(kThreads)
     uint64_t *q_full = bars + 0, *q_empty = bars + 1;
     uint64_t *kv_full = bars + 2, *kv_empty = kv_full + LY::kStages;   // [LY::kStages] each
     uint64_t *s_full = kv_empty + LY::kStages;                 // [group][buffer]
-    uint64_t *p_full = s_full + 2 * kGroups;                   // [group]
-    uint64_t *o_full = p_full + kGroups;                       // [group]
-    uint64_t *done = o_full + kGroups;                         // [group]
+    // P of a group out / P V of a group done, for even and odd tiles: a parity
+    // wait is exact only while its barrier runs at most one phase ahead of the
+    // waiter, and alternating barriers keep them so (P of tile t + 2 needs
+    // S(t + 2), issued after P V of tile t; P V of tile t + 1 needs P(t + 1),
+    // published after the wait for P V of tile t - 1)
+    uint64_t *p_full = s_full + 2 * kGroups;                   // [group][tile & 1]
+    uint64_t *o_full = p_full + 2 * kGroups;                   // [group][tile & 1]
+    uint64_t *done = o_full + 2 * kGroups;                     // [group]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(done + kGroups);
     int *stage_bad = reinterpret_cast<int *>(tslot + 1);            // [LY::kStages]
     volatile int *abort_flag = stage_bad + LY::kStages;
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads)
             mbar_init(smem_addr(&kv_empty[i]), kGroups);
         }
         for (int i = 0; i < 2 * kGroups; ++i) mbar_init(smem_addr(&s_full[i]), 1);
-        for (int i = 0; i < kGroups; ++i) {
+        for (int i = 0; i < 2 * kGroups; ++i) {
             mbar_init(smem_addr(&p_full[i]), 4);
             mbar_init(smem_addr(&o_full[i]), 1);
         }
@@ -383,21 +383,22 @@ __global__ void __launch_bounds__(kThreads)
             // P V of tile t for this group, then its share of freeing the stage
             auto issue_pv = [&](uint32_t t, bool first) {
                 const uint32_t vs = st_a + (t % LY::kStages) * LY::kStageBytes + LY::kKVBytes;
-                if (!mbar_wait(smem_addr(&p_full[gr]), t & 1u, abort_flag, p.status)) {
+                if (!mbar_wait(smem_addr(&p_full[2 * gr + (t & 1u)]), (t >> 1) & 1u, abort_flag,
+                               p.status)) {
                     ok = false;
                     return;
                 }
                 tc::fence_after_sync();
                 const uint32_t pt = tmem + 64 * (2 * gr + (t & 1u));   // P of tile t
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+                for (int part = 0; part < (BF16 ? 2 : 1); ++part)
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk) {
                         const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
                         tc::mma_f16_ts(o_t, pt + part * 32 + kk * 8, b, id_pv,
                                        !(first && part == 0 && kk == 0));
                     }
-                tc::mma_commit(smem_addr(&o_full[gr]));
+                tc::mma_commit(smem_addr(&o_full[2 * gr + (t & 1u)]));
                 tc::mma_commit(smem_addr(&kv_empty[t % LY::kStages]));
             };
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it_cnt) {
@@ -520,7 +521,10 @@ __global__ void __launch_bounds__(kThreads)
                         }
                         const uint64_t pp = pack2f(p0, p1);
                         lsum2 = add2f(lsum2, pp);
-                        split_hi_lo<BF16>(p0, p1, pp, hi[c / 2], lo[c / 2]);
+                        if constexpr (BF16)
+                            split_hi_lo<true>(p0, p1, pp, hi[c / 2], lo[c / 2]);
+                        else                   // fp16 (relative error <= 2^-11): one part
+                            hi[c / 2] = E::pack(p0, p1);
                     }
                 };
                 if (cross) weights(std::true_type{});
@@ -532,7 +536,8 @@ __global__ void __launch_bounds__(kThreads)
                 // o_full phase of the previous tile either here or after P is out
                 const bool any_resc = __any_sync(kFull, resc);
                 if (t >= 1 && any_resc) {
-                    const bool okp = mbar_wait(smem_addr(&o_full[gr]), (tg - 1) & 1u, abort_flag, p.status);
+                    const bool okp = mbar_wait(smem_addr(&o_full[2 * gr + ((tg - 1) & 1u)]),
+                                               ((tg - 1) >> 1) & 1u, abort_flag, p.status);
                     if (!__all_sync(kFull, okp)) { alive = false; break; }
                     tc::fence_after_sync();
 #pragma unroll
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(kThreads)
                 // P of this tile over its own S columns (already read): high part
                 // in the first 32, low part in the next 32
                 tc::tmem_st32(lane_base + s_col + 64 * sb, hi);
-                tc::tmem_st32(lane_base + s_col + 64 * sb + 32, lo);
+                if constexpr (BF16) tc::tmem_st32(lane_base + s_col + 64 * sb + 32, lo);
                 // zero the V rows of keys past the last visible one (last tile only)
                 const int nvis = it.nkeys - k0;
                 if (nvis < kKeys) {      // both groups write the same zeros, each before its P
@@ -565,15 +570,17 @@ __global__ void __launch_bounds__(kThreads)
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&p_full[gr]));
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[2 * gr + (tg & 1u)]));
                 if (t >= 1 && !any_resc) {
-                    const bool okp = mbar_wait(smem_addr(&o_full[gr]), (tg - 1) & 1u, abort_flag, p.status);
+                    const bool okp = mbar_wait(smem_addr(&o_full[2 * gr + ((tg - 1) & 1u)]),
+                                               ((tg - 1) >> 1) & 1u, abort_flag, p.status);
                     if (!__all_sync(kFull, okp)) { alive = false; break; }
                 }
             }
             if (!alive) break;
             // ---- the item's result: O / l once the last P V is done
-            const bool oko = mbar_wait(smem_addr(&o_full[gr]), (tg - 1) & 1u, abort_flag, p.status);
+            const bool oko = mbar_wait(smem_addr(&o_full[2 * gr + ((tg - 1) & 1u)]),
+                                       ((tg - 1) >> 1) & 1u, abort_flag, p.status);
             if (!__all_sync(kFull, oko)) break;
             tc::fence_after_sync();
             const float inv = 1.f / l;

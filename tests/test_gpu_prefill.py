@@ -117,3 +117,31 @@ def test_zero_and_negative_scale(scale):
     assert status_check(c.status) == (0, 0)
     assert torch.isfinite(out.float()).all()
     assert_close(out, _oracle(c, qb, qs), f"prefill scale {scale}")
+
+
+def test_v_beyond_fp16_range_in_some_tiles():
+    """The kernel runs P V in fp16 after converting each bf16 V tile; a tile
+    holding a value fp16 cannot represent stays bf16 and takes the high + low P
+    path.  Sequence 1's last 50 positions get V scaled by 1e5, so the tile
+    holding them is bf16 for every row of its items while earlier tiles convert.
+    Rows before those positions do not see them (causal mask) and meet the usual
+    tolerance; rows that see them are compared after dividing by 1e5, i.e. the
+    usual tolerance on the scaled problem (its absolute term is stated for
+    values of order 1)."""
+    ctx, chunks = [700, 300], [700, 150]
+    dt, hq, hkv, d = "bf16", 32, 8, 128
+    F, first_big = 1e5, 250                             # positions >= 250 of sequence 1
+    c0, qb, qs = _case(21, ctx, chunks, hq, hkv, d, dt)
+    vals = dict(c0.host)
+    f = (vals["v_new"].astype(np.uint32) << 16).view(np.float32).copy()
+    start = int(qs[1]) + (first_big - (ctx[1] - chunks[1]))
+    f[start:int(qs[2])] *= F
+    vals["v_new"] = workloads._f32_to_bf16_bits(f)
+    c = DecodeCase(c0.w, vals)
+    assert (np.abs((c.host["v_new"][start:].astype(np.uint32) << 16).view(np.float32)) > 65504).any()
+    out = _run(c, qb, qs)
+    assert status_check(c.status) == (0, 0)
+    assert torch.isfinite(out.float()).all()
+    exp = _oracle(c, qb, qs)
+    assert_close(out[:start], exp[:start], "rows without large V")
+    assert_close(out[start:].double() / F, exp[start:] / F, "rows with large V, scaled")
