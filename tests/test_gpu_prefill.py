@@ -120,14 +120,12 @@ def test_zero_and_negative_scale(scale):
 
 
 def test_v_beyond_fp16_range_in_some_tiles():
-    """The kernel runs P V in fp16 after converting each bf16 V tile; a tile
-    holding a value fp16 cannot represent stays bf16 and takes the high + low P
-    path.  Sequence 1's last 50 positions get V scaled by 1e5, so the tile
-    holding them is bf16 for every row of its items while earlier tiles convert.
-    Rows before those positions do not see them (causal mask) and meet the usual
-    tolerance; rows that see them are compared after dividing by 1e5, i.e. the
-    usual tolerance on the scaled problem (its absolute term is stated for
-    values of order 1)."""
+    """bf16 V values far outside fp16's range (sequence 1's last 50 positions
+    scaled by 1e5) must pass through P V unharmed: no step of the bf16 path may
+    narrow V to fp16.  Rows before those positions do not see them (causal
+    mask) but share K/V tiles with them, and meet the usual tolerance; rows that
+    see them are compared after dividing by 1e5, i.e. the usual tolerance on the
+    scaled problem (its absolute term is stated for values of order 1)."""
     ctx, chunks = [700, 300], [700, 150]
     dt, hq, hkv, d = "bf16", 32, 8, 128
     F, first_big = 1e5, 250                             # positions >= 250 of sequence 1
