@@ -25,7 +25,7 @@ from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV
                       PKV_Q8_BF16, PKV_Q8_F16, PagedKVError, check, lib)
 
 __all__ = ["KVPool", "PagedKVError", "cache_write", "block_copy", "gather_blocks",
-           "scatter_blocks", "paged_decode_attention",
+           "scatter_blocks", "paged_decode_attention", "CapturedDecode",
            "paged_decode_attention_noalloc", "paged_prefill_attention",
            "cache_write_q8", "paged_decode_attention_q8",
            "prefill_workspace_bytes",
@@ -306,6 +306,46 @@ def paged_decode_attention(pool: KVPool, q, block_tables, context_lens, scale: f
                                                 _stream(stream))
     check(rc, "paged_decode_attention")
     return out
+
+
+class CapturedDecode:
+    """One paged decode attention call (16-bit or 8-bit pool) captured into a
+    CUDA graph on fixed device buffers: ``replay()`` runs the prep, attention
+    and merge kernels with a single graph launch instead of a Python call and
+    three kernel launches, so a serving loop whose steps are short does not
+    leave the GPU waiting on the host.  Each replay reads the buffers' current
+    contents (q, tables, lengths) and writes ``out``, the workspace and the
+    status word; the partition size is chosen on the device as in a direct
+    call.  At capture time the buffers must hold a valid batch (zero lengths
+    will do): one untimed call on a side stream sets the kernels up first."""
+
+    def __init__(self, pool: KVPool, q, block_tables, context_lens, scale: float, workspace,
+                 status, out):
+        import torch
+        self.torch = torch
+
+        def call():
+            if pool.is_q8:
+                paged_decode_attention_q8(pool, q, block_tables, context_lens, scale, workspace,
+                                          status, out=out)
+            else:
+                paged_decode_attention(pool, q, block_tables, context_lens, scale, workspace,
+                                       status, out=out)
+
+        side = torch.cuda.Stream(device=q.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            call()
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            call()
+        self.out = out
+
+    def replay(self):
+        """Enqueue the captured call on the current stream."""
+        self.graph.replay()
+        return self.out
 
 
 def paged_decode_attention_noalloc(pool: KVPool, q, block_tables, context_lens, scale: float,

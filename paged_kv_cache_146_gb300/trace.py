@@ -26,7 +26,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import (KVPool, cache_write, decode_workspace_bytes, gather_blocks,
+from . import (CapturedDecode, KVPool, cache_write, decode_workspace_bytes, gather_blocks,
                paged_decode_attention, scatter_blocks, status_check)
 from .workloads import TraceSchedule
 
@@ -49,7 +49,7 @@ class StepRecord:
 
 
 class TraceRunner:
-    def __init__(self, sched: TraceSchedule, device="cuda", free_order=None):
+    def __init__(self, sched: TraceSchedule, device="cuda", free_order=None, graph: bool = True):
         import torch
         self.torch = torch
         self.sched = sched
@@ -89,6 +89,13 @@ class TraceRunner:
         self.h_slots = torch.zeros(S, dtype=torch.int64, pin_memory=True)
         self.d_slots = torch.zeros(S, dtype=torch.int64, device=device)
         self._copied = None
+        # the step's queries land in a fixed buffer, so the attention call can
+        # be one CUDA graph replay (all lengths are zero at capture)
+        self.q32 = torch.empty((S, sched.num_q_heads, sched.head_dim), dtype=torch.float32,
+                               device=device)
+        self.q = torch.empty((S, sched.num_q_heads, sched.head_dim), dtype=tdt, device=device)
+        self.captured = CapturedDecode(self.pool, self.q, self.d_tables, self.d_ctx, self.scale,
+                                       self.workspace, self.status, self.out) if graph else None
 
     def _stage_slots(self, slots: np.ndarray):
         """Device copy of this step's slot mapping, through pinned memory."""
@@ -205,7 +212,9 @@ class TraceRunner:
         n_tok = int(num_new.sum())
         k_new = self._draw(n_tok, sc.num_kv_heads, sc.head_dim)
         v_new = self._draw(n_tok, sc.num_kv_heads, sc.head_dim)
-        q = self._draw(self.S, sc.num_q_heads, sc.head_dim)
+        torch.randn(self.q32.shape, generator=self.gen, device=self.device, dtype=torch.float32,
+                    out=self.q32)
+        q = self.q.copy_(self.q32)
         self._wait_copied()
         if n_tok:
             cache_write(self.pool, k_new, v_new, self._stage_slots(slots), self.status)
@@ -218,8 +227,11 @@ class TraceRunner:
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev0.record()
-        paged_decode_attention(self.pool, q, self.d_tables, self.d_ctx, self.scale,
-                               self.workspace, self.status, out=self.out)
+        if self.captured is not None:
+            self.captured.replay()
+        else:
+            paged_decode_attention(self.pool, q, self.d_tables, self.d_ctx, self.scale,
+                                   self.workspace, self.status, out=self.out)
         ev1.record()
         kv_bytes = int(ctx.astype(np.int64).sum()) * sc.num_kv_heads * sc.head_dim * 2 * 2
         # finished sequences give their blocks back
@@ -241,7 +253,7 @@ class TraceRunner:
         rec.extra["swapped_in"] = swapped_in
         rec.extra["swapped_out"] = swapped_out
         if keep_tensors:
-            rec.q, rec.k_new, rec.v_new = q, k_new, v_new
+            rec.q, rec.k_new, rec.v_new = q.clone(), k_new, v_new
             rec.out = self.out.clone()
         return rec
 
