@@ -20,7 +20,9 @@ struct Params {
     int32_t num_blocks;
     int32_t auto_split_pairs;   // > 0: the prep kernel picks the size (header[2])
     float scale_log2;           // softmax scale * log2(e): scores live in the exp2 domain
-    int32_t *header;            // [0] pairs, [1] debug word, [2] blocks per partition
+    int32_t *header;            // [0] pairs, [1] debug word, [2] blocks per partition,
+                                // [3] sequences with more than one partition
+    int32_t *multi;             // [S]: those sequences (any order)
     int2 *seq_info;             // [S]: first pair index, number of partitions
     int2 *items;                // [S * ceil(maxb / P)]: (sequence, partition)
     float2 *part_ml;            // [pairs * Hkv * G]: (max, sum) of a partition; sum < 0 = poisoned

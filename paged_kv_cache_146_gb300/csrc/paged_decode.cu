@@ -142,9 +142,13 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     __shared__ int warp_bin[32][kOrderBins];   // pass 2: per-warp counts, then offsets
     __shared__ long long auto_tot[32][kAutoSizes];
     __shared__ int chosen_split;
+    __shared__ int multi_count;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_launch_dependents();   // the main kernel may set up its CTAs meanwhile
-    if (tid == 0) carry = make_int2(0, 0);
+    if (tid == 0) {
+        carry = make_int2(0, 0);
+        multi_count = 0;
+    }
     for (int i = tid; i < kOrderBins; i += 1024) bin_next[i] = 0;
     for (int i = tid; i < 32 * kOrderBins; i += 1024) (&warp_bin[0][0])[i] = 0;
     const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
             p.seq_info[s] = make_int2(excl, nsplit);
             for (int k = 0; k < nsplit - partial; ++k) p.items[excl_full + k] = make_int2(s, k);
             if (partial) atomicAdd(&bin_next[bin_of(r)], 1);
+            if (nsplit > 1) p.multi[atomicAdd(&multi_count, 1)] = s;   // for the merge kernel
             if (zero_row) {
                 uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(p.out) +
                                                      (size_t)s * p.num_q_heads * head_dim * 2);
@@ -283,6 +288,7 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     if (tid == 0) {
         p.header[0] = carry.x;
         p.header[2] = P;
+        p.header[3] = multi_count;
     }
 }
 
@@ -696,20 +702,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
 // with a fixed shuffle tree, then each lane sums its D/32 dimensions over the
 // pieces in partition order, with the piece loads independent of the sums so
 // many are in flight.  Deterministic.  A poisoned piece (sum < 0) zeroes the row.
+// One (sequence, kv head, query head h): the sequence's partition pieces
+// combined by log-sum-exp, in partition order.
 template <bool BF16, int D>
-__global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
+__device__ __forceinline__ void merge_one(const Params &p, int s, int g, int h, int lane)
 {
     using E = Elem<BF16>;
     using T = typename E::T;
     constexpr int PER_LANE = D / 32;
     const int Hkv = p.num_kv_heads, G = p.group;
-    const int s = blockIdx.x / Hkv, g = blockIdx.x - (blockIdx.x / Hkv) * Hkv;
-    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    griddep_wait();                // pieces come from the main kernel
-    if (s >= p.num_seqs || h >= G) return;
     const int2 info = p.seq_info[s];
     const int n = info.y;
-    if (n <= 1) return;
     const float2 *ml = p.part_ml + ((size_t)info.x * Hkv + g) * G + h;   // stride Hkv * G
     const size_t mstride = (size_t)Hkv * G;
     // one pass: each lane keeps (max, sum) of its pieces, then a fixed butterfly
@@ -764,9 +767,25 @@ __global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
     }
 }
 
+// The sequences the prep kernel listed as split, grid-stride over (sequence,
+// kv head); one warp per query head of the group.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
+{
+    const int Hkv = p.num_kv_heads, G = p.group;
+    const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_wait();                // pieces and the list come from the prep and main kernels
+    if (h >= G) return;
+    const int units = p.header[3] * Hkv;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int s = p.multi[u / Hkv], g = u - (u / Hkv) * Hkv;
+        merge_one<BF16, D>(p, s, g, h, lane);
+    }
+}
+
 // --------------------------------------------------------------------- host side
 struct WsLayout {
-    size_t header, seq_info, items, part_ml, part_o, total;
+    size_t header, seq_info, items, part_ml, part_o, multi, total;
     int64_t max_pairs;
 };
 
@@ -784,6 +803,7 @@ static bool ws_layout(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t max
     w->items = off; off += align256((size_t)w->max_pairs * 8);
     w->part_ml = off; off += align256((size_t)w->max_pairs * Hkv * G * 8);
     w->part_o = off; off += align256((size_t)w->max_pairs * Hkv * G * D * 4);
+    w->multi = off; off += align256((size_t)S * 4);
     w->total = off;
     return true;
 }
@@ -957,6 +977,7 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     prm.items = reinterpret_cast<int2 *>(ws + w.items);
     prm.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
     prm.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    prm.multi = reinterpret_cast<int32_t *>(ws + w.multi);
     prm.status = d_status;
     prm.kv_q8 = want_8bit ? static_cast<const uint8_t *>(k_pool) : nullptr;
     prm.max_pairs = w.max_pairs;
@@ -988,7 +1009,11 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, v.fn, tk, tv, prm) != cudaSuccess) return PKV_ERR_CUDA;
     if (maxb > P) {   // some sequence may have several partitions
-        const int64_t pairs = (int64_t)num_seqs * g.num_kv_heads;
+        // a grid-stride grid over the (sequence, kv head) units the prep kernel
+        // lists: a few waves when many sequences are split, and little to
+        // launch when none is
+        int64_t pairs = (int64_t)num_seqs * g.num_kv_heads;
+        if (pairs > (int64_t)num_sms * 8) pairs = (int64_t)num_sms * 8;
         void (*merge)(Params) =
             g.head_dim == 128 ? (bf ? decode_merge_kernel<true, 128> : decode_merge_kernel<false, 128>)
                               : (bf ? decode_merge_kernel<true, 64> : decode_merge_kernel<false, 64>);

@@ -326,6 +326,8 @@ def test_work_list_order(split, seqs, max_len, auto_split):
     raw = ws.cpu().numpy()
     P = int(raw[8:12].view(np.int32)[0])
     assert P == (split or auto_split)
+    nb_ = -(-lens.astype(np.int64) // 16)
+    assert int(raw[12:16].view(np.int32)[0]) == int(((-(-nb_ // P)) > 1).sum())   # split sequences
     assert default_split() == 32
     nb = -(-lens.astype(np.int64) // 16)
     nsplit = -(-nb // P)

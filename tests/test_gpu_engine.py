@@ -118,3 +118,33 @@ def test_host_buffer_steps_match_device_steps(pool_dtype, base):
         assert np.array_equal(to_np_bits(outs[t]), ref[t]), f"step {t}"
     assert np.array_equal(a.tables, b.tables) and np.array_equal(a.lens, b.lens)
     assert a.pool.num_free() == b.pool.num_free()
+
+
+@pytest.mark.parametrize("pool_dtype,base", [("bf16", "bf16"), ("q8_bf16", "bf16")])
+def test_captured_decode_replays_like_a_direct_call(pool_dtype, base):
+    """CapturedDecode is captured while every length is zero; the batch then
+    goes into the captured buffers in place and each replay gives the same bits
+    as a direct call on the same buffers, also after the queries change."""
+    from paged_kv_cache_146_gb300 import (CapturedDecode, decode_workspace_bytes,
+                                          paged_decode_attention, paged_decode_attention_q8)
+    w, vals, steps = _setup(47, pool_dtype, base, seqs=24, max_len=3000)
+    eng = _engine(w, vals, pool_dtype)
+    S, hq, d = w.num_seqs, w.num_q_heads, w.head_dim
+    q = torch.empty((S, hq, d), dtype=eng.out.dtype, device="cuda")
+    tables = torch.full_like(eng.d_tables, -1)
+    lens = torch.zeros_like(eng.d_lens)
+    ws = torch.empty(decode_workspace_bytes(S, hq, w.num_kv_heads, d, w.max_blocks_per_seq),
+                     dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(eng.out)
+    cap = CapturedDecode(eng.pool, q, tables, lens, w.scale, ws, status, out)
+    tables.copy_(torch.from_numpy(eng.tables).cuda())
+    lens.copy_(torch.from_numpy(eng.lens).cuda())
+    direct = paged_decode_attention_q8 if eng.pool.is_q8 else paged_decode_attention
+    for st in steps[:2]:
+        q.copy_(to_torch(st["q"], w.is_bf16, "cuda"))
+        got = cap.replay().clone()
+        ref = direct(eng.pool, q, tables, lens, w.scale, ws, status)
+        torch.cuda.synchronize()
+        assert status_check(status) == (0, 0)
+        assert torch.equal(got, ref)
