@@ -157,25 +157,49 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
         for (int j = 0; j < 4; ++j)
             if (4 * q4 + j >= valid) x[j] = -INFINITY;
     }
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-    const float mn = fmaxf(m0, mx);
-    const float a0 = fast_exp2(m0 - mn);
-    float pj[4];
+    // Lazy reference maximum: m0 moves (exactly to the row maximum, with the
+    // accumulators rescaled) only when a score exceeds it by more than
+    // kQ8Lazy, so most blocks skip the cross-lane maximum.  Weights then reach
+    // 2^kQ8Lazy = 64, and the fp16 product p * vs below stays finite while
+    // every V scale of the block is at most 1023 (64 * 1023 < 65504); a block
+    // with a larger scale (V values beyond ~1.3e5) takes the exact path, where
+    // weights stay <= 1 as they always did.
+    constexpr float kQ8Lazy = 6.f;
+    bool raise = x[0] > m0 + kQ8Lazy || x[1] > m0 + kQ8Lazy ||
+                 x[2] > m0 + kQ8Lazy || x[3] > m0 + kQ8Lazy;
+    {
+        __half2 m = __hmax2(*reinterpret_cast<const __half2 *>(&vs[0].x),
+                            *reinterpret_cast<const __half2 *>(&vs[0].y));
 #pragma unroll
-    for (int j = 0; j < 4; ++j) pj[j] = fast_exp2(x[j] - mn);
-    l0 = l0 * a0 + ((pj[0] + pj[1]) + (pj[2] + pj[3]));
-    m0 = mn;
-    if (__any_sync(kFull, a0 != 1.f)) {
-        // this lane's accumulators belong to query rows 2q4 and 2q4 + 1
-        const float f0 = __shfl_sync(kFull, a0, 8 * q4);
-        const float f1 = __shfl_sync(kFull, a0, 8 * q4 + 4);
+        for (int i = 1; i < 4; ++i) {
+            m = __hmax2(m, *reinterpret_cast<const __half2 *>(&vs[i].x));
+            m = __hmax2(m, *reinterpret_cast<const __half2 *>(&vs[i].y));
+        }
+        const float2 mf = __half22float2(m);
+        raise |= !(mf.x <= 1023.f && mf.y <= 1023.f);
+    }
+    if (__any_sync(kFull, raise)) {
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+        const float mn = fmaxf(m0, mx);
+        const float a0 = fast_exp2(m0 - mn);
+        l0 *= a0;
+        m0 = mn;
+        if (__any_sync(kFull, a0 != 1.f)) {
+            // this lane's accumulators belong to query rows 2q4 and 2q4 + 1
+            const float f0 = __shfl_sync(kFull, a0, 8 * q4);
+            const float f1 = __shfl_sync(kFull, a0, 8 * q4 + 4);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            o[t][0] *= f0; o[t][1] *= f1; o[t][2] *= f0; o[t][3] *= f1;
+            for (int t = 0; t < 8; ++t) {
+                o[t][0] *= f0; o[t][1] *= f1; o[t][2] *= f0; o[t][3] *= f1;
+            }
         }
     }
+    float pj[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pj[j] = fast_exp2(x[j] - m0);
+    l0 += (pj[0] + pj[1]) + (pj[2] + pj[3]);
     const uint32_t p01 = H::pack(pj[0], pj[1]), p23 = H::pack(pj[2], pj[3]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

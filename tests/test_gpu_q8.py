@@ -328,3 +328,28 @@ def test_q8_zero_and_negative_scale(scale):
     out = c.run()
     assert status_check(c.status) == (0, 0)
     assert_close(out, c.oracle_out(), f"q8 scale {scale}")
+
+
+def test_q8_blocks_with_large_v_scales():
+    """The kernel's softmax lets its reference maximum lag the true one (weights
+    up to 2^6) except in blocks whose V scales exceed 1023, where an fp16 weight
+    times scale product could overflow: those take the exact maximum.
+    Sequence 1 has V of 40 tokens (three blocks) scaled by 1e6 (group scales
+    ~8e3); its output is compared after dividing by 1e6, i.e. the usual
+    tolerance on the scaled problem; sequence 0 is untouched."""
+    lens, hq, hkv, dt = [900, 700], 32, 8, "bf16"
+    rng = np.random.default_rng(61)
+    T = sum(lens)
+    k = workloads.normal_bits(rng, (T, hkv, D), dt)
+    v = workloads.normal_bits(rng, (T, hkv, D), dt)
+    f = (v.astype(np.uint32) << 16).view(np.float32).copy()
+    f[lens[0] + 300:lens[0] + 340] *= 1e6
+    v = workloads._f32_to_bf16_bits(f)
+    c = Q8Case(lens, hq, hkv, dt, seed=61, rows=(k, v))
+    _assert_pools_equal(c.pool, c.ref)
+    out = c.run()
+    assert status_check(c.status) == (0, 0)
+    assert torch.isfinite(out.float()).all()
+    exp = c.oracle_out()
+    assert_close(out[:1], exp[:1], "q8 untouched sequence")
+    assert_close(out[1:].double() / 1e6, exp[1:] / 1e6, "q8 large V, scaled")
