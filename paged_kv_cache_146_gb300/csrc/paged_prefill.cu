@@ -121,10 +121,9 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
 //   warps 9 and 10, lane 0 (MMA issuers, one per query tile): S = Q K^T into
 //     one of two tensor-memory buffers (M 128, N 64), then O += P V for the
 //     previous tile (M 128, N D, V as an MN-major operand), P as a high and a
-//     low bf16 part (bf16 pools) or one fp16 part (fp16 pools).  A thread gets
-//     a new tcgen05.mma accepted only about 110 cycles after its previous one
-//     (measured, whatever N <= 128), so one issuer for both tiles left the
-//     tensor pipe idle most of the time.
+//     low bf16 part (bf16 pools) or one fp16 part (fp16 pools).  One issuer
+//     per query tile lets each group's S and P V go out as soon as that
+//     group's inputs are ready, without waiting behind the other group's.
 //   warps 0-3 and 4-7 (softmax, one warpgroup per query tile, ping-pong on the
 //     tensor pipe): thread r of a group owns row r = tensor-memory lane r.  Running
 //     maximum with lazy rescaling: the reference maximum moves only when a
@@ -369,9 +368,7 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
     } else if (warp == kIssuer || warp == kIssuer + 1) {
-        // one issuer per query tile: the tensor pipe takes a new tcgen05.mma from
-        // a thread only ~110 cycles after its previous one, so two threads keep it
-        // fed where one could not
+        // one issuer per query tile
         if (lane == 0) {
             const int gr = warp - kIssuer;
             const uint32_t id_qk = tc::idesc_f16(BF16, kRows, kKeys, 0, 0);
