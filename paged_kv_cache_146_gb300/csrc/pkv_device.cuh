@@ -89,16 +89,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            int z, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
 // Bring [src, src + bytes) into L2 (bytes a multiple of 16, src 16-byte aligned).
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
 {
@@ -217,45 +207,5 @@ struct Elem<false> {
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
     }
 };
-
-
-// Four signed 8-bit codes (one 32-bit word, byte i = code i) -> two packed
-// pairs of the element type: lo = (code0, code1), hi = (code2, code3).  Exact:
-// every integer in [-128, 127] is an fp16 and a bf16 value, and both tricks
-// below end in one packed subtraction whose result is that integer.
-//   fp16: the biased byte u = code + 128 is the low mantissa of 1024
-//         (bits 0x6400 | u = 1024 + u); subtracting 1152 leaves the code.
-//   bf16: only 7 mantissa bits.  The byte's low 7 bits m sit under 128 (bits
-//         0x4300 | m = 128 + m) and its top bit picks the subtrahend: 128
-//         (0x4300) for codes >= 0, 256 (0x4380) for codes < 0, where the code
-//         is m - 128.
-template <bool BF16>
-__device__ __forceinline__ void codes_to_pairs(uint32_t w, uint32_t &lo, uint32_t &hi);
-
-template <>
-__device__ __forceinline__ void codes_to_pairs<false>(uint32_t w, uint32_t &lo, uint32_t &hi)
-{
-    const uint32_t u = w ^ 0x80808080u;
-    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);     // (0x64, u0), (0x64, u1)
-    uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);     // (0x64, u2), (0x64, u3)
-    const uint32_t bias = 0x64806480u;                    // (1152, 1152)
-    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(a) : "r"(bias));
-    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(b) : "r"(bias));
-    lo = a;
-    hi = b;
-}
-
-template <>
-__device__ __forceinline__ void codes_to_pairs<true>(uint32_t w, uint32_t &lo, uint32_t &hi)
-{
-    const uint32_t a = __byte_perm(w, 0x43434343u, 0x4140);   // (0x43, w0), (0x43, w1)
-    const uint32_t b = __byte_perm(w, 0x43434343u, 0x4342);   // (0x43, w2), (0x43, w3)
-    uint32_t va = a & 0xff7fff7fu, vb = b & 0xff7fff7fu;      // 128 + m
-    const uint32_t sa = a & 0xff80ff80u, sb = b & 0xff80ff80u; // 128 or 256
-    asm("sub.rn.bf16x2 %0, %0, %1;" : "+r"(va) : "r"(sa));
-    asm("sub.rn.bf16x2 %0, %0, %1;" : "+r"(vb) : "r"(sb));
-    lo = va;
-    hi = vb;
-}
 
 }  // namespace pkv

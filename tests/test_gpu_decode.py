@@ -353,3 +353,31 @@ def test_work_list_order(split, seqs, max_len, auto_split):
         seqs = rest[bins == b, 0]
         assert (np.diff(seqs) > 0).all()
     assert_close(c.run_gpu(blocks_per_split=split), c.oracle_out(), f"split={split}")
+
+
+def test_partition_size_middle_choice():
+    """60 sequences of 200 blocks (GQA 32/8, D 128): 240 pairs at 64 blocks per
+    partition, 120 at 128.  The device keeps the largest size that still
+    leaves five items per resident CTA (two per SM at head_dim 128), i.e.
+    pairs * 8 kv heads >= 5 * 2 * SMs -- 64 blocks on a 152-SM GPU."""
+    from paged_kv_cache_146_gb300 import KVPool, decode_workspace_bytes, paged_decode_attention
+    S, nb, hq, hkv, d = 60, 200, 32, 8, 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    need = -(-5 * 2 * sms // hkv)
+    pairs = {P: S * -(-nb // P) for P in (32, 64, 128)}
+    expect = 128 if pairs[128] >= need else 64 if pairs[64] >= need else 32
+    pool = KVPool(S * nb, hkv, d, "bf16", device="cuda")
+    pool.k_pool.zero_()
+    pool.v_pool.zero_()
+    tables = torch.arange(S * nb, dtype=torch.int32, device="cuda").reshape(S, nb)
+    lens = torch.full((S,), nb * 16, dtype=torch.int32, device="cuda")
+    q = torch.randn(S, hq, d, device="cuda").to(torch.bfloat16)
+    ws = torch.empty(decode_workspace_bytes(S, hq, hkv, d, nb), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = paged_decode_attention(pool, q, tables, lens, 1 / 128 ** 0.5, ws, status)
+    assert status_check(status) == (0, 0)
+    raw = ws.cpu().numpy()
+    assert int(raw[8:12].view(np.int32)[0]) == expect
+    if sms == 152:
+        assert expect == 64
+    assert not out.any()                                   # V is zero
