@@ -57,13 +57,18 @@ DECODE_SOURCES = ("decode_params.h", "paged_decode.cu", "pkv_device.cuh")
 
 
 def decode_source_hash() -> str:
-    """First 16 hex digits of the SHA-256 of the sources the 16-bit decode
-    kernels compile from."""
+    """First 16 hex digits of the SHA-256 of the code the 16-bit decode kernels
+    compile from (comments removed and whitespace collapsed, so a comment edit
+    does not count as a kernel change)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_146_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_146_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

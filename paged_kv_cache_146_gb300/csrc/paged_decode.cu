@@ -697,11 +697,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
 // ---------------------------------------------------------------- merge kernel
 // Sequences cut into several partitions get their pieces combined by log-sum-exp:
 //   M = max_p m_p,  out = sum_p o_p 2^(m_p - M) / sum_p l_p 2^(m_p - M)
-// (maxima in the log2 domain).  One CTA per (sequence, kv head), one warp per
-// query head of the group: lanes reduce M and the denominator over the pieces
-// with a fixed shuffle tree, then each lane sums its D/32 dimensions over the
-// pieces in partition order, with the piece loads independent of the sums so
-// many are in flight.  Deterministic.  A poisoned piece (sum < 0) zeroes the row.
+// (maxima in the log2 domain).  The kernel walks the (sequence, kv head) units
+// of the split sequences grid-stride, one warp per query head of the group:
+// lanes reduce M and the denominator over the pieces with a fixed shuffle tree,
+// then each lane sums its D/32 dimensions over the pieces in partition order,
+// with the piece loads independent of the sums so many are in flight.
+// Deterministic.  A poisoned piece (sum < 0) zeroes the row.
+//
 // One (sequence, kv head, query head h): the sequence's partition pieces
 // combined by log-sum-exp, in partition order.
 template <bool BF16, int D>
