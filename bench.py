@@ -534,6 +534,93 @@ def prefill_arm(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def blocks_arm(args, world, rank, local):
+    """Block movement of the NEXT rows, GQA 8 kv heads x 128, bf16 (64 KiB of K+V
+    per block): ``cow`` -- one kv_block_copy call copying 8,192 random blocks
+    into 8,192 others (copy-on-write of many forks at once); ``swap`` -- a
+    2,048-block sequence (32K tokens) packed into staging (kv_gather_blocks),
+    copied to pinned host memory and back, unpacked into fresh blocks
+    (kv_scatter_blocks).  Kernel GB/s count bytes read + written."""
+    import torch
+    from paged_kv_cache_146_gb300 import (KVPool, block_copy, gather_blocks, scatter_blocks,
+                                          status_check)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    hkv, d, bs = 8, 128, 16
+    blk = 2 * hkv * bs * d * 2                         # K + V bytes of one block
+    n = 8192 if args.workload == "cow" else 2048
+    nb = 2 * n + 16
+    rng = np.random.default_rng(args.seed + 31 + rank)
+    pool = KVPool(nb, hkv, d, "bf16", device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 37 + rank)
+    pool.k_pool.copy_(torch.randn(pool.k_pool.shape, generator=gen, device=dev))
+    pool.v_pool.copy_(torch.randn(pool.v_pool.shape, generator=gen, device=dev))
+    perm = rng.permutation(nb).astype(np.int32)
+    src = torch.from_numpy(perm[:n]).to(dev)
+    dst = torch.from_numpy(perm[n:2 * n]).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        barrier(world)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b) / args.steps, world)
+
+    peak, peak_kind = peaks()
+    extra = {}
+    if args.workload == "cow":
+        ms = timed(lambda: block_copy(pool, src, dst, status))
+        nbytes = 2 * n * blk
+        ok = torch.equal(pool.k_pool[dst.long()], pool.k_pool[src.long()]) and \
+            torch.equal(pool.v_pool[dst.long()], pool.v_pool[src.long()])
+        metric, kern = "kv_block_copy GB/s (bytes read + written)", "kv_block_copy"
+        cfg = {"workload": "cow", "block_pairs": n, "kv_heads": hkv, "head_dim": d,
+               "block_size": bs, "kv_dtype": "bf16", "bytes_per_call": nbytes}
+    else:
+        staging = torch.empty((n, 2, hkv, bs, d), dtype=torch.bfloat16, device=dev)
+        host = torch.empty(staging.shape, dtype=torch.bfloat16, pin_memory=True)
+        ms = timed(lambda: gather_blocks(pool, src, staging, status))
+        ms_sc = timed(lambda: scatter_blocks(pool, dst, staging, status))
+        ms_d2h = timed(lambda: host.copy_(staging, non_blocking=True))
+        ms_h2d = timed(lambda: staging.copy_(host, non_blocking=True))
+        nbytes = 2 * n * blk
+        gather_blocks(pool, src, staging, status)
+        scatter_blocks(pool, dst, staging, status)
+        ok = torch.equal(pool.k_pool[dst.long()], pool.k_pool[src.long()])
+        extra = {"scatter_gbs": round(nbytes / (ms_sc * 1e-3) / 1e9, 2),
+                 "d2h_gbs": round(n * blk / (ms_d2h * 1e-3) / 1e9, 2),
+                 "h2d_gbs": round(n * blk / (ms_h2d * 1e-3) / 1e9, 2),
+                 "swap_out_ms": round(ms + ms_d2h, 4), "swap_in_ms": round(ms_h2d + ms_sc, 4)}
+        metric, kern = "kv_gather_blocks GB/s (bytes read + written)", "kv_gather_blocks"
+        cfg = {"workload": "swap", "blocks": n, "tokens": n * bs, "kv_heads": hkv, "head_dim": d,
+               "block_size": bs, "kv_dtype": "bf16", "bytes_per_call": nbytes}
+    rc, word = status_check(status)
+    if rc != 0 or not ok:
+        raise SystemExit(f"device status {rc} word {word:#x}, copies equal: {ok}")
+    if rank != 0:
+        return
+    gbs = nbytes * world / (ms * 1e-3) / 1e9
+    line = {"metric": metric, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 2),
+                         "peak": peak, "unit": "GB/s",
+                         "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "traffic": None,
+                         "peak_kind": peak_kind, "kernel": kern},
+            "gpu_launches": args.steps, **extra}
+    print(json.dumps(line), flush=True)
+
+
 def trace_arm(args, world, rank, local):
     """Continuous-batching trace: 500 steps (or --steps) of FCFS admission,
     prefill, decode and release; per-step attention GB/s (CUDA events around the
@@ -596,7 +683,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="gqa_long",
                     choices=["gqa_long", "gqa_long_q8", "tiny", "opt13b", "shared_prefix", "trace",
-                             "prefill"],
+                             "prefill", "cow", "swap"],
                     help="gqa_long is the headline line; the others report their own config")
     ap.add_argument("--pool-gib", type=float, default=0.0,
                     help="trace only: pool size (default 40 GiB); small pools force swapping")
@@ -617,6 +704,8 @@ def main():
         trace_arm(args, world, rank, local)
     elif args.workload == "prefill":
         prefill_arm(args, world, rank, local)
+    elif args.workload in ("cow", "swap"):
+        blocks_arm(args, world, rank, local)
     else:
         our_arm(args, world, rank, local)
     if world > 1:
