@@ -311,9 +311,11 @@ def our_arm(args, world, rank, local):
         first[0] = w.shared_prefix_tokens
         eng.prefill(vals["k_shared"], vals["v_shared"], first)
         eng.share_prefix(w.shared_prefix_tokens)
-        eng.prefill(vals["k_prompt"], vals["v_prompt"], w.prior_lens - w.shared_prefix_tokens)
+        slots_p = eng.prefill(vals["k_prompt"], vals["v_prompt"],
+                              w.prior_lens - w.shared_prefix_tokens)
     else:
-        eng.prefill(vals["k_prompt"], vals["v_prompt"], w.prior_lens)
+        slots_p = eng.prefill(vals["k_prompt"], vals["v_prompt"], w.prior_lens)
+    prompt_rows = (vals["k_prompt"], vals["v_prompt"], torch.from_numpy(slots_p).to(dev))
     vals.clear()
     gen = torch.Generator(device=dev)
     gen.manual_seed(args.seed + 7 + rank)
@@ -329,6 +331,8 @@ def our_arm(args, world, rank, local):
 
     def step(i, ev=None):
         eng.host_step()
+        if ev:
+            ev[2].record(stream)
         eng.write(ks[i], vs[i])
         if ev:
             ev[0].record(stream)
@@ -350,7 +354,7 @@ def our_arm(args, world, rank, local):
         pass
     clocks = ClockSampler(gpu_uuid)
     bytes_total, toks_total = 0, 0
-    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    attn_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
                for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.start()
@@ -367,7 +371,8 @@ def our_arm(args, world, rank, local):
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = start.elapsed_time(stop)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_ms = [a.elapsed_time(b) for a, b, _ in attn_ev]
+    cw_ms = [c.elapsed_time(a) for a, _, c in attn_ev]      # this step's cache write
     rc, word = eng.check()
     if rc != 0:
         raise SystemExit(f"device status {rc} word {word:#x} in the timed steps")
@@ -417,6 +422,31 @@ def our_arm(args, world, rank, local):
         if rc != 0:
             raise SystemExit(f"device status {rc} word {word:#x} in the e2e steps")
 
+    # the cache write, reported on its own: the decode step's (one token per
+    # sequence, timed above) and the prompts' (every prompt token, written
+    # again into the same slots -- the cache is unchanged -- and timed once)
+    k_pr, v_pr, d_slots_pr = prompt_rows
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(stream)
+    eng.write(k_pr, v_pr, d_slots_pr)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    rc, word = eng.check()
+    if rc != 0:
+        raise SystemExit(f"device status {rc} word {word:#x} in the prompt write")
+    row_out = (2 * (d + d // 32 * 2) if q8 else 2 * d * 2) * hkv     # K+V bytes stored per token
+    row_in = 2 * d * 2 * hkv                                          # K+V bytes read per token
+    T_pr = int(d_slots_pr.shape[0])
+    cw_step_ms = sum(cw_ms) / len(cw_ms)
+    cache_write_line = {
+        "bytes": "T x (K+V row bytes read + stored) + 8 T",
+        "step_tokens": S, "step_us": round(1e3 * cw_step_ms, 2),
+        "step_gbs": round(S * (row_in + row_out + 8) / (cw_step_ms * 1e-3) / 1e9, 2),
+        "prompt_tokens": T_pr, "prompt_ms": round(c0.elapsed_time(c1), 4),
+        "prompt_gbs": round(T_pr * (row_in + row_out + 8) / (c0.elapsed_time(c1) * 1e-3) / 1e9, 2)}
+    del prompt_rows, k_pr, v_pr
+
     if rank != 0:
         return
     cpu = None
@@ -453,6 +483,7 @@ def our_arm(args, world, rank, local):
                      "launch_ms": round(attn_avg_ms, 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "cache_write": cache_write_line,
         "gpu_launches": (4 if eng.maxb > (eng.split_for_step() or default_split()) else 3)
         * args.steps,
         "clocks": clk,
@@ -535,7 +566,7 @@ def prefill_arm(args, world, rank, local):
 
 
 def blocks_arm(args, world, rank, local):
-    """Block movement of the NEXT rows, GQA 8 kv heads x 128, bf16 (64 KiB of K+V
+    """Block movement for copy-on-write and swap, GQA 8 kv heads x 128, bf16 (64 KiB of K+V
     per block): ``cow`` -- one kv_block_copy call copying 8,192 random blocks
     into 8,192 others (copy-on-write of many forks at once); ``swap`` -- a
     2,048-block sequence (32K tokens) packed into staging (kv_gather_blocks),

@@ -108,7 +108,7 @@ int64_t kv_blocks_for_tokens(int64_t num_tokens, int32_t block_size);
 size_t kv_pool_bytes(int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                      int32_t head_dim, pkv_dtype dtype);
 
-/* ---------------------------------------------------- host block ledger (a1) */
+/* --------------------------------------------------------- host block ledger */
 
 /* Create the ledger of a pool of num_blocks blocks.  initial_free_order, if not
  * NULL, is a permutation of 0..num_blocks-1 giving the order in which free
@@ -152,7 +152,7 @@ int kv_block_refcount(const pkv_pool *pool, int32_t id, int32_t *out);
 /* Number of free blocks. */
 int kv_pool_num_free(const pkv_pool *pool, int32_t *out);
 
-/* ------------------------------------- on-demand allocation + slots (a1, a2) */
+/* ------------------------------------------- on-demand allocation + slots */
 
 /* Grow num_seqs sequences: sequence s holds seq_lens[s] tokens and gains
  * num_new[s] more.  The token at position n needs logical block n / block_size;
@@ -173,7 +173,7 @@ int kv_append_slots(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_lens,
                     const int32_t *num_new, int32_t *block_tables,
                     int32_t max_blocks_per_seq, int64_t *slot_mapping);
 
-/* ------------------------------------- sharing and copy-on-write (NEXT #1) */
+/* --------------------------------------------- sharing and copy-on-write */
 
 /* A child sequence starts sharing every block of its parent ("vLLM-and-
  * PagedAttention-KR", "Parallel Sampling decoding": the samples of one prompt
@@ -213,7 +213,7 @@ int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_len
 int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *dst_ids,
                   int32_t n, void *k_pool, void *v_pool, int32_t *d_status, void *stream);
 
-/* ------------------------------------------------- 8-bit cache (NEXT #3) */
+/* --------------------------------------------------------------- 8-bit cache */
 
 /* An 8-bit cache stores each token's K and V as one-byte codes with one fp16
  * scale per group of 32 values: 34 bytes per 32 values, 53.1 % of fp16
@@ -238,10 +238,13 @@ int kv_block_copy(const pkv_pool *pool, const int32_t *src_ids, const int32_t *d
 #define PKV_Q8_SLAB_BYTES 4352
 
 /* Quantising cache write: k_new / v_new are bf16 (PKV_Q8_BF16) or fp16
- * (PKV_Q8_F16) rows [num_tokens][Hkv][128]; slots as in kv_cache_write; kv_q8
- * is the pool (16-byte aligned).  Errors: PKV_ERR_INVALID_ARG (not an 8-bit
- * pool, alignment), PKV_ERR_UNSUPPORTED (head_dim other than 128 or block_size
- * other than 16), PKV_ERR_CUDA.  Slots outside the pool: PKV_DEV_BAD_SLOT. */
+ * (PKV_Q8_F16) rows [num_tokens][Hkv][128], 16-byte aligned; slots as in
+ * kv_cache_write; kv_q8 is the pool (16-byte aligned).  Codes and scales are
+ * those of the rule above, bit for bit, for every finite or infinite input;
+ * a NaN input value stores an unspecified code (its group's scale ignores it).
+ * Errors: PKV_ERR_INVALID_ARG (not an 8-bit pool, alignment),
+ * PKV_ERR_UNSUPPORTED (head_dim other than 128 or block_size other than 16),
+ * PKV_ERR_CUDA.  Slots outside the pool: PKV_DEV_BAD_SLOT. */
 int kv_cache_write_q8(const pkv_pool *pool, const void *k_new, const void *v_new,
                       const int64_t *slot_mapping, int32_t num_tokens, void *kv_q8,
                       int32_t *d_status, void *stream);
@@ -257,7 +260,7 @@ int paged_decode_attention_q8(const pkv_pool *pool, void *out, const void *q, co
                               float scale, void *workspace, size_t workspace_bytes,
                               int32_t *d_status, void *stream);
 
-/* ------------------------------------------------- swap to host (NEXT #4) */
+/* -------------------------------------------------------------- swap to host */
 
 /* Swapping ("vLLM-and-PagedAttention-KR", "Scheduling": when blocks run out, a
  * whole sequence -- the latest arrival -- is evicted and its KV blocks move to
@@ -275,7 +278,7 @@ int kv_gather_blocks(const pkv_pool *pool, const int32_t *ids, int32_t n, const 
 int kv_scatter_blocks(const pkv_pool *pool, const int32_t *ids, int32_t n, const void *staging,
                       void *k_pool, void *v_pool, int32_t *d_status, void *stream);
 
-/* ---------------------------------------------------------- cache write (a3) */
+/* --------------------------------------------------------------- cache write */
 
 /* Store num_tokens new tokens' K and V rows into their slots ("가장 기본적인
  * decoding", steps 3-4: the new token's KV goes after the tokens already in its
@@ -290,7 +293,7 @@ int kv_cache_write(const pkv_pool *pool, const void *k_new, const void *v_new,
                    const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
                    void *v_pool, int32_t *d_status, void *stream);
 
-/* ------------------------------------------- paged decode attention (a4, a5) */
+/* ---------------------------------------------------- paged decode attention */
 
 /* Workspace bytes paged_decode_attention needs for these sizes (split-K
  * partials, work list, merge counters).  0 on a bad argument. */
@@ -342,7 +345,7 @@ int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *d_status, void *stream);
 
-/* ------------------------------------------ chunked-prefill attention (NEXT #2) */
+/* ------------------------------------------------- chunked-prefill attention */
 
 /* Workspace bytes paged_prefill_attention needs.  0 on a bad argument. */
 size_t paged_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,

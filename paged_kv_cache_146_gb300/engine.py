@@ -149,11 +149,11 @@ class DecodeEngine:
         self._used[self._set].record(self.torch.cuda.current_stream())
 
     def host_step(self) -> None:
-        """a1 + a2: the ledger step and the hand-off of its arrays to the device."""
+        """The ledger step and the hand-off of its arrays to the device."""
         self._stage()
 
     def write(self, k_new, v_new, d_slots=None) -> None:
-        """a3: cache write of K/V rows into their slots (this step's by default)."""
+        """Cache write of K/V rows into their slots (this step's by default)."""
         d_slots = self.d_slots if d_slots is None else d_slots
         if self.pool.is_q8:
             cache_write_q8(self.pool, k_new, v_new, d_slots, self.status)
@@ -162,7 +162,7 @@ class DecodeEngine:
         self._mark_used()
 
     def attend(self, q):
-        """a4/a5: paged attention of every sequence over its blocks."""
+        """Paged attention of every sequence over its blocks."""
         return self._attend_into(q, self.out)
 
     def _attend_into(self, q, out):
@@ -182,7 +182,7 @@ class DecodeEngine:
         return self.split
 
     def device_step(self, q, k_new, v_new):
-        """a3 + a4/a5: cache write of this step's K/V, then paged attention."""
+        """Cache write of this step's K/V, then paged attention."""
         self.write(k_new, v_new)
         return self.attend(q)
 
@@ -247,7 +247,7 @@ class DecodeEngine:
         return self._io
 
     def release(self, seqs) -> None:
-        """a6: finished sequences give back their blocks."""
+        """Finished sequences give back their blocks."""
         self._wait_copy()
         bs = self.pool.block_size
         for s in seqs:

@@ -190,6 +190,109 @@ def test_q8_cache_write_special_rows():
         assert (ks[np.isfinite(ks)] <= 65504).all()
 
 
+# The 8-bit write takes 16-token windows (whole blocks in one go) from 8192
+# windows of (16 tokens, kv head) up, one warp per row below that; each case
+# runs on both sides.
+BLOCK_MODE_WINDOWS = 8192
+
+
+@pytest.mark.parametrize("dt,reps", [("bf16", 1), ("f16", 1), ("bf16", 560), ("f16", 560)])
+def test_q8_cache_write_whole_and_partial_blocks(dt, reps):
+    """One call whose tokens fill some blocks whole (16 consecutive tokens in
+    slot order, at token offsets not a multiple of 16) and others not: a run
+    cut by a padding slot, a block written in reverse slot order, a block begun
+    before the first token of the call and one left open at its end (the
+    pattern repeated `reps` times over fresh blocks).  Every block's bytes
+    equal the oracle's, the padding slots' bytes stay untouched."""
+    rng = np.random.default_rng(17 if dt == "bf16" else 18)
+    bf, hkv, nb1 = dt == "bf16", 3, 8
+    one = np.concatenate([
+        3 * 16 + np.arange(8, 16),              # tokens 0..7: block 3, offsets 8..15
+        2 * 16 + np.arange(16),                 # tokens 8..23: block 2 whole
+        5 * 16 + np.arange(16),                 # tokens 24..39: block 5, token 28 padding
+        1 * 16 + np.arange(16)[::-1],           # tokens 40..55: block 1 in reverse order
+        0 * 16 + np.arange(16),                 # tokens 56..71: block 0 whole
+        6 * 16 + np.arange(8),                  # tokens 72..79: block 6, offsets 0..7
+    ]).astype(np.int64)
+    one[28] = -1
+    nb = nb1 * reps
+    slots = np.concatenate([np.where(one < 0, -1, one + 16 * nb1 * i) for i in range(reps)])
+    T = len(slots)
+    assert (-(-T // 16) * hkv >= BLOCK_MODE_WINDOWS) == (reps > 1)
+    k_rows = workloads.normal_bits(rng, (T, hkv, D), dt)
+    v_rows = workloads.normal_bits(rng, (T, hkv, D), dt)
+    pool = KVPool(nb, hkv, D, "q8_" + dt, device="cuda")
+    _fill_sentinel(pool)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache_write_q8(pool, to_torch(k_rows, bf, "cuda"), to_torch(v_rows, bf, "cuda"),
+                   torch.from_numpy(slots).cuda(), status)
+    assert status_check(status) == (0, 0)
+    ref = _oracle_pools(nb, hkv)
+    assert oracle.load().cache_write_q8(k_rows, v_rows, slots, ref, 16, bf) == 0
+    _assert_pools_equal(pool, ref)
+    k_codes = _host_pools(pool)[0]
+    assert (k_codes[5::nb1, :, 4] == 127).all()              # the padding tokens' slots
+
+
+def _all_pattern_rows(dt, seed):
+    """Every bf16 / fp16 bit pattern but NaN (±inf included), four times, as rows
+    [T][1][128]: once in groups of 32 neighbours by magnitude, three times
+    shuffled inside windows of about four octaves, so each value meets group
+    maxima from its own magnitude to about 16 times it."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    if dt == "bf16":
+        vals = (pats.astype(np.uint32) << 16).view(np.float32)
+        window = 512                              # 128 patterns per octave
+    else:
+        with np.errstate(invalid="ignore"):
+            vals = pats.view(np.float16).astype(np.float32)
+        window = 4096                             # 1024 patterns per octave
+    keep = ~np.isnan(vals)
+    pats, vals = pats[keep], vals[keep]
+    order = pats[np.argsort(np.abs(vals), kind="stable")]
+    rng = np.random.default_rng(seed)
+    passes = [order]
+    for _ in range(3):
+        p = order.copy()
+        for w in range(0, len(p), window):
+            rng.shuffle(p[w:w + window])
+        passes.append(p)
+    rows = []
+    for p in passes:
+        pad = (-len(p)) % 128
+        rows.append(np.concatenate([p, np.zeros(pad, np.uint16)]).reshape(-1, 1, 128))
+    return np.concatenate(rows)
+
+
+@pytest.mark.parametrize("dt,hkv,reps", [("bf16", 1, 1), ("f16", 1, 1), ("bf16", 2, 65),
+                                         ("f16", 2, 68)])
+def test_q8_cache_write_every_bit_pattern(dt, hkv, reps):
+    """The quantiser against the oracle on every input bit pattern (no NaN), bit
+    for bit, through the whole-block path (tokens in slot order) and the
+    per-token path (the same rows, slots shuffled); the rows repeated `reps`
+    times over `hkv` heads so that the larger cases write in 16-token windows."""
+    bf = dt == "bf16"
+    rows = _all_pattern_rows(dt, seed=3 if bf else 4)
+    half = len(rows) // 2
+    k_rows = np.tile(rows[:half], (reps, hkv, 1)).reshape(-1, hkv, D)
+    v_rows = np.tile(rows[half:2 * half], (reps, hkv, 1)).reshape(-1, hkv, D)
+    T = len(k_rows)
+    assert (-(-T // 16) * hkv >= BLOCK_MODE_WINDOWS) == (reps > 1)
+    nb = -(-T // 16)
+    o = oracle.load()
+    rng = np.random.default_rng(5)
+    for slots in (np.arange(T, dtype=np.int64), rng.permutation(nb * 16)[:T].astype(np.int64)):
+        pool = KVPool(nb, hkv, D, "q8_" + dt, device="cuda")
+        _fill_sentinel(pool)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        cache_write_q8(pool, to_torch(k_rows, bf, "cuda"), to_torch(v_rows, bf, "cuda"),
+                       torch.from_numpy(slots).cuda(), status)
+        assert status_check(status) == (0, 0)
+        ref = _oracle_pools(nb, hkv)
+        assert o.cache_write_q8(k_rows, v_rows, slots, ref, 16, bf) == 0
+        _assert_pools_equal(pool, ref)
+
+
 def test_q8_stale_slots_never_read():
     """Slots past each context hold codes 127 and NaN scales (the sentinel); the
     result must stay finite and match the oracle, which never reads them."""

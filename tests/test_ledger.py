@@ -1,5 +1,5 @@
 """The library's host ledger (C++) against the independent model, call by call,
-bit-exact (row a1/a2 of the step).  CPU only."""
+bit-exact (the ledger stages of the step).  CPU only."""
 import numpy as np
 import pytest
 
