@@ -493,7 +493,8 @@ def our_arm(args, world, rank, local):
 
 def prefill_arm(args, world, rank, local):
     """Chunked-prefill attention: 16 prompts of 2048 tokens (GQA 32/8, D 128,
-    bf16) whose K/V are cached, attended in one call; causal flops over time."""
+    bf16, or fp16 with --kv-dtype f16) whose K/V are cached, attended in one
+    call; causal flops over time."""
     import torch
     from paged_kv_cache_146_gb300 import (KVPool, cache_write, paged_prefill_attention,
                                           prefill_workspace_bytes, workloads)
@@ -504,14 +505,16 @@ def prefill_arm(args, world, rank, local):
     maxb = P // 16
     rng = np.random.default_rng(args.seed + rank)
     order = rng.permutation(S * maxb + 16).astype(np.int32)
-    pool = KVPool(S * maxb + 16, hkv, d, "bf16", free_order=order, device=dev)
+    kvd = args.kv_dtype
+    tdt = torch.bfloat16 if kvd == "bf16" else torch.float16
+    pool = KVPool(S * maxb + 16, hkv, d, kvd, free_order=order, device=dev)
     tables = np.full((S, maxb), -1, dtype=np.int32)
     slots = pool.append_slots(np.zeros(S, np.int32), np.full(S, P, np.int32), tables)
     gen = torch.Generator(device=dev)
     gen.manual_seed(args.seed + 17 + rank)
-    k = torch.randn(T, hkv, d, generator=gen, device=dev).to(torch.bfloat16)
-    v = torch.randn(T, hkv, d, generator=gen, device=dev).to(torch.bfloat16)
-    q = torch.randn(T, hq, d, generator=gen, device=dev).to(torch.bfloat16)
+    k = torch.randn(T, hkv, d, generator=gen, device=dev).to(tdt)
+    v = torch.randn(T, hkv, d, generator=gen, device=dev).to(tdt)
+    q = torch.randn(T, hq, d, generator=gen, device=dev).to(tdt)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     cache_write(pool, k, v, torch.from_numpy(slots).to(dev), status)
     d_tables = torch.from_numpy(tables).to(dev)
@@ -553,14 +556,16 @@ def prefill_arm(args, world, rank, local):
     line = {"metric": "chunked-prefill attention TFLOP/s", "value": round(tflops, 2),
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": kvd, "data": "synthetic",
             "config": {"workload": "prefill", "num_seqs": S, "prompt_tokens": P,
                        "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
                          "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
                          "traffic": None, "peak_kind": tkind,
                          "note": "tcgen05.mma kind::f16 (TMEM accumulators), 128 query rows x "
-                                 "64-key tiles, two query tiles per CTA, P as bf16 high + low parts"},
+                                 "64-key tiles, two query tiles per CTA, "
+                                 + ("P as bf16 high + low parts" if kvd == "bf16" else
+                                    "P as one fp16 part")},
             "gpu_launches": 2 * args.steps}
     print(json.dumps(line), flush=True)
 
@@ -722,6 +727,8 @@ def main():
                     help="sequences per GPU (256 is the workload; fewer only for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "f16"],
+                    help="cache dtype of the prefill workload")
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture, if current")
