@@ -41,6 +41,7 @@ LENGTHS = {
     "opt13b": "U[128, 2048]",
     "shared_prefix": "1024 shared + U[64, 512] private",
 }
+DECODE_WORKLOADS = tuple(LENGTHS)
 
 
 def peaks():
@@ -72,10 +73,11 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(workload: str = "gqa_long"):
     """DRAM bytes (read + write) per attention call from the committed ncu
-    launch-list summary, or None when the kernel sources changed since then."""
-    prof = os.path.join(ROOT, "profiles", "paged_decode_gqa_long_launches.md")
+    launch-list summary of the workload (at its default size), or None when there
+    is none or the kernel sources changed since it was taken."""
+    prof = os.path.join(ROOT, "profiles", f"paged_decode_{workload}_launches.md")
     try:
         fields = dict(line.split(": ", 1) for line in open(prof).read().splitlines()
                       if line.startswith(("attention_traffic_bytes_per_launch:", "source_sha256_16:")))
@@ -191,17 +193,41 @@ def barrier(world):
 # ---------------------------------------------------------------- oracle arm
 class OracleSample:
     """The oracle (fp64 C, all host cores) on the first ``k`` sequences of the
-    workload: the same length law, shapes and dtype, bounded in size."""
+    named decode workload: the same length law, shapes and dtype, bounded in
+    size.  A shared prefix is stored with each sampled sequence (the oracle
+    gathers every sequence's context on its own, so the work is the same)."""
 
-    def __init__(self, seed: int, k: int, q8: bool = False):
+    def __init__(self, seed: int, k: int, q8: bool = False, workload: str = "gqa_long"):
+        import dataclasses
+
         import oracle
         from oracle.allocator_model import BlockLedger
         from paged_kv_cache_146_gb300 import workloads
 
         self.o = oracle.load()
         self.threads = self.o.max_threads()
-        w = workloads.gqa_long(seed, num_seqs=k, growth_tokens=16)
+        if workload in ("gqa_long", "gqa_long_q8"):
+            w = workloads.gqa_long(seed, num_seqs=k, growth_tokens=16)
+            full = 256
+        else:
+            wf = workloads.CONFIGS[workload](seed)
+            full = wf.num_seqs
+            k = min(k, full)
+            prior, new = wf.prior_lens[:k].copy(), wf.new_tokens[:k].copy()
+            need = int(sum(-(-int(a + b) // 16) for a, b in zip(prior, new)))
+            w = dataclasses.replace(
+                wf, prior_lens=prior, new_tokens=new, num_blocks=need,
+                free_order=np.random.default_rng(seed + 7).permutation(need).astype(np.int32))
         v = workloads.host_values(w)
+        k_prompt, v_prompt = v["k_prompt"], v["v_prompt"]
+        if w.shared_prefix_tokens:          # rows of every cached token, sequence after sequence
+            P, off, ks, vs = w.shared_prefix_tokens, 0, [], []
+            for s in range(k):
+                n = int(w.prior_lens[s]) - P
+                ks += [v["k_shared"], k_prompt[off:off + n]]
+                vs += [v["v_shared"], v_prompt[off:off + n]]
+                off += n
+            k_prompt, v_prompt = np.concatenate(ks), np.concatenate(vs)
         led = BlockLedger(w.num_blocks, 16, w.free_order)
         tables = [[-1] * w.max_blocks_per_seq for _ in range(k)]
         slots_p = led.append([0] * k, [int(x) for x in w.prior_lens], tables)
@@ -213,13 +239,12 @@ class OracleSample:
             self.pools = (np.zeros(shape, np.int8), np.zeros((nb, hkv, d, 16), np.int8),
                           np.zeros((nb, hkv, 16, d // 32), np.uint16),
                           np.zeros((nb, hkv, 16, d // 32), np.uint16))
-            for kr, vr, sl in ((v["k_prompt"], v["v_prompt"], slots_p),
-                               (v["k_new"], v["v_new"], slots_n)):
+            for kr, vr, sl in ((k_prompt, v_prompt, slots_p), (v["k_new"], v["v_new"], slots_n)):
                 self.o.cache_write_q8(kr, vr, np.array(sl, dtype=np.int64), self.pools, 16, True)
         else:
             self.kp = np.zeros(shape, dtype=np.uint16)
             self.vp = np.zeros(shape, dtype=np.uint16)
-            self.o.cache_write(v["k_prompt"], v["v_prompt"], np.array(slots_p, dtype=np.int64),
+            self.o.cache_write(k_prompt, v_prompt, np.array(slots_p, dtype=np.int64),
                                self.kp, self.vp, 16)
             self.o.cache_write(v["k_new"], v["v_new"], np.array(slots_n, dtype=np.int64),
                                self.kp, self.vp, 16)
@@ -231,7 +256,9 @@ class OracleSample:
         self.nbytes = self.tokens * w.num_kv_heads * per_head + \
             2 * k * w.num_q_heads * w.head_dim * 2 + \
             4 * int(sum(-(-int(n) // 16) for n in self.lens)) + 4 * k
-        self.desc = f"first {k} of 256 sequences ({self.tokens} context tokens), one decode call"
+        self.desc = (f"first {k} of {full} sequences of {workload} ({self.tokens} context tokens"
+                     + (", each storing the shared prefix itself" if w.shared_prefix_tokens else "")
+                     + "), one decode call")
 
     def run(self) -> float:
         t0 = time.perf_counter()
@@ -240,16 +267,17 @@ class OracleSample:
                                    self.threads)
         else:
             self.o.paged_decode(self.q, self.kp, self.vp, self.tables, self.lens, self.w.scale,
-                                True, self.threads)
+                                self.w.is_bf16, self.threads)
         return time.perf_counter() - t0
 
 
-def oracle_calibrated(seed: int, target_s: float, q8: bool = False) -> OracleSample:
+def oracle_calibrated(seed: int, target_s: float, q8: bool = False,
+                      workload: str = "gqa_long") -> OracleSample:
     """An oracle sample whose one call takes about ``target_s`` seconds."""
-    probe = OracleSample(seed, 2, q8)
+    probe = OracleSample(seed, 2, q8, workload)
     dt = probe.run()
     k = int(min(256, max(2, round(2 * target_s / max(dt, 1e-3)))))
-    return OracleSample(seed, k, q8)
+    return OracleSample(seed, k, q8, workload)
 
 
 def reference_arm(args, world, rank):
@@ -257,7 +285,17 @@ def reference_arm(args, world, rank):
     if rank != 0:
         return
     per_step = min(args.ref_seconds, 150.0 / (args.steps + args.warmup))
-    sample = oracle_calibrated(args.seed, per_step)
+    if args.workload not in DECODE_WORKLOADS:
+        print(json.dumps({"impl": "reference", "unavailable":
+                          f"the oracle baseline covers the decode workloads, not {args.workload}"}),
+              flush=True)
+        return
+    from paged_kv_cache_146_gb300 import workloads
+    q8 = args.workload == "gqa_long_q8"
+    sample = oracle_calibrated(args.seed, per_step, q8, args.workload)
+    w = sample.w
+    w_full_seqs = (workloads.CONFIGS[args.workload](args.seed).num_seqs
+                   if args.workload in workloads.CONFIGS and args.workload != "gqa_long" else 256)
     for _ in range(args.warmup):
         sample.run()
     secs = [sample.run() for _ in range(args.steps)]
@@ -266,9 +304,13 @@ def reference_arm(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * statistics.median(secs), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "gqa_long", "num_seqs": 256, "q_heads": 32, "kv_heads": 8,
-                       "head_dim": 128, "block_size": 16, "kv_dtype": "bf16",
-                       "lengths": "clip(round(LogNormal(ln 4096, 1)), 64, 32768)"},
+            "config": {"workload": args.workload,
+                       "num_seqs": args.num_seqs if args.workload in ("gqa_long", "gqa_long_q8")
+                       else w_full_seqs,
+                       "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                       "head_dim": w.head_dim, "block_size": 16,
+                       "kv_dtype": "q8_bf16" if q8 else w.dtype, "lengths": LENGTHS[args.workload],
+                       "shared_prefix_tokens": w.shared_prefix_tokens},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": sample.threads,
                              "kind": "oracle", "sample": sample.desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -451,11 +493,21 @@ def our_arm(args, world, rank, local):
         return
     cpu = None
     if args.cpu_seconds > 0 and world == 1:
-        sample = oracle_calibrated(args.seed, args.cpu_seconds, q8)
+        sample = oracle_calibrated(args.seed, args.cpu_seconds, q8, args.workload)
         dt = sample.run()
         cpu = {"value": round(sample.nbytes / dt / 1e9, 4), "unit": "GB/s",
                "cores": sample.threads, "kind": "oracle", "sample": sample.desc,
                "seconds": round(dt, 2)}
+    traffic = args.traffic
+    if traffic is None and args.num_seqs == 256 and args.seed == 0 and not q8:
+        traffic = profiled_traffic(args.workload)
+    # where cached bytes are shared (a common prefix read by many sequences)
+    # DRAM moves fewer bytes than the algorithmic count: report both
+    dram = None
+    if traffic is not None and args.workload == "shared_prefix":
+        dram = {"bytes_per_launch": int(traffic),
+                "gbs": round(traffic / (attn_avg_ms * 1e-3) / 1e9, 2),
+                "pct_of_peak": round(100.0 * traffic / (attn_avg_ms * 1e-3) / 1e9 / peak, 2)}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -467,15 +519,16 @@ def our_arm(args, world, rank, local):
                    "shared_prefix_tokens": w.shared_prefix_tokens,
                    "mean_context": round(toks_total / args.steps / S, 1),
                    "pool_blocks": w.num_blocks,
-                   "l2": "inputs larger than L2 (KV per step ~%.1f GB vs 129 MB L2)" % (bytes_per_launch / 1e9),
+                   "l2": ("inputs larger than L2 (KV per step ~%.1f GB vs 129 MB L2)" % (bytes_per_launch / 1e9)
+                          if not w.shared_prefix_tokens else
+                          "unique KV larger than L2; the shared prefix (%d tokens) is re-read from L2"
+                          % w.shared_prefix_tokens),
                    "step": "host ledger + table/lens/slots H2D + cache_write + paged attention"},
         "seq_tokens_per_s": round(toks_all / (elapsed_ms * 1e-3), 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": args.traffic if args.traffic is not None else (
-                         profiled_traffic() if (args.workload, args.num_seqs, args.seed) == ("gqa_long", 256, 0)
-                         else None),
+                     "traffic": traffic,
                      "peak_kind": peak_kind,
                      "kernel": ("paged_decode_attention_q8" if q8 else "paged_decode_attention")
                      + " (prep + main + merge kernels)",
@@ -484,6 +537,7 @@ def our_arm(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "cache_write": cache_write_line,
+        **({"dram": dram} if dram else {}),
         "gpu_launches": (4 if eng.maxb > (eng.split_for_step() or default_split()) else 3)
         * args.steps,
         "clocks": clk,
