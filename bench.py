@@ -574,7 +574,11 @@ def prefill_arm(args, world, rank, local):
     d_tables = torch.from_numpy(tables).to(dev)
     qs = torch.from_numpy(np.arange(0, T + 1, P, dtype=np.int32)).to(dev)
     lens = torch.full((S,), P, dtype=torch.int32, device=dev)
-    ws = torch.empty(prefill_workspace_bytes(S, T, hq, hkv), dtype=torch.uint8, device=dev)
+    # bf16 pools: room for the fp16 copy of V (made inside every timed call)
+    # unless --prefill-plain asks for P V with two bf16 parts of P
+    staged = kvd == "bf16" and not args.prefill_plain
+    extra = (d, maxb) if staged else ()
+    ws = torch.empty(prefill_workspace_bytes(S, T, hq, hkv, *extra), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     scale = 1.0 / math.sqrt(d)
 
@@ -618,9 +622,11 @@ def prefill_arm(args, world, rank, local):
                          "traffic": None, "peak_kind": tkind,
                          "note": "tcgen05.mma kind::f16 (TMEM accumulators), 128 query rows x "
                                  "64-key tiles, two query tiles per CTA, "
-                                 + ("P as bf16 high + low parts" if kvd == "bf16" else
+                                 + ("P as one fp16 part, V copied to fp16 (scaled per sequence and kv "
+                                    "head) by two kernels inside each call" if staged else
+                                    "P as bf16 high + low parts" if kvd == "bf16" else
                                     "P as one fp16 part")},
-            "gpu_launches": 2 * args.steps}
+            "gpu_launches": (4 if staged else 2) * args.steps}
     print(json.dumps(line), flush=True)
 
 
@@ -783,6 +789,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "f16"],
                     help="cache dtype of the prefill workload")
+    ap.add_argument("--prefill-plain", action="store_true",
+                    help="prefill on a bf16 pool without the fp16 copy of V")
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture, if current")

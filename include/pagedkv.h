@@ -351,6 +351,20 @@ int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
 size_t paged_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
                                      int32_t num_kv_heads);
 
+/* Workspace bytes with room for an fp16 copy of V (bf16 pools; an addition of
+ * this library, not in the pages).  Given at least this much,
+ * paged_prefill_attention over a bf16 pool first copies V of every token it
+ * will attend to (2 * head_dim bytes per token and kv head, for
+ * num_seqs * max_blocks_per_seq blocks) as fp16, scaled per (sequence, kv
+ * head) by a power of two that puts the largest |v| just under 2^16, and then
+ * forms P V with one fp16 part of P instead of two bf16 parts.  Every V value
+ * within 2^30 of its (sequence, kv head)'s largest converts exactly; smaller
+ * ones round to fp16's subnormal spacing.  The result meets the same
+ * tolerance; fp16 pools ignore the extra room.  0 on a bad argument. */
+size_t paged_prefill_workspace_bytes_staged(int32_t num_seqs, int32_t num_tokens,
+                                            int32_t num_q_heads, int32_t num_kv_heads,
+                                            int32_t head_dim, int32_t max_blocks_per_seq);
+
 /* Attention of a chunk of prompt tokens per sequence over the paged cache
  * ("vLLM과 Ollama의 차이": chunked prefill cuts a long prompt into chunks that
  * run beside the decoding sequences; "LLM 추론 배칭 전략 정리", section 0).
@@ -365,7 +379,8 @@ size_t paged_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32
  * context exceeds its table row gets zero rows and PKV_DEV_BAD_LEN; bad table
  * entries set PKV_DEV_BAD_BLOCK.  Requirements as paged_decode_attention
  * (block_size 16, head_dim 64 or 128, G <= 16); workspace of
- * paged_prefill_workspace_bytes(...) bytes, 256-byte aligned.
+ * paged_prefill_workspace_bytes(...) bytes (or ..._staged(...) for the fp16
+ * copy of V), 256-byte aligned.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA. */
 int paged_prefill_attention(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
                             const void *v_pool, const int32_t *block_tables,

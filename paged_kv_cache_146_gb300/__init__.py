@@ -367,8 +367,17 @@ def paged_decode_attention_noalloc(pool: KVPool, q, block_tables, context_lens, 
 
 
 def prefill_workspace_bytes(num_seqs: int, num_tokens: int, num_q_heads: int,
-                            num_kv_heads: int) -> int:
-    return lib().paged_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, num_kv_heads)
+                            num_kv_heads: int, head_dim: int | None = None,
+                            max_blocks_per_seq: int | None = None) -> int:
+    """Workspace bytes of ``paged_prefill_attention``; with ``head_dim`` and
+    ``max_blocks_per_seq`` also room for the fp16 copy of V that a bf16 pool
+    then uses (one fp16 part of P in P V instead of two bf16 parts)."""
+    if head_dim is None and max_blocks_per_seq is None:
+        return lib().paged_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, num_kv_heads)
+    if head_dim is None or max_blocks_per_seq is None:
+        raise ValueError("head_dim and max_blocks_per_seq go together")
+    return lib().paged_prefill_workspace_bytes_staged(num_seqs, num_tokens, num_q_heads,
+                                                      num_kv_heads, head_dim, max_blocks_per_seq)
 
 
 def paged_prefill_attention(pool: KVPool, q, block_tables, query_start, context_lens,

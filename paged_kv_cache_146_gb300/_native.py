@@ -54,6 +54,7 @@ SIGNATURES = [
      [_p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _f32, _i32, _p, _sz, _p, _p]),
     ("paged_decode_default_split", _i32, []),
     ("paged_prefill_workspace_bytes", _sz, [_i32, _i32, _i32, _i32]),
+    ("paged_prefill_workspace_bytes_staged", _sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     ("paged_prefill_attention", ctypes.c_int,
      [_p, _p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _f32, _p, _sz, _p, _p]),
     ("paged_decode_attention_noalloc", ctypes.c_int,

@@ -16,6 +16,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -40,7 +41,21 @@ struct Params {
     int2 *items;                    // (sequence, tile)
     int64_t max_items;
     int32_t *status;
+    // fp16 copy of V (bf16 pools with a workspace that holds it; else null):
+    // [num_seqs * max_blocks_per_seq][Hkv][16][D] by logical block, and per
+    // (sequence, kv head) the largest bf16 exponent field of its V
+    uint16_t *v16;
+    int32_t *v_emax;                // [num_seqs][Hkv]
 };
+
+// Scale of a (sequence, kv head)'s fp16 copy of V: v16 = v * 2^-k with
+// k = E - 142, E the largest bf16 exponent field of its V, so the largest |v|
+// (below 2^(E - 126)) lands in [2^15, 2^16), under fp16's largest value; k is
+// clamped to [-100, 113] so both 2^k and 2^-k are normal fp32 numbers.
+__device__ __forceinline__ int v16_shift(int emax)
+{
+    return min(113, max(-100, emax - 142));
+}
 
 // (sequence, tile) pairs and zero rows for chunks of invalid sequences.
 __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t head_dim)
@@ -50,6 +65,8 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_launch_dependents();
     if (tid == 0) carry = 0;
+    if (p.v_emax)       // the staging kernels that follow take maxima into these
+        for (int i = tid; i < p.num_seqs * p.num_kv_heads; i += 1024) p.v_emax[i] = 0;
     __syncthreads();
     const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
     for (int base = 0; base < p.num_seqs; base += 1024) {
@@ -108,6 +125,96 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
         const bool fits = (int64_t)carry <= p.max_items;   // overlapping row ranges overflow it
         if (!fits) atomicOr(p.status, PKV_DEV_BAD_LEN);
         p.header[0] = fits ? carry : 0;
+    }
+}
+
+// ======================================= fp16 copy of V (bf16 pools)
+// With bf16 K/V, P V needs P as two bf16 parts (one bf16 part is too coarse
+// for the tolerance); with V in fp16, one fp16 part of P will do and the P V
+// products halve.  So, when the caller's workspace holds it, V of every
+// attended token is copied once per call as fp16, scaled per (sequence, kv
+// head) by a power of two (v16_shift): a bf16 significand (8 bits) fits in
+// fp16's 11, so every value within 2^30 of the largest converts exactly; only
+// values below that (fp16 subnormals) round, by at most 2^(k-25).  The
+// attention kernel multiplies its result by 2^k.  Two passes over 256-token
+// chunks: the largest exponent field (atomicMax into v_emax, zeroed by the
+// prep kernel), then the conversion.  Tokens past a sequence's length are not
+// written (the attention kernel zeroes those V rows in shared memory), nor
+// are blocks with a bad table entry (flagged by the attention kernel).
+constexpr int kStageTokens = 256;
+
+__device__ __forceinline__ int stage_len(const Params &p, int s)
+{
+    const int L = __ldg(p.context_lens + s);
+    return (L < 0 || (int64_t)L > (int64_t)p.max_blocks_per_seq * kBlock) ? 0 : L;
+}
+
+template <int D, bool CONVERT>
+__global__ void __launch_bounds__(256) prefill_v16_kernel(const uint16_t *__restrict__ v_pool,
+                                                          const Params p)
+{
+    // a CTA takes 256 tokens (16 blocks) of one (sequence, kv head); a block's
+    // slab is 16 rows of D values, one 16-byte piece per thread (D = 128) or
+    // per half of the threads (D = 64)
+    constexpr int kBlocks = kStageTokens / kBlock;
+    constexpr int kPieces = kBlock * D / 8;             // 16-byte pieces per slab
+    constexpr int kPerThread = (kPieces + 255) / 256;
+    const int Hkv = p.num_kv_heads;
+    const int chunks = (p.max_blocks_per_seq * kBlock + kStageTokens - 1) / kStageTokens;
+    const int64_t units = (int64_t)p.num_seqs * Hkv * chunks;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const int64_t sg = u / chunks;
+        const int c = (int)(u - sg * chunks);
+        const int s = (int)(sg / Hkv), g = (int)(sg - (int64_t)s * Hkv);
+        const int L = stage_len(p, s), t0 = c * kStageTokens;
+        if (t0 >= L) continue;                      // the same for the whole CTA
+        const int j0 = t0 / kBlock, nblk = min(kBlocks, (L - t0 + kBlock - 1) / kBlock);
+        const int32_t *row = p.block_tables + (int64_t)s * p.max_blocks_per_seq + j0;
+        float scale = 1.f;
+        if constexpr (CONVERT) scale = __int_as_float((127 - v16_shift(p.v_emax[sg])) << 23);
+        unsigned emax2 = 0;                         // two exponent fields per word
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int piece = threadIdx.x + 256 * k;
+            if (piece >= kPieces) break;
+            const int r = piece / (D / 8), q = piece % (D / 8);   // row (token) in the block
+            uint4 w[kBlocks];
+            bool ok[kBlocks];
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b) {     // every load of the thread in flight at once
+                const int id = b < nblk ? __ldg(row + b) : -1;
+                // the largest exponent counts visible tokens only
+                ok[b] = id >= 0 && id < p.num_blocks && (CONVERT || t0 + b * kBlock + r < L);
+                w[b] = ok[b] ? __ldg(reinterpret_cast<const uint4 *>(
+                                       v_pool + (((int64_t)id * Hkv + g) * kBlock + r) * D) + q)
+                             : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b) {
+                if (!ok[b]) continue;
+                if constexpr (CONVERT) {
+                    const uint32_t in[4] = {w[b].x, w[b].y, w[b].z, w[b].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __half2 h = __floats2half2_rn(__uint_as_float(in[i] << 16) * scale,
+                                                            __uint_as_float(in[i] & 0xffff0000u) * scale);
+                        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+                    }
+                    *(reinterpret_cast<uint4 *>(
+                          p.v16 + ((((int64_t)s * p.max_blocks_per_seq + j0 + b) * Hkv + g) * kBlock + r) * D) +
+                      q) = make_uint4(o[0], o[1], o[2], o[3]);
+                } else {
+                    emax2 = __vmaxu2(emax2, __vmaxu2(__vmaxu2(w[b].x & 0x7f807f80u, w[b].y & 0x7f807f80u),
+                                                     __vmaxu2(w[b].z & 0x7f807f80u, w[b].w & 0x7f807f80u)));
+                }
+            }
+        }
+        if constexpr (!CONVERT) {
+            unsigned e = max((emax2 >> 7) & 0xffu, (emax2 >> 23) & 0xffu);
+            e = __reduce_max_sync(kFull, e);
+            if ((threadIdx.x & 31) == 0 && e > 0) atomicMax(p.v_emax + sg, (int)e);
+        }
     }
 }
 
@@ -245,11 +352,15 @@ __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int
     return it;
 }
 
-template <int D, bool BF16>
+// VS: V comes from the fp16 copy (tmV maps it; bf16 pools only), so P V takes
+// one fp16 part of P and the result is scaled by 2^k.
+template <int D, bool BF16, bool VS>
 __global__ void __launch_bounds__(kThreads)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmQ, const Params p)
 {
+    static_assert(BF16 || !VS, "fp16 pools take V as it is");
+    constexpr bool kTwoParts = BF16 && !VS;    // P as bf16 high + low parts
     using E = Elem<BF16>;
     using T = typename E::T;
     using LY = Layout<D>;
@@ -345,11 +456,15 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
                         const int y = (ids[b] * Hkv + it.g) * kBlock;
+                        // the fp16 copy is by logical block
+                        const int yv = VS ? ((it.s * p.max_blocks_per_seq + min(4 * t + b, nb - 1)) * Hkv +
+                                             it.g) * kBlock
+                                          : y;
 #pragma unroll
                         for (int rg = 0; rg < LY::kRegions; ++rg) {
                             const uint32_t off = rg * kKeys * 128 + b * kBlock * 128;
                             tma_load_2d(ks + off, &tmK, rg * 64, y, fb);
-                            tma_load_2d(vs + off, &tmV, rg * 64, y, fb);
+                            tma_load_2d(vs + off, &tmV, rg * 64, yv, fb);
                         }
                     }
                 }
@@ -372,7 +487,7 @@ __global__ void __launch_bounds__(kThreads)
         if (lane == 0) {
             const int gr = warp - kIssuer;
             const uint32_t id_qk = tc::idesc_f16(BF16, kRows, kKeys, 0, 0);
-            const uint32_t id_pv = tc::idesc_f16(BF16, kRows, D, 0, 1);
+            const uint32_t id_pv = tc::idesc_f16(kTwoParts, kRows, D, 0, 1);   // P and V: same type
             const uint32_t q_a = smem_addr(q_s) + gr * LY::kQBytes, st_a = smem_addr(stage_s);
             const uint32_t o_t = tmem + 256 + 128 * gr;
             uint32_t tg = 0, it_cnt = 0;
@@ -388,7 +503,7 @@ __global__ void __launch_bounds__(kThreads)
                 tc::fence_after_sync();
                 const uint32_t pt = tmem + 64 * (2 * gr + (t & 1u));   // P of tile t
 #pragma unroll
-                for (int part = 0; part < (BF16 ? 2 : 1); ++part)
+                for (int part = 0; part < (kTwoParts ? 2 : 1); ++part)
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk) {
                         const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
@@ -518,10 +633,10 @@ __global__ void __launch_bounds__(kThreads)
                         }
                         const uint64_t pp = pack2f(p0, p1);
                         lsum2 = add2f(lsum2, pp);
-                        if constexpr (BF16)
+                        if constexpr (kTwoParts)
                             split_hi_lo<true>(p0, p1, pp, hi[c / 2], lo[c / 2]);
                         else                   // fp16 (relative error <= 2^-11): one part
-                            hi[c / 2] = E::pack(p0, p1);
+                            hi[c / 2] = Elem<false>::pack(p0, p1);
                     }
                 };
                 if (cross) weights(std::true_type{});
@@ -550,7 +665,7 @@ __global__ void __launch_bounds__(kThreads)
                 // P of this tile over its own S columns (already read): high part
                 // in the first 32, low part in the next 32
                 tc::tmem_st32(lane_base + s_col + 64 * sb, hi);
-                if constexpr (BF16) tc::tmem_st32(lane_base + s_col + 64 * sb + 32, lo);
+                if constexpr (kTwoParts) tc::tmem_st32(lane_base + s_col + 64 * sb + 32, lo);
                 // zero the V rows of keys past the last visible one (last tile only)
                 const int nvis = it.nkeys - k0;
                 if (nvis < kKeys) {      // both groups write the same zeros, each before its P
@@ -588,14 +703,22 @@ __global__ void __launch_bounds__(kThreads)
                 uint32_t v[32];
                 tc::tmem_ld32(lane_base + o_col + c0, v);
                 tc::tmem_wait_ld();
+                if constexpr (VS) {     // O / l in the fp16 copy's units, then times 2^k
+                    const float p2k = __int_as_float(
+                        (127 + v16_shift(p.v_emax[(size_t)it.s * Hkv + it.g])) << 23);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        v[c] = __float_as_uint(__uint_as_float(v[c]) * inv * p2k);
+                }
+                const float vin = VS ? 1.f : inv;
                 if (valid) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 8) {
                         uint4 w;
-                        w.x = bad ? 0u : E::pack(__uint_as_float(v[c]) * inv, __uint_as_float(v[c + 1]) * inv);
-                        w.y = bad ? 0u : E::pack(__uint_as_float(v[c + 2]) * inv, __uint_as_float(v[c + 3]) * inv);
-                        w.z = bad ? 0u : E::pack(__uint_as_float(v[c + 4]) * inv, __uint_as_float(v[c + 5]) * inv);
-                        w.w = bad ? 0u : E::pack(__uint_as_float(v[c + 6]) * inv, __uint_as_float(v[c + 7]) * inv);
+                        w.x = bad ? 0u : E::pack(__uint_as_float(v[c]) * vin, __uint_as_float(v[c + 1]) * vin);
+                        w.y = bad ? 0u : E::pack(__uint_as_float(v[c + 2]) * vin, __uint_as_float(v[c + 3]) * vin);
+                        w.z = bad ? 0u : E::pack(__uint_as_float(v[c + 4]) * vin, __uint_as_float(v[c + 5]) * vin);
+                        w.w = bad ? 0u : E::pack(__uint_as_float(v[c + 6]) * vin, __uint_as_float(v[c + 7]) * vin);
                         *reinterpret_cast<uint4 *>(out + c0 + c) = w;
                     }
                 }
@@ -624,6 +747,21 @@ static size_t ws_bytes(int64_t S, int64_t T, int64_t G)
     return 256 + align256((size_t)max_items(S, T, tile_tokens((int)G)) * 8);
 }
 
+// The workspace with room for the fp16 copy of V after the work list: the
+// per-(sequence, kv head) exponent maxima, then [S * maxb][Hkv][16][D] fp16.
+struct StagedLayout {
+    size_t emax, v16, total;
+};
+static StagedLayout staged_layout(int64_t S, int64_t T, int64_t G, int64_t Hkv, int64_t D,
+                                  int64_t maxb)
+{
+    StagedLayout l;
+    l.emax = ws_bytes(S, T, G);
+    l.v16 = l.emax + align256((size_t)(S * Hkv) * 4);
+    l.total = l.v16 + align256((size_t)(S * maxb) * Hkv * kBlock * D * 2);
+    return l;
+}
+
 using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
 
 static EncodeFn encode_fn()
@@ -641,21 +779,27 @@ static EncodeFn encode_fn()
     return fn;
 }
 
-static bool make_pool_map(CUtensorMap *map, const void *pool, const PoolGeometry &g)
+// Rows of head_dim values (a pool viewed as [blocks * Hkv * 16][D], or the fp16
+// copy of V as [S * maxb * Hkv * 16][D]); a box is 16 rows of 64 values.
+static bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows, int head_dim, bool bf16)
 {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)g.head_dim,
-                          (cuuint64_t)g.num_blocks * g.num_kv_heads * g.block_size};
-    cuuint64_t strides[1] = {(cuuint64_t)g.head_dim * 2};
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
     cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kBlock};
     cuuint32_t estr[2] = {1, 1};
-    return enc(map, g.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-               2, const_cast<void *>(pool), dims, strides, box, estr,
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+               2, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_pool_map(CUtensorMap *map, const void *pool, const PoolGeometry &g)
+{
+    return make_rows_map(map, pool, (int64_t)g.num_blocks * g.num_kv_heads * g.block_size,
+                         g.head_dim, g.dtype == PKV_BF16);
 }
 
 // Query rows [T][Hq][D] as a 4-D view (D, G, Hkv, T): a box (64, G, 1, QT)
@@ -678,15 +822,19 @@ static bool make_q_map(CUtensorMap *map, const void *q, int64_t T, int Hkv, int 
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
 
-static bool pick_tc(int D, bool bf16, TcKernelFn *fn, int *smem)
+static bool pick_tc(int D, bool bf16, bool staged, TcKernelFn *fn, int *smem)
 {
     if (D == 128) {
-        *fn = bf16 ? &tcp::prefill_tc_kernel<128, true> : &tcp::prefill_tc_kernel<128, false>;
+        *fn = !bf16 ? &tcp::prefill_tc_kernel<128, false, false>
+              : staged ? &tcp::prefill_tc_kernel<128, true, true>
+                       : &tcp::prefill_tc_kernel<128, true, false>;
         *smem = tcp::Layout<128>::kTotal;
         return true;
     }
     if (D == 64) {
-        *fn = bf16 ? &tcp::prefill_tc_kernel<64, true> : &tcp::prefill_tc_kernel<64, false>;
+        *fn = !bf16 ? &tcp::prefill_tc_kernel<64, false, false>
+              : staged ? &tcp::prefill_tc_kernel<64, true, true>
+                       : &tcp::prefill_tc_kernel<64, true, false>;
         *smem = tcp::Layout<64>::kTotal;
         return true;
     }
@@ -737,6 +885,19 @@ extern "C" size_t paged_prefill_workspace_bytes(int32_t num_seqs, int32_t num_to
     return pkv::prefill::ws_bytes(num_seqs, num_tokens, num_q_heads / num_kv_heads);
 }
 
+extern "C" size_t paged_prefill_workspace_bytes_staged(int32_t num_seqs, int32_t num_tokens,
+                                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                                       int32_t head_dim, int32_t max_blocks_per_seq)
+{
+    if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 16 ||
+        (head_dim != 64 && head_dim != 128) || max_blocks_per_seq <= 0)
+        return 0;
+    return pkv::prefill::staged_layout(num_seqs, num_tokens, num_q_heads / num_kv_heads,
+                                       num_kv_heads, head_dim, max_blocks_per_seq)
+        .total;
+}
+
 extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const void *q,
                                        const void *k_pool, const void *v_pool,
                                        const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -754,9 +915,15 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_INVALID_ARG;
     const int G = num_q_heads / g.num_kv_heads;
     if (g.block_size != pkv::kBlock || G > 16) return PKV_ERR_UNSUPPORTED;
+    // a bf16 pool whose caller gave room for the fp16 copy of V takes it
+    const StagedLayout sl = staged_layout(num_seqs, num_tokens, G, g.num_kv_heads, g.head_dim,
+                                          max_blocks_per_seq);
+    const bool staged = g.dtype == PKV_BF16 && workspace_bytes >= sl.total &&
+                        (int64_t)num_seqs * max_blocks_per_seq * g.num_kv_heads * pkv::kBlock <
+                            ((int64_t)1 << 31);
     TcKernelFn fn;
     int smem = 0;
-    if (!pick_tc(g.head_dim, g.dtype == PKV_BF16, &fn, &smem)) return PKV_ERR_UNSUPPORTED;
+    if (!pick_tc(g.head_dim, g.dtype == PKV_BF16, staged, &fn, &smem)) return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
     if (!out || !q || !k_pool || !v_pool || !block_tables || !query_start || !context_lens ||
         !workspace || !d_status)
@@ -769,8 +936,14 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     if (workspace_bytes < ws_bytes(num_seqs, num_tokens, G)) return PKV_ERR_INVALID_ARG;
     if ((int64_t)g.num_blocks * g.num_kv_heads * g.block_size > (int64_t)1 << 31)
         return PKV_ERR_UNSUPPORTED;
+    char *ws = static_cast<char *>(workspace);
     CUtensorMap tk, tv, tq;
-    if (!make_pool_map(&tk, k_pool, g) || !make_pool_map(&tv, v_pool, g) ||
+    const bool vmap = staged ? make_rows_map(&tv, ws + sl.v16,
+                                             (int64_t)num_seqs * max_blocks_per_seq * g.num_kv_heads *
+                                                 pkv::kBlock,
+                                             g.head_dim, false)
+                             : make_pool_map(&tv, v_pool, g);
+    if (!make_pool_map(&tk, k_pool, g) || !vmap ||
         !make_q_map(&tq, q, num_tokens, g.num_kv_heads, G, g.head_dim, tcp::kRows / G,
                     g.dtype == PKV_BF16))
         return PKV_ERR_CUDA;
@@ -794,6 +967,8 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     prm.items = reinterpret_cast<int2 *>(static_cast<char *>(workspace) + 256);
     prm.max_items = max_items(num_seqs, num_tokens, prm.tile_tokens);
     prm.status = d_status;
+    prm.v16 = staged ? reinterpret_cast<uint16_t *>(ws + sl.v16) : nullptr;
+    prm.v_emax = staged ? reinterpret_cast<int32_t *>(ws + sl.emax) : nullptr;
 
     int sms = 0;
     const int per_sm = resident(reinterpret_cast<const void *>(fn), smem, tcp::kThreads, &sms);
@@ -804,6 +979,20 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     prefill_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (staged) {       // exponent maxima, then the fp16 copy of V
+        const int64_t units = (int64_t)num_seqs * g.num_kv_heads *
+                              ((max_blocks_per_seq * pkv::kBlock + kStageTokens - 1) / kStageTokens);
+        const unsigned sgrid = (unsigned)std::min<int64_t>(units, (int64_t)sms * 8);
+        const uint16_t *vp = static_cast<const uint16_t *>(v_pool);
+        if (g.head_dim == 128) {
+            prefill_v16_kernel<128, false><<<sgrid, 256, 0, st>>>(vp, prm);
+            prefill_v16_kernel<128, true><<<sgrid, 256, 0, st>>>(vp, prm);
+        } else {
+            prefill_v16_kernel<64, false><<<sgrid, 256, 0, st>>>(vp, prm);
+            prefill_v16_kernel<64, true><<<sgrid, 256, 0, st>>>(vp, prm);
+        }
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;

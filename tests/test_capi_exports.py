@@ -49,3 +49,9 @@ def test_host_only_calls():
     assert lib.kv_pool_bytes(64, 16, 2, 64, 0) == 64 * 2 * 16 * 64 * 2
     assert lib.paged_decode_workspace_bytes(4, 4, 2, 64, 8) > 0
     assert lib.paged_decode_workspace_bytes(4, 5, 2, 64, 8) == 0      # Hq not a multiple of Hkv
+    # prefill: the staged size adds the fp16 copy of V ([S * maxb][Hkv][16][D] x 2 B)
+    base = lib.paged_prefill_workspace_bytes(3, 500, 32, 8)
+    staged = lib.paged_prefill_workspace_bytes_staged(3, 500, 32, 8, 128, 40)
+    assert base > 0 and staged >= base + 3 * 40 * 8 * 16 * 128 * 2
+    assert lib.paged_prefill_workspace_bytes_staged(3, 500, 32, 8, 96, 40) == 0   # head_dim
+    assert lib.paged_prefill_workspace_bytes_staged(3, 500, 32, 8, 128, 0) == 0

@@ -3,6 +3,8 @@
 Each sequence holds a cached prefix and a chunk of new prompt tokens whose
 K/V the library's cache write has stored; every chunk query attends causally
 over its sequence.  |gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise.
+bf16 cases run twice: with the plain workspace (P V from two bf16 parts of P)
+and with room for the fp16 copy of V (``staged``: one fp16 part).
 """
 import numpy as np
 import pytest
@@ -38,10 +40,11 @@ def _case(seed, ctx, chunks, hq, hkv, d, dt):
     return c, qb, qs
 
 
-def _run(c, qb, qs, lens=None):
+def _run(c, qb, qs, lens=None, staged=False):
     w = c.w
     T = qb.shape[0]
-    ws = torch.empty(prefill_workspace_bytes(w.num_seqs, T, w.num_q_heads, w.num_kv_heads),
+    extra = (w.head_dim, w.max_blocks_per_seq) if staged else ()
+    ws = torch.empty(prefill_workspace_bytes(w.num_seqs, T, w.num_q_heads, w.num_kv_heads, *extra),
                      dtype=torch.uint8, device="cuda")
     lens = c.d_lens if lens is None else lens
     return paged_prefill_attention(c.pool, to_torch(qb, w.is_bf16, "cuda"), c.d_tables,
@@ -67,31 +70,34 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("staged", [False, True])
 @pytest.mark.parametrize("case", CASES, ids=[str(c[:2]) for c in CASES])
-def test_prefill_matches_oracle(case):
+def test_prefill_matches_oracle(case, staged):
     ctx, chunks, hq, hkv, d, dt = case
     c, qb, qs = _case(len(ctx) * 7 + d, ctx, chunks, hq, hkv, d, dt)
     c.check_indexing()
     c.check_pools()
-    out = _run(c, qb, qs)
+    out = _run(c, qb, qs, staged=staged)
     assert status_check(c.status) == (0, 0)
-    assert_close(out, _oracle(c, qb, qs), f"prefill {case[:2]}")
+    assert_close(out, _oracle(c, qb, qs), f"prefill {case[:2]} staged={staged}")
     # repeated launches give the same bits
-    assert torch.equal(_run(c, qb, qs), out)
+    assert torch.equal(_run(c, qb, qs, staged=staged), out)
 
 
-def test_first_prompt_token_is_v_exactly():
+@pytest.mark.parametrize("staged", [False, True])
+def test_first_prompt_token_is_v_exactly(staged):
     c, qb, qs = _case(3, [20, 50], [20, 50], 8, 2, 128, "bf16")
-    out = to_np_bits(_run(c, qb, qs))
+    out = to_np_bits(_run(c, qb, qs, staged=staged))
     for s in range(2):
         r = qs[s]
         for h in range(8):
             assert np.array_equal(out[r, h], c.host["v_new"][r, h // 4])
 
 
-def test_one_token_chunks_match_decode():
+@pytest.mark.parametrize("staged", [False, True])
+def test_one_token_chunks_match_decode(staged):
     c, qb, qs = _case(9, [500, 1200, 33], [1, 1, 1], 32, 8, 128, "bf16")
-    out = _run(c, qb, qs)
+    out = _run(c, qb, qs, staged=staged)
     dec = c.run_gpu(q=to_torch(qb, True, "cuda"))
     assert_close(out, dec.double().cpu().numpy(), "prefill vs decode")
 
@@ -107,19 +113,21 @@ def test_bad_chunk_is_rejected():
     assert_close(out[:50], _oracle(c, qb, qs)[:50], "other sequence unaffected")
 
 
+@pytest.mark.parametrize("staged", [False, True])
 @pytest.mark.parametrize("scale", [0.0, -0.0883883])
-def test_zero_and_negative_scale(scale):
+def test_zero_and_negative_scale(scale, staged):
     """A zero scale gives uniform weights over the visible keys; a negative one
     makes the smallest score the largest weight: both against the oracle."""
     c, qb, qs = _case(13, [300, 70], [120, 70], 32, 8, 128, "bf16")
     c.w.scale = scale
-    out = _run(c, qb, qs)
+    out = _run(c, qb, qs, staged=staged)
     assert status_check(c.status) == (0, 0)
     assert torch.isfinite(out.float()).all()
     assert_close(out, _oracle(c, qb, qs), f"prefill scale {scale}")
 
 
-def test_v_beyond_fp16_range_in_some_tiles():
+@pytest.mark.parametrize("staged", [False, True])
+def test_v_beyond_fp16_range_in_some_tiles(staged):
     """bf16 V values far outside fp16's range (sequence 1's last 50 positions
     scaled by 1e5) must pass through P V unharmed: no step of the bf16 path may
     narrow V to fp16.  Rows before those positions do not see them (causal
@@ -137,9 +145,34 @@ def test_v_beyond_fp16_range_in_some_tiles():
     vals["v_new"] = workloads._f32_to_bf16_bits(f)
     c = DecodeCase(c0.w, vals)
     assert (np.abs((c.host["v_new"][start:].astype(np.uint32) << 16).view(np.float32)) > 65504).any()
-    out = _run(c, qb, qs)
+    out = _run(c, qb, qs, staged=staged)
     assert status_check(c.status) == (0, 0)
     assert torch.isfinite(out.float()).all()
     exp = _oracle(c, qb, qs)
     assert_close(out[:start], exp[:start], "rows without large V")
     assert_close(out[start:].double() / F, exp[start:] / F, "rows with large V, scaled")
+
+
+def test_staged_v_tiny_and_zero_values():
+    """The fp16 copy's scale follows each (sequence, kv head)'s largest V:
+    sequence 0's V scaled by 1e-25 (the copy is then scaled up by about 2^97,
+    inside the clamp) and sequence 1's V all zero (the clamp's end, 2^100)
+    still give the oracle's result; sequence 0 compared after dividing by the
+    factor."""
+    ctx, chunks = [300, 120], [150, 120]
+    c0, qb, qs = _case(41, ctx, chunks, 32, 8, 128, "bf16")
+    vals = dict(c0.host)
+    F = 1e-25
+    for key in ("v_prompt", "v_new"):
+        f = (vals[key].astype(np.uint32) << 16).view(np.float32).copy()
+        n0 = ctx[0] - chunks[0] if key == "v_prompt" else chunks[0]
+        f[:n0] *= F                                     # sequence 0
+        f[n0:] = 0.0                                    # sequence 1
+        vals[key] = workloads._f32_to_bf16_bits(f)
+    c = DecodeCase(c0.w, vals)
+    out = _run(c, qb, qs, staged=True)
+    assert status_check(c.status) == (0, 0)
+    exp = _oracle(c, qb, qs)
+    r1 = int(qs[1])
+    assert_close(out[:r1].double() / F, exp[:r1] / F, "tiny V, scaled")
+    assert not out[r1:].any()
