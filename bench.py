@@ -55,16 +55,17 @@ def peaks():
 
 
 DECODE_SOURCES = ("decode_params.h", "paged_decode.cu", "pkv_device.cuh")
+PREFILL_SOURCES = ("paged_prefill.cu", "tc_device.cuh", "pkv_device.cuh")
 
 
-def decode_source_hash() -> str:
-    """First 16 hex digits of the SHA-256 of the code the 16-bit decode kernels
-    compile from (comments removed and whitespace collapsed, so a comment edit
-    does not count as a kernel change)."""
+def decode_source_hash(sources=DECODE_SOURCES) -> str:
+    """First 16 hex digits of the SHA-256 of the code the kernels compile from
+    (the 16-bit decode kernels by default; comments removed and whitespace
+    collapsed, so a comment edit does not count as a kernel change)."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in DECODE_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_146_gb300", "csrc", f)) as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -73,15 +74,16 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str = "gqa_long"):
+def profiled_traffic(workload: str = "gqa_long", summary: str | None = None,
+                     sources=DECODE_SOURCES):
     """DRAM bytes (read + write) per attention call from the committed ncu
     launch-list summary of the workload (at its default size), or None when there
     is none or the kernel sources changed since it was taken."""
-    prof = os.path.join(ROOT, "profiles", f"paged_decode_{workload}_launches.md")
+    prof = os.path.join(ROOT, "profiles", summary or f"paged_decode_{workload}_launches.md")
     try:
         fields = dict(line.split(": ", 1) for line in open(prof).read().splitlines()
                       if line.startswith(("attention_traffic_bytes_per_launch:", "source_sha256_16:")))
-        current = decode_source_hash()
+        current = decode_source_hash(sources)
         if fields.get("source_sha256_16", "").strip() != current:
             return None
         return int(fields["attention_traffic_bytes_per_launch"])
@@ -619,7 +621,10 @@ def prefill_arm(args, world, rank, local):
                        "q_heads": hq, "kv_heads": hkv, "head_dim": d, "block_size": 16},
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak,
                          "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
-                         "traffic": None, "peak_kind": tkind,
+                         "traffic": (profiled_traffic(summary="paged_prefill_tc_launches.md",
+                                                      sources=PREFILL_SOURCES)
+                                     if staged and args.seed == 0 else None),
+                         "peak_kind": tkind,
                          "note": "tcgen05.mma kind::f16 (TMEM accumulators), 128 query rows x "
                                  "64-key tiles, two query tiles per CTA, "
                                  + ("P as one fp16 part, V copied to fp16 (scaled per sequence and kv "
