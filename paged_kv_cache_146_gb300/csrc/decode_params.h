@@ -44,5 +44,26 @@ struct Q8KernelInfo {
 };
 Q8KernelInfo q8_kernel_info(bool bf16_queries);
 
+#ifdef __CUDACC__
+// Output rows of sequences with no context, or with a length the table cannot
+// hold, are zeros.  context_lens is an input of the call, not something the
+// prep kernel writes, so each main kernel's CTAs store these rows before they
+// wait for the prep kernel's work list, while it still runs (grid-stride over
+// sequences, the CTA's threads over the row's 16-byte pieces).  Not inlined,
+// so it leaves the main loop's register allocation alone; its arguments are
+// values, so no copy of the kernel's parameters is taken.
+static __device__ __noinline__ void zero_idle_rows(void *out, const int32_t *context_lens,
+                                                   int num_seqs, int row_bytes, int64_t max_tokens)
+{
+    const int n16 = row_bytes / 16;
+    for (int s = blockIdx.x; s < num_seqs; s += gridDim.x) {
+        const int L = __ldg(context_lens + s);
+        if (L > 0 && (int64_t)L <= max_tokens) continue;
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(out) + (size_t)s * row_bytes);
+        for (int i = threadIdx.x; i < n16; i += blockDim.x) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+#endif
+
 }  // namespace decode
 }  // namespace pkv

@@ -189,19 +189,16 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     const int P = chosen_split;
     // bin of a partial last partition of r blocks, 0 < r < P: larger r, lower bin
     auto bin_of = [P](int r) { return (int)((int64_t)(P - 1 - r) * kOrderBins / P); };
-    // pass 1: partitions, pair offsets, full partitions, size histogram, zero rows
+    // pass 1: partitions, pair offsets, full partitions, size histogram (a
+    // sequence with no context or a bad length gets no partition)
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int s = base + tid;
         int nsplit = 0, partial = 0, r = 0;
-        bool zero_row = false;
         if (s < p.num_seqs) {
             const int L = p.context_lens[s];
             if (L < 0 || (int64_t)L > max_tokens) {
                 atomicOr(p.status, PKV_DEV_BAD_LEN);
-                zero_row = true;
-            } else if (L == 0) {
-                zero_row = true;
-            } else {
+            } else if (L > 0) {
                 const int nb = (L + kBlock - 1) / kBlock;
                 nsplit = (nb + P - 1) / P;
                 r = nb - (nsplit - 1) * P;
@@ -221,12 +218,7 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
             for (int k = 0; k < nsplit - partial; ++k) p.items[excl_full + k] = make_int2(s, k);
             if (partial) atomicAdd(&bin_next[bin_of(r)], 1);
             if (nsplit > 1) p.multi[atomicAdd(&multi_count, 1)] = s;   // for the merge kernel
-            if (zero_row) {
-                uint4 *o = reinterpret_cast<uint4 *>(static_cast<char *>(p.out) +
-                                                     (size_t)s * p.num_q_heads * head_dim * 2);
-                const int n16 = p.num_q_heads * head_dim * 2 / 16;
-                for (int i = 0; i < n16; ++i) o[i] = make_uint4(0, 0, 0, 0);
-            }
+            // (a zero row's output is written by the main kernel: zero_idle_rows)
         }
         __syncthreads();
         if (tid == 0) carry = make_int2(c0.x + warp_tot[31].x, c0.y + warp_tot[31].y);
@@ -342,6 +334,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    zero_idle_rows(p.out, p.context_lens, p.num_seqs, p.num_q_heads * D * 2,
+                   (int64_t)p.max_blocks_per_seq * kBlock);
     griddep_wait();                // the work list comes from the prep kernel
 
     const int Hkv = p.num_kv_heads, G = p.group, P = p.header[2];   // chosen by the prep kernel

@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    zero_idle_rows(p.out, p.context_lens, p.num_seqs, p.num_q_heads * D * 2,
+                   (int64_t)p.max_blocks_per_seq * kBlock);
     griddep_wait();                // the work list comes from the prep kernel
 
     const int Hkv = p.num_kv_heads, G = p.group;
