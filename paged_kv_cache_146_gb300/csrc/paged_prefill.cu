@@ -224,11 +224,12 @@ __global__ void __launch_bounds__(256) prefill_v16_kernel(const uint16_t *__rest
 // against the same KV tiles of 64 keys (4 blocks) up to the second tile's last
 // position, so each K/V tile is loaded once for 256 rows.
 //   warp 8 (producer): TMA of the item's Q rows (one 4-D box per 64 columns)
-//     and of each KV tile's 4 K and 4 V blocks into a 2-stage ring.
+//     and of each KV tile's 4 K and 4 V blocks into the stage ring.
 //   warps 9 and 10, lane 0 (MMA issuers, one per query tile): S = Q K^T into
 //     one of two tensor-memory buffers (M 128, N 64), then O += P V for the
 //     previous tile (M 128, N D, V as an MN-major operand), P as a high and a
-//     low bf16 part (bf16 pools) or one fp16 part (fp16 pools).  One issuer
+//     low bf16 part (bf16 pools) or one fp16 part (fp16 pools, and bf16 pools
+//     whose V was copied to fp16 for the call).  One issuer
 //     per query tile lets each group's S and P V go out as soon as that
 //     group's inputs are ready, without waiting behind the other group's.
 //   warps 0-3 and 4-7 (softmax, one warpgroup per query tile, ping-pong on the
