@@ -16,9 +16,10 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 import libbuild  # noqa: E402
+import oracle  # noqa: E402
 from decode_case import DecodeCase, assert_close, to_np_bits, to_torch  # noqa: E402
-from paged_kv_cache_146_gb300 import (paged_prefill_attention, prefill_workspace_bytes,  # noqa: E402
-                                      status_check, workloads)
+from paged_kv_cache_146_gb300 import (KVPool, cache_write, paged_prefill_attention,  # noqa: E402
+                                      prefill_workspace_bytes, status_check, workloads)
 
 libbuild.ensure_built()
 
@@ -176,3 +177,43 @@ def test_staged_v_tiny_and_zero_values():
     r1 = int(qs[1])
     assert_close(out[:r1].double() / F, exp[:r1] / F, "tiny V, scaled")
     assert not out[r1:].any()
+
+
+def test_prefill_bench_config_sampled():
+    """16 prompts of 2,048 tokens (GQA 32/8, D 128, bf16) in the launch
+    configuration the bench times (the workspace holds the fp16 copy of V).
+    A query at position p attends over tokens 0..p, which is the decode step
+    with context p + 1, so sampled rows are checked against the oracle's
+    decode over the first p + 1 tokens of their prompt; every row is finite."""
+    S, P, hq, hkv, d = 16, 2048, 32, 8, 128
+    T, maxb = S * P, P // 16
+    order = np.random.default_rng(0).permutation(S * maxb + 16).astype(np.int32)
+    pool = KVPool(S * maxb + 16, hkv, d, "bf16", free_order=order, device="cuda")
+    tables = np.full((S, maxb), -1, dtype=np.int32)
+    slots = pool.append_slots(np.zeros(S, np.int32), np.full(S, P, np.int32), tables)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(17)
+    k = torch.randn(T, hkv, d, generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn(T, hkv, d, generator=gen, device="cuda").to(torch.bfloat16)
+    q = torch.randn(T, hq, d, generator=gen, device="cuda").to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache_write(pool, k, v, torch.from_numpy(slots).cuda(), status)
+    qs = torch.from_numpy(np.arange(0, T + 1, P, dtype=np.int32)).cuda()
+    lens = torch.full((S,), P, dtype=torch.int32, device="cuda")
+    ws = torch.empty(prefill_workspace_bytes(S, T, hq, hkv, d, maxb), dtype=torch.uint8,
+                     device="cuda")
+    scale = 1.0 / np.sqrt(d)
+    out = paged_prefill_attention(pool, q, torch.from_numpy(tables).cuda(), qs, lens, scale, ws,
+                                  status)
+    assert status_check(status) == (0, 0)
+    assert torch.isfinite(out.float()).all()
+    o = oracle.load()
+    kp, vp = to_np_bits(pool.k_pool), to_np_bits(pool.v_pool)
+    for s_ in (0, 9, 15):
+        for p in (0, 1, 15, 16, 63, 64, 65, 1000, 2047):
+            r = s_ * P + p
+            exp, bad = o.paged_decode(to_np_bits(q[r:r + 1]), kp, vp, tables[s_:s_ + 1],
+                                      np.array([p + 1], dtype=np.int32), scale, True,
+                                      o.max_threads())
+            assert bad == 0
+            assert_close(out[r:r + 1], exp, f"prefill sequence {s_} position {p}")
