@@ -111,8 +111,9 @@ def pin_number_formats(o):
     """fp16/bf16 decoding: every finite fp16 pattern against numpy's float16, and
     bf16 patterns against float32 with the low half zero (IEEE-754 definitions)."""
     allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
-    f16 = allbits.view(np.float16).astype(np.float64)
-    bf = (allbits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):           # NaN patterns; only finite ones are compared
+        f16 = allbits.view(np.float16).astype(np.float64)
+        bf = (allbits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     for i in range(0, 65536, 7):          # a stride covering every exponent and many fractions
         if np.isfinite(f16[i]):
             assert o.f16_to_double(i) == f16[i], (hex(i), o.f16_to_double(i), f16[i])
