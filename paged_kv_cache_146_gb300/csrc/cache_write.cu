@@ -245,7 +245,7 @@ __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c,
 constexpr int64_t kQ8WindowsForBlocks = 8192;
 
 template <bool BF16>
-__global__ void __launch_bounds__(128, 3)
+__global__ void __launch_bounds__(128, 4)
 cache_write_q8_kernel(const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
                       const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
                       int32_t num_kv_heads, int64_t num_slots, bool whole_blocks,
