@@ -18,8 +18,9 @@ if not torch.cuda.is_available():
 import libbuild  # noqa: E402
 import oracle  # noqa: E402
 from decode_case import DecodeCase, assert_close, to_np_bits, to_torch  # noqa: E402
-from paged_kv_cache_146_gb300 import (KVPool, cache_write, paged_prefill_attention,  # noqa: E402
-                                      prefill_workspace_bytes, status_check, workloads)
+from paged_kv_cache_146_gb300 import (DEV_BAD_BLOCK, KVPool, cache_write,  # noqa: E402
+                                      paged_prefill_attention, prefill_workspace_bytes,
+                                      status_check, workloads)
 
 libbuild.ensure_built()
 
@@ -41,14 +42,15 @@ def _case(seed, ctx, chunks, hq, hkv, d, dt):
     return c, qb, qs
 
 
-def _run(c, qb, qs, lens=None, staged=False):
+def _run(c, qb, qs, lens=None, staged=False, tables=None):
     w = c.w
     T = qb.shape[0]
     extra = (w.head_dim, w.max_blocks_per_seq) if staged else ()
     ws = torch.empty(prefill_workspace_bytes(w.num_seqs, T, w.num_q_heads, w.num_kv_heads, *extra),
                      dtype=torch.uint8, device="cuda")
     lens = c.d_lens if lens is None else lens
-    return paged_prefill_attention(c.pool, to_torch(qb, w.is_bf16, "cuda"), c.d_tables,
+    tables = c.d_tables if tables is None else tables
+    return paged_prefill_attention(c.pool, to_torch(qb, w.is_bf16, "cuda"), tables,
                                    torch.from_numpy(qs).cuda(), lens, w.scale, ws, c.status)
 
 
@@ -112,6 +114,22 @@ def test_bad_chunk_is_rejected():
     assert rc == -5 and word & 4
     assert not out[50:].any()
     assert_close(out[:50], _oracle(c, qb, qs)[:50], "other sequence unaffected")
+
+
+@pytest.mark.parametrize("staged", [False, True])
+def test_bad_block_in_a_table(staged):
+    """A table entry outside the pool (sequence 1's first block, which every one
+    of its items reads) is flagged and that sequence's rows come out as zeros,
+    with or without the fp16 copy of V; sequence 0 is unaffected."""
+    c, qb, qs = _case(31, [400, 300], [200, 300], 32, 8, 128, "bf16")
+    tables = c.d_tables.clone()
+    tables[1, 0] = c.w.num_blocks + 5
+    out = _run(c, qb, qs, staged=staged, tables=tables)
+    rc, word = status_check(c.status)
+    assert rc == -5 and word & DEV_BAD_BLOCK
+    r1 = int(qs[1])
+    assert not out[r1:].any()
+    assert_close(out[:r1], _oracle(c, qb, qs)[:r1], "sequence with a good table")
 
 
 @pytest.mark.parametrize("staged", [False, True])
