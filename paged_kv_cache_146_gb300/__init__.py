@@ -56,6 +56,19 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _check_layout(contiguous: dict, int32: dict | None = None, int64: dict | None = None):
+    """Tensors the C ABI reads as plain row-major arrays must be contiguous, and
+    its index arrays of the stated integer type (a raise here launches nothing)."""
+    import torch
+    for name, t in contiguous.items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for want, group in ((torch.int32, int32 or {}), (torch.int64, int64 or {})):
+        for name, t in group.items():
+            if t.dtype != want:
+                raise TypeError(f"{name} must be {str(want).replace('torch.', '')}")
+
+
 def _torch_dtype(code: int):
     """Element type of K/V rows and queries for a pool type (8-bit pools take
     bf16 / fp16 rows and quantise them)."""
@@ -219,6 +232,8 @@ def _pools(pool: KVPool, k_pool, v_pool):
 def block_copy(pool: KVPool, src_ids, dst_ids, status, k_pool=None, v_pool=None,
                stream=None) -> None:
     """Launch the block-copy kernel (int32 device tensors of block ids)."""
+    _check_layout({"src_ids": src_ids, "dst_ids": dst_ids},
+                  int32={"src_ids": src_ids, "dst_ids": dst_ids})
     k_pool, v_pool = _pools(pool, k_pool, v_pool)
     n = int(src_ids.shape[0])
     if int(dst_ids.shape[0]) != n:
@@ -238,6 +253,7 @@ def cache_write(pool: KVPool, k_new, v_new, slot_mapping, status, k_pool=None, v
         raise ValueError("k_new/v_new rows must match slot_mapping")
     if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
         raise ValueError("inputs must be contiguous")
+    _check_layout({}, int64={"slot_mapping": slot_mapping})
     check(lib().kv_cache_write(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping), T,
                                _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status), _stream(stream)),
           "kv_cache_write")
@@ -247,6 +263,7 @@ def gather_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, 
     """Pack blocks ``ids`` (int32 device tensor) into ``staging`` (device,
     [n][2][Hkv][16][D] in the pool dtype; 8-bit pools [n][Hkv][4352] bytes) for
     one host copy (swap out)."""
+    _check_layout({"ids": ids, "staging": staging}, int32={"ids": ids})
     k_pool, v_pool = _pools(pool, k_pool, v_pool)
     check(lib().kv_gather_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(k_pool),
                                  _t_ptr(v_pool), _t_ptr(staging), _t_ptr(status),
@@ -255,6 +272,7 @@ def gather_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, 
 
 def scatter_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, stream=None):
     """Unpack ``staging`` into blocks ``ids`` (swap in)."""
+    _check_layout({"ids": ids, "staging": staging}, int32={"ids": ids})
     k_pool, v_pool = _pools(pool, k_pool, v_pool)
     check(lib().kv_scatter_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(staging),
                                   _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status),
@@ -354,6 +372,8 @@ def paged_decode_attention_noalloc(pool: KVPool, q, block_tables, context_lens, 
     caller workspace; the library allocates nothing (for callers that cannot
     allocate device memory at decode time).  ``out`` must be given.  Calls on one
     device share the scratch: do not overlap them on the GPU."""
+    _check_layout({"q": q, "out": out, "block_tables": block_tables, "context_lens": context_lens},
+                  int32={"block_tables": block_tables, "context_lens": context_lens})
     k_pool = pool.k_pool if k_pool is None else k_pool
     v_pool = pool.v_pool if v_pool is None else v_pool
     S, hq, d = q.shape
@@ -386,6 +406,10 @@ def paged_prefill_attention(pool: KVPool, q, block_tables, query_start, context_
     """Chunked-prefill attention: ``q`` [T][Hq][D] device rows of all chunks,
     ``query_start`` int32 device [S+1], ``context_lens`` int32 device [S]."""
     import torch
+    _check_layout({"q": q, "out": out, "block_tables": block_tables, "query_start": query_start,
+                   "context_lens": context_lens, "workspace": workspace},
+                  int32={"block_tables": block_tables, "query_start": query_start,
+                         "context_lens": context_lens})
     k_pool = pool.k_pool if k_pool is None else k_pool
     v_pool = pool.v_pool if v_pool is None else v_pool
     T, hq, d = q.shape
@@ -411,6 +435,7 @@ def cache_write_q8(pool: KVPool, k_new, v_new, slot_mapping, status, stream=None
         raise ValueError("k_new/v_new rows must match slot_mapping")
     if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
         raise ValueError("inputs must be contiguous")
+    _check_layout({}, int64={"slot_mapping": slot_mapping})
     check(lib().kv_cache_write_q8(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping),
                                   T, _t_ptr(pool.kv), _t_ptr(status), _stream(stream)),
           "kv_cache_write_q8")
