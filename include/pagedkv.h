@@ -358,9 +358,10 @@ size_t paged_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32
  * num_seqs * max_blocks_per_seq blocks) as fp16, scaled per (sequence, kv
  * head) by a power of two that puts the largest |v| just under 2^16, and then
  * forms P V with one fp16 part of P instead of two bf16 parts.  Every V value
- * within 2^30 of its (sequence, kv head)'s largest converts exactly; smaller
- * ones round to fp16's subnormal spacing.  The result meets the same
- * tolerance; fp16 pools ignore the extra room.  0 on a bad argument. */
+ * within 2^30 of its (sequence, kv head)'s largest converts exactly (when that
+ * largest is at least 2^-85; below it the scale stops at 2^100); smaller ones
+ * round to fp16's subnormal spacing.  The result meets the same tolerance;
+ * fp16 pools ignore the extra room.  0 on a bad argument. */
 size_t paged_prefill_workspace_bytes_staged(int32_t num_seqs, int32_t num_tokens,
                                             int32_t num_q_heads, int32_t num_kv_heads,
                                             int32_t head_dim, int32_t max_blocks_per_seq);

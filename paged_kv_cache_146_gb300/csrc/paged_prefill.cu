@@ -134,8 +134,9 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(Params p, int32_t he
 // products halve.  So, when the caller's workspace holds it, V of every
 // attended token is copied once per call as fp16, scaled per (sequence, kv
 // head) by a power of two (v16_shift): a bf16 significand (8 bits) fits in
-// fp16's 11, so every value within 2^30 of the largest converts exactly; only
-// values below that (fp16 subnormals) round, by at most 2^(k-25).  The
+// fp16's 11, so every value within 2^30 of the largest converts exactly (for a
+// largest |v| of at least 2^-85, where the shift is not clamped); only values
+// below that (fp16 subnormals) round, by at most 2^(k-25).  The
 // attention kernel multiplies its result by 2^k.  Two passes over 256-token
 // chunks: the largest exponent field (atomicMax into v_emax, zeroed by the
 // prep kernel), then the conversion.  Tokens past a sequence's length are not
