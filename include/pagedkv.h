@@ -407,7 +407,9 @@ int32_t paged_decode_default_split(void);
  * pools, tables, lengths, status word).
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream
- *     capture.
+ *     capture.  Resetting the device after that first call (cudaDeviceReset,
+ *     or a reset of its primary context) is not supported: the cached address
+ *     would then name memory the reloaded module no longer owns.
  *   - The partition size is the default when the scratch fits, otherwise the
  *     smallest number of partitions per sequence that fits.  Shapes that do
  *     not fit even with one partition per sequence are rejected with

@@ -19,7 +19,7 @@
  *   - "kv-cache-by-model" (sotaaz.com), section 1 "Full attention":
  *     per layer, per token, 2 (K and V) x kv_heads x head_dim x 2 bytes.
  *
- * Readings where the pages are silent (all restated in the design doc):
+ * Readings where the pages are silent:
  *   R1  pool layout [num_blocks][num_kv_heads][block_size][head_dim];
  *   R2  slot = physical_block * block_size + offset, negative slot = skip;
  *   R3  query head h reads kv head h / (num_q_heads / num_kv_heads);

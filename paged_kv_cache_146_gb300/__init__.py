@@ -69,6 +69,90 @@ def _check_layout(contiguous: dict, int32: dict | None = None, int64: dict | Non
                 raise TypeError(f"{name} must be {str(want).replace('torch.', '')}")
 
 
+def _check_rows(name: str, t, rows, heads, head_dim: int, dtype, device) -> None:
+    """``t`` must be a [rows][heads][head_dim] tensor of ``dtype`` on ``device``
+    (``rows`` or ``heads`` None: any).  The library sizes every read and write of
+    such an array from the pool's geometry and the counts it is given, so a
+    tensor of another shape, type or device would be read or written past its
+    end; a raise here launches nothing."""
+    shape = tuple(t.shape)
+    if (len(shape) != 3 or (rows is not None and shape[0] != rows)
+            or (heads is not None and shape[1] != heads) or shape[2] != head_dim):
+        want = f"[{'n' if rows is None else rows}][{'h' if heads is None else heads}][{head_dim}]"
+        raise ValueError(f"{name} must be {want}, got {list(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {str(dtype).replace('torch.', '')}, got "
+                        f"{str(t.dtype).replace('torch.', '')}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's rows are on {device}")
+
+
+def _check_vector(name: str, t, n: int | None, device, ndim: int = 1) -> None:
+    """An index array with ``n`` rows (None: any) on ``device``."""
+    if t.dim() != ndim or (n is not None and t.shape[0] != n):
+        raise ValueError(f"{name} must have {ndim} dimension(s) and {n} rows, got "
+                         f"{list(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's rows are on {device}")
+
+
+def _check_device_call(q, status, workspace=None, pools=()) -> None:
+    """Last check before a launch: every buffer the kernels touch sits on the
+    same CUDA device (host tensors would hand the kernels host addresses)."""
+    if q.device.type != "cuda":
+        raise ValueError(f"the call's tensors must be CUDA tensors, got {q.device}")
+    if status.dtype != _torch_int32() or status.numel() < 1:
+        raise TypeError("status must be an int32 tensor of at least one element")
+    for name, t in (("status", status), ("workspace", workspace)) + tuple(pools):
+        if t is not None and t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, the call's rows are on {q.device}")
+
+
+def _torch_int32():
+    import torch
+    return torch.int32
+
+
+def _check_pool_tensor(name: str, t, pool: "KVPool") -> None:
+    """A caller-supplied pool tensor must hold the pool's whole geometry."""
+    if pool.is_q8:
+        want, dt = pool.num_blocks * pool.num_kv_heads * _native.PKV_Q8_SLAB_BYTES, None
+    else:
+        want = pool.num_blocks * pool.num_kv_heads * pool.block_size * pool.head_dim
+        dt = _torch_dtype(pool.dtype_code)
+    if t.numel() != want or (dt is not None and t.dtype != dt):
+        raise ValueError(f"{name} does not match the pool's geometry and type")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_decode_args(pool: "KVPool", q, out, block_tables, context_lens, status,
+                       workspace=None, k_pool=None, v_pool=None) -> None:
+    """Shapes, types and devices of a decode call: q and out [S][Hq][D] in the
+    pool's row type, block_tables [S][max_blocks], context_lens [S]."""
+    import torch
+    _check_layout({"q": q, "out": out, "block_tables": block_tables,
+                   "context_lens": context_lens, "workspace": workspace},
+                  int32={"block_tables": block_tables, "context_lens": context_lens})
+    dt = _torch_dtype(pool.dtype_code)
+    _check_rows("q", q, None, None, pool.head_dim, dt, None)
+    S, hq = int(q.shape[0]), int(q.shape[1])
+    if hq % pool.num_kv_heads:
+        raise ValueError(f"q has {hq} heads, not a multiple of the pool's "
+                         f"{pool.num_kv_heads} kv heads")
+    _check_rows("out", out, S, hq, pool.head_dim, dt, q.device)
+    _check_vector("block_tables", block_tables, S, q.device, ndim=2)
+    _check_vector("context_lens", context_lens, S, q.device)
+    if workspace is not None and workspace.dtype != torch.uint8:
+        raise TypeError("workspace must be a uint8 tensor")
+    pools = []
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+        if t is not None:
+            _check_pool_tensor(name, t, pool)
+            pools.append((name, t))
+    _check_device_call(q, status, workspace, pools)
+
+
 def _torch_dtype(code: int):
     """Element type of K/V rows and queries for a pool type (8-bit pools take
     bf16 / fp16 rows and quantise them)."""
@@ -235,11 +319,30 @@ def block_copy(pool: KVPool, src_ids, dst_ids, status, k_pool=None, v_pool=None,
     _check_layout({"src_ids": src_ids, "dst_ids": dst_ids},
                   int32={"src_ids": src_ids, "dst_ids": dst_ids})
     k_pool, v_pool = _pools(pool, k_pool, v_pool)
+    _check_vector("src_ids", src_ids, None, None)
     n = int(src_ids.shape[0])
-    if int(dst_ids.shape[0]) != n:
-        raise ValueError("src_ids and dst_ids differ in length")
+    _check_vector("dst_ids", dst_ids, n, src_ids.device)
+    _check_block_pools(pool, src_ids, status, k_pool, v_pool)
     check(lib().kv_block_copy(pool.handle, _t_ptr(src_ids), _t_ptr(dst_ids), n, _t_ptr(k_pool),
                               _t_ptr(v_pool), _t_ptr(status), _stream(stream)), "kv_block_copy")
+
+
+def _check_write_args(pool: KVPool, k_new, v_new, slot_mapping, status, pools) -> None:
+    """Rows [T][Hkv][D] in the pool's row type for T int64 slots."""
+    _check_layout({"k_new": k_new, "v_new": v_new, "slot_mapping": slot_mapping},
+                  int64={"slot_mapping": slot_mapping})
+    _check_vector("slot_mapping", slot_mapping, None, None)
+    T = int(slot_mapping.shape[0])
+    dt = _torch_dtype(pool.dtype_code)
+    _check_rows("k_new", k_new, T, pool.num_kv_heads, pool.head_dim, dt, None)
+    _check_rows("v_new", v_new, T, pool.num_kv_heads, pool.head_dim, dt, k_new.device)
+    _check_vector("slot_mapping", slot_mapping, T, k_new.device)
+    checked = []
+    for name, t in pools:
+        if t is not None:
+            _check_pool_tensor(name, t, pool)
+            checked.append((name, t))
+    _check_device_call(k_new, status, None, checked)
 
 
 def cache_write(pool: KVPool, k_new, v_new, slot_mapping, status, k_pool=None, v_pool=None,
@@ -248,15 +351,31 @@ def cache_write(pool: KVPool, k_new, v_new, slot_mapping, status, k_pool=None, v
     go to their slots (int64 device tensor [T]) in the pools."""
     k_pool = pool.k_pool if k_pool is None else k_pool
     v_pool = pool.v_pool if v_pool is None else v_pool
+    _check_write_args(pool, k_new, v_new, slot_mapping, status,
+                      (("k_pool", k_pool), ("v_pool", v_pool)))
     T = int(slot_mapping.shape[0])
-    if k_new.shape[0] != T or v_new.shape[0] != T:
-        raise ValueError("k_new/v_new rows must match slot_mapping")
-    if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
-        raise ValueError("inputs must be contiguous")
-    _check_layout({}, int64={"slot_mapping": slot_mapping})
     check(lib().kv_cache_write(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping), T,
                                _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status), _stream(stream)),
           "kv_cache_write")
+
+
+def _check_block_pools(pool: KVPool, ids, status, k_pool, v_pool, staging=None) -> None:
+    """Pool tensors of a block-movement call hold the pool's geometry; a staging
+    buffer holds every listed block; all on the ids' device."""
+    pools = []
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+        if t is not None:
+            _check_pool_tensor(name, t, pool)
+            pools.append((name, t))
+    if staging is not None:
+        _check_vector("ids", ids, None, None)
+        per_block = (pool.num_kv_heads * _native.PKV_Q8_SLAB_BYTES if pool.is_q8 else
+                     2 * pool.num_kv_heads * pool.block_size * pool.head_dim * 2)
+        if staging.numel() * staging.element_size() < int(ids.shape[0]) * per_block:
+            raise ValueError(f"staging holds fewer than {int(ids.shape[0])} blocks of "
+                             f"{per_block} bytes")
+        pools.append(("staging", staging))
+    _check_device_call(ids, status, None, pools)
 
 
 def gather_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, stream=None):
@@ -265,6 +384,7 @@ def gather_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None, 
     one host copy (swap out)."""
     _check_layout({"ids": ids, "staging": staging}, int32={"ids": ids})
     k_pool, v_pool = _pools(pool, k_pool, v_pool)
+    _check_block_pools(pool, ids, status, k_pool, v_pool, staging)
     check(lib().kv_gather_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(k_pool),
                                  _t_ptr(v_pool), _t_ptr(staging), _t_ptr(status),
                                  _stream(stream)), "kv_gather_blocks")
@@ -274,6 +394,7 @@ def scatter_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None,
     """Unpack ``staging`` into blocks ``ids`` (swap in)."""
     _check_layout({"ids": ids, "staging": staging}, int32={"ids": ids})
     k_pool, v_pool = _pools(pool, k_pool, v_pool)
+    _check_block_pools(pool, ids, status, k_pool, v_pool, staging)
     check(lib().kv_scatter_blocks(pool.handle, _t_ptr(ids), int(ids.shape[0]), _t_ptr(staging),
                                   _t_ptr(k_pool), _t_ptr(v_pool), _t_ptr(status),
                                   _stream(stream)), "kv_scatter_blocks")
@@ -298,15 +419,11 @@ def paged_decode_attention(pool: KVPool, q, block_tables, context_lens, scale: f
     import torch
     k_pool = pool.k_pool if k_pool is None else k_pool
     v_pool = pool.v_pool if v_pool is None else v_pool
-    S, hq, d = q.shape
     if out is None:
         out = torch.empty_like(q)
-    for t, name in ((q, "q"), (out, "out"), (block_tables, "block_tables"),
-                    (context_lens, "context_lens")):
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
-        raise TypeError("block_tables and context_lens must be int32")
+    _check_decode_args(pool, q, out, block_tables, context_lens, status, workspace,
+                       k_pool, v_pool)
+    S, hq, d = q.shape
     maxb = int(block_tables.shape[1])
     nbytes = workspace.numel() * workspace.element_size()
     if blocks_per_split is None:
@@ -372,10 +489,9 @@ def paged_decode_attention_noalloc(pool: KVPool, q, block_tables, context_lens, 
     caller workspace; the library allocates nothing (for callers that cannot
     allocate device memory at decode time).  ``out`` must be given.  Calls on one
     device share the scratch: do not overlap them on the GPU."""
-    _check_layout({"q": q, "out": out, "block_tables": block_tables, "context_lens": context_lens},
-                  int32={"block_tables": block_tables, "context_lens": context_lens})
     k_pool = pool.k_pool if k_pool is None else k_pool
     v_pool = pool.v_pool if v_pool is None else v_pool
+    _check_decode_args(pool, q, out, block_tables, context_lens, status, None, k_pool, v_pool)
     S, hq, d = q.shape
     rc = lib().paged_decode_attention_noalloc(pool.handle, _t_ptr(out), _t_ptr(q),
                                               _t_ptr(k_pool), _t_ptr(v_pool),
@@ -412,10 +528,27 @@ def paged_prefill_attention(pool: KVPool, q, block_tables, query_start, context_
                          "context_lens": context_lens})
     k_pool = pool.k_pool if k_pool is None else k_pool
     v_pool = pool.v_pool if v_pool is None else v_pool
-    T, hq, d = q.shape
     if out is None:
         out = torch.empty_like(q)
+    dt = _torch_dtype(pool.dtype_code)
+    _check_rows("q", q, None, None, pool.head_dim, dt, None)
+    T, hq, d = q.shape
+    if hq % pool.num_kv_heads:
+        raise ValueError(f"q has {hq} heads, not a multiple of the pool's "
+                         f"{pool.num_kv_heads} kv heads")
+    _check_rows("out", out, T, hq, pool.head_dim, dt, q.device)
+    _check_vector("context_lens", context_lens, None, q.device)
     S = int(context_lens.shape[0])
+    _check_vector("block_tables", block_tables, S, q.device, ndim=2)
+    _check_vector("query_start", query_start, S + 1, q.device)
+    if workspace.dtype != torch.uint8:
+        raise TypeError("workspace must be a uint8 tensor")
+    pools = []
+    for name, t in (("k_pool", k_pool), ("v_pool", v_pool)):
+        if t is not None:
+            _check_pool_tensor(name, t, pool)
+            pools.append((name, t))
+    _check_device_call(q, status, workspace, pools)
     nbytes = workspace.numel() * workspace.element_size()
     check(lib().paged_prefill_attention(pool.handle, _t_ptr(out), _t_ptr(q), _t_ptr(k_pool),
                                         _t_ptr(v_pool), _t_ptr(block_tables),
@@ -430,12 +563,8 @@ def cache_write_q8(pool: KVPool, k_new, v_new, slot_mapping, status, stream=None
     """Quantising cache write into an 8-bit pool: rows of ``k_new``/``v_new``
     [T][Hkv][128] (bf16 for q8_bf16, fp16 for q8_f16) go to their slots as codes
     and fp16 scales."""
+    _check_write_args(pool, k_new, v_new, slot_mapping, status, (("kv", pool.kv),))
     T = int(slot_mapping.shape[0])
-    if k_new.shape[0] != T or v_new.shape[0] != T:
-        raise ValueError("k_new/v_new rows must match slot_mapping")
-    if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
-        raise ValueError("inputs must be contiguous")
-    _check_layout({}, int64={"slot_mapping": slot_mapping})
     check(lib().kv_cache_write_q8(pool.handle, _t_ptr(k_new), _t_ptr(v_new), _t_ptr(slot_mapping),
                                   T, _t_ptr(pool.kv), _t_ptr(status), _stream(stream)),
           "kv_cache_write_q8")
@@ -447,15 +576,11 @@ def paged_decode_attention_q8(pool: KVPool, q, block_tables, context_lens, scale
     the result in bf16 (q8_bf16) or fp16 (q8_f16); workspace as for
     ``decode_workspace_bytes``."""
     import torch
-    S, hq, d = q.shape
     if out is None:
         out = torch.empty_like(q)
-    for t, name in ((q, "q"), (out, "out"), (block_tables, "block_tables"),
-                    (context_lens, "context_lens")):
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
-        raise TypeError("block_tables and context_lens must be int32")
+    _check_decode_args(pool, q, out, block_tables, context_lens, status, workspace,
+                       pool.kv if pool.kv is not None else None)
+    S, hq, d = q.shape
     nbytes = workspace.numel() * workspace.element_size()
     check(lib().paged_decode_attention_q8(pool.handle, _t_ptr(out), _t_ptr(q), _t_ptr(pool.kv),
                                           _t_ptr(block_tables), int(block_tables.shape[1]),
