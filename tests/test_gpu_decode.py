@@ -73,9 +73,12 @@ def test_shared_prefix_config():
     assert c.pool.num_free() == w.num_blocks
 
 
-def test_gqa_long_config_sampled():
-    """Full-size GQA 32/8 long context in the launch configuration the bench times;
-    the oracle checks a sample of sequences (the longest, the shortest, random)."""
+def test_gqa_long_config():
+    """Full-size GQA 32/8 long context (256 sequences, log-normal lengths up to
+    32K) in the launch configuration the bench times: every output row of every
+    sequence against the oracle.  The work-list order, the partition size the
+    device picks and the CTA that takes each item all depend on the whole
+    batch, so only the whole batch covers the paths this launch takes."""
     w = workloads.gqa_long(0)
     vals = workloads.device_values(w, "cuda")
     c = DecodeCase(w, vals)
@@ -83,13 +86,7 @@ def test_gqa_long_config_sampled():
     c.check_pools()
     out = c.run_gpu()
     assert status_check(c.status) == (0, 0)
-    lens = c.context_lens
-    rng = np.random.default_rng(7)
-    sample = sorted({int(np.argmax(lens)), int(np.argmin(lens)),
-                     *rng.choice(w.num_seqs, 6, replace=False).tolist()})
-    assert_close(out[sample], c.oracle_out(sample), "gqa_long sample")
-    # properties over every row: finite, and bounded by the V range
-    assert torch.isfinite(out.float()).all()
+    assert_close(out, c.oracle_out(), "gqa_long, all 256 sequences")
 
 
 # -------------------------------------------------------------- randomised

@@ -197,16 +197,20 @@ def test_staged_v_tiny_and_zero_values():
     assert not out[r1:].any()
 
 
-def test_prefill_bench_config_sampled():
+def test_prefill_bench_config():
     """16 prompts of 2,048 tokens (GQA 32/8, D 128, bf16) in the launch
     configuration the bench times (the workspace holds the fp16 copy of V).
-    A query at position p attends over tokens 0..p, which is the decode step
-    with context p + 1, so sampled rows are checked against the oracle's
-    decode over the first p + 1 tokens of their prompt; every row is finite."""
+    The oracle builds its own tables (ledger model, same free order) and its
+    own pools (its cache write of the same K/V bits).  Every query row of two
+    whole prompts is compared with the oracle's prefill; in the other prompts,
+    sampled rows at block and tile edges are compared with the oracle's decode
+    over the first p + 1 tokens (a query at position p attends over tokens
+    0..p)."""
     S, P, hq, hkv, d = 16, 2048, 32, 8, 128
     T, maxb = S * P, P // 16
-    order = np.random.default_rng(0).permutation(S * maxb + 16).astype(np.int32)
-    pool = KVPool(S * maxb + 16, hkv, d, "bf16", free_order=order, device="cuda")
+    nb = S * maxb + 16
+    order = np.random.default_rng(0).permutation(nb).astype(np.int32)
+    pool = KVPool(nb, hkv, d, "bf16", free_order=order, device="cuda")
     tables = np.full((S, maxb), -1, dtype=np.int32)
     slots = pool.append_slots(np.zeros(S, np.int32), np.full(S, P, np.int32), tables)
     gen = torch.Generator(device="cuda")
@@ -216,22 +220,45 @@ def test_prefill_bench_config_sampled():
     q = torch.randn(T, hq, d, generator=gen, device="cuda").to(torch.bfloat16)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     cache_write(pool, k, v, torch.from_numpy(slots).cuda(), status)
-    qs = torch.from_numpy(np.arange(0, T + 1, P, dtype=np.int32)).cuda()
-    lens = torch.full((S,), P, dtype=torch.int32, device="cuda")
+    qs_np = np.arange(0, T + 1, P, dtype=np.int32)
+    lens_np = np.full(S, P, dtype=np.int32)
     ws = torch.empty(prefill_workspace_bytes(S, T, hq, hkv, d, maxb), dtype=torch.uint8,
                      device="cuda")
     scale = 1.0 / np.sqrt(d)
-    out = paged_prefill_attention(pool, q, torch.from_numpy(tables).cuda(), qs, lens, scale, ws,
-                                  status)
+    out = paged_prefill_attention(pool, q, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(qs_np).cuda(), torch.from_numpy(lens_np).cuda(),
+                                  scale, ws, status)
     assert status_check(status) == (0, 0)
-    assert torch.isfinite(out.float()).all()
+
+    # the oracle's side: its own ledger, tables, slots and pools
+    from oracle.allocator_model import BlockLedger
+    led = BlockLedger(nb, 16, order)
+    t_or = [[-1] * maxb for _ in range(S)]
+    or_slots = led.append([0] * S, [P] * S, t_or)
+    t_or = np.array(t_or, dtype=np.int32)
+    assert np.array_equal(t_or, tables) and slots.tolist() == list(or_slots)
     o = oracle.load()
-    kp, vp = to_np_bits(pool.k_pool), to_np_bits(pool.v_pool)
-    for s_ in (0, 9, 15):
-        for p in (0, 1, 15, 16, 63, 64, 65, 1000, 2047):
+    kp = np.full((nb, hkv, 16, d), 0xFFFF, np.uint16)
+    vp = np.full((nb, hkv, 16, d), 0xFFFF, np.uint16)
+    assert o.cache_write(to_np_bits(k), to_np_bits(v), np.array(or_slots, np.int64), kp, vp,
+                         16) == 0
+    qh = to_np_bits(q)
+    got = out.double().cpu().numpy()
+    whole = (0, 9)
+    for s_ in whole:
+        exp, bad = o.paged_prefill(qh[s_ * P:(s_ + 1) * P], kp, vp, t_or[s_:s_ + 1],
+                                   np.array([0, P], np.int32), lens_np[s_:s_ + 1], scale, True,
+                                   o.max_threads())
+        assert bad == 0
+        assert_close(torch.from_numpy(got[s_ * P:(s_ + 1) * P]), exp,
+                     f"prefill sequence {s_}, every row")
+    for s_ in range(S):
+        if s_ in whole:
+            continue
+        for p in (0, 1, 15, 16, 63, 64, 65, 127, 128, 1000, 2047):
             r = s_ * P + p
-            exp, bad = o.paged_decode(to_np_bits(q[r:r + 1]), kp, vp, tables[s_:s_ + 1],
+            exp, bad = o.paged_decode(qh[r:r + 1], kp, vp, t_or[s_:s_ + 1],
                                       np.array([p + 1], dtype=np.int32), scale, True,
                                       o.max_threads())
             assert bad == 0
-            assert_close(out[r:r + 1], exp, f"prefill sequence {s_} position {p}")
+            assert_close(torch.from_numpy(got[r:r + 1]), exp, f"prefill sequence {s_} position {p}")
