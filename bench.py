@@ -93,7 +93,7 @@ def profiled_traffic(workload: str = "gqa_long", summary: str | None = None,
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -105,7 +105,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", "100"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -274,12 +274,18 @@ class OracleSample:
 
 
 def oracle_calibrated(seed: int, target_s: float, q8: bool = False,
-                      workload: str = "gqa_long") -> OracleSample:
-    """An oracle sample whose one call takes about ``target_s`` seconds."""
+                      workload: str = "gqa_long", threads: int | None = None) -> OracleSample:
+    """An oracle sample whose one call takes about ``target_s`` seconds on
+    ``threads`` host threads (default: all)."""
     probe = OracleSample(seed, 2, q8, workload)
+    if threads:
+        probe.threads = threads
     dt = probe.run()
     k = int(min(256, max(2, round(2 * target_s / max(dt, 1e-3)))))
-    return OracleSample(seed, k, q8, workload)
+    sample = OracleSample(seed, k, q8, workload)
+    if threads:
+        sample.threads = threads
+    return sample
 
 
 def reference_arm(args, world, rank):
@@ -321,22 +327,24 @@ def reference_arm(args, world, rank):
 
 
 # ------------------------------------------------------------------ our arm
-def our_arm(args, world, rank, local):
+def decode_run(args, workload: str, world: int, rank: int, dev, steps: int, warmup: int,
+               repeats: int = 1, e2e_steps: int = 0, prompt_write: bool = False,
+               clocks: "ClockSampler | None" = None) -> dict:
+    """Decode steps of one workload through DecodeEngine: ``warmup`` untimed
+    steps, then ``repeats`` timed regions of ``steps`` steps each (barrier and
+    synchronisation on both sides of every region), optionally ``e2e_steps``
+    steps through the host-buffer call and one write of every prompt token."""
     import torch
-    from paged_kv_cache_146_gb300 import (KVPool, cache_write, paged_decode_attention,
-                                          default_split, workloads)
+    from paged_kv_cache_146_gb300 import KVPool, default_split, workloads
     from paged_kv_cache_146_gb300.engine import DecodeEngine
 
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    e2e_steps = args.e2e_steps
     e2e_warmup = 3 if e2e_steps > 0 else 0
-    n_steps = args.warmup + args.steps + e2e_warmup + e2e_steps
-    q8 = args.workload == "gqa_long_q8"
-    if args.workload in ("gqa_long", "gqa_long_q8"):
+    n_steps = warmup + steps * repeats + e2e_warmup + e2e_steps
+    q8 = workload == "gqa_long_q8"
+    if workload in ("gqa_long", "gqa_long_q8"):
         w = rank_workload(args.seed, rank, args.num_seqs, n_steps + 16)
     else:
-        w = workloads.CONFIGS[args.workload](args.seed + rank)
+        w = workloads.CONFIGS[workload](args.seed + rank)
         # room for the timed steps' growth
         need_b = -(-(int(w.prior_lens.max()) + n_steps + 16) // 16)
         if need_b > w.max_blocks_per_seq:
@@ -368,89 +376,94 @@ def our_arm(args, world, rank, local):
     def draw(*shape):
         return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(tdt)
 
-    qs = [draw(S, hq, d) for _ in range(args.warmup + args.steps)]
-    ks = [draw(S, hkv, d) for _ in range(args.warmup + args.steps)]
-    vs = [draw(S, hkv, d) for _ in range(args.warmup + args.steps)]
+    n_draw = warmup + steps          # the repeats cycle through the same step inputs
+    qs = [draw(S, hq, d) for _ in range(n_draw)]
+    ks = [draw(S, hkv, d) for _ in range(n_draw)]
+    vs = [draw(S, hkv, d) for _ in range(n_draw)]
     stream = torch.cuda.current_stream()
 
     def step(i, ev=None):
         eng.host_step()
         if ev:
             ev[2].record(stream)
-        eng.write(ks[i], vs[i])
+        eng.write(ks[i % n_draw], vs[i % n_draw])
         if ev:
             ev[0].record(stream)
-        eng.attend(qs[i])
+        eng.attend(qs[i % n_draw])
         if ev:
             ev[1].record(stream)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     rc, word = eng.check()
     if rc != 0:
-        raise SystemExit(f"device status {rc} word {word:#x} after warm-up")
+        raise SystemExit(f"device status {rc} word {word:#x} after warm-up ({workload})")
 
-    gpu_uuid = None
-    try:
-        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    clocks = ClockSampler(gpu_uuid)
-    bytes_total, toks_total = 0, 0
-    attn_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
-               for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks.start()
-    time.sleep(0.25)
-    barrier(world)
-    torch.cuda.synchronize()
-    start.record(stream)
-    for k in range(args.steps):
-        step(args.warmup + k, attn_ev[k])
-        bytes_total += eng.step_bytes()
-        toks_total += int(eng.lens.astype(np.int64).sum())
-    stop.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    attn_ms = [a.elapsed_time(b) for a, b, _ in attn_ev]
-    cw_ms = [c.elapsed_time(a) for a, _, c in attn_ev]      # this step's cache write
+    ev = lambda: torch.cuda.Event(enable_timing=True)    # noqa: E731
+    region_ms, region_bytes, region_toks, attn_ms, cw_ms = [], [], [], [], []
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.25)
+    i = warmup
+    for _ in range(repeats):
+        attn_ev = [(ev(), ev(), ev()) for _ in range(steps)]
+        start, stop = ev(), ev()
+        nbytes, toks = 0, 0
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(steps):
+            step(i, attn_ev[k])
+            i += 1
+            nbytes += eng.step_bytes()
+            toks += int(eng.lens.astype(np.int64).sum())
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        region_ms.append(max_over_ranks(start.elapsed_time(stop), world))
+        region_bytes.append(nbytes)
+        region_toks.append(toks)
+        attn_ms += [a.elapsed_time(b) for a, b, _ in attn_ev]
+        cw_ms += [c.elapsed_time(a) for a, _, c in attn_ev]
+    clk = clocks.stop() if clocks is not None else None
     rc, word = eng.check()
     if rc != 0:
-        raise SystemExit(f"device status {rc} word {word:#x} in the timed steps")
-    elapsed_ms = max_over_ranks(elapsed_ms, world)
-    bytes_all = bytes_total * world
-    toks_all = toks_total * world
-    value = job_rate(bytes_total, world, elapsed_ms)
-    peak, peak_kind = peaks()
+        raise SystemExit(f"device status {rc} word {word:#x} in the timed steps ({workload})")
+    rates = [job_rate(b, world, t) for b, t in zip(region_bytes, region_ms)]
+    med = sorted(range(repeats), key=lambda r: rates[r])[repeats // 2]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    bytes_per_launch = bytes_total / args.steps
-    achieved = bytes_per_launch / (attn_avg_ms * 1e-3) / 1e9
+    bytes_per_launch = sum(region_bytes) / (steps * repeats)
+    res = {"w": w, "pool": pool, "q8": q8, "S": S, "hq": hq, "hkv": hkv, "d": d,
+           "value": rates[med], "repeat_values": [round(r, 2) for r in rates],
+           "ms_per_step": region_ms[med] / steps, "region_toks": region_toks[med],
+           "region_ms": region_ms[med], "bytes_per_launch": bytes_per_launch,
+           "attn_avg_ms": attn_avg_ms, "attn_median_ms": statistics.median(attn_ms),
+           "toks_per_step": region_toks[med] / steps, "clocks": clk,
+           "launches_per_step": 1 + (3 if eng.maxb > (eng.split_for_step() or default_split())
+                                     else 2)}
 
     # ---- end to end through the public API with host buffers
-    e2e = None
     if e2e_steps > 0:
         n_e = e2e_warmup + e2e_steps
-        hq_h = [qs[i % len(qs)].cpu().pin_memory() for i in range(n_e)]
-        hk_h = [ks[i % len(ks)].cpu().pin_memory() for i in range(n_e)]
-        hv_h = [vs[i % len(vs)].cpu().pin_memory() for i in range(n_e)]
+        hq_h = [qs[j % n_draw].cpu().pin_memory() for j in range(n_e)]
+        hk_h = [ks[j % n_draw].cpu().pin_memory() for j in range(n_e)]
+        hv_h = [vs[j % n_draw].cpu().pin_memory() for j in range(n_e)]
         out_h = [torch.empty_like(eng.out, device="cpu").pin_memory() for _ in range(n_e)]
-        for i in range(e2e_warmup):      # untimed: copy streams and buffers come up here
-            eng.decode_step_host(hq_h[i], hk_h[i], hv_h[i], out_h[i])
+        for j in range(e2e_warmup):      # untimed: copy streams and buffers come up here
+            eng.decode_step_host(hq_h[j], hk_h[j], hv_h[j], out_h[j])
         eng.join_copies()
         hq_h, hk_h, hv_h, out_h = (x[e2e_warmup:] for x in (hq_h, hk_h, hv_h, out_h))
-        e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_start, e_stop = ev(), ev()
         e_bytes = 0
         barrier(world)
         torch.cuda.synchronize()
         e_start.record(stream)
         eng.copies_after(e_start)
-        for i in range(e2e_steps):
+        for j in range(e2e_steps):
             # inputs from pinned host memory, output back to it: transfers overlap
             # the neighbouring steps' kernels and stay inside the timed region
-            eng.decode_step_host(hq_h[i], hk_h[i], hv_h[i], out_h[i])
+            eng.decode_step_host(hq_h[j], hk_h[j], hv_h[j], out_h[j])
             e_bytes += eng.step_bytes()
         eng.join_copies()
         e_stop.record(stream)
@@ -459,37 +472,102 @@ def our_arm(args, world, rank, local):
         e_ms = max_over_ranks(e_start.elapsed_time(e_stop), world)
         h2d = (hq_h[0].numel() + hk_h[0].numel() + hv_h[0].numel()) * 2 + \
             eng.h_tables.numel() * 4 + eng.h_lens.numel() * 4 + eng.h_slots.numel() * 8
-        e2e = {"value": round(e_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out_h[0].numel() * 2),
-               "ms_per_step": round(e_ms / e2e_steps, 4)}
+        res["e2e"] = {"value": round(e_bytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": int(h2d),
+                      "d2h_bytes_per_step": int(out_h[0].numel() * 2),
+                      "ms_per_step": round(e_ms / e2e_steps, 4)}
         rc, word = eng.check()
         if rc != 0:
             raise SystemExit(f"device status {rc} word {word:#x} in the e2e steps")
 
-    # the cache write, reported on its own: the decode step's (one token per
-    # sequence, timed above) and the prompts' (every prompt token, written
-    # again into the same slots -- the cache is unchanged -- and timed once)
-    k_pr, v_pr, d_slots_pr = prompt_rows
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    c0.record(stream)
-    eng.write(k_pr, v_pr, d_slots_pr)
-    c1.record(stream)
-    torch.cuda.synchronize()
-    rc, word = eng.check()
-    if rc != 0:
-        raise SystemExit(f"device status {rc} word {word:#x} in the prompt write")
-    row_out = (2 * (d + d // 32 * 2) if q8 else 2 * d * 2) * hkv     # K+V bytes stored per token
-    row_in = 2 * d * 2 * hkv                                          # K+V bytes read per token
-    T_pr = int(d_slots_pr.shape[0])
-    cw_step_ms = sum(cw_ms) / len(cw_ms)
-    cache_write_line = {
-        "bytes": "T x (K+V row bytes read + stored) + 8 T",
-        "step_tokens": S, "step_us": round(1e3 * cw_step_ms, 2),
-        "step_gbs": round(S * (row_in + row_out + 8) / (cw_step_ms * 1e-3) / 1e9, 2),
-        "prompt_tokens": T_pr, "prompt_ms": round(c0.elapsed_time(c1), 4),
-        "prompt_gbs": round(T_pr * (row_in + row_out + 8) / (c0.elapsed_time(c1) * 1e-3) / 1e9, 2)}
-    del prompt_rows, k_pr, v_pr
+    if prompt_write:
+        # the cache write, reported on its own: the decode step's (one token per
+        # sequence, timed above) and the prompts' (every prompt token, written
+        # again into the same slots -- the cache is unchanged -- and timed once)
+        k_pr, v_pr, d_slots_pr = prompt_rows
+        c0, c1 = ev(), ev()
+        torch.cuda.synchronize()
+        c0.record(stream)
+        eng.write(k_pr, v_pr, d_slots_pr)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        rc, word = eng.check()
+        if rc != 0:
+            raise SystemExit(f"device status {rc} word {word:#x} in the prompt write")
+        row_out = (2 * (d + d // 32 * 2) if q8 else 2 * d * 2) * hkv   # K+V bytes stored per token
+        row_in = 2 * d * 2 * hkv                                        # K+V bytes read per token
+        T_pr = int(d_slots_pr.shape[0])
+        cw_step_ms = sum(cw_ms) / len(cw_ms)
+        res["cache_write"] = {
+            "bytes": "T x (K+V row bytes read + stored) + 8 T",
+            "step_tokens": S, "step_us": round(1e3 * cw_step_ms, 2),
+            "step_gbs": round(S * (row_in + row_out + 8) / (cw_step_ms * 1e-3) / 1e9, 2),
+            "prompt_tokens": T_pr, "prompt_ms": round(c0.elapsed_time(c1), 4),
+            "prompt_gbs": round(T_pr * (row_in + row_out + 8) / (c0.elapsed_time(c1) * 1e-3) / 1e9,
+                                2)}
+    del prompt_rows, qs, ks, vs, eng
+    return res
+
+
+def config_summary(args, workload: str, world: int, rank: int, dev) -> dict:
+    """Attention-call rate of a further decode workload (20 timed steps after 3
+    warm-ups), for the ``configs`` object of the headline line."""
+    import torch
+    r = decode_run(args, workload, world, rank, dev, steps=20, warmup=3)
+    peak, _ = peaks()
+    achieved = r["bytes_per_launch"] / (r["attn_avg_ms"] * 1e-3) / 1e9
+    out = {"attention_gbs": round(achieved, 2), "pct_of_peak": round(100 * achieved / peak, 2),
+           "attention_ms": round(r["attn_avg_ms"], 4),
+           "step_gbs": round(r["value"], 2),
+           "seq_tokens_per_s": round(r["toks_per_step"] / (r["attn_avg_ms"] * 1e-3), 1),
+           "bytes_per_call": int(r["bytes_per_launch"]),
+           "num_seqs": r["S"], "q_heads": r["hq"], "kv_heads": r["hkv"], "head_dim": r["d"],
+           "kv_dtype": r["pool"].dtype, "lengths": LENGTHS[workload]}
+    if workload == "shared_prefix":
+        traffic = profiled_traffic(workload) if args.seed == 0 else None
+        out["dram_bytes_per_call"] = traffic
+        if traffic:
+            out["dram_gbs"] = round(traffic / (r["attn_avg_ms"] * 1e-3) / 1e9, 2)
+            out["dram_pct_of_peak"] = round(100 * out["dram_gbs"] / peak, 2)
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
+def our_arm(args, world, rank, local):
+    import torch
+
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid)
+    r = decode_run(args, args.workload, world, rank, dev, args.steps, args.warmup,
+                   repeats=args.repeats, e2e_steps=args.e2e_steps, prompt_write=True,
+                   clocks=clocks)
+    w, q8, S, hq, hkv, d = r["w"], r["q8"], r["S"], r["hq"], r["hkv"], r["d"]
+    peak, peak_kind = peaks()
+    value = r["value"]
+    attn_avg_ms = r["attn_avg_ms"]
+    bytes_per_launch = r["bytes_per_launch"]
+    achieved = bytes_per_launch / (attn_avg_ms * 1e-3) / 1e9
+    dtype_name, pool_dtype = w.dtype, r["pool"].dtype
+    e2e, cache_write_line = r.get("e2e"), r.get("cache_write")
+    toks_region, region_ms = r["region_toks"], r["region_ms"]
+    clk, repeat_values, launches = r["clocks"], r["repeat_values"], r["launches_per_step"]
+    del r
+    torch.cuda.empty_cache()
+
+    # the other decode configurations, after the headline's timed regions
+    configs = None
+    if args.configs and args.workload == "gqa_long" and args.num_seqs == 256:
+        configs = {}
+        for wl in ("opt13b", "shared_prefix", "gqa_long_q8", "tiny"):
+            configs[wl] = config_summary(args, wl, world, rank, dev)
+        configs["trace"] = trace_summary(args, world, rank, dev)
 
     if rank != 0:
         return
@@ -500,6 +578,10 @@ def our_arm(args, world, rank, local):
         cpu = {"value": round(sample.nbytes / dt / 1e9, 4), "unit": "GB/s",
                "cores": sample.threads, "kind": "oracle", "sample": sample.desc,
                "seconds": round(dt, 2)}
+        one = oracle_calibrated(args.seed, args.cpu_seconds / 2, q8, args.workload, threads=1)
+        dt1 = one.run()
+        cpu["single_thread"] = {"value": round(one.nbytes / dt1 / 1e9, 4), "unit": "GB/s",
+                                "cores": 1, "sample": one.desc, "seconds": round(dt1, 2)}
     traffic = args.traffic
     if traffic is None and args.num_seqs == 256 and args.seed == 0 and not q8:
         traffic = profiled_traffic(args.workload)
@@ -513,25 +595,32 @@ def our_arm(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "ms_per_step": round(region_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name, "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": S, "q_heads": hq, "kv_heads": hkv,
-                   "head_dim": d, "block_size": 16, "kv_dtype": pool.dtype,
+                   "head_dim": d, "block_size": 16, "kv_dtype": pool_dtype,
                    "lengths": LENGTHS[args.workload],
                    "shared_prefix_tokens": w.shared_prefix_tokens,
-                   "mean_context": round(toks_total / args.steps / S, 1),
+                   "mean_context": round(toks_region / args.steps / S, 1),
                    "pool_blocks": w.num_blocks,
-                   "l2": ("inputs larger than L2 (KV per step ~%.1f GB vs 129 MB L2)" % (bytes_per_launch / 1e9)
+                   "l2": ("inputs larger than L2 (KV per step ~%.1f GB vs 129 MB L2)"
+                          % (bytes_per_launch / 1e9)
                           if not w.shared_prefix_tokens else
                           "unique KV larger than L2; the shared prefix (%d tokens) is re-read from L2"
                           % w.shared_prefix_tokens),
+                   "timed": (f"{args.repeats} regions of {args.steps} steps, each bracketed by a "
+                             "barrier and a synchronisation; value, ms_per_step = the median "
+                             "region"),
                    "step": "host ledger + table/lens/slots H2D + cache_write + paged attention"},
-        "seq_tokens_per_s": round(toks_all / (elapsed_ms * 1e-3), 1),
+        "seq_tokens_per_s": round(toks_region * world / (region_ms * 1e-3), 1),
         "pct_of_peak": round(100.0 * value / peak, 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / 8000.0, 2),
+        "repeat_values": repeat_values,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
                      "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
                      "kernel": ("paged_decode_attention_q8" if q8 else "paged_decode_attention")
                      + " (prep + main + merge kernels)",
                      "bytes_per_launch": int(bytes_per_launch),
@@ -540,8 +629,8 @@ def our_arm(args, world, rank, local):
         "e2e": e2e,
         "cache_write": cache_write_line,
         **({"dram": dram} if dram else {}),
-        "gpu_launches": (4 if eng.maxb > (eng.split_for_step() or default_split()) else 3)
-        * args.steps,
+        **({"configs": configs} if configs else {}),
+        "gpu_launches": launches * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -722,56 +811,102 @@ def blocks_arm(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
-def trace_arm(args, world, rank, local):
-    """Continuous-batching trace: 500 steps (or --steps) of FCFS admission,
-    prefill, decode and release; per-step attention GB/s (CUDA events around the
-    attention call) and whole-step wall time including the host ledger."""
+def _pct(xs, q):
+    xs = sorted(xs)
+    return xs[int(q * (len(xs) - 1))]
+
+
+def trace_run(args, world, rank, dev, steps: int | None = None) -> dict:
+    """The continuous-batching trace (500 steps of FCFS admission, prefill,
+    decode and release), the host enqueueing step after step with no
+    synchronisation in between, so the host side of step t + 1 overlaps the
+    GPU work of step t.  Per step: host seconds of each phase (perf_counter)
+    and device milliseconds of each phase (CUDA events)."""
     import torch
     from paged_kv_cache_146_gb300 import workloads
     from paged_kv_cache_146_gb300.trace import TraceRunner
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
     sched = workloads.trace(seed=5 + args.seed + rank,
                             pool_bytes=int(args.pool_gib * 2**30) if args.pool_gib else 40 * 2**30)
-    steps = min(args.steps, sched.steps) if args.steps != 20 else sched.steps
+    steps = sched.steps if steps is None else min(steps, sched.steps)
     order = np.random.default_rng(sched.seed).permutation(sched.num_blocks).astype(np.int32)
     run = TraceRunner(sched, dev, free_order=order)
-    rates, walls, attn = [], [], []
+    recs = []
+    torch.cuda.synchronize()
+    barrier(world)
     t_all = time.perf_counter()
     for t in range(steps):
-        t0 = time.perf_counter()
         rec = run.step(t)
-        torch.cuda.synchronize()
-        walls.append(time.perf_counter() - t0)
-        e0, e1 = rec.extra["events"]
-        ms = e0.elapsed_time(e1)
-        if ms and rec.kv_bytes:
-            attn.append(ms)
-            rates.append(rec.kv_bytes / (ms * 1e-3) / 1e9)
-    total_s = time.perf_counter() - t_all
+        recs.append((rec.kv_bytes, rec.extra["phase_events"], rec.extra["host_s"],
+                     int(rec.ctx.astype(np.int64).sum())))
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t_all
+    barrier(world)
     rc, word = run.check()
     if rc != 0:
         raise SystemExit(f"device status {rc} word {word:#x}")
+    rates, attn, h2d, cw = [], [], [], []
+    host = [[], [], [], []]
+    for kv_bytes, evs, hs, _ in recs:
+        ms = evs[2].elapsed_time(evs[3])
+        h2d.append(1e3 * evs[0].elapsed_time(evs[1]))
+        cw.append(1e3 * evs[1].elapsed_time(evs[2]))
+        for i in range(4):
+            host[i].append(1e6 * hs[i])
+        if ms and kv_bytes:
+            attn.append(ms)
+            rates.append(kv_bytes / (ms * 1e-3) / 1e9)
+    peak, _ = peaks()
+    names = ("schedule_and_ledger", "wait_for_previous_handoff", "enqueue_device_work",
+             "release_finished")
+
+    def dist(xs):
+        return {"median": round(statistics.median(xs), 2), "p90": round(_pct(xs, 0.9), 2)}
+
+    res = {"steps": steps, "pool_blocks": sched.num_blocks,
+           "attention_gbs_median": round(statistics.median(rates), 2),
+           "attention_gbs_p90": round(_pct(rates, 0.9), 2),
+           "attention_gbs_p10": round(_pct(rates, 0.1), 2),
+           "pct_of_peak_median": round(100 * statistics.median(rates) / peak, 2),
+           "attention_ms_median": round(statistics.median(attn), 4),
+           "step_ms_pipelined": round(1e3 * wall_s / steps, 4),
+           "phases": {"unit": "host phases in us (perf_counter), device phases in us "
+                              "(CUDA events): median and p90 over steps",
+                      "host": {n: dist(x) for n, x in zip(names, host)},
+                      "device": {"h2d_tables_lens_slots": dist(h2d),
+                                 "cache_write": dist(cw),
+                                 "attention": dist([1e3 * a for a in attn])}},
+           "swapped_gb": round(run.swapped_bytes / 1e9, 3),
+           "total_s": round(wall_s, 2)}
+    del run, recs
+    torch.cuda.empty_cache()
+    return res
+
+
+def trace_summary(args, world, rank, dev) -> dict:
+    return trace_run(args, world, rank, dev)
+
+
+def trace_arm(args, world, rank, local):
+    """Continuous-batching trace: 500 steps (or --steps) of FCFS admission,
+    prefill, decode and release; per-step attention GB/s (CUDA events around the
+    attention call), the pipelined step time and the per-phase split."""
+    import torch
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    r = trace_run(args, world, rank, dev, steps=None if args.steps == 20 else args.steps)
     if rank != 0:
         return
-    peak, kind = peaks()
-    rates_sorted = sorted(rates)
-    line = {"metric": METRIC, "value": round(statistics.median(rates), 2), "unit": "GB/s",
-            "n_gpus": world, "steps": steps, "warmup": 0,
-            "ms_per_step": round(1e3 * statistics.median(walls), 4), "higher_is_better": True,
+    line = {"metric": METRIC, "value": r["attention_gbs_median"], "unit": "GB/s",
+            "n_gpus": world, "steps": r["steps"], "warmup": 0,
+            "ms_per_step": r["step_ms_pipelined"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "trace", "arrivals_per_step": 8, "prompt": "U[64,1024]",
                        "output": "Geometric(1/200) capped at 2048", "max_running": 512,
-                       "pool_blocks": sched.num_blocks,
-                       "value": "median over steps of attention GB/s"},
-            "p90_gbs": round(rates_sorted[int(0.9 * (len(rates) - 1))], 2),
-            "p10_gbs": round(rates_sorted[int(0.1 * (len(rates) - 1))], 2),
-            "pct_of_peak_median": round(100 * statistics.median(rates) / peak, 2),
-            "attention_ms_median": round(statistics.median(attn), 4),
-            "step_wall_ms_median": round(1e3 * statistics.median(walls), 4),
-            "step_wall_ms_p90": round(1e3 * sorted(walls)[int(0.9 * (len(walls) - 1))], 4),
-            "total_s": round(total_s, 2),
-            "swapped_gb": round(run.swapped_bytes / 1e9, 3)}
+                       "pool_blocks": r["pool_blocks"],
+                       "value": "median over steps of attention GB/s",
+                       "ms_per_step": "wall time of the whole run / steps, host and GPU "
+                                      "pipelined (no synchronisation between steps)"},
+            **{k: v for k, v in r.items() if k not in ("steps", "pool_blocks")}}
     print(json.dumps(line), flush=True)
 
 
@@ -791,6 +926,10 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=256,
                     help="sequences per GPU (256 is the workload; fewer only for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--repeats", type=int, default=10,
+                    help="timed regions of --steps steps each; the median region is reported")
+    ap.add_argument("--configs", type=int, default=1,
+                    help="1: the headline line also carries the other decode configurations")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "f16"],
                     help="cache dtype of the prefill workload")

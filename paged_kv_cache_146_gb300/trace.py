@@ -18,9 +18,17 @@ sequences return, earliest arrival first, as soon as their blocks fit.
 
 Batch rows are fixed ([max_running] rows in every table and tensor); a row with
 context length 0 is idle, so the kernels see one shape for the whole run.
+
+The synthetic K/V rows and queries a model would produce are drawn once, before
+the run (N(0,1) from the schedule's seed), and each step takes its rows from
+them, so a step's cost is the serving loop's own: host scheduling and ledger,
+the hand-off of tables, lengths and slots to the GPU, the cache write, the
+attention call and the release of finished sequences.  Each step records the
+host time of its phases and CUDA events around its device phases.
 """
 from __future__ import annotations
 
+import time
 from collections import deque
 from dataclasses import dataclass, field
 
@@ -76,6 +84,12 @@ class TraceRunner:
         self.out = torch.zeros((S, sched.num_q_heads, sched.head_dim), dtype=tdt, device=device)
         self.gen = torch.Generator(device=device)
         self.gen.manual_seed(sched.seed + 2000)
+        # the step inputs, drawn once: K/V rows (a window per step) and a few
+        # query sets (one per step, in turn)
+        self.kv_rows = 32768
+        self.k_src = self._draw(self.kv_rows, sched.num_kv_heads, sched.head_dim)
+        self.v_src = self._draw(self.kv_rows, sched.num_kv_heads, sched.head_dim)
+        self.q_src = [self._draw(S, sched.num_q_heads, sched.head_dim) for _ in range(4)]
         self.scale = 1.0 / float(np.sqrt(sched.head_dim))
         self.swapped = deque()                            # evicted: (state, length, host, ids)
         self.swapped_bytes = 0
@@ -91,11 +105,16 @@ class TraceRunner:
         self._copied = None
         # the step's queries land in a fixed buffer, so the attention call can
         # be one CUDA graph replay (all lengths are zero at capture)
-        self.q32 = torch.empty((S, sched.num_q_heads, sched.head_dim), dtype=torch.float32,
-                               device=device)
         self.q = torch.empty((S, sched.num_q_heads, sched.head_dim), dtype=tdt, device=device)
         self.captured = CapturedDecode(self.pool, self.q, self.d_tables, self.d_ctx, self.scale,
                                        self.workspace, self.status, self.out) if graph else None
+
+    def _step_rows(self, t: int, n: int):
+        """K/V rows of a step's n new tokens: a window of the rows drawn up front."""
+        if n > self.kv_rows:
+            raise ValueError(f"step {t} appends {n} tokens, more than the {self.kv_rows} drawn")
+        off = (t * 7919) % (self.kv_rows - n + 1)
+        return self.k_src[off:off + n], self.v_src[off:off + n]
 
     def _stage_slots(self, slots: np.ndarray):
         """Device copy of this step's slot mapping, through pinned memory."""
@@ -161,6 +180,7 @@ class TraceRunner:
 
     def step(self, t: int, keep_tensors: bool = False) -> StepRecord:
         torch, sc, bs = self.torch, self.sched, self.sched.block_size
+        h0 = time.perf_counter()
         for prompt, out_len in sc.arrivals[t]:
             self.waiting.append((self.next_id, prompt, out_len))
             self.next_id += 1
@@ -208,31 +228,35 @@ class TraceRunner:
         ctx = np.zeros(self.S, dtype=np.int32)
         for r in decoding:
             ctx[r] = self.lens[r]
+        h1 = time.perf_counter()
         # hand-off to the GPU and the device steps
         n_tok = int(num_new.sum())
-        k_new = self._draw(n_tok, sc.num_kv_heads, sc.head_dim)
-        v_new = self._draw(n_tok, sc.num_kv_heads, sc.head_dim)
-        torch.randn(self.q32.shape, generator=self.gen, device=self.device, dtype=torch.float32,
-                    out=self.q32)
-        q = self.q.copy_(self.q32)
+        k_new, v_new = self._step_rows(t, n_tok)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        q = self.q.copy_(self.q_src[t % len(self.q_src)])     # this step's queries arrive
         self._wait_copied()
-        if n_tok:
-            cache_write(self.pool, k_new, v_new, self._stage_slots(slots), self.status)
+        h2 = time.perf_counter()
+        # the ledger's arrays to the GPU (slots, tables, lengths), then the write
+        # of the new K/V, then attention
+        evs[0].record()
+        d_slots = self._stage_slots(slots) if n_tok else None
         self.h_tables.numpy()[:] = self.tables
         self.h_ctx.numpy()[:] = ctx
         self.d_tables.copy_(self.h_tables, non_blocking=True)
         self.d_ctx.copy_(self.h_ctx, non_blocking=True)
         self._copied = torch.cuda.Event()
         self._copied.record()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record()
+        evs[1].record()
+        if n_tok:
+            cache_write(self.pool, k_new, v_new, d_slots, self.status)
+        evs[2].record()
         if self.captured is not None:
             self.captured.replay()
         else:
             paged_decode_attention(self.pool, q, self.d_tables, self.d_ctx, self.scale,
                                    self.workspace, self.status, out=self.out)
-        ev1.record()
+        evs[3].record()
+        h3 = time.perf_counter()
         kv_bytes = int(ctx.astype(np.int64).sum()) * sc.num_kv_heads * sc.head_dim * 2 * 2
         # finished sequences give their blocks back
         finished = []
@@ -248,8 +272,13 @@ class TraceRunner:
             self.lens[r] = 0
             del self.state[r]
             self.free_rows.append(r)
+        h4 = time.perf_counter()
         rec = StepRecord(t, admitted, decoding, finished, num_new, slots, ctx, kv_bytes)
-        rec.extra["events"] = (ev0, ev1)
+        rec.extra["events"] = (evs[2], evs[3])       # around the attention call
+        rec.extra["phase_events"] = evs             # h2d | cache write | attention
+        # host seconds: scheduling + ledger, waiting for the previous hand-off,
+        # enqueueing the device work, releasing finished sequences
+        rec.extra["host_s"] = (h1 - h0, h2 - h1, h3 - h2, h4 - h3)
         rec.extra["swapped_in"] = swapped_in
         rec.extra["swapped_out"] = swapped_out
         if keep_tensors:
