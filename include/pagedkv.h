@@ -152,6 +152,13 @@ int kv_block_refcount(const pkv_pool *pool, int32_t id, int32_t *out);
 /* Number of free blocks. */
 int kv_pool_num_free(const pkv_pool *pool, int32_t *out);
 
+/* Number of blocks currently referenced by two or more sequences ("vLLM의 핵심
+ * 원리 PagedAttention 파헤치기", section "같은 블록을 여러 요청이 나눠 쓴다":
+ * requests with a common prompt point their tables at the same physical
+ * blocks).  paged_decode_attention reads it to decide whether to look for
+ * shared table prefixes in the batch. */
+int kv_pool_num_shared(const pkv_pool *pool, int64_t *out);
+
 /* ------------------------------------------- on-demand allocation + slots */
 
 /* Grow num_seqs sequences: sequence s holds seq_lens[s] tokens and gains
@@ -296,7 +303,9 @@ int kv_cache_write(const pkv_pool *pool, const void *k_new, const void *v_new,
 /* ---------------------------------------------------- paged decode attention */
 
 /* Workspace bytes paged_decode_attention needs for these sizes (split-K
- * partials, work list, merge counters).  0 on a bad argument. */
+ * partials, work list, merge counters, and room for shared prefixes: up to 4
+ * more pieces per sequence and the shared-prefix work list).  0 on a bad
+ * argument. */
 size_t paged_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                     int32_t num_kv_heads, int32_t head_dim,
                                     int32_t max_blocks_per_seq);
@@ -321,6 +330,21 @@ size_t paged_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * Sequences with context_len == 0 get zero rows (R7); a sequence with a bad
  * length or table entry gets a zero row and a status bit.  The result is
  * identical whatever the physical placement of the blocks.
+ *
+ * Shared prefixes ("PagedAttention 파헤치기", section "같은 블록을 여러 요청이
+ * 나눠 쓴다": requests with a common prompt share its physical blocks).  When the
+ * pool's ledger holds blocks with a reference count of 2 or more at the time of
+ * the call (kv_pool_num_shared > 0), the call looks at the tables on the device:
+ * neighbouring sequences whose rows agree on at least 16 leading valid block ids
+ * (counted up to the block before each one's last token) are linked, and a run
+ * of two or more linked sequences reads its shortest link's blocks once -- one
+ * tcgen05 contraction of all members' query rows against those keys, in up to 4
+ * key chunks -- while each member's partitions cover only the blocks after
+ * them; the pieces merge by the same log-sum-exp rule.  The result is the same
+ * attention, within fp32 rounding of a different summation order; sequences
+ * outside runs are untouched.  Only the ledger's count decides whether the call
+ * looks (a CUDA graph captured while it is 0 never looks); only the tables
+ * decide what is shared.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA. */
 int paged_decode_attention(const pkv_pool *pool, void *out, const void *q,
                            const void *k_pool, const void *v_pool,

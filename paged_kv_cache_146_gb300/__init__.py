@@ -255,6 +255,12 @@ class KVPool:
         check(lib().kv_block_refcount(self.handle, block_id, ctypes.byref(out)), "kv_block_refcount")
         return out.value
 
+    def num_shared(self) -> int:
+        """Blocks referenced by two or more sequences."""
+        out = ctypes.c_int64()
+        check(lib().kv_pool_num_shared(self.handle, ctypes.byref(out)), "kv_pool_num_shared")
+        return out.value
+
     def num_free(self) -> int:
         out = ctypes.c_int32()
         check(lib().kv_pool_num_free(self.handle, ctypes.byref(out)), "kv_pool_num_free")

@@ -39,6 +39,7 @@ SIGNATURES = [
     ("kv_block_free", ctypes.c_int, [_p, _i32, _p]),
     ("kv_block_refcount", ctypes.c_int, [_p, _i32, _pi32]),
     ("kv_pool_num_free", ctypes.c_int, [_p, _pi32]),
+    ("kv_pool_num_shared", ctypes.c_int, [_p, ctypes.POINTER(_i64)]),
     ("kv_append_slots", ctypes.c_int, [_p, _i32, _p, _p, _p, _i32, _p]),
     ("kv_seq_fork", ctypes.c_int, [_p, _p, _i32, _p, _i32]),
     ("kv_append_slots_cow", ctypes.c_int, [_p, _i32, _p, _p, _p, _i32, _p, _p, _p, _pi32]),

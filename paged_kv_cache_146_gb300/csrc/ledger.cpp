@@ -27,6 +27,21 @@ struct pkv_pool {
     pkv_dtype dtype;
     std::vector<int32_t> stack;   // free blocks; back() is handed out next
     std::vector<int32_t> refs;    // refcount per block, 0 = free
+    int64_t shared = 0;           // blocks whose refcount is 2 or more
+
+    // every reference-count change goes through these two, which keep `shared`
+    void take(int32_t id) { refs[(size_t)id] = 1; }
+    void add_ref(int32_t id)
+    {
+        if (++refs[(size_t)id] == 2) ++shared;
+    }
+    // returns the new count
+    int32_t drop_ref(int32_t id)
+    {
+        const int32_t r = --refs[(size_t)id];
+        if (r == 1) --shared;
+        return r;
+    }
 };
 
 namespace pkv {
@@ -40,6 +55,8 @@ bool pool_geometry(const pkv_pool *p, PoolGeometry *g)
     g->dtype = p->dtype;
     return true;
 }
+
+bool pool_has_shared_blocks(const pkv_pool *p) { return p && p->shared > 0; }
 }  // namespace pkv
 
 extern "C" {
@@ -151,7 +168,7 @@ int kv_block_alloc(pkv_pool *pool, int32_t n, int32_t *out_ids)
     for (int32_t i = 0; i < n; ++i) {
         int32_t id = pool->stack.back();
         pool->stack.pop_back();
-        pool->refs[(size_t)id] = 1;
+        pool->take(id);
         out_ids[i] = id;
     }
     return PKV_OK;
@@ -163,7 +180,7 @@ int kv_block_ref(pkv_pool *pool, int32_t n, const int32_t *ids)
     for (int32_t i = 0; i < n; ++i)
         if (ids[i] < 0 || ids[i] >= pool->num_blocks || pool->refs[(size_t)ids[i]] < 1)
             return PKV_ERR_BAD_BLOCK;
-    for (int32_t i = 0; i < n; ++i) pool->refs[(size_t)ids[i]] += 1;
+    for (int32_t i = 0; i < n; ++i) pool->add_ref(ids[i]);
     return PKV_OK;
 }
 
@@ -183,7 +200,7 @@ int kv_block_free(pkv_pool *pool, int32_t n, const int32_t *ids)
     // apply in argument order: a block joins the free stack when it reaches 0
     for (int32_t i = 0; i < n; ++i) {
         int32_t id = ids[i];
-        if (--pool->refs[(size_t)id] == 0) pool->stack.push_back(id);
+        if (pool->drop_ref(id) == 0) pool->stack.push_back(id);
     }
     return PKV_OK;
 }
@@ -200,6 +217,13 @@ int kv_pool_num_free(const pkv_pool *pool, int32_t *out)
 {
     if (!pool || !out) return PKV_ERR_INVALID_ARG;
     *out = (int32_t)pool->stack.size();
+    return PKV_OK;
+}
+
+int kv_pool_num_shared(const pkv_pool *pool, int64_t *out)
+{
+    if (!pool || !out) return PKV_ERR_INVALID_ARG;
+    *out = pool->shared;
     return PKV_OK;
 }
 
@@ -235,7 +259,7 @@ int kv_append_slots(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_lens,
             if (pos % bs == 0) {
                 int32_t id = pool->stack.back();
                 pool->stack.pop_back();
-                pool->refs[(size_t)id] = 1;
+                pool->take(id);
                 row[pos / bs] = id;
             }
             slot_mapping[t++] = (int64_t)row[pos / bs] * bs + pos % bs;
@@ -256,7 +280,7 @@ int kv_seq_fork(pkv_pool *pool, const int32_t *parent_row, int32_t parent_len,
         if (id < 0 || id >= pool->num_blocks || pool->refs[(size_t)id] < 1) return PKV_ERR_BAD_BLOCK;
     }
     for (int64_t i = 0; i < nb; ++i) {
-        pool->refs[(size_t)parent_row[i]] += 1;
+        pool->add_ref(parent_row[i]);
         child_row[i] = parent_row[i];
     }
     for (int64_t i = nb; i < max_blocks_per_seq; ++i) child_row[i] = -1;
@@ -305,8 +329,8 @@ int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_len
             if (pool->refs[(size_t)tail] > 1) {   // copy on write
                 const int32_t fresh = pool->stack.back();
                 pool->stack.pop_back();
-                pool->refs[(size_t)fresh] = 1;
-                pool->refs[(size_t)tail] -= 1;
+                pool->take(fresh);
+                pool->drop_ref(tail);
                 copy_src[copies] = tail;
                 copy_dst[copies] = fresh;
                 ++copies;
@@ -317,7 +341,7 @@ int kv_append_slots_cow(pkv_pool *pool, int32_t num_seqs, const int32_t *seq_len
             if (pos % bs == 0) {
                 const int32_t id = pool->stack.back();
                 pool->stack.pop_back();
-                pool->refs[(size_t)id] = 1;
+                pool->take(id);
                 row[pos / bs] = id;
             }
             slot_mapping[t++] = (int64_t)row[pos / bs] * bs + pos % bs;

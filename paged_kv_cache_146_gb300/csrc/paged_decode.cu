@@ -134,6 +134,133 @@ __device__ __forceinline__ int2 prep_scan2(int2 x, int2 (&warp_tot)[32], int lan
     return x;
 }
 
+// Shared prefixes, found from the tables (first part of the prep kernel when
+// the call looks for them).  The link from sequence s to s + 1 is the number
+// of leading table entries they share, up to the blocks that lie before the
+// last token of both (so each keeps at least one token of its own), counting
+// valid block ids only.  Links of at least kPrefixMinBlocks join sequences
+// into runs; a run of two or more members shares its shortest link: those
+// blocks are read once, split into at most kPrefixMaxPieces key chunks, each
+// chunk one piece per member (written by the shared-prefix kernel), and each
+// member's decode partitions start after them.  Writes seq_skip for every
+// sequence, the shared-prefix work list and its count (header[4]).
+__device__ void prep_prefix_runs(const Params &p, int2 (&warp_tot)[32], int tid, int lane,
+                                 int warp)
+{
+    const int S = p.num_seqs;
+    int32_t *lcp = p.prefix_scratch, *run_start = lcp + S, *run_min = run_start + S,
+            *run_n = run_min + S;
+    __shared__ int carry_start, n_items;
+    const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
+    // links: one warp per neighbouring pair, 128 table entries per round
+    for (int s = warp; s < S; s += 32) {
+        int link = 0;
+        if (s + 1 < S) {
+            const int La = p.context_lens[s], Lb = p.context_lens[s + 1];
+            int f = 0;
+            if (La > 0 && (int64_t)La <= max_tokens && Lb > 0 && (int64_t)Lb <= max_tokens)
+                f = min((La - 1) / kBlock, (Lb - 1) / kBlock);
+            const int32_t *ra = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
+            const int32_t *rb = ra + p.max_blocks_per_seq;
+            for (int base = 0; base < f; base += 128) {
+                int a[4], b[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = base + 32 * j + lane;
+                    a[j] = i < f ? __ldg(ra + i) : 0;
+                    b[j] = i < f ? __ldg(rb + i) : 0;
+                }
+                int first = 128;
+#pragma unroll
+                for (int j = 3; j >= 0; --j) {
+                    const int i = base + 32 * j + lane;
+                    const bool eq = i >= f || (a[j] == b[j] && a[j] >= 0 && a[j] < p.num_blocks);
+                    const unsigned ne = __ballot_sync(kFull, !eq);
+                    if (ne) first = 32 * j + __ffs(ne) - 1;
+                }
+                if (first < 128) {
+                    link = base + first;
+                    break;
+                }
+                link = min(f, base + 128);
+            }
+        }
+        if (lane == 0) {
+            lcp[s] = link;
+            run_min[s] = 0x7fffffff;
+            run_n[s] = 0;
+        }
+    }
+    if (tid == 0) {
+        carry_start = 0;
+        n_items = 0;
+    }
+    __syncthreads();
+    // runs: the start of s's run is the last t <= s not linked from t - 1 (a
+    // prefix maximum); every member counts itself into its run, every link
+    // takes part in the run's minimum
+    for (int base = 0; base < S; base += 1024) {
+        const int s = base + tid;
+        const bool in = s < S;
+        const bool from_prev = in && s > 0 && lcp[s - 1] >= kPrefixMinBlocks;
+        const bool to_next = in && lcp[s] >= kPrefixMinBlocks;
+        int x = in && !from_prev ? s : -1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x = max(x, y);
+        }
+        if (lane == 31) warp_tot[warp].x = x;
+        __syncthreads();
+        if (warp == 0) {
+            int t = warp_tot[lane].x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, t, o);
+                if (lane >= o) t = max(t, y);
+            }
+            warp_tot[lane].x = t;
+        }
+        __syncthreads();
+        const int rs = max(max(x, warp > 0 ? warp_tot[warp - 1].x : -1), carry_start);
+        if (in) {
+            run_start[s] = rs;
+            if (to_next) atomicMin(&run_min[rs], lcp[s]);
+            if (to_next || from_prev) atomicAdd(&run_n[rs], 1);
+        }
+        __syncthreads();
+        if (tid == 0) carry_start = max(carry_start, warp_tot[31].x);
+        __syncthreads();
+    }
+    // members: skip and pieces; the first member of a run lists its work
+    for (int s = tid; s < S; s += 1024) {
+        const int rs = run_start[s];
+        const int n = run_n[rs];
+        int2 sk = make_int2(0, 0);
+        if (n >= 2) {
+            const int pb = run_min[rs];
+            const int pieces = min(kPrefixMaxPieces, (pb + kPrefixMinBlocks - 1) / kPrefixMinBlocks);
+            sk = make_int2(pb, pieces);
+            if (s == rs) {
+                const int cb = (pb + pieces - 1) / pieces;
+                const int tt = p.prefix_tile_seqs;
+                const int tiles = (n + tt - 1) / tt;
+                const int at = atomicAdd(&n_items, tiles * pieces);
+                for (int t = 0; t < tiles; ++t)
+                    for (int j = 0; j < pieces; ++j) {
+                        const int k = at + t * pieces + j;
+                        if (dbg_fail(k < p.max_prefix_items, p.debug, 14, k)) continue;
+                        p.prefix_items[k] = make_int4(rs + t * tt, min(tt, n - t * tt) | (j << 16),
+                                                      j * cb, min(pb, (j + 1) * cb));
+                    }
+            }
+        }
+        p.seq_skip[s] = sk;
+    }
+    __syncthreads();
+    if (tid == 0) p.header[4] = min(n_items, p.max_prefix_items);
+}
+
 __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t head_dim)
 {
     __shared__ int2 warp_tot[32];
@@ -142,16 +269,25 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     __shared__ int warp_bin[32][kOrderBins];   // pass 2: per-warp counts, then offsets
     __shared__ long long auto_tot[32][kAutoSizes];
     __shared__ int chosen_split;
-    __shared__ int multi_count;
+    __shared__ int multi_count, n_partial;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_launch_dependents();   // the main kernel may set up its CTAs meanwhile
     if (tid == 0) {
         carry = make_int2(0, 0);
         multi_count = 0;
+        n_partial = 0;
     }
     for (int i = tid; i < kOrderBins; i += 1024) bin_next[i] = 0;
     for (int i = tid; i < 32 * kOrderBins; i += 1024) (&warp_bin[0][0])[i] = 0;
     const int64_t max_tokens = (int64_t)p.max_blocks_per_seq * kBlock;
+    const bool prefix = p.seq_skip != nullptr;
+    if (prefix) prep_prefix_runs(p, warp_tot, tid, lane, warp);
+    // blocks of sequence s its decode partitions cover, and its shared-prefix pieces
+    auto own = [&](int s, int nb) {
+        if (!prefix) return make_int2(nb, 0);
+        const int2 sk = p.seq_skip[s];
+        return make_int2(nb - sk.x, sk.y);
+    };
     // pass 0 (automatic partition size): pairs at P0, 2 P0, 4 P0 blocks per
     // partition; the largest size that still gives auto_split_pairs pairs wins
     if (p.auto_split_pairs > 0) {
@@ -159,7 +295,7 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
         for (int s = tid; s < p.num_seqs; s += 1024) {
             const int L = p.context_lens[s];
             if (L <= 0 || (int64_t)L > max_tokens) continue;
-            const int nb = (L + kBlock - 1) / kBlock;
+            const int nb = own(s, (L + kBlock - 1) / kBlock).x;
 #pragma unroll
             for (int k = 0; k < kAutoSizes; ++k) {
                 const int Pk = p.blocks_per_split << k;
@@ -191,33 +327,42 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
     auto bin_of = [P](int r) { return (int)((int64_t)(P - 1 - r) * kOrderBins / P); };
     // pass 1: partitions, pair offsets, full partitions, size histogram (a
     // sequence with no context or a bad length gets no partition)
+    // (pieces of a sequence: its shared-prefix pieces, then its partitions;
+    // carry.x counts pieces, carry.y full partitions, n_partial the rest)
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int s = base + tid;
-        int nsplit = 0, partial = 0, r = 0;
+        int nsplit = 0, partial = 0, r = 0, npre = 0;
         if (s < p.num_seqs) {
             const int L = p.context_lens[s];
             if (L < 0 || (int64_t)L > max_tokens) {
                 atomicOr(p.status, PKV_DEV_BAD_LEN);
             } else if (L > 0) {
-                const int nb = (L + kBlock - 1) / kBlock;
-                nsplit = (nb + P - 1) / P;
-                r = nb - (nsplit - 1) * P;
+                const int2 o = own(s, (L + kBlock - 1) / kBlock);
+                npre = o.y;
+                nsplit = (o.x + P - 1) / P;
+                r = o.x - (nsplit - 1) * P;
                 partial = r < P;
             }
         }
-        const int2 inc = prep_scan2(make_int2(nsplit, nsplit - partial), warp_tot, lane, warp);
+        const int npieces = npre + nsplit;
+        const int2 inc = prep_scan2(make_int2(npieces, nsplit - partial), warp_tot, lane, warp);
         const int2 c0 = carry;
-        const int excl = c0.x + inc.x - nsplit;
+        const int excl = c0.x + inc.x - npieces;
         const int excl_full = c0.y + inc.y - (nsplit - partial);
-        if (s < p.num_seqs && dbg_fail((int64_t)excl + nsplit <= p.max_pairs, p.debug, 12, excl)) {
+        if (s < p.num_seqs &&
+            dbg_fail((int64_t)excl + npieces <= p.max_pairs, p.debug, 12, excl)) {
             nsplit = 0;
             partial = 0;
+            npre = 0;
         }
         if (s < p.num_seqs) {
-            p.seq_info[s] = make_int2(excl, nsplit);
+            p.seq_info[s] = make_int2(excl, npre + nsplit);
             for (int k = 0; k < nsplit - partial; ++k) p.items[excl_full + k] = make_int2(s, k);
-            if (partial) atomicAdd(&bin_next[bin_of(r)], 1);
-            if (nsplit > 1) p.multi[atomicAdd(&multi_count, 1)] = s;   // for the merge kernel
+            if (partial) {
+                atomicAdd(&bin_next[bin_of(r)], 1);
+                atomicAdd(&n_partial, 1);
+            }
+            if (npre + nsplit > 1) p.multi[atomicAdd(&multi_count, 1)] = s;   // for the merge kernel
             // (a zero row's output is written by the main kernel: zero_idle_rows)
         }
         __syncthreads();
@@ -248,9 +393,10 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
         const int s = base + tid;
         int bin = -1, nsplit = 0;
         if (s < p.num_seqs) {
-            nsplit = p.seq_info[s].y;
-            if (nsplit > 0) {
-                const int nb = (p.context_lens[s] + kBlock - 1) / kBlock;
+            const int L = p.context_lens[s];
+            if (L > 0 && (int64_t)L <= max_tokens && p.seq_info[s].y > 0) {
+                const int nb = own(s, (L + kBlock - 1) / kBlock).x;
+                nsplit = (nb + P - 1) / P;
                 const int r = nb - (nsplit - 1) * P;
                 if (r < P) bin = bin_of(r);
             }
@@ -278,9 +424,10 @@ __global__ void __launch_bounds__(1024) decode_prep_kernel(Params p, int32_t hea
         __syncthreads();
     }
     if (tid == 0) {
-        p.header[0] = carry.x;
+        p.header[0] = carry.y + n_partial;      // decode items: full and partial partitions
         p.header[2] = P;
         p.header[3] = multi_count;
+        p.header[5] = carry.x;                  // pieces
     }
 }
 
@@ -353,36 +500,45 @@ __global__ void __launch_bounds__(kThreads, MINB)
         int2 it_cur = item < total_items ? p.items[item / Hkv] : make_int2(0, 0);
         int2 it_nxt = item + stride < total_items ? p.items[(item + stride) / Hkv]
                                                   : make_int2(0, 0);
-        auto fetch = [&](int2 it, int valid, int &L, int2 &info, int &id) {
-            L = 0; info = make_int2(0, 0); id = 0;
+        // info = (first piece of this partition, pieces of the sequence);
+        // b0 = first block of the partition (after a shared prefix, if any)
+        auto fetch = [&](int2 it, int valid, int &L, int2 &info, int &b0, int &id) {
+            L = 0; info = make_int2(0, 0); b0 = 0; id = 0;
             if (!valid) return;
             L = __ldg(p.context_lens + it.x);
             info = __ldg(p.seq_info + it.x);
-            const int b = it.y * P + lane;
+            b0 = it.y * P;
+            info.x += it.y;
+            if (p.seq_skip) {
+                const int2 sk = __ldg(p.seq_skip + it.x);
+                b0 += sk.x;
+                info.x += sk.y;
+            }
+            const int b = b0 + lane;
             if (b < p.max_blocks_per_seq)
                 id = __ldg(p.block_tables + (int64_t)it.x * p.max_blocks_per_seq + b);
         };
-        int L_cur, id_cur;
+        int L_cur, id_cur, b0_cur;
         int2 info_cur;
-        fetch(it_cur, item < total_items, L_cur, info_cur, id_cur);
+        fetch(it_cur, item < total_items, L_cur, info_cur, b0_cur, id_cur);
         for (int k = 0; item < total_items; ++k, item += stride) {
             // prefetch
             const int2 it_fut = item + 2 * stride < total_items ? p.items[(item + 2 * stride) / Hkv]
                                                                 : make_int2(0, 0);
-            int L_nxt, id_nxt;
+            int L_nxt, id_nxt, b0_nxt;
             int2 info_nxt;
-            fetch(it_nxt, item + stride < total_items, L_nxt, info_nxt, id_nxt);
+            fetch(it_nxt, item + stride < total_items, L_nxt, info_nxt, b0_nxt, id_nxt);
 
             const int g = item - (item / Hkv) * Hkv;
             const int s = it_cur.x;
             const int nb = (L_cur + kBlock - 1) / kBlock;
-            const int b0 = it_cur.y * P, b1 = min(b0 + P, nb);
+            const int b0 = b0_cur, b1 = min(b0 + P, nb);
             // Q rows + metadata for the consumers
             if (lane == 0) {
                 const int qs = k & 1;
                 const uint32_t qpar = (k >> 1) & 1;
                 if (mbar_wait(smem_addr(&qempty_bar[qs]), qpar ^ 1u, sm_abort, p.status)) {
-                    sm_meta[qs] = ItemMeta{s, g, L_cur, b0, b1, info_cur.y, info_cur.x + it_cur.y, 0};
+                    sm_meta[qs] = ItemMeta{s, g, L_cur, b0, b1, info_cur.y, info_cur.x, 0};
                     const uint32_t qb = smem_addr(&qfull_bar[qs]);
                     mbar_arrive_expect_tx(qb, q_bytes);
                     bulk_load(smem_addr(qbuf + qs * SM::kQSlotBytes),
@@ -432,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 }
             }
             it_cur = it_nxt; it_nxt = it_fut;
-            L_cur = L_nxt; id_cur = id_nxt; info_cur = info_nxt;
+            L_cur = L_nxt; id_cur = id_nxt; info_cur = info_nxt; b0_cur = b0_nxt;
         }
         // drain: every copy this warp issued must land before the CTA exits
         if (lane == 0) {
@@ -782,17 +938,23 @@ __global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
 // --------------------------------------------------------------------- host side
 struct WsLayout {
     size_t header, seq_info, items, part_ml, part_o, multi, total;
-    int64_t max_pairs;
+    size_t seq_skip, prefix_scratch, prefix_items;   // shared-prefix layouts only
+    int64_t max_pairs, max_prefix_items;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// With `prefix`, room for shared prefixes: kPrefixMaxPieces more pieces per
+// sequence, the per-sequence skips, the run scratch and the shared-prefix work
+// list (at most 2.25 S items: a run has two members or more, and its items are
+// ceil(members / tile) <= members / 16 + 1 tiles times at most 4 chunks).
 static bool ws_layout(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t maxb, int32_t P,
-                      WsLayout *w)
+                      bool prefix, WsLayout *w)
 {
     if (S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || maxb <= 0 || P <= 0 || Hq % Hkv) return false;
     const int64_t G = Hq / Hkv;
-    w->max_pairs = S * ((maxb + P - 1) / P);
+    w->max_pairs = S * ((maxb + P - 1) / P + (prefix ? kPrefixMaxPieces : 0));
+    w->max_prefix_items = prefix ? 3 * S : 0;
     size_t off = 0;
     w->header = off; off += 256;
     w->seq_info = off; off += align256((size_t)S * 8);
@@ -800,6 +962,12 @@ static bool ws_layout(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t max
     w->part_ml = off; off += align256((size_t)w->max_pairs * Hkv * G * 8);
     w->part_o = off; off += align256((size_t)w->max_pairs * Hkv * G * D * 4);
     w->multi = off; off += align256((size_t)S * 4);
+    w->seq_skip = w->prefix_scratch = w->prefix_items = 0;
+    if (prefix) {
+        w->seq_skip = off; off += align256((size_t)S * 8);
+        w->prefix_scratch = off; off += align256((size_t)S * 16);
+        w->prefix_items = off; off += align256((size_t)w->max_prefix_items * 16);
+    }
     w->total = off;
     return true;
 }
@@ -943,8 +1111,13 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
         ((uintptr_t)block_tables & 3u) || ((uintptr_t)context_lens & 3u) ||
         ((uintptr_t)d_status & 3u))
         return PKV_ERR_INVALID_ARG;
+    // the automatic 16-bit call lays its workspace out for shared prefixes; it
+    // looks for them when the ledger says some block is shared right now
+    const bool prefix_layout = auto_split && !want_8bit;
+    const bool prefix = prefix_layout && pool_has_shared_blocks(pool) &&
+                        maxb > kPrefixMinBlocks && prefill::shared_prefix_supported(g, G);
     WsLayout w;
-    if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, P, &w) ||
+    if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, P, prefix_layout, &w) ||
         workspace_bytes < w.total)
         return PKV_ERR_INVALID_ARG;
     if ((int64_t)g.num_blocks * g.num_kv_heads * g.block_size > (int64_t)1 << 31)
@@ -978,6 +1151,11 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     prm.kv_q8 = want_8bit ? static_cast<const uint8_t *>(k_pool) : nullptr;
     prm.max_pairs = w.max_pairs;
     prm.debug = prm.header + 1;
+    prm.seq_skip = prefix ? reinterpret_cast<int2 *>(ws + w.seq_skip) : nullptr;
+    prm.prefix_scratch = prefix ? reinterpret_cast<int32_t *>(ws + w.prefix_scratch) : nullptr;
+    prm.prefix_items = prefix ? reinterpret_cast<int4 *>(ws + w.prefix_items) : nullptr;
+    prm.max_prefix_items = (int32_t)w.max_prefix_items;
+    prm.prefix_tile_seqs = prefix ? prefill::shared_prefix_tile_seqs(G) : 0;
 
     int num_sms = 0;
     const int per_sm = persistent_ctas(v, &num_sms);
@@ -993,6 +1171,28 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
 #endif
     decode_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (prefix) {     // shared prefixes: their pieces, before the partitions after them
+        prefill::SharedPrefixLaunch a;
+        a.geometry = g;
+        a.k_pool = k_pool;
+        a.v_pool = v_pool;
+        a.q = q;
+        a.block_tables = block_tables;
+        a.max_blocks_per_seq = maxb;
+        a.num_seqs = num_seqs;
+        a.num_q_heads = num_q_heads;
+        a.scale_log2 = prm.scale_log2;
+        a.items = prm.prefix_items;
+        a.count = prm.header + 4;
+        a.max_items = prm.max_prefix_items;
+        a.piece_info = prm.seq_info;
+        a.part_ml = prm.part_ml;
+        a.part_o = prm.part_o;
+        a.status = d_status;
+        a.stream = st;
+        const int rc = prefill::launch_shared_prefix(a);
+        if (rc != PKV_OK) return rc;
+    }
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1004,7 +1204,7 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, v.fn, tk, tv, prm) != cudaSuccess) return PKV_ERR_CUDA;
-    if (maxb > P) {   // some sequence may have several partitions
+    if (maxb > P || prefix) {   // some sequence may have several pieces
         // a grid-stride grid over the (sequence, kv head) units the prep kernel
         // lists: a few waves when many sequences are split, and little to
         // launch when none is
@@ -1037,7 +1237,7 @@ size_t paged_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
 {
     pkv::decode::WsLayout w;
     if (!pkv::decode::ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                                blocks_per_split, &w))
+                                blocks_per_split, false, &w))
         return 0;
     return w.total;
 }
@@ -1045,8 +1245,11 @@ size_t paged_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
 size_t paged_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, int32_t max_blocks_per_seq)
 {
-    return paged_decode_workspace_bytes_split(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                              max_blocks_per_seq, pkv::decode::kDefaultSplit);
+    pkv::decode::WsLayout w;
+    if (!pkv::decode::ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                pkv::decode::kDefaultSplit, true, &w))
+        return 0;
+    return w.total;
 }
 
 int paged_decode_attention_split(const pkv_pool *pool, void *out, const void *q,
@@ -1143,7 +1346,7 @@ extern "C" int paged_decode_attention_noalloc(const pkv_pool *pool, void *out, c
     for (int32_t k = (maxb + kDefaultSplit - 1) / kDefaultSplit; k >= 1; --k) {
         const int32_t cand = (maxb + k - 1) / k;
         WsLayout w;
-        if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, cand, &w))
+        if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, cand, false, &w))
             return PKV_ERR_INVALID_ARG;
         if (w.total <= kNoallocScratchBytes) {
             P = cand;

@@ -21,6 +21,7 @@
 #include <type_traits>
 
 #include "pagedkv.h"
+#include "decode_params.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 #include "tc_device.cuh"
@@ -46,6 +47,17 @@ struct Params {
     // (sequence, kv head) the largest bf16 exponent field of its V
     uint16_t *v16;
     int32_t *v_emax;                // [num_seqs][Hkv]
+    // Shared-prefix mode (a decode call whose neighbouring sequences share
+    // their leading blocks): an item is (first member, members | chunk << 16,
+    // first block, end block) of a run; the member sequences' queries (rows of
+    // q [num_seqs][Hq][D]) attend over those blocks of the first member's table,
+    // without a causal limit, and each row leaves its unnormalised output,
+    // maximum and sum as piece piece_info[member].x + chunk of the decode call.
+    const int4 *prefix_items;
+    const int32_t *prefix_count;
+    const int2 *piece_info;
+    float2 *part_ml;                // [pieces * Hkv * G]
+    float *part_o;                  // [pieces * Hkv * G * D]
 };
 
 // Scale of a (sequence, kv head)'s fp16 copy of V: v16 = v * 2^-k with
@@ -333,8 +345,10 @@ struct Layout {
 // (group 1) of one sequence's chunk and one kv head; keys 0 .. nkeys - 1.
 struct Item {
     int s, g, r0, C, L, t0, t1, nkeys, ntiles;
+    int kb0, chunk;      // shared-prefix mode: first block of the keys, piece of the chunk
 };
 
+template <bool PREFIX>
 __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int QT)
 {
     Item it;
@@ -342,6 +356,22 @@ __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int
     const int Hkv = p.num_kv_heads;
     const int sj = id / Hkv;
     it.g = id - sj * Hkv;
+    if constexpr (PREFIX) {
+        const int4 e = __ldg(p.prefix_items + sj);
+        it.s = e.x;                         // every member's table begins with these blocks
+        it.r0 = e.x;
+        it.C = e.y & 0xffff;
+        it.chunk = e.y >> 16;
+        it.kb0 = e.z;
+        it.L = (e.w - e.z) * kBlock;
+        it.t0 = 0;
+        it.t1 = it.C;
+        it.nkeys = it.L;
+        it.ntiles = (it.nkeys + kKeys - 1) / kKeys;
+        return it;
+    }
+    it.kb0 = 0;
+    it.chunk = 0;
     const int2 e = p.items[sj];
     it.s = e.x;
     it.r0 = __ldg(p.query_start + e.x);
@@ -356,12 +386,15 @@ __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int
 
 // VS: V comes from the fp16 copy (tmV maps it; bf16 pools only), so P V takes
 // one fp16 part of P and the result is scaled by 2^k.
-template <int D, bool BF16, bool VS>
+// PREFIX: shared-prefix mode of a decode call (see Params): items from
+// prefix_items, no causal limit, pieces instead of output rows.
+template <int D, bool BF16, bool VS, bool PREFIX>
 __global__ void __launch_bounds__(kThreads)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmQ, const Params p)
 {
     static_assert(BF16 || !VS, "fp16 pools take V as it is");
+    static_assert(!(VS && PREFIX), "the shared-prefix mode reads V from the pool");
     constexpr bool kTwoParts = BF16 && !VS;    // P as bf16 high + low parts
     using E = Elem<BF16>;
     using T = typename E::T;
@@ -412,7 +445,7 @@ __global__ void __launch_bounds__(kThreads)
     griddep_wait();
 
     const int Hkv = p.num_kv_heads, G = p.group, QT = p.tile_tokens / kGroups;   // one query tile
-    const int total = p.header[0] * Hkv;
+    const int total = (PREFIX ? *p.prefix_count : p.header[0]) * Hkv;
 
     if (warp == kProducer) {
         if (lane == 0) {
@@ -420,7 +453,7 @@ __global__ void __launch_bounds__(kThreads)
             int last_par[LY::kStages], last_q = -1;          // phases of the last copies issued
             for (int k = 0; k < LY::kStages; ++k) last_par[k] = -1;
             for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++it_cnt) {
-                const Item it = load_item(p, i, total, QT);
+                const Item it = load_item<PREFIX>(p, i, total, QT);
                 if (it_cnt > 0 &&
                     !mbar_wait(smem_addr(q_empty), (it_cnt - 1) & 1u, abort_flag, p.status))
                     break;
@@ -431,7 +464,7 @@ __global__ void __launch_bounds__(kThreads)
                     for (int rg = 0; rg < LY::kRegions; ++rg)
                         tc::tma_load_4d(smem_addr(q_s + gr * LY::kQBytes + rg * kRows * 128), &tmQ,
                                         rg * 64, 0, it.g, it.r0 + it.t0 + gr * QT, qb);
-                const int32_t *row = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq;
+                const int32_t *row = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq + it.kb0;
                 const int nb = (it.nkeys + kBlock - 1) / kBlock;
                 for (int t = 0; t < it.ntiles; ++t, ++kv_cnt) {
                     const int st = (int)(kv_cnt % LY::kStages);
@@ -516,7 +549,7 @@ __global__ void __launch_bounds__(kThreads)
                 tc::mma_commit(smem_addr(&kv_empty[t % LY::kStages]));
             };
             for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it_cnt) {
-                const Item it = load_item(p, i, total, QT);
+                const Item it = load_item<PREFIX>(p, i, total, QT);
                 if (!mbar_wait(smem_addr(q_full), it_cnt & 1u, abort_flag, p.status)) break;
                 for (int t = 0; t < it.ntiles && ok; ++t, ++tg) {
                     const uint32_t st = tg % LY::kStages, sb = tg & 1u;
@@ -559,11 +592,11 @@ __global__ void __launch_bounds__(kThreads)
         uint32_t tg = 0, it_cnt = 0;
         bool alive = true;
         for (int i = blockIdx.x; i < total && alive; i += gridDim.x, ++it_cnt) {
-            const Item it = load_item(p, i, total, QT);
+            const Item it = load_item<PREFIX>(p, i, total, QT);
             const int jj = r / G, h = r - (r / G) * G;
             const int tg0 = it.t0 + gr * QT;            // this group's first token
             const bool valid = r < QT * G && tg0 + jj < it.t1;
-            const int pos = valid ? it.L - it.C + tg0 + jj : it.nkeys - 1;
+            const int pos = valid && !PREFIX ? it.L - it.C + tg0 + jj : it.nkeys - 1;
             float m_ref = -INFINITY, l = 0.f;
             int bad = 0;
             for (int t = 0; t < it.ntiles; ++t, ++tg) {
@@ -697,6 +730,30 @@ __global__ void __launch_bounds__(kThreads)
                                        ((tg - 1) >> 1) & 1u, abort_flag, p.status);
             if (!__all_sync(kFull, oko)) break;
             tc::fence_after_sync();
+            if constexpr (PREFIX) {
+                // the row's piece: O as it stands (weights taken against m_ref), m_ref, l
+                size_t piece = 0;
+                if (valid) {
+                    const int member = it.r0 + tg0 + jj;
+                    piece = ((size_t)(__ldg(p.piece_info + member).x + it.chunk) * Hkv + it.g) * G + h;
+                    p.part_ml[piece] = make_float2(m_ref, bad ? -1.f : l);
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lane_base + o_col + c0, v);
+                    tc::tmem_wait_ld();
+                    if (valid) {
+                        float4 *dst = reinterpret_cast<float4 *>(p.part_o + piece * D + c0);
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4)
+                            dst[c / 4] = make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                                                     __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+                    }
+                }
+                tc::fence_before_sync();
+                continue;
+            }
             const float inv = 1.f / l;
             T *out = static_cast<T *>(p.out) +
                      ((size_t)(it.r0 + tg0 + jj) * p.num_q_heads + (size_t)it.g * G + h) * D;
@@ -827,16 +884,16 @@ using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
 static bool pick_tc(int D, bool bf16, bool staged, TcKernelFn *fn, int *smem)
 {
     if (D == 128) {
-        *fn = !bf16 ? &tcp::prefill_tc_kernel<128, false, false>
-              : staged ? &tcp::prefill_tc_kernel<128, true, true>
-                       : &tcp::prefill_tc_kernel<128, true, false>;
+        *fn = !bf16 ? &tcp::prefill_tc_kernel<128, false, false, false>
+              : staged ? &tcp::prefill_tc_kernel<128, true, true, false>
+                       : &tcp::prefill_tc_kernel<128, true, false, false>;
         *smem = tcp::Layout<128>::kTotal;
         return true;
     }
     if (D == 64) {
-        *fn = !bf16 ? &tcp::prefill_tc_kernel<64, false, false>
-              : staged ? &tcp::prefill_tc_kernel<64, true, true>
-                       : &tcp::prefill_tc_kernel<64, true, false>;
+        *fn = !bf16 ? &tcp::prefill_tc_kernel<64, false, false, false>
+              : staged ? &tcp::prefill_tc_kernel<64, true, true, false>
+                       : &tcp::prefill_tc_kernel<64, true, false, false>;
         *smem = tcp::Layout<64>::kTotal;
         return true;
     }
@@ -1007,3 +1064,79 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fn, tk, tv, tq, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
+
+// ------------------------------------------------- shared-prefix launcher
+// Called by the decode launcher (paged_decode.cu) between its prep kernel,
+// which lists the work, and its main kernel; see prefill_tc_kernel's PREFIX mode.
+namespace pkv {
+namespace prefill {
+
+int shared_prefix_tile_seqs(int G) { return tile_tokens(G); }
+
+bool shared_prefix_supported(const PoolGeometry &g, int G)
+{
+    return is_16bit(g) && g.block_size == kBlock && (g.head_dim == 64 || g.head_dim == 128) &&
+           G >= 1 && G <= 16;
+}
+
+int launch_shared_prefix(const SharedPrefixLaunch &a)
+{
+    const PoolGeometry &g = a.geometry;
+    const int G = a.num_q_heads / g.num_kv_heads;
+    if (!shared_prefix_supported(g, G)) return PKV_ERR_UNSUPPORTED;
+    const bool bf16 = g.dtype == PKV_BF16;
+    TcKernelFn fn;
+    int smem;
+    if (g.head_dim == 128) {
+        fn = bf16 ? &tcp::prefill_tc_kernel<128, true, false, true>
+                  : &tcp::prefill_tc_kernel<128, false, false, true>;
+        smem = tcp::Layout<128>::kTotal;
+    } else {
+        fn = bf16 ? &tcp::prefill_tc_kernel<64, true, false, true>
+                  : &tcp::prefill_tc_kernel<64, false, false, true>;
+        smem = tcp::Layout<64>::kTotal;
+    }
+    CUtensorMap tk, tv, tq;
+    if (!make_pool_map(&tk, a.k_pool, g) || !make_pool_map(&tv, a.v_pool, g) ||
+        !make_q_map(&tq, a.q, a.num_seqs, g.num_kv_heads, G, g.head_dim, tcp::kRows / G, bf16))
+        return PKV_ERR_CUDA;
+    Params prm = {};
+    prm.q = a.q;
+    prm.block_tables = a.block_tables;
+    prm.num_seqs = a.num_seqs;
+    prm.num_tokens = a.num_seqs;
+    prm.num_q_heads = a.num_q_heads;
+    prm.num_kv_heads = g.num_kv_heads;
+    prm.group = G;
+    prm.max_blocks_per_seq = a.max_blocks_per_seq;
+    prm.num_blocks = g.num_blocks;
+    prm.tile_tokens = tile_tokens(G);
+    prm.scale_log2 = a.scale_log2;
+    prm.status = a.status;
+    prm.prefix_items = a.items;
+    prm.prefix_count = a.count;
+    prm.piece_info = a.piece_info;
+    prm.part_ml = a.part_ml;
+    prm.part_o = a.part_o;
+    int sms = 0;
+    const int per_sm = resident(reinterpret_cast<const void *>(fn), smem, tcp::kThreads, &sms);
+    if (per_sm < 1) return PKV_ERR_CUDA;
+    // persistent: the number of items is known on the device only
+    int64_t grid = (int64_t)per_sm * sms;
+    if (grid > (int64_t)a.max_items * g.num_kv_heads) grid = (int64_t)a.max_items * g.num_kv_heads;
+    if (grid < 1) grid = 1;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(tcp::kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = a.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, tk, tv, tq, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace prefill
+}  // namespace pkv

@@ -17,6 +17,9 @@ struct PoolGeometry {
 // Geometry of a pool ledger; false on NULL.
 bool pool_geometry(const pkv_pool *p, PoolGeometry *g);
 
+// Some block of the pool is referenced by two or more sequences right now.
+bool pool_has_shared_blocks(const pkv_pool *p);
+
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Element type of the pool is fp16 or bf16 (not an 8-bit cache).

@@ -99,6 +99,7 @@ def test_random_sequence_matches_model(seed):
         assert lib_pool.num_free() == model.num_free()
         for b in range(n):
             assert lib_pool.refcount(b) == model.refcount(b)
+        assert lib_pool.num_shared() == sum(model.refcount(b) >= 2 for b in range(n))
 
 
 def test_errors_are_all_or_nothing():
@@ -220,3 +221,4 @@ def test_random_forks_match_model(seed):
         assert pool.num_free() == model.num_free()
         for b in range(n):
             assert pool.refcount(b) == model.refcount(b)
+        assert pool.num_shared() == sum(model.refcount(b) >= 2 for b in range(n))
