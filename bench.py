@@ -505,7 +505,28 @@ def decode_run(args, workload: str, world: int, rank: int, dev, steps: int, warm
             "prompt_tokens": T_pr, "prompt_ms": round(c0.elapsed_time(c1), 4),
             "prompt_gbs": round(T_pr * (row_in + row_out + 8) / (c0.elapsed_time(c1) * 1e-3) / 1e9,
                                 2)}
-    del prompt_rows, qs, ks, vs, eng
+    # the attention call alone on the final state, replayed back to back from a
+    # CUDA graph on the engine's current buffers: one launch per call, so the
+    # host's Python and launch overhead leaves no gaps in short calls
+    from paged_kv_cache_146_gb300 import CapturedDecode
+    qbuf = qs[0].clone()
+    cap = CapturedDecode(pool, qbuf, eng.d_tables, eng.d_lens, w.scale, eng.workspace,
+                         eng.status, eng.out)
+    for _ in range(3):
+        cap.replay()
+    gev = [(ev(), ev()) for _ in range(20)]
+    torch.cuda.synchronize()
+    for a, b in gev:
+        a.record(stream)
+        cap.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    rc, word = eng.check()
+    if rc != 0:
+        raise SystemExit(f"device status {rc} word {word:#x} in the graph replays")
+    res["graph_ms"] = statistics.median(a.elapsed_time(b) for a, b in gev)
+    res["graph_bytes"] = eng.step_bytes()
+    del prompt_rows, qs, ks, vs, eng, cap
     return res
 
 
@@ -515,19 +536,24 @@ def config_summary(args, workload: str, world: int, rank: int, dev) -> dict:
     import torch
     r = decode_run(args, workload, world, rank, dev, steps=20, warmup=3)
     peak, _ = peaks()
-    achieved = r["bytes_per_launch"] / (r["attn_avg_ms"] * 1e-3) / 1e9
+    gms = r["graph_ms"]
+    achieved = r["graph_bytes"] / (gms * 1e-3) / 1e9
     out = {"attention_gbs": round(achieved, 2), "pct_of_peak": round(100 * achieved / peak, 2),
-           "attention_ms": round(r["attn_avg_ms"], 4),
+           "attention_ms": round(gms, 4),
+           "attention": "the call replayed back to back from a CUDA graph on the final state "
+                        "(median of 20); attention_ms_in_step: the direct call inside the timed "
+                        "steps, host launch gaps included",
+           "attention_ms_in_step": round(r["attn_avg_ms"], 4),
            "step_gbs": round(r["value"], 2),
-           "seq_tokens_per_s": round(r["toks_per_step"] / (r["attn_avg_ms"] * 1e-3), 1),
-           "bytes_per_call": int(r["bytes_per_launch"]),
+           "seq_tokens_per_s": round(r["toks_per_step"] / (gms * 1e-3), 1),
+           "bytes_per_call": int(r["graph_bytes"]),
            "num_seqs": r["S"], "q_heads": r["hq"], "kv_heads": r["hkv"], "head_dim": r["d"],
            "kv_dtype": r["pool"].dtype, "lengths": LENGTHS[workload]}
     if workload == "shared_prefix":
         traffic = profiled_traffic(workload) if args.seed == 0 else None
         out["dram_bytes_per_call"] = traffic
         if traffic:
-            out["dram_gbs"] = round(traffic / (r["attn_avg_ms"] * 1e-3) / 1e9, 2)
+            out["dram_gbs"] = round(traffic / (gms * 1e-3) / 1e9, 2)
             out["dram_pct_of_peak"] = round(100 * out["dram_gbs"] / peak, 2)
     del r
     torch.cuda.empty_cache()
@@ -557,6 +583,10 @@ def our_arm(args, world, rank, local):
     dtype_name, pool_dtype = w.dtype, r["pool"].dtype
     e2e, cache_write_line = r.get("e2e"), r.get("cache_write")
     toks_region, region_ms = r["region_toks"], r["region_ms"]
+    graph = {"ms": round(r["graph_ms"], 4),
+             "gbs": round(r["graph_bytes"] / (r["graph_ms"] * 1e-3) / 1e9, 2),
+             "what": "the attention call replayed back to back from a CUDA graph on the final "
+                     "state, median of 20"}
     clk, repeat_values, launches = r["clocks"], r["repeat_values"], r["launches_per_step"]
     del r
     torch.cuda.empty_cache()
@@ -625,6 +655,7 @@ def our_arm(args, world, rank, local):
                      + " (prep + main + merge kernels)",
                      "bytes_per_launch": int(bytes_per_launch),
                      "launch_ms": round(attn_avg_ms, 4)},
+        "attention_graph": graph,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "cache_write": cache_write_line,
