@@ -357,7 +357,8 @@ def decode_run(args, workload: str, world: int, rank: int, dev, steps: int, warm
     vals = workloads.device_values(w, dev)
     pool = KVPool(w.num_blocks, hkv, d, "q8_" + w.dtype if q8 else w.dtype,
                   free_order=w.free_order, device=dev)
-    eng = DecodeEngine(pool, S, hq, w.max_blocks_per_seq, w.scale, dev)
+    eng = DecodeEngine(pool, S, hq, w.max_blocks_per_seq, w.scale, dev,
+                       plan_on_host=not args.device_plan)
     if w.shared_prefix_tokens:
         first = np.zeros(S, dtype=np.int32)
         first[0] = w.shared_prefix_tokens
@@ -440,8 +441,10 @@ def decode_run(args, workload: str, world: int, rank: int, dev, steps: int, warm
            "region_ms": region_ms[med], "bytes_per_launch": bytes_per_launch,
            "attn_avg_ms": attn_avg_ms, "attn_median_ms": statistics.median(attn_ms),
            "toks_per_step": region_toks[med] / steps, "clocks": clk,
-           "launches_per_step": 1 + (3 if eng.maxb > (eng.split_for_step() or default_split())
-                                     else 2)}
+           # cache write + (planned: main [+ shared-prefix kernel]; 8-bit: prep +
+           # main [+ merge]; fixed partition size: prep + main)
+           "launches_per_step": 1 + (1 + (eng.plan_prefix_items > 0) if eng.planned else
+                                     3 if q8 and eng.maxb > default_split() else 2)}
 
     # ---- end to end through the public API with host buffers
     if e2e_steps > 0:
@@ -511,7 +514,8 @@ def decode_run(args, workload: str, world: int, rank: int, dev, steps: int, warm
     from paged_kv_cache_146_gb300 import CapturedDecode
     qbuf = qs[0].clone()
     cap = CapturedDecode(pool, qbuf, eng.d_tables, eng.d_lens, w.scale, eng.workspace,
-                         eng.status, eng.out)
+                         eng.status, eng.out,
+                         planned_prefix_items=eng.plan_prefix_items if eng.planned else None)
     for _ in range(3):
         cap.replay()
     gev = [(ev(), ev()) for _ in range(20)]
@@ -652,7 +656,8 @@ def our_arm(args, world, rank, local):
                      "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
                      "kernel": ("paged_decode_attention_q8" if q8 else "paged_decode_attention")
-                     + " (prep + main + merge kernels)",
+                     + (" (main kernel; work plan built on the host)" if not q8 else
+                        " (prep + main + merge kernels)"),
                      "bytes_per_launch": int(bytes_per_launch),
                      "launch_ms": round(attn_avg_ms, 4)},
         "attention_graph": graph,
@@ -957,6 +962,9 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=256,
                     help="sequences per GPU (256 is the workload; fewer only for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--device-plan", action="store_true",
+                    help="decode workloads: the attention call plans its work on the device "
+                         "(prep kernel) instead of taking the engine's host-built plan")
     ap.add_argument("--repeats", type=int, default=10,
                     help="timed regions of --steps steps each; the median region is reported")
     ap.add_argument("--configs", type=int, default=1,

@@ -414,6 +414,53 @@ int paged_prefill_attention(const pkv_pool *pool, void *out, const void *q, cons
                             int32_t num_q_heads, float scale, void *workspace,
                             size_t workspace_bytes, int32_t *d_status, void *stream);
 
+/* ------------------------------------------- decode work planned on the host
+ *
+ * "LLM 추론 배칭 전략 정리", section 5: the CPU keeps the ledger and hands the
+ * GPU its block table every step.  A caller that holds the step's context
+ * lengths and tables on the host can also hand over the attention call's work
+ * plan -- the one paged_decode_attention's first kernel builds on the device --
+ * and save that kernel: paged_decode_plan builds it into host memory,
+ * the caller copies its paged_decode_plan_bytes(...) bytes to the start of the
+ * workspace (with its other host-to-device copies of the step), then calls
+ * paged_decode_attention_planned with the same arguments as
+ * paged_decode_attention.  The plan is identical to the device's (partition
+ * size, work-list order, shared-prefix runs), so the result is too, bit for
+ * bit. */
+
+/* Bytes of the work plan (a prefix of the workspace of
+ * paged_decode_workspace_bytes(...)).  0 on a bad argument. */
+size_t paged_decode_plan_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t max_blocks_per_seq);
+
+/* Build the plan into `plan` (host memory, plan_bytes >= paged_decode_plan_bytes)
+ * from host copies of context_lens [num_seqs] and block_tables
+ * [num_seqs][max_blocks_per_seq] (NULL: no shared-prefix runs are looked for;
+ * otherwise they are looked for as on the device, when the ledger holds shared
+ * blocks).  *shared_prefix_items (may be NULL) receives the number of
+ * shared-prefix work items, to pass to paged_decode_attention_planned.  Needs
+ * the CUDA device current (the partition size depends on its SM count).
+ * Errors: PKV_ERR_INVALID_ARG (also for a length < 0 or beyond the table row),
+ * PKV_ERR_UNSUPPORTED (shapes the 16-bit kernels do not take), PKV_ERR_CUDA. */
+int paged_decode_plan(const pkv_pool *pool, const int32_t *context_lens,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                      int32_t num_q_heads, void *plan, size_t plan_bytes,
+                      int32_t *shared_prefix_items);
+
+/* paged_decode_attention whose workspace already begins with the plan that
+ * paged_decode_plan built for the same lengths and tables (enqueued before this
+ * call on the same stream, or on one it waits for); shared_prefix_items as
+ * returned there.  A plan built from other lengths or tables gives wrong rows
+ * (every access stays inside the workspace, the pools and the tables).
+ * Errors: as paged_decode_attention. */
+int paged_decode_attention_planned(const pkv_pool *pool, void *out, const void *q,
+                                   const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, float scale, int32_t shared_prefix_items,
+                                   void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                   void *stream);
+
 /* Smallest partition size (blocks) paged_decode_attention considers, the one
  * its workspace is laid out for; the 8-bit decode uses exactly this size. */
 int32_t paged_decode_default_split(void);

@@ -27,6 +27,7 @@ from ._native import (DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_BAD_SLOT, DEV_TIMEOUT, PKV
 __all__ = ["KVPool", "PagedKVError", "cache_write", "block_copy", "gather_blocks",
            "scatter_blocks", "paged_decode_attention", "CapturedDecode",
            "paged_decode_attention_noalloc", "paged_prefill_attention",
+           "decode_plan", "decode_plan_bytes", "paged_decode_attention_planned",
            "cache_write_q8", "paged_decode_attention_q8",
            "prefill_workspace_bytes",
            "decode_workspace_bytes", "status_check", "kv_bytes_per_token",
@@ -406,6 +407,71 @@ def scatter_blocks(pool: KVPool, ids, staging, status, k_pool=None, v_pool=None,
                                   _stream(stream)), "kv_scatter_blocks")
 
 
+def decode_plan_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                      max_blocks_per_seq: int) -> int:
+    """Bytes of the host-built work plan (the start of the decode workspace)."""
+    return lib().paged_decode_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                         max_blocks_per_seq)
+
+
+def _host_ptr_bytes(buf):
+    """(pointer, bytes) of a host buffer: a numpy array or a CPU torch tensor."""
+    if isinstance(buf, np.ndarray):
+        if not buf.flags.c_contiguous:
+            raise ValueError("plan must be contiguous")
+        return buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes
+    if buf.device.type != "cpu" or not buf.is_contiguous():
+        raise ValueError("plan must be a contiguous host tensor")
+    return ctypes.c_void_p(buf.data_ptr()), buf.numel() * buf.element_size()
+
+
+def decode_plan(pool: KVPool, context_lens: np.ndarray, block_tables, num_q_heads: int,
+                plan) -> int:
+    """Build the decode work plan on the host (paged_decode_plan) from host
+    int32 ``context_lens`` [S] and ``block_tables`` [S][max_blocks] (or None)
+    into ``plan`` (a host buffer of ``decode_plan_bytes(...)`` bytes, pinned for
+    an asynchronous copy).  Returns the number of shared-prefix work items."""
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    S = len(lens)
+    if block_tables is not None:
+        if not (isinstance(block_tables, np.ndarray) and block_tables.dtype == np.int32 and
+                block_tables.flags.c_contiguous and block_tables.ndim == 2 and
+                block_tables.shape[0] == S):
+            raise TypeError("block_tables must be a C-contiguous int32 numpy array [S][max_blocks]")
+        maxb, tptr = block_tables.shape[1], _np_ptr(block_tables)
+    else:
+        maxb, tptr = None, None
+    ptr, nbytes = _host_ptr_bytes(plan)
+    if maxb is None:
+        raise ValueError("block_tables (host) are needed for the table width")
+    n = ctypes.c_int32()
+    check(lib().paged_decode_plan(pool.handle, _np_ptr(lens), tptr, maxb, S, num_q_heads, ptr,
+                                  nbytes, ctypes.byref(n)), "paged_decode_plan")
+    return n.value
+
+
+def paged_decode_attention_planned(pool: KVPool, q, block_tables, context_lens, scale: float,
+                                   shared_prefix_items: int, workspace, status, out=None,
+                                   stream=None):
+    """paged_decode_attention whose ``workspace`` already begins with a plan
+    from ``decode_plan`` for the same lengths and tables."""
+    import torch
+    if out is None:
+        out = torch.empty_like(q)
+    _check_decode_args(pool, q, out, block_tables, context_lens, status, workspace,
+                       pool.k_pool, pool.v_pool)
+    S, hq, d = q.shape
+    nbytes = workspace.numel() * workspace.element_size()
+    check(lib().paged_decode_attention_planned(pool.handle, _t_ptr(out), _t_ptr(q),
+                                               _t_ptr(pool.k_pool), _t_ptr(pool.v_pool),
+                                               _t_ptr(block_tables), int(block_tables.shape[1]),
+                                               _t_ptr(context_lens), S, hq, float(scale),
+                                               int(shared_prefix_items), _t_ptr(workspace), nbytes,
+                                               _t_ptr(status), _stream(stream)),
+          "paged_decode_attention_planned")
+    return out
+
+
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                            max_blocks_per_seq: int, blocks_per_split: int | None = None) -> int:
     if blocks_per_split is None:
@@ -461,7 +527,11 @@ class CapturedDecode:
     will do): one untimed call on a side stream sets the kernels up first."""
 
     def __init__(self, pool: KVPool, q, block_tables, context_lens, scale: float, workspace,
-                 status, out):
+                 status, out, planned_prefix_items: int | None = None):
+        """``planned_prefix_items`` not None: capture the planned call
+        (``paged_decode_attention_planned``, 16-bit pools): every replay then
+        expects the workspace to begin with a host plan with that many
+        shared-prefix items (the capture itself needs a valid plan there)."""
         import torch
         self.torch = torch
 
@@ -469,6 +539,9 @@ class CapturedDecode:
             if pool.is_q8:
                 paged_decode_attention_q8(pool, q, block_tables, context_lens, scale, workspace,
                                           status, out=out)
+            elif planned_prefix_items is not None:
+                paged_decode_attention_planned(pool, q, block_tables, context_lens, scale,
+                                               planned_prefix_items, workspace, status, out=out)
             else:
                 paged_decode_attention(pool, q, block_tables, context_lens, scale, workspace,
                                        status, out=out)

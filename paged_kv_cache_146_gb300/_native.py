@@ -54,6 +54,10 @@ SIGNATURES = [
     ("paged_decode_attention_split", ctypes.c_int,
      [_p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _f32, _i32, _p, _sz, _p, _p]),
     ("paged_decode_default_split", _i32, []),
+    ("paged_decode_plan_bytes", _sz, [_i32, _i32, _i32, _i32, _i32]),
+    ("paged_decode_plan", ctypes.c_int, [_p, _p, _p, _i32, _i32, _i32, _p, _sz, _pi32]),
+    ("paged_decode_attention_planned", ctypes.c_int,
+     [_p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _f32, _i32, _p, _sz, _p, _p]),
     ("paged_prefill_workspace_bytes", _sz, [_i32, _i32, _i32, _i32]),
     ("paged_prefill_workspace_bytes_staged", _sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     ("paged_prefill_attention", ctypes.c_int,

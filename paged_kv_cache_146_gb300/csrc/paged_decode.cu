@@ -40,7 +40,10 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "pagedkv.h"
 #include "decode_params.h"
@@ -83,7 +86,9 @@ struct Smem {
         1024 + kStagesBytes + kQBytes + kBarBytes + kMetaBytes + kScratchBytes;
 };
 
-// Item metadata the producer hands to the consumers with each item's Q rows.
+// Item metadata the producer hands to the consumers with each item's Q rows:
+// sequence, kv head, context length, blocks [b0, b1), the sequence's pieces
+// and this partition's piece.
 struct ItemMeta {
     int s, g, L, b0, b1, nsplit, pair, pad;
 };
@@ -845,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 }
 
 // ---------------------------------------------------------------- merge kernel
-// Sequences cut into several partitions get their pieces combined by log-sum-exp:
+// Sequences cut into several pieces get their pieces combined by log-sum-exp:
 //   M = max_p m_p,  out = sum_p o_p 2^(m_p - M) / sum_p l_p 2^(m_p - M)
 // (maxima in the log2 domain).  The kernel walks the (sequence, kv head) units
 // of the split sequences grid-stride, one warp per query head of the group:
@@ -936,9 +941,13 @@ __global__ void __launch_bounds__(512, 2) decode_merge_kernel(const Params p)
 }
 
 // --------------------------------------------------------------------- host side
+// The work plan comes first (header, per-sequence info, items, the split
+// sequences and, with shared prefixes, the skips, the shared-prefix items and
+// the run scratch), then the pieces.
 struct WsLayout {
-    size_t header, seq_info, items, part_ml, part_o, multi, total;
-    size_t seq_skip, prefix_scratch, prefix_items;   // shared-prefix layouts only
+    size_t header, seq_info, items, multi, part_ml, part_o, total;
+    size_t seq_skip, prefix_items, prefix_scratch;   // shared-prefix layouts only
+    size_t plan;                                      // bytes of the plan
     int64_t max_pairs, max_prefix_items;
 };
 
@@ -959,15 +968,16 @@ static bool ws_layout(int64_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t max
     w->header = off; off += 256;
     w->seq_info = off; off += align256((size_t)S * 8);
     w->items = off; off += align256((size_t)w->max_pairs * 8);
-    w->part_ml = off; off += align256((size_t)w->max_pairs * Hkv * G * 8);
-    w->part_o = off; off += align256((size_t)w->max_pairs * Hkv * G * D * 4);
     w->multi = off; off += align256((size_t)S * 4);
     w->seq_skip = w->prefix_scratch = w->prefix_items = 0;
     if (prefix) {
         w->seq_skip = off; off += align256((size_t)S * 8);
-        w->prefix_scratch = off; off += align256((size_t)S * 16);
         w->prefix_items = off; off += align256((size_t)w->max_prefix_items * 16);
+        w->prefix_scratch = off; off += align256((size_t)S * 16);
     }
+    w->plan = off;
+    w->part_ml = off; off += align256((size_t)w->max_pairs * Hkv * G * 8);
+    w->part_o = off; off += align256((size_t)w->max_pairs * Hkv * G * D * 4);
     w->total = off;
     return true;
 }
@@ -1076,15 +1086,24 @@ static int persistent_ctas(const Variant &v, int *num_sms_out)
             return n;
         }
     }
-    return -1;
+    int n = 0;    // the table is full: measure without caching
+    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(v.fn),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void *>(v.fn),
+                                                      v.threads, v.smem) != cudaSuccess)
+        return -1;
+    return n;
 }
 
 // 8-bit pool (k_pool = the record pool, v_pool unused) or 16-bit K and V pools.
+// planned >= 0: the work plan is already at the start of the workspace (built
+// by paged_decode_plan on the host), no prep kernel; `planned` is its number
+// of shared-prefix items.
 static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_pool,
                   const void *v_pool, bool want_8bit, const int32_t *block_tables, int32_t maxb,
                   const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
                   int32_t P, bool auto_split, void *workspace, size_t workspace_bytes,
-                  int32_t *d_status, void *stream)
+                  int32_t *d_status, void *stream, int32_t planned = -1)
 {
     PoolGeometry g;
     if (!pool_geometry(pool, &g)) return PKV_ERR_INVALID_ARG;
@@ -1114,11 +1133,13 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     // the automatic 16-bit call lays its workspace out for shared prefixes; it
     // looks for them when the ledger says some block is shared right now
     const bool prefix_layout = auto_split && !want_8bit;
-    const bool prefix = prefix_layout && pool_has_shared_blocks(pool) &&
-                        maxb > kPrefixMinBlocks && prefill::shared_prefix_supported(g, G);
+    const bool prefix = planned >= 0 ? planned > 0
+                                     : prefix_layout && pool_has_shared_blocks(pool) &&
+                                           maxb > kPrefixMinBlocks &&
+                                           prefill::shared_prefix_supported(g, G);
     WsLayout w;
     if (!ws_layout(num_seqs, num_q_heads, g.num_kv_heads, g.head_dim, maxb, P, prefix_layout, &w) ||
-        workspace_bytes < w.total)
+        workspace_bytes < w.total || planned > w.max_prefix_items)
         return PKV_ERR_INVALID_ARG;
     if ((int64_t)g.num_blocks * g.num_kv_heads * g.block_size > (int64_t)1 << 31)
         return PKV_ERR_UNSUPPORTED;   // TMA row coordinate is a signed 32-bit value
@@ -1151,11 +1172,13 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     prm.kv_q8 = want_8bit ? static_cast<const uint8_t *>(k_pool) : nullptr;
     prm.max_pairs = w.max_pairs;
     prm.debug = prm.header + 1;
+    // (a plan without shared-prefix items has zero skips: the kernels need not read them)
     prm.seq_skip = prefix ? reinterpret_cast<int2 *>(ws + w.seq_skip) : nullptr;
     prm.prefix_scratch = prefix ? reinterpret_cast<int32_t *>(ws + w.prefix_scratch) : nullptr;
     prm.prefix_items = prefix ? reinterpret_cast<int4 *>(ws + w.prefix_items) : nullptr;
     prm.max_prefix_items = (int32_t)w.max_prefix_items;
     prm.prefix_tile_seqs = prefix ? prefill::shared_prefix_tile_seqs(G) : 0;
+
 
     int num_sms = 0;
     const int per_sm = persistent_ctas(v, &num_sms);
@@ -1167,10 +1190,12 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     if (grid > upper) grid = upper;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 #ifdef PKV_DEBUG_CHECKS
-    if (cudaMemsetAsync(prm.header, 0, 8, st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(prm.header + 1, 0, 4, st) != cudaSuccess) return PKV_ERR_CUDA;
 #endif
-    decode_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (planned < 0) {
+        decode_prep_kernel<<<1, 1024, 0, st>>>(prm, g.head_dim);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
     if (prefix) {     // shared prefixes: their pieces, before the partitions after them
         prefill::SharedPrefixLaunch a;
         a.geometry = g;
@@ -1224,12 +1249,176 @@ static int launch(const pkv_pool *pool, void *out, const void *q, const void *k_
     return PKV_OK;
 }
 
+// ------------------------------------------------------------ host planner
+// The prep kernel's work plan, built on the host from host copies of the
+// context lengths and (for shared prefixes) the block tables, in the same
+// layout and order: a caller that already holds them (the ledger wrote them)
+// copies the plan to the workspace with its other per-step copies, and the
+// call then starts with the main kernel.
+static int plan_on_host(const pkv_pool *pool, const int32_t *lens, const int32_t *tables,
+                        int32_t maxb, int32_t S, int32_t Hq, void *plan, size_t plan_bytes,
+                        int32_t *prefix_items_out)
+{
+    PoolGeometry g;
+    if (!pool_geometry(pool, &g) || !is_16bit(g) || !lens || !plan || S < 0 || Hq <= 0 ||
+        maxb <= 0 || Hq % g.num_kv_heads)
+        return PKV_ERR_INVALID_ARG;
+    const int G = Hq / g.num_kv_heads, Hkv = g.num_kv_heads;
+    const bool bf = g.dtype == PKV_BF16;
+    Variant v;
+    if (g.block_size != kBlock || G > 16 || !pick_variant(g.head_dim, bf, G, &v))
+        return PKV_ERR_UNSUPPORTED;
+    WsLayout w;
+    if (!ws_layout(S, Hq, Hkv, g.head_dim, maxb, kDefaultSplit, true, &w) || plan_bytes < w.plan)
+        return PKV_ERR_INVALID_ARG;
+    const int64_t max_tokens = (int64_t)maxb * kBlock;
+    for (int32_t s = 0; s < S; ++s)
+        if (lens[s] < 0 || lens[s] > max_tokens) return PKV_ERR_INVALID_ARG;
+    char *base = static_cast<char *>(plan);
+    std::memset(base, 0, w.plan);
+    int32_t *header = reinterpret_cast<int32_t *>(base + w.header);
+    int2 *seq_info = reinterpret_cast<int2 *>(base + w.seq_info);
+    int2 *items = reinterpret_cast<int2 *>(base + w.items);
+    int32_t *multi = reinterpret_cast<int32_t *>(base + w.multi);
+    int2 *seq_skip = reinterpret_cast<int2 *>(base + w.seq_skip);
+    int4 *pitems = reinterpret_cast<int4 *>(base + w.prefix_items);
+    auto nblocks = [](int32_t L) { return (L + kBlock - 1) / kBlock; };
+
+    // shared prefixes: links between neighbours, runs, the shortest link of each
+    int32_t n_pitems = 0;
+    if (tables && pool_has_shared_blocks(pool) && maxb > kPrefixMinBlocks &&
+        prefill::shared_prefix_supported(g, G)) {
+        std::vector<int32_t> link((size_t)S, 0);
+        for (int32_t s = 0; s + 1 < S; ++s) {
+            const int32_t La = lens[s], Lb = lens[s + 1];
+            if (La <= 0 || Lb <= 0) continue;
+            const int32_t f = std::min((La - 1) / kBlock, (Lb - 1) / kBlock);
+            const int32_t *ra = tables + (int64_t)s * maxb, *rb = ra + maxb;
+            int32_t k = 0;
+            while (k < f && ra[k] == rb[k] && ra[k] >= 0 && ra[k] < g.num_blocks) ++k;
+            link[(size_t)s] = k;
+        }
+        const int tt = prefill::shared_prefix_tile_seqs(G);
+        for (int32_t s = 0; s < S;) {
+            int32_t e = s;   // run [s, e]
+            int32_t pb = 0x7fffffff;
+            while (e + 1 < S && link[(size_t)e] >= kPrefixMinBlocks) pb = std::min(pb, link[(size_t)e++]);
+            const int32_t n = e - s + 1;
+            if (n >= 2) {
+                const int pieces = std::min(kPrefixMaxPieces, (pb + kPrefixMinBlocks - 1) / kPrefixMinBlocks);
+                const int cb = (pb + pieces - 1) / pieces;
+                for (int32_t m = s; m <= e; ++m) seq_skip[m] = make_int2(pb, pieces);
+                for (int t = 0; t * tt < n; ++t)
+                    for (int j = 0; j < pieces; ++j) {
+                        if (n_pitems >= w.max_prefix_items) return PKV_ERR_INVALID_ARG;
+                        pitems[n_pitems++] = make_int4(s + t * tt, std::min(tt, n - t * tt) | (j << 16),
+                                                       j * cb, std::min(pb, (j + 1) * cb));
+                    }
+            }
+            s = e + 1;
+        }
+    }
+    auto own = [&](int32_t s) {
+        return make_int2(nblocks(lens[s]) - seq_skip[s].x, seq_skip[s].y);
+    };
+    // partition size: as the prep kernel chooses it
+    int num_sms = 0;
+    const int per_sm = persistent_ctas(v, &num_sms);
+    if (per_sm < 1) return PKV_ERR_CUDA;
+    const int64_t grid = (int64_t)per_sm * num_sms;
+    const int64_t want = (kAutoItemsPerCta * grid + Hkv - 1) / Hkv;
+    int P = kDefaultSplit;
+    for (int k = 1; k < kAutoSizes; ++k) {
+        const int Pk = kDefaultSplit << k;
+        int64_t pairs = 0;
+        for (int32_t s = 0; s < S; ++s)
+            if (lens[s] > 0) pairs += (own(s).x + Pk - 1) / Pk;
+        if (pairs >= want) P = Pk;
+    }
+    // pieces, full partitions in sequence order, partial ones by size bin
+    int32_t piece = 0, n_items = 0, n_multi = 0;
+    std::vector<int32_t> bin_count(kOrderBins, 0);
+    auto bin_of = [P](int r) { return (int)((int64_t)(P - 1 - r) * kOrderBins / P); };
+    for (int32_t s = 0; s < S; ++s) {
+        int nsplit = 0, npre = 0;
+        if (lens[s] > 0) {
+            const int2 o = own(s);
+            npre = o.y;
+            nsplit = (o.x + P - 1) / P;
+            const int r = o.x - (nsplit - 1) * P;
+            const int full = r < P ? nsplit - 1 : nsplit;
+            for (int k = 0; k < full; ++k) items[n_items++] = make_int2(s, k);
+            if (r < P) ++bin_count[(size_t)bin_of(r)];
+        }
+        seq_info[s] = make_int2(piece, npre + nsplit);
+        piece += npre + nsplit;
+        if (npre + nsplit > 1) multi[n_multi++] = s;
+    }
+    std::vector<int32_t> bin_at(kOrderBins, 0);
+    for (int b = 0, at = n_items; b < kOrderBins; ++b) {
+        bin_at[(size_t)b] = at;
+        at += bin_count[(size_t)b];
+    }
+    for (int32_t s = 0; s < S; ++s) {
+        if (lens[s] <= 0) continue;
+        const int2 o = own(s);
+        const int nsplit = (o.x + P - 1) / P;
+        const int r = o.x - (nsplit - 1) * P;
+        if (r < P) {
+            items[bin_at[(size_t)bin_of(r)]++] = make_int2(s, nsplit - 1);
+            ++n_items;
+        }
+    }
+    if (piece > w.max_pairs) return PKV_ERR_INVALID_ARG;
+    header[0] = n_items;
+    header[2] = P;
+    header[3] = n_multi;
+    header[4] = n_pitems;
+    header[5] = piece;
+    if (prefix_items_out) *prefix_items_out = n_pitems;
+    return PKV_OK;
+}
+
 }  // namespace decode
 }  // namespace pkv
 
 extern "C" {
 
 int32_t paged_decode_default_split(void) { return pkv::decode::kDefaultSplit; }
+
+size_t paged_decode_plan_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t max_blocks_per_seq)
+{
+    pkv::decode::WsLayout w;
+    if (!pkv::decode::ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                pkv::decode::kDefaultSplit, true, &w))
+        return 0;
+    return w.plan;
+}
+
+int paged_decode_plan(const pkv_pool *pool, const int32_t *context_lens,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                      int32_t num_q_heads, void *plan, size_t plan_bytes,
+                      int32_t *shared_prefix_items)
+{
+    return pkv::decode::plan_on_host(pool, context_lens, block_tables, max_blocks_per_seq,
+                                     num_seqs, num_q_heads, plan, plan_bytes, shared_prefix_items);
+}
+
+int paged_decode_attention_planned(const pkv_pool *pool, void *out, const void *q,
+                                   const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, float scale, int32_t shared_prefix_items,
+                                   void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                   void *stream)
+{
+    if (shared_prefix_items < 0) return PKV_ERR_INVALID_ARG;
+    return pkv::decode::launch(pool, out, q, k_pool, v_pool, false, block_tables,
+                               max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale,
+                               pkv::decode::kDefaultSplit, true, workspace, workspace_bytes,
+                               d_status, stream, shared_prefix_items);
+}
 
 size_t paged_decode_workspace_bytes_split(int32_t num_seqs, int32_t num_q_heads,
                                           int32_t num_kv_heads, int32_t head_dim,

@@ -900,9 +900,12 @@ static bool pick_tc(int D, bool bf16, bool staged, TcKernelFn *fn, int *smem)
     return false;
 }
 
+// Resident CTAs per SM of a kernel on the current device, cached per device
+// (every kernel of this file fits the table; one that did not would be
+// measured again on each call rather than fail).
 static int resident(const void *fn, int smem, int threads, int *sms_out)
 {
-    constexpr int kMaxDev = 64, kMaxVar = 8;
+    constexpr int kMaxDev = 64, kMaxVar = 16;
     static std::mutex mu;
     static const void *fns[kMaxDev][kMaxVar];
     static int ctas[kMaxDev][kMaxVar];
@@ -929,7 +932,11 @@ static int resident(const void *fn, int smem, int threads, int *sms_out)
             return n;
         }
     }
-    return -1;
+    int n = 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
+        return -1;
+    return n;
 }
 
 }  // namespace prefill

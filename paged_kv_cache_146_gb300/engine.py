@@ -18,18 +18,26 @@ waits for that copy and carries kernels only.  The host side of step t+1
 overlaps the kernels of step t: before it rewrites the pinned arrays it waits
 only for step t's copy, which starts once step t-2's kernels are done.
 ``decode_step_host`` moves the step's q/k/v in and its output out the same way.
+
+The attention call's work plan (partition size, work list, shared-prefix
+runs) is built on the host from the ledger's lengths and tables
+(``decode_plan``) and travels with them, into the workspace of the same device
+set, so the call starts with its main kernel (16-bit pools, automatic
+partition size; the 8-bit path and a fixed partition size plan on the device).
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import (KVPool, cache_write, cache_write_q8, decode_workspace_bytes,
-               paged_decode_attention, paged_decode_attention_q8, status_check)
+from . import (KVPool, cache_write, cache_write_q8, decode_plan, decode_plan_bytes,
+               decode_workspace_bytes, paged_decode_attention, paged_decode_attention_planned,
+               paged_decode_attention_q8, status_check)
 
 
 class DecodeEngine:
     def __init__(self, pool: KVPool, num_seqs: int, num_q_heads: int, max_blocks_per_seq: int,
-                 scale: float, device, blocks_per_split: int | None = None):
+                 scale: float, device, blocks_per_split: int | None = None,
+                 plan_on_host: bool = True):
         import torch
         self.torch = torch
         self.pool = pool
@@ -62,7 +70,20 @@ class DecodeEngine:
         self._io = None                              # q/k/v/out sets of decode_step_host
         nbytes = decode_workspace_bytes(num_seqs, num_q_heads, pool.num_kv_heads, pool.head_dim,
                                         max_blocks_per_seq, blocks_per_split)
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        # host-planned calls: one workspace per device set (a set's plan lands
+        # while the other set's kernels run) and a pinned plan buffer per set
+        self.planned = plan_on_host and not pool.is_q8 and blocks_per_split is None
+        for st in self._sets[:2 if self.planned else 1]:
+            st["workspace"] = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        if not self.planned:
+            self._sets[1]["workspace"] = self._sets[0]["workspace"]
+        if self.planned:
+            pb = decode_plan_bytes(num_seqs, num_q_heads, pool.num_kv_heads, pool.head_dim,
+                                   max_blocks_per_seq)
+            self.plan_bytes = pb
+            for st in self._sets:
+                st["h_plan"] = torch.zeros(pb, dtype=torch.uint8, pin_memory=True)
+                st["prefix_items"] = 0
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         tdt = torch.bfloat16 if pool.dtype in ("bf16", "q8_bf16") else torch.float16
         self.out = torch.empty((num_seqs, num_q_heads, pool.head_dim), dtype=tdt, device=device)
@@ -81,6 +102,15 @@ class DecodeEngine:
     @property
     def d_slots(self):
         return self._sets[self._set]["slots"]
+
+    @property
+    def workspace(self):
+        return self._sets[self._set]["workspace"]
+
+    @property
+    def plan_prefix_items(self):
+        """Shared-prefix work items of the current set's plan (planned calls)."""
+        return self._sets[self._set]["prefix_items"]
 
     # ------------------------------------------------------------------ prompt
     def prefill(self, k_rows, v_rows, num_new) -> np.ndarray:
@@ -132,11 +162,16 @@ class DecodeEngine:
         self._ledger_step()
         b = self._set ^ 1
         dst = self._sets[b]
+        if self.planned:      # set b's plan buffer was last copied two steps ago
+            dst["prefix_items"] = decode_plan(self.pool, self.lens, self.tables, self.hq,
+                                              dst["h_plan"])
         self._h2d.wait_event(self._used[b])     # set b's last readers were enqueued
         with torch.cuda.stream(self._h2d):
             dst["tables"].copy_(self.h_tables, non_blocking=True)
             dst["lens"].copy_(self.h_lens, non_blocking=True)
             dst["slots"].copy_(self.h_slots, non_blocking=True)
+            if self.planned:
+                dst["workspace"][:self.plan_bytes].copy_(dst["h_plan"], non_blocking=True)
             for d, h in extra:
                 d.copy_(h, non_blocking=True)
             self._loaded[b].record(self._h2d)
@@ -169,6 +204,10 @@ class DecodeEngine:
         if self.pool.is_q8:
             r = paged_decode_attention_q8(self.pool, q, self.d_tables, self.d_lens, self.scale,
                                           self.workspace, self.status, out=out)
+        elif self.planned:
+            r = paged_decode_attention_planned(self.pool, q, self.d_tables, self.d_lens,
+                                               self.scale, self.plan_prefix_items,
+                                               self.workspace, self.status, out=out)
         else:
             r = paged_decode_attention(self.pool, q, self.d_tables, self.d_lens, self.scale,
                                        self.workspace, self.status, out=out,

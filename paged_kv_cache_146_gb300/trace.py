@@ -34,8 +34,9 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import (CapturedDecode, KVPool, cache_write, decode_workspace_bytes, gather_blocks,
-               paged_decode_attention, scatter_blocks, status_check)
+from . import (CapturedDecode, KVPool, cache_write, decode_plan, decode_plan_bytes,
+               decode_workspace_bytes, gather_blocks, paged_decode_attention_planned,
+               scatter_blocks, status_check)
 from .workloads import TraceSchedule
 
 
@@ -103,11 +104,24 @@ class TraceRunner:
         self.h_slots = torch.zeros(S, dtype=torch.int64, pin_memory=True)
         self.d_slots = torch.zeros(S, dtype=torch.int64, device=device)
         self._copied = None
+        # The attention call's work plan is built on the host from the ledger's
+        # lengths and tables (no prep kernel) and copied to the start of the
+        # workspace with the other per-step copies.
+        self.plan_bytes = decode_plan_bytes(S, sched.num_q_heads, sched.num_kv_heads,
+                                            sched.head_dim, self.maxb)
+        self.h_plan = torch.zeros(self.plan_bytes, dtype=torch.uint8, pin_memory=True)
         # the step's queries land in a fixed buffer, so the attention call can
         # be one CUDA graph replay (all lengths are zero at capture)
         self.q = torch.empty((S, sched.num_q_heads, sched.head_dim), dtype=tdt, device=device)
-        self.captured = CapturedDecode(self.pool, self.q, self.d_tables, self.d_ctx, self.scale,
-                                       self.workspace, self.status, self.out) if graph else None
+        self.captured = None
+        if graph:
+            n_pre = decode_plan(self.pool, np.zeros(S, np.int32), self.tables,
+                                sched.num_q_heads, self.h_plan)
+            self.workspace[:self.plan_bytes].copy_(self.h_plan)
+            self.captured = CapturedDecode(self.pool, self.q, self.d_tables, self.d_ctx,
+                                           self.scale, self.workspace, self.status, self.out,
+                                           planned_prefix_items=n_pre)
+            self.captured_prefix_items = n_pre
 
     def _step_rows(self, t: int, n: int):
         """K/V rows of a step's n new tokens: a window of the rows drawn up front."""
@@ -238,23 +252,25 @@ class TraceRunner:
         h2 = time.perf_counter()
         # the ledger's arrays to the GPU (slots, tables, lengths), then the write
         # of the new K/V, then attention
+        n_pre = decode_plan(self.pool, ctx, self.tables, sc.num_q_heads, self.h_plan)
         evs[0].record()
         d_slots = self._stage_slots(slots) if n_tok else None
         self.h_tables.numpy()[:] = self.tables
         self.h_ctx.numpy()[:] = ctx
         self.d_tables.copy_(self.h_tables, non_blocking=True)
         self.d_ctx.copy_(self.h_ctx, non_blocking=True)
+        self.workspace[:self.plan_bytes].copy_(self.h_plan, non_blocking=True)
         self._copied = torch.cuda.Event()
         self._copied.record()
         evs[1].record()
         if n_tok:
             cache_write(self.pool, k_new, v_new, d_slots, self.status)
         evs[2].record()
-        if self.captured is not None:
+        if self.captured is not None and n_pre == self.captured_prefix_items:
             self.captured.replay()
         else:
-            paged_decode_attention(self.pool, q, self.d_tables, self.d_ctx, self.scale,
-                                   self.workspace, self.status, out=self.out)
+            paged_decode_attention_planned(self.pool, q, self.d_tables, self.d_ctx, self.scale,
+                                           n_pre, self.workspace, self.status, out=self.out)
         evs[3].record()
         h3 = time.perf_counter()
         kv_bytes = int(ctx.astype(np.int64).sum()) * sc.num_kv_heads * sc.head_dim * 2 * 2
