@@ -9,7 +9,8 @@
 // busy:
 //
 //   * Work items are (sequence, kv head, partition of up to P blocks); a
-//     persistent grid walks them in a fixed stride.  A prep kernel turns the
+//     persistent grid walks them in rounds of one item per CTA, alternate
+//     rounds from the other end of the list.  A prep kernel turns the
 //     device-side context lengths into the item list (no host round trip).
 //   * Per CTA: one producer warp issues 2-D TMA copies (cp.async.bulk.tensor,
 //     128-byte swizzle) of each block's K and V slab for the item's kv head
@@ -97,8 +98,8 @@ struct ItemMeta {
 // One CTA: partitions per sequence, their prefix sum, the item list, and zero
 // rows for empty or invalid sequences.
 //
-// Item order: the persistent grid takes items in a fixed stride, so the list
-// ends with the smallest ones and every CTA's last item is short.  Full
+// Item order: the persistent grid takes items in rounds of one per CTA, so the
+// list ends with the smallest ones and every CTA's last item is short.  Full
 // partitions (P blocks) come first, in sequence order; then each sequence's
 // partial last partition, by size from large to small (kOrderBins size bins,
 // sequence order inside a bin).  The list must not vary between launches with
@@ -493,6 +494,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int Hkv = p.num_kv_heads, G = p.group, P = p.header[2];   // chosen by the prep kernel
     const int total_items = p.header[0] * Hkv;
     const int stride = gridDim.x;
+    // The CTA's k-th item.  The list runs from the largest items to the
+    // smallest, so the CTAs take each round of `stride` items in turn from
+    // opposite ends (CTA b takes the b-th of even rounds and the b-th from the
+    // end of odd ones): every CTA's total stays close to the mean, where a
+    // plain stride would give CTA 0 the largest item of every round.  Still a
+    // fixed function of the list, so equal inputs give equal bits.
+    auto item_of = [&](int k) {
+        return k * stride + ((k & 1) ? stride - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    };
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
@@ -501,10 +511,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // first 32 block ids one item ahead of that.
         uint32_t cnt = 0, issued = 0, issued_par = 0, q_issued = 0, q_par = 0;
         const uint32_t q_bytes = (uint32_t)(G * D * 2);
-        int item = blockIdx.x;
+        int item = item_of(0);
         int2 it_cur = item < total_items ? p.items[item / Hkv] : make_int2(0, 0);
-        int2 it_nxt = item + stride < total_items ? p.items[(item + stride) / Hkv]
-                                                  : make_int2(0, 0);
+        int2 it_nxt = item_of(1) < total_items ? p.items[item_of(1) / Hkv] : make_int2(0, 0);
         // info = (first piece of this partition, pieces of the sequence);
         // b0 = first block of the partition (after a shared prefix, if any)
         auto fetch = [&](int2 it, int valid, int &L, int2 &info, int &b0, int &id) {
@@ -526,13 +535,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         int L_cur, id_cur, b0_cur;
         int2 info_cur;
         fetch(it_cur, item < total_items, L_cur, info_cur, b0_cur, id_cur);
-        for (int k = 0; item < total_items; ++k, item += stride) {
+        for (int k = 0; item < total_items; ++k, item = item_of(k)) {
             // prefetch
-            const int2 it_fut = item + 2 * stride < total_items ? p.items[(item + 2 * stride) / Hkv]
-                                                                : make_int2(0, 0);
+            const int item2 = item_of(k + 2);
+            const int2 it_fut = item2 < total_items ? p.items[item2 / Hkv] : make_int2(0, 0);
             int L_nxt, id_nxt, b0_nxt;
             int2 info_nxt;
-            fetch(it_nxt, item + stride < total_items, L_nxt, info_nxt, b0_nxt, id_nxt);
+            fetch(it_nxt, item_of(k + 1) < total_items, L_nxt, info_nxt, b0_nxt, id_nxt);
 
             const int g = item - (item / Hkv) * Hkv;
             const int s = it_cur.x;
@@ -625,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const int v_tok = ((mi & 1) << 3) + r8, v_chunk = mi >> 1;   // V^T pairs of 8-dim tiles
     const int q_row = ((mi & 1) << 3) + r8, q_chunk = mi >> 1;   // Q: rows x (chunk, chunk+1)
 
-    for (int k = 0, item = blockIdx.x; item < total_items; ++k, item += stride) {
+    for (int k = 0; item_of(k) < total_items; ++k) {
         const int qs = k & 1;
         const bool q_landed = mbar_wait(smem_addr(&qfull_bar[qs]), (k >> 1) & 1, sm_abort, p.status);
         const bool q_ok = __all_sync(kFull, q_landed);
