@@ -872,20 +872,20 @@ def trace_run(args, world, rank, dev, steps: int | None = None) -> dict:
     t_all = time.perf_counter()
     for t in range(steps):
         rec = run.step(t)
-        recs.append((rec.kv_bytes, rec.extra["phase_events"], rec.extra["host_s"],
-                     int(rec.ctx.astype(np.int64).sum())))
+        recs.append((rec.kv_bytes, rec.extra["host_s"]))
     torch.cuda.synchronize()
     wall_s = time.perf_counter() - t_all
     barrier(world)
+    device = run.finish()
     rc, word = run.check()
     if rc != 0:
         raise SystemExit(f"device status {rc} word {word:#x}")
     rates, attn, h2d, cw = [], [], [], []
     host = [[], [], [], []]
-    for kv_bytes, evs, hs, _ in recs:
-        ms = evs[2].elapsed_time(evs[3])
-        h2d.append(1e3 * evs[0].elapsed_time(evs[1]))
-        cw.append(1e3 * evs[1].elapsed_time(evs[2]))
+    for t, (kv_bytes, hs) in enumerate(recs):
+        h2d_ms, cw_ms, ms = device[t]
+        h2d.append(1e3 * h2d_ms)
+        cw.append(1e3 * cw_ms)
         for i in range(4):
             host[i].append(1e6 * hs[i])
         if ms and kv_bytes:

@@ -1284,7 +1284,8 @@ static int plan_on_host(const pkv_pool *pool, const int32_t *lens, const int32_t
     for (int32_t s = 0; s < S; ++s)
         if (lens[s] < 0 || lens[s] > max_tokens) return PKV_ERR_INVALID_ARG;
     char *base = static_cast<char *>(plan);
-    std::memset(base, 0, w.plan);
+    std::memset(base + w.header, 0, 256);                  // every other word is written below
+    std::memset(base + w.seq_skip, 0, (size_t)S * 8);     // zero outside shared-prefix runs
     int32_t *header = reinterpret_cast<int32_t *>(base + w.header);
     int2 *seq_info = reinterpret_cast<int2 *>(base + w.seq_info);
     int2 *items = reinterpret_cast<int2 *>(base + w.items);

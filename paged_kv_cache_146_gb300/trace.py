@@ -44,7 +44,7 @@ from .workloads import TraceSchedule
 class StepRecord:
     step: int
     admitted: list                 # rows admitted (prefilled) this step
-    decoding: list                 # rows that decoded this step
+    decoding: np.ndarray           # rows that decoded this step (ascending)
     finished: list                 # rows released at the end of this step
     num_new: np.ndarray            # tokens appended per row this step
     slots: np.ndarray              # slots of the appended tokens, row by row
@@ -70,7 +70,13 @@ class TraceRunner:
                            block_size=bs, free_order=free_order, device=device)
         self.tables = np.full((S, self.maxb), -1, dtype=np.int32)
         self.lens = np.zeros(S, dtype=np.int32)           # tokens held per row
-        self.state = {}                                   # row -> [req id, prompt, out_len, generated]
+        # per-row request state (numpy, so a step's bookkeeping is a few array
+        # operations rather than a Python loop over the batch)
+        self.running = np.zeros(S, dtype=bool)
+        self.req_id = np.zeros(S, dtype=np.int64)
+        self.prompt = np.zeros(S, dtype=np.int32)
+        self.out_len = np.zeros(S, dtype=np.int32)
+        self.generated = np.zeros(S, dtype=np.int32)
         self.free_rows = deque(range(S))
         self.waiting = deque()
         self.next_id = 0
@@ -100,6 +106,14 @@ class TraceRunner:
         # GPU without waiting, and rewrites them only after the previous step's
         # copies have landed (self._copied).
         self.h_tables = torch.full((S, self.maxb), -1, dtype=torch.int32, pin_memory=True)
+        self._h_tables = self.h_tables.numpy()
+        self._dirty = np.zeros(S, dtype=bool)      # table rows changed since the last hand-off
+        # CUDA events around each step's device phases, in a ring: a set is
+        # read (its step finished long before) when it comes round again
+        self._ev_ring = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                         for _ in range(8)]
+        self._ev_step = [None] * len(self._ev_ring)
+        self.device_ms = {}        # step -> (hand-off copies, cache write, attention) in ms
         self.h_ctx = torch.zeros(S, dtype=torch.int32, pin_memory=True)
         self.h_slots = torch.zeros(S, dtype=torch.int64, pin_memory=True)
         self.d_slots = torch.zeros(S, dtype=torch.int64, device=device)
@@ -165,7 +179,7 @@ class TraceRunner:
         host = torch.empty(staging.shape, dtype=self.tdt, pin_memory=True)
         host.copy_(staging, non_blocking=True)
         self.pool.free(ids)
-        rec = (self.state.pop(row), int(self.lens[row]), host, ids)
+        rec = (self._take_state(row), int(self.lens[row]), host, ids)
         self.tables[row, :] = -1
         self.lens[row] = 0
         self.free_rows.append(row)
@@ -184,13 +198,44 @@ class TraceRunner:
         scatter_blocks(self.pool, torch.from_numpy(ids).to(self.device), staging, self.status)
         self.tables[row, :nb] = ids
         self.lens[row] = length
-        self.state[row] = st
+        self._put_state(row, st)
         self.swapped_bytes += host.numel() * host.element_size()
         return row, ids
 
+    def _take_state(self, row: int) -> tuple:
+        """(request id, prompt, output length, generated) of a row, which stops running."""
+        self.running[row] = False
+        return (int(self.req_id[row]), int(self.prompt[row]), int(self.out_len[row]),
+                int(self.generated[row]))
+
+    def _put_state(self, row: int, st) -> None:
+        self.req_id[row], self.prompt[row], self.out_len[row], self.generated[row] = st
+        self.running[row] = True
+
+    def _read_events(self, slot: int) -> None:
+        evs, step = self._ev_ring[slot], self._ev_step[slot]
+        if step is None:
+            return
+        evs[3].synchronize()
+        self.device_ms[step] = (evs[0].elapsed_time(evs[1]), evs[1].elapsed_time(evs[2]),
+                                evs[2].elapsed_time(evs[3]))
+        self._ev_step[slot] = None
+
+    def _take_events(self, t: int):
+        slot = t % len(self._ev_ring)
+        self._read_events(slot)
+        self._ev_step[slot] = t
+        return self._ev_ring[slot]
+
+    def finish(self) -> dict:
+        """Wait for the last steps and return the device times of every step."""
+        for slot in range(len(self._ev_ring)):
+            self._read_events(slot)
+        return self.device_ms
+
     def _growth(self, rows) -> int:
-        bs = self.sched.block_size
-        return sum(1 for r in rows if self.lens[r] % bs == 0)
+        """Rows (an index array) whose next token opens a block."""
+        return int(np.count_nonzero(self.lens[rows] % self.sched.block_size == 0))
 
     def step(self, t: int, keep_tensors: bool = False) -> StepRecord:
         torch, sc, bs = self.torch, self.sched, self.sched.block_size
@@ -204,20 +249,20 @@ class TraceRunner:
         while self.swapped and self.free_rows:
             st, length, host, _ = self.swapped[0]
             need = -(-length // bs) + (1 if length % bs == 0 else 0)
-            if need + self._growth(self.state) > self.pool.num_free():
+            if need + self._growth(np.flatnonzero(self.running)) > self.pool.num_free():
                 break
             self.swapped.popleft()
             row, ids = self._swap_in((st, length, host, None))
             swapped_in.append((row, st[0], ids))
-        decoding = sorted(self.state)                     # rows running before this step
+        decoding = np.flatnonzero(self.running)           # rows running before this step
         # out of blocks: evict the latest arrival, all of its blocks (FCFS)
-        while decoding and self._growth(decoding) > self.pool.num_free():
-            victim = max(decoding, key=lambda r: self.state[r][0])
+        while len(decoding) and self._growth(decoding) > self.pool.num_free():
+            victim = int(decoding[np.argmax(self.req_id[decoding])])
             entry = self._swap_out(victim)
             swapped_out.append((victim, entry[0][0], entry[3]))
             self.swapped.append(entry)
             self.swapped = deque(sorted(self.swapped, key=lambda e: e[0][0]))
-            decoding.remove(victim)
+            decoding = decoding[decoding != victim]
         # FCFS admission while rows and blocks last (all of a prompt or nothing);
         # none while evicted sequences wait to come back
         admitted = []
@@ -230,23 +275,25 @@ class TraceRunner:
             self.waiting.popleft()
             free_blocks -= need
             row = self.free_rows.popleft()
-            self.state[row] = [rid, prompt, out_len, 0]
+            self._put_state(row, (rid, prompt, out_len, 0))
             admitted.append(row)
         num_new = np.zeros(self.S, dtype=np.int32)
-        for r in decoding:
-            num_new[r] = 1
-        for r in admitted:
-            num_new[r] = self.state[r][1]
+        num_new[decoding] = 1
+        num_new[admitted] = self.prompt[admitted]
+        self._dirty |= (self.lens + num_new + bs - 1) // bs > (self.lens + bs - 1) // bs
+        for row, _, _ in swapped_in:
+            self._dirty[row] = True
+        for row, _, _ in swapped_out:
+            self._dirty[row] = True
         slots = self.pool.append_slots(self.lens, num_new, self.tables)
         self.lens += num_new
         ctx = np.zeros(self.S, dtype=np.int32)
-        for r in decoding:
-            ctx[r] = self.lens[r]
+        ctx[decoding] = self.lens[decoding]
         h1 = time.perf_counter()
         # hand-off to the GPU and the device steps
         n_tok = int(num_new.sum())
         k_new, v_new = self._step_rows(t, n_tok)
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        evs = self._take_events(t)
         q = self.q.copy_(self.q_src[t % len(self.q_src)])     # this step's queries arrive
         self._wait_copied()
         h2 = time.perf_counter()
@@ -255,7 +302,9 @@ class TraceRunner:
         n_pre = decode_plan(self.pool, ctx, self.tables, sc.num_q_heads, self.h_plan)
         evs[0].record()
         d_slots = self._stage_slots(slots) if n_tok else None
-        self.h_tables.numpy()[:] = self.tables
+        rows = np.flatnonzero(self._dirty)          # only changed rows reach the pinned copy
+        self._h_tables[rows] = self.tables[rows]
+        self._dirty[:] = False
         self.h_ctx.numpy()[:] = ctx
         self.d_tables.copy_(self.h_tables, non_blocking=True)
         self.d_ctx.copy_(self.h_ctx, non_blocking=True)
@@ -274,24 +323,20 @@ class TraceRunner:
         evs[3].record()
         h3 = time.perf_counter()
         kv_bytes = int(ctx.astype(np.int64).sum()) * sc.num_kv_heads * sc.head_dim * 2 * 2
-        # finished sequences give their blocks back
-        finished = []
-        for r in decoding:
-            st = self.state[r]
-            st[3] += 1
-            if st[3] >= st[2]:
-                finished.append(r)
-        for r in finished:
-            nb = -(-int(self.lens[r]) // bs)
-            self.pool.free(self.tables[r, :nb])
-            self.tables[r, :] = -1
-            self.lens[r] = 0
-            del self.state[r]
-            self.free_rows.append(r)
+        # finished sequences give their blocks back (one ledger call, rows in order)
+        self.generated[decoding] += 1
+        fin = decoding[self.generated[decoding] >= self.out_len[decoding]]
+        finished = fin.tolist()
+        if finished:
+            nbs = -(-self.lens[fin] // bs)
+            self.pool.free(np.concatenate([self.tables[r, :n] for r, n in zip(finished, nbs)]))
+            self.tables[fin, :] = -1
+            self._dirty[fin] = True
+            self.lens[fin] = 0
+            self.running[fin] = False
+            self.free_rows.extend(finished)
         h4 = time.perf_counter()
         rec = StepRecord(t, admitted, decoding, finished, num_new, slots, ctx, kv_bytes)
-        rec.extra["events"] = (evs[2], evs[3])       # around the attention call
-        rec.extra["phase_events"] = evs             # h2d | cache write | attention
         # host seconds: scheduling + ledger, waiting for the previous hand-off,
         # enqueueing the device work, releasing finished sequences
         rec.extra["host_s"] = (h1 - h0, h2 - h1, h3 - h2, h4 - h3)

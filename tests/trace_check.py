@@ -68,7 +68,7 @@ def run_checked_trace(sched, steps, check_every=25, device="cuda", cap=40000):
             slots_c = compact(blocks) * bs + rec.slots % bs
             assert o.cache_write(to_np_bits(rec.k_new), to_np_bits(rec.v_new), slots_c, kp, vp,
                                  bs) == 0
-        rows = rec.decoding
+        rows = rec.decoding.tolist()
         stats["peak_running"] = max(stats["peak_running"], len(rows))
         if check and rows:
             stats["checks"] += 1
