@@ -525,6 +525,12 @@ __global__ void __launch_bounds__(kThreads)
             const uint32_t id_pv = tc::idesc_f16(kTwoParts, kRows, D, 0, 1);   // P and V: same type
             const uint32_t q_a = smem_addr(q_s) + gr * LY::kQBytes, st_a = smem_addr(stage_s);
             const uint32_t o_t = tmem + 256 + 128 * gr;
+            // Descriptors are built once per operand base; each MMA adds its
+            // constant offset to the address field (offset >> 4: no carry
+            // leaves the field, shared memory is below 256 KB), which keeps the
+            // issuing thread's instruction stream short -- it shares its
+            // scheduler with two softmax warps.
+            const uint64_t qa_d = tc::desc_sw128(q_a, 16, 1024);
             uint32_t tg = 0, it_cnt = 0;
             bool ok = true;
             // P V of tile t for this group, then its share of freeing the stage
@@ -537,11 +543,12 @@ __global__ void __launch_bounds__(kThreads)
                 }
                 tc::fence_after_sync();
                 const uint32_t pt = tmem + 64 * (2 * gr + (t & 1u));   // P of tile t
+                const uint64_t vb_d = tc::desc_sw128(vs, kKeys * 128, 1024);
 #pragma unroll
                 for (int part = 0; part < (kTwoParts ? 2 : 1); ++part)
 #pragma unroll
                     for (int kk = 0; kk < kKeys / 16; ++kk) {
-                        const uint64_t b = tc::desc_sw128(vs + kk * 16 * 128, kKeys * 128, 1024);
+                        const uint64_t b = vb_d + (uint64_t)((kk * 16 * 128) >> 4);
                         tc::mma_f16_ts(o_t, pt + part * 32 + kk * 8, b, id_pv,
                                        !(first && part == 0 && kk == 0));
                     }
@@ -559,12 +566,12 @@ __global__ void __launch_bounds__(kThreads)
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t ks = st_a + st * LY::kStageBytes;
+                    const uint64_t kb_d = tc::desc_sw128(st_a + st * LY::kStageBytes, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
-                        const uint64_t a = tc::desc_sw128(q_a + (kk >> 2) * kRows * 128 + off, 16, 1024);
-                        const uint64_t b = tc::desc_sw128(ks + (kk >> 2) * kKeys * 128 + off, 16, 1024);
+                        const uint64_t a = qa_d + (uint64_t)(((kk >> 2) * kRows * 128 + off) >> 4);
+                        const uint64_t b = kb_d + (uint64_t)(((kk >> 2) * kKeys * 128 + off) >> 4);
                         tc::mma_f16(tmem + 64 * (2 * gr + sb), a, b, id_qk, kk > 0);
                     }
                     tc::mma_commit(smem_addr(&s_full[2 * gr + sb]));
