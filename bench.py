@@ -75,11 +75,13 @@ def decode_source_hash(sources=DECODE_SOURCES) -> str:
 
 
 def profiled_traffic(workload: str = "gqa_long", summary: str | None = None,
-                     sources=DECODE_SOURCES):
+                     sources=None):
     """DRAM bytes (read + write) per attention call from the committed ncu
     launch-list summary of the workload (at its default size), or None when there
     is none or the kernel sources changed since it was taken."""
     prof = os.path.join(ROOT, "profiles", summary or f"paged_decode_{workload}_launches.md")
+    if sources is None:     # the shared-prefix path also runs the tcgen05 kernel
+        sources = DECODE_SOURCES + (PREFILL_SOURCES[:2] if workload == "shared_prefix" else ())
     try:
         fields = dict(line.split(": ", 1) for line in open(prof).read().splitlines()
                       if line.startswith(("attention_traffic_bytes_per_launch:", "source_sha256_16:")))
@@ -441,10 +443,12 @@ def decode_run(args, workload: str, world: int, rank: int, dev, steps: int, warm
            "region_ms": region_ms[med], "bytes_per_launch": bytes_per_launch,
            "attn_avg_ms": attn_avg_ms, "attn_median_ms": statistics.median(attn_ms),
            "toks_per_step": region_toks[med] / steps, "clocks": clk,
-           # cache write + (planned: main [+ shared-prefix kernel]; 8-bit: prep +
-           # main [+ merge]; fixed partition size: prep + main)
-           "launches_per_step": 1 + (1 + (eng.plan_prefix_items > 0) if eng.planned else
-                                     3 if q8 and eng.maxb > default_split() else 2)}
+           # cache write, then: planned call -- [shared-prefix kernel] + main
+           # [+ merge]; otherwise prep + main [+ merge] (the merge kernel runs
+           # when a sequence may have several pieces)
+           "launches_per_step": 1 + (1 + (eng.plan_prefix_items > 0) if eng.planned else 2)
+           + (1 if eng.maxb > default_split() or (eng.planned and eng.plan_prefix_items > 0)
+              else 0)}
 
     # ---- end to end through the public API with host buffers
     if e2e_steps > 0:
