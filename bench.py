@@ -95,7 +95,7 @@ def profiled_traffic(workload: str = "gqa_long", summary: str | None = None,
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -107,7 +107,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "100"]
+               "-lms", "50"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
