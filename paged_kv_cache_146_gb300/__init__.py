@@ -426,11 +426,13 @@ def _host_ptr_bytes(buf):
 
 
 def decode_plan(pool: KVPool, context_lens: np.ndarray, block_tables, num_q_heads: int,
-                plan) -> int:
+                plan, max_blocks_per_seq: int | None = None) -> int:
     """Build the decode work plan on the host (paged_decode_plan) from host
-    int32 ``context_lens`` [S] and ``block_tables`` [S][max_blocks] (or None)
-    into ``plan`` (a host buffer of ``decode_plan_bytes(...)`` bytes, pinned for
-    an asynchronous copy).  Returns the number of shared-prefix work items."""
+    int32 ``context_lens`` [S] and ``block_tables`` [S][max_blocks] into
+    ``plan`` (a host buffer of ``decode_plan_bytes(...)`` bytes, pinned for an
+    asynchronous copy).  With ``block_tables=None`` no shared-prefix runs are
+    looked for and ``max_blocks_per_seq`` gives the table width.  Returns the
+    number of shared-prefix work items."""
     lens = np.ascontiguousarray(context_lens, dtype=np.int32)
     S = len(lens)
     if block_tables is not None:
@@ -440,10 +442,10 @@ def decode_plan(pool: KVPool, context_lens: np.ndarray, block_tables, num_q_head
             raise TypeError("block_tables must be a C-contiguous int32 numpy array [S][max_blocks]")
         maxb, tptr = block_tables.shape[1], _np_ptr(block_tables)
     else:
-        maxb, tptr = None, None
+        if max_blocks_per_seq is None:
+            raise ValueError("without block_tables, max_blocks_per_seq gives the table width")
+        maxb, tptr = int(max_blocks_per_seq), None
     ptr, nbytes = _host_ptr_bytes(plan)
-    if maxb is None:
-        raise ValueError("block_tables (host) are needed for the table width")
     n = ctypes.c_int32()
     check(lib().paged_decode_plan(pool.handle, _np_ptr(lens), tptr, maxb, S, num_q_heads, ptr,
                                   nbytes, ctypes.byref(n)), "paged_decode_plan")

@@ -118,3 +118,13 @@ def test_prefill_and_writes_check_shapes():
     with pytest.raises(ValueError, match="dst_ids must have 1 dimension"):
         block_copy(_pool(), torch.zeros(2, dtype=torch.int32), torch.zeros(3, dtype=torch.int32),
                    status)
+
+
+def test_decode_plan_wants_a_width_and_host_buffers():
+    from paged_kv_cache_146_gb300 import decode_plan
+    lens = torch.ones(3, dtype=torch.int32).numpy()
+    with pytest.raises(ValueError, match="max_blocks_per_seq gives the table width"):
+        decode_plan(_pool(), lens, None, 8, torch.zeros(64, dtype=torch.uint8))
+    with pytest.raises(TypeError, match="block_tables must be"):
+        decode_plan(_pool(), lens, torch.zeros((3, 4), dtype=torch.int32), 8,
+                    torch.zeros(64, dtype=torch.uint8))

@@ -93,6 +93,13 @@ def test_host_plan_equals_device_plan(shape):
                           w.scale, c.status)
     assert n_pre == 0
     assert_close(out, c.oracle_out(), f"planned {shape}")
+    # with no shared blocks in the ledger the tables change nothing in the plan
+    pb = decode_plan_bytes(S, hq, hkv, d, c.tables.shape[1])
+    a, b = np.zeros(pb, np.uint8), np.zeros(pb, np.uint8)
+    assert decode_plan(c.pool, c.context_lens, c.tables, hq, a) == 0
+    assert decode_plan(c.pool, c.context_lens, None, hq, b,
+                       max_blocks_per_seq=c.tables.shape[1]) == 0
+    assert np.array_equal(a, b)
 
 
 def test_host_plan_full_size_gqa_long():
