@@ -14,18 +14,32 @@ namespace pkv {
 namespace decode {
 
 // Four stored bytes (byte i = code i + 128) -> fp16 pairs lo = (code0, code1),
-// hi = (code2, code3), exact: the byte u is the low mantissa of 1024 (fp16 bits
-// 0x6400 | u = 1024 + u) and one packed subtraction of 1152 leaves the code.
-__device__ __forceinline__ void biased_to_pairs(uint32_t w, uint32_t &lo, uint32_t &hi)
+// hi = (code2, code3), each value carrying an offset of 1152: the byte u is
+// the low mantissa of 1024 (fp16 bits 0x6400 | u = 1024 + u = 1152 + code),
+// exact.
+__device__ __forceinline__ void offset_pairs(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    uint32_t a = __byte_perm(w, 0x64646464u, 0x4140);     // (0x64, u0), (0x64, u1)
-    uint32_t b = __byte_perm(w, 0x64646464u, 0x4342);     // (0x64, u2), (0x64, u3)
-    const uint32_t bias = 0x64806480u;                    // (1152, 1152)
-    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(a) : "r"(bias));
-    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(b) : "r"(bias));
-    lo = a;
-    hi = b;
+    lo = __byte_perm(w, 0x64646464u, 0x4140);     // (0x64, u0), (0x64, u1)
+    hi = __byte_perm(w, 0x64646464u, 0x4342);     // (0x64, u2), (0x64, u3)
 }
+
+// The same pairs without the offset: one packed subtraction of 1152, exact.
+__device__ __forceinline__ void code_pairs(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    offset_pairs(w, lo, hi);
+    const uint32_t bias = 0x64806480u;                    // (1152, 1152)
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
+}
+
+// (-1152, -1152) as an fp16 pair.  The score products take K codes with their
+// offset and start their accumulators from -1152 x (the query row's sum over
+// the group), which a product with an all -1152 operand gives:
+//   sum_d q_d (-1152) + sum_d q_d (1152 + c_d) = sum_d q_d c_d.
+// Every product of an fp16 value and 1152 + c (11 significant bits each) is
+// exact in fp32; the offset only makes the terms of the fp32 sums larger
+// (up to 1279 |q| instead of 127 |q|), and with them their rounding.
+constexpr uint32_t kNegOffset = 0xE480E480u;
 
 // An 8-bit pool ("kv-cache-by-model", section 1: one-byte codes with one fp16
 // scale per 32 values) keeps each (block, kv head) slab as one record of
@@ -70,7 +84,8 @@ constexpr int kMinBlocks = PKV_Q8_CTAS;          // CTAs per SM
 #endif
 constexpr int kPrefetch = PKV_Q8_PREFETCH;       // L2 prefetch this many blocks past the copy
 constexpr int kQBytes = 8 * 128 * 2;              // one item's query rows (G <= 8), fp16/bf16
-constexpr int kWarpBytes = kSlots * kSlab + kQBytes + 128;   // stages, query rows, barriers
+constexpr int kQOffBytes = 8 * 4 * 4;             // -1152 x query sums, [8 rows][4 groups] fp32
+constexpr int kWarpBytes = kSlots * kSlab + kQBytes + kQOffBytes + 128;   // + barriers
 constexpr int kSmemBytes = 128 + kWarps * kWarpBytes;
 static_assert(kSlab % 128 == 0 && kWarpBytes % 128 == 0, "stages stay 128-byte aligned");
 }  // namespace q8
@@ -85,13 +100,18 @@ static_assert(kSlab % 128 == 0 && kWarpBytes % 128 == 0, "stages stay 128-byte a
 // 4q4 .. 4q4 + 3 of query row hrow; the K scales multiply the partial score of
 // each 32-dimension group.
 //   S[t] = sum_i ks[t][i] * (q . codes[t]) over group i
+// (the code values enter with an offset of 1152 that the accumulators' start
+// value, -1152 x the row's query sum over the group, cancels)
 // O^T = V^T P^T: V codes as A (16 dimensions per MMA, k = the 16 tokens), the
 // softmax weights times the V scale of the group as B -- exactly the four weights
 // the lane holds -- so o[t] covers dimensions 16t + r and 16t + r + 8 (r = lane/4)
 // of query rows 2q4 and 2q4 + 1.
 //   O[d][h] += sum_t vcode[d][t] * (p[h][t] * vs[t][d / 32])
+// (the V codes enter without the offset: cancelling it there cost a product
+// per tile, more than the subtraction)
 __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *scales,
-                                                 const uint32_t (&qa)[8][4], float (&o)[8][4],
+                                                 const uint32_t (&qa)[8][4],
+                                                 const float *qoff_row, float (&o)[8][4],
                                                  float &m0, float &l0, int valid,
                                                  float scale_row, int lane)
 {
@@ -104,6 +124,8 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
 
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
     {
+        const float4 qo = *reinterpret_cast<const float4 *>(qoff_row);
+        const float qoff[4] = {qo.x, qo.y, qo.z, qo.w};
         float ks[4][4];        // [token j][group i]
         const uint4 a = *reinterpret_cast<const uint4 *>(scales + 32 * q4);
         const uint4 b = *reinterpret_cast<const uint4 *>(scales + 32 * q4 + 16);
@@ -118,15 +140,16 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
         for (int i = 0; i < 4; ++i) {
             uint32_t kr[4];
             ldsm_x4(kr, krow + (((2 * i + kstep_hi) ^ r8) << 4));
-            float c0[4], c1[4];
+            // start from -1152 x (the row's query sum over group i)
+            float c0[4] = {qoff[i], qoff[i], 0.f, 0.f}, c1[4] = {qoff[i], qoff[i], 0.f, 0.f};
             uint32_t lo, hi;
-            biased_to_pairs(kr[0], lo, hi);
-            H::mma0(c0, qa[2 * i], lo, hi);
-            biased_to_pairs(kr[1], lo, hi);
-            H::mma0(c1, qa[2 * i], lo, hi);
-            biased_to_pairs(kr[2], lo, hi);
+            offset_pairs(kr[0], lo, hi);
+            H::mma(c0, qa[2 * i], lo, hi);
+            offset_pairs(kr[1], lo, hi);
+            H::mma(c1, qa[2 * i], lo, hi);
+            offset_pairs(kr[2], lo, hi);
             H::mma(c0, qa[2 * i + 1], lo, hi);
-            biased_to_pairs(kr[3], lo, hi);
+            offset_pairs(kr[3], lo, hi);
             H::mma(c1, qa[2 * i + 1], lo, hi);
             sc[0] = fmaf(ks[0][i], c0[0], sc[0]);
             sc[1] = fmaf(ks[1][i], c0[1], sc[1]);
@@ -213,8 +236,8 @@ __device__ __forceinline__ void consume_q8_block(uint32_t kb, const uint8_t *sca
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             uint32_t a[4];
-            biased_to_pairs(vr[2 * t], a[0], a[2]);
-            biased_to_pairs(vr[2 * t + 1], a[1], a[3]);
+            code_pairs(vr[2 * t], a[0], a[2]);
+            code_pairs(vr[2 * t + 1], a[1], a[3]);
             H::mma(o[2 * i + t], a, b0, b1);
         }
     }
@@ -266,7 +289,8 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
     const int hrow = lane >> 2, q4 = lane & 3;
     uint8_t *ring = base + warp * kWarpBytes;
     uint8_t *qbuf = ring + kSlots * kSlab;                       // [8 rows][128]
-    uint64_t *full = reinterpret_cast<uint64_t *>(qbuf + kQBytes);
+    float *qoff_buf = reinterpret_cast<float *>(qbuf + kQBytes);  // [8 rows][4 groups]
+    uint64_t *full = reinterpret_cast<uint64_t *>(qbuf + kQBytes + kQOffBytes);
     uint64_t *qfull = full + kSlots;
     volatile int *abort_flag = &cta_abort;
     if (threadIdx.x == 0) cta_abort = 0;
@@ -390,6 +414,23 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
                 qa[kk][0] = w.x; qa[kk][1] = 0u; qa[kk][2] = w.y; qa[kk][3] = 0u;
             }
         }
+        // -1152 x the row's query sum over each 32-dimension group, taken by
+        // the tensor cores from the same fp16 operands the scores use
+        // (kept in shared memory, [row][group], to spare registers)
+        {
+            const uint32_t neg = kNegOffset;
+            float qoff[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float c[4];
+                Elem<false>::mma0(c, qa[2 * i], neg, neg);
+                Elem<false>::mma(c, qa[2 * i + 1], neg, neg);
+                qoff[i] = c[0];
+            }
+            if (q4 == 0)
+                *reinterpret_cast<float4 *>(qoff_buf + 4 * hrow) =
+                    make_float4(qoff[0], qoff[1], qoff[2], qoff[3]);
+        }
         // the buffer is free: the next item's rows may come in (async proxy)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -413,7 +454,8 @@ __global__ void __launch_bounds__(q8::kThreads, q8::kMinBlocks)
             if (!b) {
                 const int valid = min(kBlock, cur.L - (cur.b0 + j) * kBlock);
                 uint8_t *st = ring + slot * kSlab;
-                consume_q8_block(smem_addr(st), st + 4096, qa, o, m0, l0, valid, scale_row, lane);
+                consume_q8_block(smem_addr(st), st + 4096, qa, qoff_buf + 4 * hrow, o, m0, l0,
+                                 valid, scale_row, lane);
             }
             // the next copy into this stage goes through the async proxy: order
             // this warp's reads of it first
