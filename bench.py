@@ -132,7 +132,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sms, maxes, reasons = [], [], set()
+        sms, maxes, watts, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -143,13 +143,20 @@ class ClockSampler:
                 maxes.append(float(parts[1]))
             except ValueError:
                 continue
+            try:
+                watts.append(float(parts[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sms:
             return None
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
-                "reasons": sorted(reasons), "samples": len(sms)}
+        out = {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+               "reasons": sorted(reasons), "samples": len(sms)}
+        if watts:
+            out["power_w"] = statistics.median(watts)
+        return out
 
 
 # ------------------------------------------------------------- distributed
@@ -719,13 +726,21 @@ def prefill_arm(args, world, rank, local):
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid)     # a timed region of ~0.65 ms per step: pass --steps 300+
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
+    clocks.start()
     start.record()
     for _ in range(args.steps):
         call()
     stop.record()
     torch.cuda.synchronize()
+    clk = clocks.stop()
     ms = max_over_ranks(start.elapsed_time(stop) / args.steps, world)
     rc, word = __import__("paged_kv_cache_146_gb300").status_check(status)
     if rc != 0:
@@ -754,13 +769,13 @@ def prefill_arm(args, world, rank, local):
                                                       sources=PREFILL_SOURCES)
                                      if staged and args.seed == 0 else None),
                          "peak_kind": tkind,
-                         "note": "tcgen05.mma kind::f16 (TMEM accumulators), 128 query rows x "
-                                 "64-key tiles, two query tiles per CTA, "
-                                 + ("P as one fp16 part, V copied to fp16 (scaled per sequence and kv "
-                                    "head) by two kernels inside each call" if staged else
-                                    "P as bf16 high + low parts" if kvd == "bf16" else
-                                    "P as one fp16 part")},
-            "gpu_launches": (4 if staged else 2) * args.steps}
+                         "note": "tcgen05.mma kind::f16 (TMEM accumulators), two query tiles of "
+                                 "128 rows per CTA, "
+                                 + ("128-key tiles, P as one fp16 part, V copied to fp16 (scaled per "
+                                    "sequence and kv head) by two kernels inside each call" if staged else
+                                    "64-key tiles, "
+                                    + ("P as bf16 high + low parts" if kvd == "bf16" else "P as one fp16 part"))},
+            "gpu_launches": (4 if staged else 2) * args.steps, "clocks": clk}
     print(json.dumps(line), flush=True)
 
 

@@ -7,11 +7,11 @@
 // its queries, at position p, attends causally over the sequence's tokens 0..p,
 // gathered through the block table exactly like decode.
 //
-// Design (GB300): a tcgen05 kernel (see the section "tcgen05 prefill kernel"):
-// per item, 128 query rows of one kv group against 64-key tiles of the
-// sequence's cache, S and O accumulated in tensor memory by tcgen05.mma from
-// TMA-filled, 128-byte-swizzled shared memory, softmax by four warps that each
-// own 32 tensor-memory lanes.
+// Design (GB300): two tcgen05 kernels (sections "tcgen05 prefill kernel" and
+// "..., 128-key tiles"): per item, two query tiles of 128 rows of one kv group
+// against the sequence's cache in tiles of 64 or 128 keys, S and O accumulated
+// in tensor memory by tcgen05.mma from TMA-filled, 128-byte-swizzled shared
+// memory, softmax by warpgroups whose threads each own one tensor-memory lane.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -300,6 +300,12 @@ __device__ __forceinline__ uint64_t add2f(uint64_t a, uint64_t b)
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ uint64_t mul2f(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ uint64_t sub2f(uint64_t a, uint64_t b)
 {
     uint64_t d;
@@ -348,7 +354,7 @@ struct Item {
     int kb0, chunk;      // shared-prefix mode: first block of the keys, piece of the chunk
 };
 
-template <bool PREFIX>
+template <bool PREFIX, int KEYS = kKeys>
 __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int QT)
 {
     Item it;
@@ -367,7 +373,7 @@ __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int
         it.t0 = 0;
         it.t1 = it.C;
         it.nkeys = it.L;
-        it.ntiles = (it.nkeys + kKeys - 1) / kKeys;
+        it.ntiles = (it.nkeys + KEYS - 1) / KEYS;
         return it;
     }
     it.kb0 = 0;
@@ -380,7 +386,7 @@ __device__ __forceinline__ Item load_item(const Params &p, int i, int total, int
     it.t0 = e.y * kGroups * QT;
     it.t1 = min(it.t0 + kGroups * QT, it.C);
     it.nkeys = it.L - it.C + it.t1;
-    it.ntiles = (it.nkeys + kKeys - 1) / kKeys;
+    it.ntiles = (it.nkeys + KEYS - 1) / KEYS;
     return it;
 }
 
@@ -800,6 +806,626 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace tcp
 
+// ======================================= tcgen05 prefill kernel, 128-key tiles
+// For P in one fp16 part (fp16 pools; bf16 pools whose V was copied to fp16 for
+// the call).  The same items as the 64-key kernel, but each K/V tile holds 128
+// keys (8 blocks), so S = Q K^T runs at N 128 (the full MMA rate) and a row's
+// softmax takes twice the keys per turn.  Tensor memory (512 columns) then
+// holds one S buffer per query tile (128 columns each) and the two O (128
+// each):
+//   warp 8 (producer): TMA of the item's Q rows and of each tile's K and V
+//     into two rings that fill and drain separately (K is free once both query
+//     tiles' S is done, V once both P V are); blocks past the keys are copied
+//     from past the end of the tensor, which fills them with zeros.  It also
+//     brings the next item's query rows into L2.
+//   warps 9 and 10, lane 0 (MMA issuers, one per query tile): for each tile t,
+//     O += P V of tile t - 1, then S = Q K^T of tile t into the query tile's S
+//     buffer.  P of tile t - 1 lives in that buffer's columns; the tensor core
+//     runs one thread's MMAs in the order issued, so S(t) overwrites them only
+//     after P V(t - 1) has read them, and the commit that signals S(t) also
+//     signals P V(t - 1).
+//   warps 0-3 and 4-7 (softmax, one warpgroup per query tile): thread r owns
+//     row r = tensor-memory lane r and holds the row's 128 scores of a tile in
+//     registers; the two warpgroups take turns at the weights (their
+//     exponentials share the SFU, and while one computes, the tensor core runs
+//     the other's P V and next S).  Weights are taken against a lazy
+//     reference maximum in one pass; the tile's maximum is computed only for
+//     an item's first tile and when a score exceeds the reference by more
+//     than 8 (log2 units), which moves the reference, rescales O and the sum
+//     and takes the weights again.  The output of an item goes through shared
+//     memory, so that its stores write whole lines.
+//   warp 11 holds no role: the copy/issue warpgroup gives its registers to the
+//     softmax warpgroups (setmaxnreg).
+// Every wait is bounded; on expiry the kernel flags PKV_DEV_TIMEOUT and stops.
+namespace tcw {
+
+using tcp::add2f;
+using tcp::fma2f;
+using tcp::Item;
+using tcp::kGroups;
+using tcp::kRows;
+using tcp::max3f;
+using tcp::min3f;
+using tcp::mul2f;
+using tcp::pack2f;
+using tcp::unpack2f;
+
+constexpr int kKeys = 128;             // keys per KV tile (N of S = Q K^T)
+constexpr int kTileBlocks = kKeys / kBlock;
+constexpr int kThreads = 12 * 32;      // softmax 0-7, producer 8, issuers 9 and 10, warp 11
+constexpr int kProducer = 4 * kGroups, kIssuer = 4 * kGroups + 1;
+// registers per thread: the launch gives kLaunchRegs = 65536 / 384 rounded
+// down to 8; the copy/issue warpgroup keeps kRegsIo and hands the rest to the
+// two softmax warpgroups, 2 * 128 * kRegsSoftmax + 128 * kRegsIo = 384 *
+// kLaunchRegs.  A launch with fewer registers would leave setmaxnreg.inc
+// waiting for ever, so the host launches only a build whose kernels use
+// exactly kLaunchRegs (launch_regs_ok).
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsIo = 72, kRegsSoftmax = 216;
+static_assert(2 * kRegsSoftmax + kRegsIo == 3 * kLaunchRegs, "register split of the launch");
+constexpr float kLazy = 8.f;           // rescale threshold (log2 units)
+
+template <int D>
+struct Layout {
+    static constexpr int kRegions = D / 64;
+    static constexpr int kStages = D == 128 ? 2 : 5;           // K/V tiles in flight
+    static constexpr int kQBytes = kRegions * kRows * 128;     // one query tile: [region][row][128 B]
+    static constexpr int kKVBytes = kRegions * kKeys * 128;    // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kKVBytes;           // K tile, then V tile
+    static constexpr int kStage0 = kGroups * kQBytes;
+    static constexpr int kMisc = kStage0 + kStages * kStageBytes;   // barriers and flags
+    // output staging of the softmax warps: 32 rows x 128 bytes each
+    static constexpr int kEpi = kMisc + 512;
+    static constexpr int kEpiWarpBytes = 32 * 128;
+    static constexpr int kTotal = 1024 + kEpi + 4 * kGroups * kEpiWarpBytes;
+    // S of group g at kKeys g, overwritten by that tile's P (its first
+    // kKeys / 2 columns); O of group g at 256 + 128 g
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kTotal <= 227 * 1024, "shared memory of one CTA");
+    static_assert(kKeys == 128, "the softmax takes a tile as four 32-key chunks");
+};
+
+// VS: V comes from the fp16 copy (tmV maps it; bf16 pools), so P V takes one
+// fp16 part of P and the result is scaled by 2^k.  Pools and calls that need
+// P in two parts (bf16 V as it is) or the shared-prefix mode take the 64-key
+// kernel.
+template <int D, bool BF16, bool VS>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmQ, const Params p)
+{
+    static_assert(BF16 || !VS, "fp16 pools take V as it is");
+    static_assert(!BF16 || VS, "P takes one fp16 part: fp16 pools, or bf16 pools with V in fp16");
+    using E = Elem<BF16>;
+    using T = typename E::T;
+    using LY = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *q_s = base;
+    uint8_t *stage_s = base + LY::kStage0;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + LY::kMisc);
+    uint64_t *q_full = bars + 0, *q_empty = bars + 1;
+    // K and V of a stage fill and drain separately: K is free once both query
+    // tiles' S is done, V once both P V are, so the next K tile can come in
+    // while the softmax still runs on this one
+    uint64_t *k_full = bars + 2, *k_empty = k_full + LY::kStages;      // [LY::kStages] each
+    uint64_t *v_full = k_empty + LY::kStages, *v_empty = v_full + LY::kStages;
+    // per group: S of the tile (and, with it, P V of the one before) done;
+    // P of the tile out; the item's last P V done.  Each waiter is at most one
+    // phase behind its barrier: S(t + 1) is issued after P(t), which the
+    // softmax publishes after its wait for S(t); P(t + 1) follows S(t + 1).
+    uint64_t *s_full = v_empty + LY::kStages;                  // [group]
+    uint64_t *p_full = s_full + kGroups;                       // [group]
+    uint64_t *o_full = p_full + kGroups;                       // [group], one phase per item
+    uint64_t *done = o_full + kGroups;                         // [group]
+    // the two query tiles take turns at the weights (their exponentials share
+    // the SFU, and while one computes, the tensor core runs the other's P V
+    // and next S): group g's weights of a tile done
+    uint64_t *w_done = done + kGroups;                         // [group]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(w_done + kGroups);
+    int *stage_bad = reinterpret_cast<int *>(tslot + 1);            // [LY::kStages]
+    volatile int *abort_flag = stage_bad + LY::kStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(q_full), 1);
+        mbar_init(smem_addr(q_empty), kGroups);     // one commit per issuer
+        for (int i = 0; i < LY::kStages; ++i) {
+            mbar_init(smem_addr(&k_full[i]), 1);
+            mbar_init(smem_addr(&k_empty[i]), kGroups);
+            mbar_init(smem_addr(&v_full[i]), 1);
+            mbar_init(smem_addr(&v_empty[i]), kGroups);
+        }
+        for (int i = 0; i < kGroups; ++i) {
+            mbar_init(smem_addr(&s_full[i]), 1);
+            mbar_init(smem_addr(&p_full[i]), 4);
+            mbar_init(smem_addr(&o_full[i]), 1);
+            mbar_init(smem_addr(&done[i]), 1);
+            mbar_init(smem_addr(&w_done[i]), 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) tc::tmem_alloc(tslot, LY::kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    griddep_wait();
+
+    const int Hkv = p.num_kv_heads, G = p.group, QT = p.tile_tokens / kGroups;   // one query tile
+    const int total = p.header[0] * Hkv;
+
+    // the register split is taken inside each role's branch, so that every
+    // block of a role's code lies under one limit
+    if (warp >= kProducer) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIo));
+        if (warp == kProducer) {
+            if (lane == 0) {
+                uint32_t kv_cnt = 0, it_cnt = 0;
+                const int k_rows = p.num_blocks * Hkv * kBlock;
+                const int v_rows = VS ? p.num_seqs * p.max_blocks_per_seq * Hkv * kBlock : k_rows;
+                // phases of the last copies issued: K of each stage, V of each stage, Q
+                int last_par[2 * LY::kStages + 1];
+                for (int k = 0; k <= 2 * LY::kStages; ++k) last_par[k] = -1;
+                // every role reads an item's description one item ahead, so the
+                // dependent loads behind it are off the path between items
+                Item nxt = {};
+                if ((int)blockIdx.x < total) nxt = tcp::load_item<false, kKeys>(p, blockIdx.x, total, QT);
+                for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++it_cnt) {
+                    const Item it = nxt;
+                    if (i + (int)gridDim.x < total) nxt = tcp::load_item<false, kKeys>(p, i + gridDim.x, total, QT);
+                    if (it_cnt > 0 &&
+                        !mbar_wait(smem_addr(q_empty), (it_cnt - 1) & 1u, abort_flag, p.status))
+                        break;
+                    const uint32_t qb = smem_addr(q_full);
+                    last_par[2 * LY::kStages] = (int)(it_cnt & 1u);
+                    mbar_arrive_expect_tx(qb, (uint32_t)(kGroups * LY::kRegions * QT * G * 128));
+                    for (int gr = 0; gr < kGroups; ++gr)
+                        for (int rg = 0; rg < LY::kRegions; ++rg)
+                            tc::tma_load_4d(smem_addr(q_s + gr * LY::kQBytes + rg * kRows * 128), &tmQ,
+                                            rg * 64, 0, it.g, it.r0 + it.t0 + gr * QT, qb);
+                    // the next item's query rows into L2 now: its load above comes
+                    // only once this item's last S is done, about one softmax
+                    // before its first S
+                    if (i + (int)gridDim.x < total) {
+                        for (int gr = 0; gr < kGroups; ++gr)
+                            for (int rg = 0; rg < LY::kRegions; ++rg)
+                                tc::tma_prefetch_4d(&tmQ, rg * 64, 0, nxt.g, nxt.r0 + nxt.t0 + gr * QT);
+                    }
+                    const int32_t *row = p.block_tables + (int64_t)it.s * p.max_blocks_per_seq + it.kb0;
+                    const int nb = (it.nkeys + kBlock - 1) / kBlock;
+                    for (int t = 0; t < it.ntiles; ++t, ++kv_cnt) {
+                        const int st = (int)(kv_cnt % LY::kStages);
+                        const uint32_t fill = kv_cnt / LY::kStages;
+                        // rows of K/V for every block of the tile; blocks past the
+                        // keys' last are copied from past the end of the tensor,
+                        // which the copy fills with zeros
+                        int yk[kTileBlocks], yv[kTileBlocks];
+                        int bad = 0;
+#pragma unroll
+                        for (int b = 0; b < kTileBlocks; ++b) {
+                            const int lb = kTileBlocks * t + b;
+                            const int id = lb < nb ? __ldg(row + lb) : 0;
+                            const bool ok = id >= 0 && id < p.num_blocks;
+                            bad |= !ok;
+                            yk[b] = lb < nb ? (ok ? id : 0) * Hkv * kBlock + it.g * kBlock : k_rows;
+                            if constexpr (VS)   // the fp16 copy is by logical block
+                                yv[b] = lb < nb ? ((it.s * p.max_blocks_per_seq + lb) * Hkv + it.g) * kBlock
+                                                : v_rows;
+                            else
+                                yv[b] = yk[b];
+                        }
+                        if (bad) atomicOr(p.status, PKV_DEV_BAD_BLOCK);
+                        const uint32_t ks = smem_addr(stage_s + st * LY::kStageBytes);
+                        const uint32_t vs = ks + LY::kKVBytes;
+                        // K of the tile, once both S of the tile two back are done
+                        if (fill >= 1 && !mbar_wait(smem_addr(&k_empty[st]), (fill - 1) & 1u,
+                                                    abort_flag, p.status))
+                            break;
+                        last_par[st] = (int)(fill & 1u);
+                        const uint32_t kfb = smem_addr(&k_full[st]);
+                        mbar_arrive_expect_tx(kfb, (uint32_t)LY::kKVBytes);
+#pragma unroll
+                        for (int b = 0; b < kTileBlocks; ++b) {
+#pragma unroll
+                            for (int rg = 0; rg < LY::kRegions; ++rg)
+                                tma_load_2d(ks + rg * kKeys * 128 + b * kBlock * 128, &tmK, rg * 64, yk[b], kfb);
+                        }
+                        // V, once both P V of the tile two back are done (issued
+                        // before the S above, so this rarely waits); the bad-block
+                        // flag goes with V, which the softmax waits for
+                        if (fill >= 1 && !mbar_wait(smem_addr(&v_empty[st]), (fill - 1) & 1u,
+                                                    abort_flag, p.status))
+                            break;
+                        stage_bad[st] = bad;
+                        last_par[LY::kStages + st] = (int)(fill & 1u);
+                        const uint32_t vfb = smem_addr(&v_full[st]);
+                        mbar_arrive_expect_tx(vfb, (uint32_t)LY::kKVBytes);
+#pragma unroll
+                        for (int b = 0; b < kTileBlocks; ++b) {
+#pragma unroll
+                            for (int rg = 0; rg < LY::kRegions; ++rg)
+                                tma_load_2d(vs + rg * kKeys * 128 + b * kBlock * 128, &tmV, rg * 64, yv[b], vfb);
+                        }
+                    }
+                }
+                // after a timed-out wait: let the copies still in flight land first
+                if (*abort_flag) {
+                    for (int k = 0; k <= 2 * LY::kStages; ++k) {
+                        const int par = last_par[k];
+                        if (par < 0) continue;
+                        const uint32_t fb = smem_addr(k < LY::kStages       ? &k_full[k]
+                                                      : k < 2 * LY::kStages ? &v_full[k - LY::kStages]
+                                                                            : q_full);
+                        const unsigned long long t0 = globaltimer();
+                        while (!mbar_try_wait(fb, (uint32_t)par)) {
+                            if (globaltimer() - t0 > kTimeoutNs) break;
+                        }
+                    }
+                }
+            }
+        } else if (warp == kIssuer || warp == kIssuer + 1) {
+            // one issuer per query tile
+            if (lane == 0) {
+                const int gr = warp - kIssuer;
+                const uint32_t id_qk = tc::idesc_f16(BF16, kRows, kKeys, 0, 0);
+                const uint32_t id_pv = tc::idesc_f16(false, kRows, D, 0, 1);       // P and V: fp16
+                const uint32_t q_a = smem_addr(q_s) + gr * LY::kQBytes, st_a = smem_addr(stage_s);
+                const uint32_t s_t = tmem + kKeys * gr, o_t = tmem + 256 + 128 * gr;
+                // Descriptors are built once per operand base; each MMA adds its
+                // constant offset to the address field (offset >> 4: no carry
+                // leaves the field, shared memory is below 256 KB), which keeps the
+                // issuing thread's instruction stream short.
+                const uint64_t qa_d = tc::desc_sw128(q_a, 16, 1024);
+                uint32_t tg = 0, it_cnt = 0;
+                bool ok = true;
+                // P V of tile t for this group, then its share of freeing the stage
+                auto issue_pv = [&](uint32_t t, bool first) {
+                    const uint32_t vs = st_a + (t % LY::kStages) * LY::kStageBytes + LY::kKVBytes;
+                    if (!mbar_wait(smem_addr(&p_full[gr]), t & 1u, abort_flag, p.status) ||
+                        !mbar_wait(smem_addr(&v_full[t % LY::kStages]), (t / LY::kStages) & 1u, abort_flag,
+                                   p.status)) {
+                        ok = false;
+                        return;
+                    }
+                    tc::fence_after_sync();
+                    const uint64_t vb_d = tc::desc_sw128(vs, kKeys * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk) {
+                        const uint64_t b = vb_d + (uint64_t)((kk * 16 * 128) >> 4);
+                        tc::mma_f16_ts(o_t, s_t + kk * 8, b, id_pv, !(first && kk == 0));
+                    }
+                    tc::mma_commit(smem_addr(&v_empty[t % LY::kStages]));
+                };
+                Item nxt = {};
+                if ((int)blockIdx.x < total) nxt = tcp::load_item<false, kKeys>(p, blockIdx.x, total, QT);
+                for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it_cnt) {
+                    const Item it = nxt;
+                    if (i + (int)gridDim.x < total) nxt = tcp::load_item<false, kKeys>(p, i + gridDim.x, total, QT);
+                    if (!mbar_wait(smem_addr(q_full), it_cnt & 1u, abort_flag, p.status)) break;
+                    for (int t = 0; t < it.ntiles && ok; ++t, ++tg) {
+                        if (t >= 1) {
+                            issue_pv(tg - 1, t == 1);
+                            if (!ok) break;
+                        }
+                        const uint32_t st = tg % LY::kStages;
+                        if (!mbar_wait(smem_addr(&k_full[st]), (tg / LY::kStages) & 1u, abort_flag,
+                                       p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint64_t kb_d = tc::desc_sw128(st_a + st * LY::kStageBytes, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk & 3) * 32;     // 16 values inside the row
+                            const uint64_t a = qa_d + (uint64_t)(((kk >> 2) * kRows * 128 + off) >> 4);
+                            const uint64_t b = kb_d + (uint64_t)(((kk >> 2) * kKeys * 128 + off) >> 4);
+                            tc::mma_f16(s_t, a, b, id_qk, kk > 0);
+                        }
+                        tc::mma_commit(smem_addr(&s_full[gr]));
+                        tc::mma_commit(smem_addr(&k_empty[st]));
+                        if (t == it.ntiles - 1) tc::mma_commit(smem_addr(q_empty));
+                    }
+                    if (!ok) break;
+                    issue_pv(tg - 1, it.ntiles == 1);
+                    if (ok) tc::mma_commit(smem_addr(&o_full[gr]));
+                }
+                // every MMA this thread issued has completed before the columns are freed
+                tc::mma_commit(smem_addr(&done[gr]));
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(smem_addr(&done[gr]), 0)) {
+                    if (globaltimer() - t0 > kTimeoutNs) {
+                        atomicOr(p.status, PKV_DEV_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        // ---------------------------------------------------------- softmax
+        const int gr = warp >> 2;                   // query tile of this warpgroup
+        const int r = threadIdx.x - kRows * gr;     // row = tensor-memory lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const uint32_t s_col = kKeys * gr, o_col = 256 + 128 * gr;
+        uint32_t tg = 0, it_cnt = 0;
+        bool alive = true;
+        Item nxt = {};
+        if ((int)blockIdx.x < total) nxt = tcp::load_item<false, kKeys>(p, blockIdx.x, total, QT);
+        for (int i = blockIdx.x; i < total && alive; i += gridDim.x, ++it_cnt) {
+            const Item it = nxt;
+            if (i + (int)gridDim.x < total) nxt = tcp::load_item<false, kKeys>(p, i + gridDim.x, total, QT);
+            const int jj = r / G, h = r - (r / G) * G;
+            const int tg0 = it.t0 + gr * QT;            // this group's first token
+            const bool valid = r < QT * G && tg0 + jj < it.t1;
+            const int pos = valid ? it.L - it.C + tg0 + jj : it.nkeys - 1;
+            // the fp16 copy's scale 2^k, loaded now so its latency is hidden
+            float p2k = 1.f;
+            if constexpr (VS)
+                p2k = __int_as_float((127 + v16_shift(__ldg(p.v_emax + (size_t)it.s * Hkv + it.g))) << 23);
+            float m_ref = -INFINITY, l = 0.f;
+            int bad = 0;
+            for (int t = 0; t < it.ntiles; ++t, ++tg) {
+                const uint32_t st = tg % LY::kStages;
+                const bool okS = mbar_wait(smem_addr(&s_full[gr]), tg & 1u, abort_flag, p.status);
+                if (!__all_sync(kFull, okS)) { alive = false; break; }
+                tc::fence_after_sync();
+                float x[kKeys];
+#pragma unroll
+                for (int q = 0; q < kKeys / 32; ++q) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lane_base + s_col + 32 * q, v);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) x[32 * q + c] = __uint_as_float(v[c]);
+                }
+                tc::tmem_wait_ld();
+                // raw scores; the scale enters inside the exponent (one FFMA each).
+                // Per 32-key chunk, warp-wide: every row of the warp sees all of it,
+                // none of it (no maximum, weights 0, no exponentials), or some of
+                // it (hidden keys kept out of the maximum and given weight 0).  A
+                // warp's rows are consecutive tokens, so at most a chunk or two
+                // of the tile is mixed.
+                const int k0 = t * kKeys;
+                const int nv = pos - k0 + 1;          // keys of the tile this row sees
+                uint32_t vis = 0, hid = 0;
+#pragma unroll
+                for (int q = 0; q < kKeys / 32; ++q) {
+                    vis |= (uint32_t)__all_sync(kFull, nv >= 32 * (q + 1)) << q;
+                    hid |= (uint32_t)__all_sync(kFull, nv <= 32 * q) << q;
+                }
+                const bool neg = p.scale_log2 < 0.f;   // the largest scaled score is the smallest raw one
+                const float hide = neg ? INFINITY : -INFINITY;
+                constexpr uint32_t kAll = (1u << (kKeys / 32)) - 1;
+                // the largest scaled score of the keys the row sees (hidden keys'
+                // scores are overwritten with `hide`)
+                auto tile_max = [&]() -> float {
+                    float mx = hide;
+                    if (vis == kAll) {          // the usual tile: two chains, no branches
+                        if (!neg) {
+                            float ma = fmaxf(x[0], x[1]), mb = fmaxf(x[64], x[65]);
+#pragma unroll
+                            for (int c = 2; c < 64; c += 2) {
+                                ma = max3f(ma, x[c], x[c + 1]);
+                                mb = max3f(mb, x[64 + c], x[64 + c + 1]);
+                            }
+                            mx = fmaxf(ma, mb);
+                        } else {
+                            float ma = fminf(x[0], x[1]), mb = fminf(x[64], x[65]);
+#pragma unroll
+                            for (int c = 2; c < 64; c += 2) {
+                                ma = min3f(ma, x[c], x[c + 1]);
+                                mb = min3f(mb, x[64 + c], x[64 + c + 1]);
+                            }
+                            mx = fminf(ma, mb);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < kKeys / 32; ++q) {
+                            if ((hid >> q) & 1u) continue;
+                            float *xq = x + 32 * q;
+                            if (!((vis >> q) & 1u)) {
+#pragma unroll
+                                for (int c = 0; c < 32; ++c)
+                                    if (32 * q + c >= nv) xq[c] = hide;
+                            }
+                            float m;
+                            if (!neg) {
+                                m = fmaxf(xq[0], xq[1]);
+#pragma unroll
+                                for (int c = 2; c < 32; c += 2) m = max3f(m, xq[c], xq[c + 1]);
+                                mx = fmaxf(mx, m);
+                            } else {
+                                m = fminf(xq[0], xq[1]);
+#pragma unroll
+                                for (int c = 2; c < 32; c += 2) m = min3f(m, xq[c], xq[c + 1]);
+                                mx = fminf(mx, m);
+                            }
+                        }
+                    }
+                    return mx * p.scale_log2;
+                };
+                // weights 2^(scale x - m_ref) in pairs (packed fp32 arithmetic,
+                // f32x2), stored as fp16 P over the tile's S columns (all read
+                // above), columns [0, kKeys / 2), 16 per chunk of 32 keys.
+                // Hidden keys get exponent -inf (weight 0).  emax is the largest
+                // exponent of a key the row sees.
+                const uint64_t sc2 = pack2f(p.scale_log2, p.scale_log2);
+                uint64_t lsum2 = pack2f(0.f, 0.f);
+                float emax = -INFINITY;
+                auto weights = [&](auto masked, const int q, const uint64_t nm2) {
+                    uint32_t hi[16];
+#pragma unroll
+                    for (int cc = 0; cc < 32; cc += 2) {
+                        const int c = 32 * q + cc;
+                        float2 e = unpack2f(fma2f(pack2f(x[c], x[c + 1]), sc2, nm2));
+                        if constexpr (decltype(masked)::value) {
+                            if (c >= nv) e.x = -INFINITY;
+                            if (c + 1 >= nv) e.y = -INFINITY;
+                        }
+                        emax = max3f(emax, e.x, e.y);
+                        const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+                        const uint64_t pp = pack2f(p0, p1);
+                        lsum2 = add2f(lsum2, pp);
+                        hi[cc / 2] = Elem<false>::pack(p0, p1);   // fp16: relative error <= 2^-11
+                    }
+                    tc::tmem_st16(lane_base + s_col + 16 * q, hi);
+                };
+                // the chunk choice is warp-uniform, as the warp-wide tcgen05.st in
+                // each branch needs
+                auto weights_pass = [&]() {
+                    const uint64_t nm2 = pack2f(-m_ref, -m_ref);
+                    lsum2 = pack2f(0.f, 0.f);
+                    emax = -INFINITY;
+                    if (vis == kAll) {
+#pragma unroll
+                        for (int q = 0; q < kKeys / 32; ++q) weights(std::false_type{}, q, nm2);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < kKeys / 32; ++q) {
+                            if ((hid >> q) & 1u) {
+                                uint32_t z[16];
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) z[k] = 0u;
+                                tc::tmem_st16(lane_base + s_col + 16 * q, z);
+                            } else if ((vis >> q) & 1u) {
+                                weights(std::false_type{}, q, nm2);
+                            } else {
+                                weights(std::true_type{}, q, nm2);
+                            }
+                        }
+                    }
+                };
+                // Lazy reference maximum: weights are taken against m_ref as it
+                // stands; only when a score the row sees exceeds it by more than
+                // kLazy (log2 units) does m_ref move to the tile's maximum, with O
+                // and the sum rescaled and the weights taken again (over the P
+                // just stored).  Weights thus stay <= 2^kLazy.  The first tile of
+                // an item sets m_ref from its maximum.
+                float f = 1.f;
+                if (t == 0) m_ref = tile_max();
+                // turns: group 0's tile tg after group 1's tile tg - 1, group 1's
+                // tile tg after group 0's tile tg (each waiter is at most one
+                // phase behind: the other group's next turn needs this one's)
+                if (gr == 1 || tg > 0) {
+                    const uint32_t ph = gr == 0 ? tg - 1 : tg;
+                    const bool okw = mbar_wait(smem_addr(&w_done[gr ^ 1]), ph & 1u, abort_flag, p.status);
+                    if (!__all_sync(kFull, okw)) { alive = false; break; }
+                }
+                weights_pass();
+                if (__any_sync(kFull, emax > kLazy)) {
+                    const float mx = tile_max();
+                    bool resc = false;
+                    if (mx > m_ref + kLazy) {
+                        f = fast_exp2(m_ref - mx);
+                        resc = true;
+                        m_ref = mx;
+                    }
+                    // O is rescaled before P V of this tile: S of this tile being
+                    // done means P V of the previous one is too (issued before it)
+                    if (__any_sync(kFull, resc)) {
+#pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t v[32];
+                            tc::tmem_ld32(lane_base + o_col + c0, v);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
+                            tc::tmem_st32(lane_base + o_col + c0, v);
+                        }
+                    }
+                    weights_pass();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&w_done[gr]));
+                const float2 ls = unpack2f(lsum2);
+                l = l * f + (ls.x + ls.y);
+                // V of the tile has landed (its bad-block flag comes with it; the
+                // next V into this stage waits for this tile's P V)
+                const bool okV = mbar_wait(smem_addr(&v_full[st]), (tg / LY::kStages) & 1u, abort_flag,
+                                           p.status);
+                if (!__all_sync(kFull, okV)) { alive = false; break; }
+                bad |= stage_bad[st];
+                // zero the V rows of keys past the last one inside its block (the
+                // rest of the last block: stale pool rows; blocks after it came in
+                // as zeros)
+                const int nvis = it.nkeys - k0;
+                const int nstale = min(kKeys, ((it.nkeys + kBlock - 1) / kBlock) * kBlock - k0) - nvis;
+                if (nstale > 0) {      // both groups write the same zeros, each before its P
+                    uint8_t *vs = stage_s + st * LY::kStageBytes + LY::kKVBytes;
+                    const int nrows = nstale;
+                    for (int e = r; e < nrows * LY::kRegions * 8; e += kRows) {
+                        const int row = nvis + e / (LY::kRegions * 8);
+                        const int rem = e % (LY::kRegions * 8);
+                        *reinterpret_cast<uint4 *>(vs + (rem >> 3) * kKeys * 128 + row * 128 +
+                                                   (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&p_full[gr]));
+            }
+            if (!alive) break;
+            // ---- the item's result: O / l once the last P V is done
+            const bool oko = mbar_wait(smem_addr(&o_full[gr]), it_cnt & 1u, abort_flag, p.status);
+            if (!__all_sync(kFull, oko)) break;
+            tc::fence_after_sync();
+            // O / l (VS: in the fp16 copy's units, times 2^k), 64 columns at a
+            // time through this warp's staging rows, so that every store
+            // instruction writes whole 128-byte lines: lane l writes its row
+            // (16-byte chunk j at position j ^ (l & 7), free of bank conflicts),
+            // then the warp stores 4 rows x 128 bytes per instruction.
+            const float scl = (1.f / l) * p2k;
+            const uint64_t scl2 = pack2f(scl, scl);
+            T *out = static_cast<T *>(p.out) +
+                     ((size_t)(it.r0 + tg0 + jj) * p.num_q_heads + (size_t)it.g * G + h) * D;
+            uint8_t *ep = base + LY::kEpi + warp * LY::kEpiWarpBytes;
+#pragma unroll
+            for (int half = 0; half < D / 64; ++half) {
+                uint32_t v[2][32];
+                tc::tmem_ld32(lane_base + o_col + 64 * half, v[0]);
+                tc::tmem_ld32(lane_base + o_col + 64 * half + 32, v[1]);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t *x = &v[j >> 2][8 * (j & 3)];
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 y = unpack2f(
+                            mul2f(pack2f(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])), scl2));
+                        w[e] = bad ? 0u : E::pack(y.x, y.y);
+                    }
+                    *reinterpret_cast<uint4 *>(ep + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 4 * i + (lane >> 3), j = lane & 7;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(ep + row * 128 + ((j ^ (row & 7)) << 4));
+                    const unsigned long long dst =
+                        __shfl_sync(kFull, (unsigned long long)reinterpret_cast<uintptr_t>(out), row);
+                    if (__shfl_sync(kFull, (int)valid, row))
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(dst) + 64 * half + 8 * j) = w;
+                }
+                __syncwarp();
+            }
+            tc::fence_before_sync();
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, LY::kTmemCols);
+}
+
+}  // namespace tcw
+
 // --------------------------------------------------------------------- host side
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -888,23 +1514,43 @@ static bool make_q_map(CUtensorMap *map, const void *q, int64_t T, int Hkv, int 
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params);
 
-static bool pick_tc(int D, bool bf16, bool staged, TcKernelFn *fn, int *smem)
+// The kernel for a call: bf16 pools whose V is copied to fp16 take the 128-key
+// kernel; P in two bf16 parts takes the 64-key one (whose two S buffers per
+// query tile hide the doubled P V), and so do fp16 pools, where it measured
+// 1 % faster (0.574 against 0.580 ms on 16 x 2,048-token prompts).
+struct TcPick {
+    TcKernelFn fn;
+    int smem, threads;
+    bool reg_split;     // setmaxnreg kernel: the launch must give tcw::kLaunchRegs
+};
+
+static bool pick_tc(int D, bool bf16, bool staged, TcPick *k)
 {
-    if (D == 128) {
-        *fn = !bf16 ? &tcp::prefill_tc_kernel<128, false, false, false>
-              : staged ? &tcp::prefill_tc_kernel<128, true, true, false>
-                       : &tcp::prefill_tc_kernel<128, true, false, false>;
-        *smem = tcp::Layout<128>::kTotal;
+    if (D != 128 && D != 64) return false;
+    if (!bf16 || !staged) {
+        k->fn = D == 128 ? (bf16 ? &tcp::prefill_tc_kernel<128, true, false, false>
+                                 : &tcp::prefill_tc_kernel<128, false, false, false>)
+                         : (bf16 ? &tcp::prefill_tc_kernel<64, true, false, false>
+                                 : &tcp::prefill_tc_kernel<64, false, false, false>);
+        k->smem = D == 128 ? tcp::Layout<128>::kTotal : tcp::Layout<64>::kTotal;
+        k->threads = tcp::kThreads;
+        k->reg_split = false;
         return true;
     }
-    if (D == 64) {
-        *fn = !bf16 ? &tcp::prefill_tc_kernel<64, false, false, false>
-              : staged ? &tcp::prefill_tc_kernel<64, true, true, false>
-                       : &tcp::prefill_tc_kernel<64, true, false, false>;
-        *smem = tcp::Layout<64>::kTotal;
-        return true;
-    }
-    return false;
+    k->fn = D == 128 ? &tcw::prefill_tc_kernel<128, true, true> : &tcw::prefill_tc_kernel<64, true, true>;
+    k->smem = D == 128 ? tcw::Layout<128>::kTotal : tcw::Layout<64>::kTotal;
+    k->threads = tcw::kThreads;
+    k->reg_split = true;
+    return true;
+}
+
+// The 128-key kernel's register split assumes the launch gives every thread
+// exactly tcw::kLaunchRegs registers (see tcw::kRegsIo).
+static bool launch_regs_ok(TcKernelFn fn)
+{
+    cudaFuncAttributes a;
+    return cudaFuncGetAttributes(&a, reinterpret_cast<const void *>(fn)) == cudaSuccess &&
+           a.numRegs == tcw::kLaunchRegs;
 }
 
 // Resident CTAs per SM of a kernel on the current device, cached per device
@@ -994,9 +1640,8 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     const bool staged = g.dtype == PKV_BF16 && workspace_bytes >= sl.total &&
                         (int64_t)num_seqs * max_blocks_per_seq * g.num_kv_heads * pkv::kBlock <
                             ((int64_t)1 << 31);
-    TcKernelFn fn;
-    int smem = 0;
-    if (!pick_tc(g.head_dim, g.dtype == PKV_BF16, staged, &fn, &smem)) return PKV_ERR_UNSUPPORTED;
+    TcPick kp;
+    if (!pick_tc(g.head_dim, g.dtype == PKV_BF16, staged, &kp)) return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
     if (!out || !q || !k_pool || !v_pool || !block_tables || !query_start || !context_lens ||
         !workspace || !d_status)
@@ -1044,8 +1689,8 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     prm.v_emax = staged ? reinterpret_cast<int32_t *>(ws + sl.emax) : nullptr;
 
     int sms = 0;
-    const int per_sm = resident(reinterpret_cast<const void *>(fn), smem, tcp::kThreads, &sms);
-    if (per_sm < 1) return PKV_ERR_CUDA;
+    const int per_sm = resident(reinterpret_cast<const void *>(kp.fn), kp.smem, kp.threads, &sms);
+    if (per_sm < 1 || (kp.reg_split && !launch_regs_ok(kp.fn))) return PKV_ERR_CUDA;
     int64_t grid = (int64_t)per_sm * sms;
     const int64_t upper = prm.max_items * g.num_kv_heads;
     if (grid > upper) grid = upper;
@@ -1071,12 +1716,12 @@ extern "C" int paged_prefill_attention(const pkv_pool *pool, void *out, const vo
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(tcp::kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.blockDim = dim3(kp.threads);
+    cfg.dynamicSmemBytes = (size_t)kp.smem;
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, tk, tv, tq, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, kp.fn, tk, tv, tq, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // ------------------------------------------------- shared-prefix launcher
