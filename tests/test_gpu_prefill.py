@@ -172,6 +172,31 @@ def test_v_beyond_fp16_range_in_some_tiles(staged):
     assert_close(out[start:].double() / F, exp[start:] / F, "rows with large V, scaled")
 
 
+@pytest.mark.parametrize("staged", [False, True])
+def test_scores_rising_far_above_the_reference(staged):
+    """Keys whose scores jump far above every earlier key's (K rows scaled up
+    at later positions of both sequences) move the running maximum by much more
+    than the kernels' lazy threshold (2^8) in a later key tile, so O and the
+    sum are rescaled in tensor memory mid-item, and the 128-key kernel (staged)
+    takes that tile's weights a second time.  Every row against the oracle."""
+    ctx, chunks = [700, 500], [300, 500]
+    dt, hq, hkv, d = "bf16", 32, 8, 128
+    c0, qb, qs = _case(51, ctx, chunks, hq, hkv, d, dt)
+    vals = dict(c0.host)
+    kp = (vals["k_prompt"].astype(np.uint32) << 16).view(np.float32).copy()
+    kn = (vals["k_new"].astype(np.uint32) << 16).view(np.float32).copy()
+    kp[300:340] *= 8.0                  # sequence 0, positions 300-339 (its cached prefix)
+    kn[100:110] *= 16.0                 # sequence 0, positions 500-509 (its chunk)
+    kn[300 + 200:300 + 230] *= 12.0     # sequence 1, positions 200-229
+    vals["k_prompt"] = workloads._f32_to_bf16_bits(kp)
+    vals["k_new"] = workloads._f32_to_bf16_bits(kn)
+    c = DecodeCase(c0.w, vals)
+    out = _run(c, qb, qs, staged=staged)
+    assert status_check(c.status) == (0, 0)
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, _oracle(c, qb, qs), f"prefill with rising scores staged={staged}")
+
+
 def test_staged_v_tiny_and_zero_values():
     """The fp16 copy's scale follows each (sequence, kv head)'s largest V:
     sequence 0's V scaled by 1e-25 (the copy is then scaled up by about 2^97,
