@@ -886,9 +886,9 @@ struct Layout {
 };
 
 // VS: V comes from the fp16 copy (tmV maps it; bf16 pools), so P V takes one
-// fp16 part of P and the result is scaled by 2^k.  Pools and calls that need
-// P in two parts (bf16 V as it is) or the shared-prefix mode take the 64-key
-// kernel.
+// fp16 part of P and the result is scaled by 2^k.  The host sends this kernel
+// the staged bf16 calls only; calls that need P in two parts (bf16 V as it
+// is), fp16 pools and the shared-prefix mode take the 64-key kernel.
 template <int D, bool BF16, bool VS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
