@@ -1315,7 +1315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!__all_sync(kFull, okw)) { alive = false; break; }
                 }
                 weights_pass();
-                if (__any_sync(kFull, emax > kLazy)) {
+                // rows past the query tile's tokens (stale query rows) do not vote:
+                // their weights never reach an output
+                if (__any_sync(kFull, valid && emax > kLazy)) {
                     const float mx = tile_max();
                     bool resc = false;
                     if (mx > m_ref + kLazy) {
