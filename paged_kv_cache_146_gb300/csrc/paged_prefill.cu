@@ -919,11 +919,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_full + kGroups;                       // [group]
     uint64_t *o_full = p_full + kGroups;                       // [group], one phase per item
     uint64_t *done = o_full + kGroups;                         // [group]
-    // the two query tiles take turns at the weights (their exponentials share
-    // the SFU, and while one computes, the tensor core runs the other's P V
-    // and next S): group g's weights of a tile done
-    uint64_t *w_done = done + kGroups;                         // [group]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(w_done + kGroups);
+    // the two query tiles take turns at the weights, warp by warp: softmax
+    // warps w and w + 4 share a scheduler (and its SFU, which their
+    // exponentials keep busy), and while one computes, the tensor core runs
+    // the other's P V and next S.  Warp w's weights of a tile done:
+    uint64_t *w_done = done + kGroups;                         // [softmax warp]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(w_done + 4 * kGroups);
     int *stage_bad = reinterpret_cast<int *>(tslot + 1);            // [LY::kStages]
     volatile int *abort_flag = stage_bad + LY::kStages;
 
@@ -937,12 +938,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&v_full[i]), 1);
             mbar_init(smem_addr(&v_empty[i]), kGroups);
         }
+        for (int i = 0; i < 4 * kGroups; ++i) mbar_init(smem_addr(&w_done[i]), 1);
         for (int i = 0; i < kGroups; ++i) {
             mbar_init(smem_addr(&s_full[i]), 1);
             mbar_init(smem_addr(&p_full[i]), 4);
             mbar_init(smem_addr(&o_full[i]), 1);
             mbar_init(smem_addr(&done[i]), 1);
-            mbar_init(smem_addr(&w_done[i]), 4);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1306,12 +1307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // an item sets m_ref from its maximum.
                 float f = 1.f;
                 if (t == 0) m_ref = tile_max();
-                // turns: group 0's tile tg after group 1's tile tg - 1, group 1's
-                // tile tg after group 0's tile tg (each waiter is at most one
-                // phase behind: the other group's next turn needs this one's)
+                // turns: warp w (group 0) takes tile tg after warp w + 4's tile
+                // tg - 1, warp w + 4 (group 1) after warp w's tile tg (each waiter
+                // is at most one phase behind: the other warp's next turn needs
+                // this one's)
                 if (gr == 1 || tg > 0) {
                     const uint32_t ph = gr == 0 ? tg - 1 : tg;
-                    const bool okw = mbar_wait(smem_addr(&w_done[gr ^ 1]), ph & 1u, abort_flag, p.status);
+                    const bool okw = mbar_wait(smem_addr(&w_done[warp ^ 4]), ph & 1u, abort_flag, p.status);
                     if (!__all_sync(kFull, okw)) { alive = false; break; }
                 }
                 weights_pass();
@@ -1341,7 +1343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     weights_pass();
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&w_done[gr]));
+                if (lane == 0) mbar_arrive(smem_addr(&w_done[warp]));
                 const float2 ls = unpack2f(lsum2);
                 l = l * f + (ls.x + ls.y);
                 // V of the tile has landed (its bad-block flag comes with it; the
