@@ -826,14 +826,15 @@ __global__ void __launch_bounds__(kThreads)
 //     signals P V(t - 1).
 //   warps 0-3 and 4-7 (softmax, one warpgroup per query tile): thread r owns
 //     row r = tensor-memory lane r and holds the row's 128 scores of a tile in
-//     registers; the two warpgroups take turns at the weights (their
-//     exponentials share the SFU, and while one computes, the tensor core runs
-//     the other's P V and next S).  Weights are taken against a lazy
-//     reference maximum in one pass; the tile's maximum is computed only for
-//     an item's first tile and when a score exceeds the reference by more
-//     than 8 (log2 units), which moves the reference, rescales O and the sum
-//     and takes the weights again.  The output of an item goes through shared
-//     memory, so that its stores write whole lines.
+//     registers; the two warpgroups take turns at the weights, warp by warp
+//     (warps w and w + 4 share a scheduler and its SFU, and while one
+//     computes, the tensor core runs the other's P V and next S).  Weights
+//     are taken against a lazy reference maximum in one pass; the tile's
+//     maximum is computed only for an item's first tile and when a score
+//     exceeds the reference by more than 8 (log2 units), which moves the
+//     reference, rescales O and the sum and takes the weights again.  The
+//     output of an item goes through shared memory, so that its stores write
+//     whole lines.
 //   warp 11 holds no role: the copy/issue warpgroup gives its registers to the
 //     softmax warpgroups (setmaxnreg).
 // Every wait is bounded; on expiry the kernel flags PKV_DEV_TIMEOUT and stops.
