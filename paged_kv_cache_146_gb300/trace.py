@@ -322,7 +322,13 @@ class TraceRunner:
                                            n_pre, self.workspace, self.status, out=self.out)
         evs[3].record()
         h3 = time.perf_counter()
-        kv_bytes = int(ctx.astype(np.int64).sum()) * sc.num_kv_heads * sc.head_dim * 2 * 2
+        # the call's algorithmic bytes, as for the other decode workloads: K/V
+        # of every context token, q and out of the decoding rows, and the
+        # table entries and lengths read
+        n_dec = len(decoding)
+        kv_bytes = (int(ctx.astype(np.int64).sum()) * sc.num_kv_heads * sc.head_dim * 2 * 2
+                    + 2 * n_dec * sc.num_q_heads * sc.head_dim * 2
+                    + 4 * int((-(-ctx[decoding].astype(np.int64) // bs)).sum()) + 4 * self.S)
         # finished sequences give their blocks back (one ledger call, rows in order)
         self.generated[decoding] += 1
         fin = decoding[self.generated[decoding] >= self.out_len[decoding]]
