@@ -385,7 +385,10 @@ size_t paged_prefill_workspace_bytes(int32_t num_seqs, int32_t num_tokens, int32
  * within 2^30 of its (sequence, kv head)'s largest converts exactly (when that
  * largest is at least 2^-85; below it the scale stops at 2^100); smaller ones
  * round to fp16's subnormal spacing.  The result meets the same tolerance;
- * fp16 pools ignore the extra room.  0 on a bad argument. */
+ * fp16 pools ignore the extra room.  Such calls run a kernel with 128-key
+ * tiles (the others 64-key tiles); it splits its threads' registers with
+ * setmaxnreg and launches only from a build whose kernels got the register
+ * count that split assumes (otherwise PKV_ERR_CUDA).  0 on a bad argument. */
 size_t paged_prefill_workspace_bytes_staged(int32_t num_seqs, int32_t num_tokens,
                                             int32_t num_q_heads, int32_t num_kv_heads,
                                             int32_t head_dim, int32_t max_blocks_per_seq);
